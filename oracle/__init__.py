@@ -1,0 +1,169 @@
+"""CPU oracle for the Q8_0 x Q8_0 matmul -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never does, and there is no CPU fallback through it.
+
+The arithmetic lives in the plain C file ``q8_oracle.c`` beside this one
+(built with gcc, no fast-math, no FMA contraction); this wrapper only
+marshals numpy arrays.  Every function is pinned by tests that do not use the
+oracle's own code (see ``tests/test_oracle_pins.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "q8_oracle.c")
+_LIB = os.path.join(_HERE, "libq8oracle.so")
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+_lock = threading.Lock()
+_lib = None
+
+QK = 32
+QBYTES = 34
+
+
+def compile_lib(src: str, dst: str) -> str:
+    """Compile an oracle source file into a shared library (used by build() and the mutation tests)."""
+    tmp = dst + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, src, "-lm"])
+    os.replace(tmp, dst)
+    return dst
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+        compile_lib(SOURCE, _LIB)
+    return _LIB
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the real one, or a test mutant)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        vp, u64, u32, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int
+        lib.q8o_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.q8o_f32_to_f16.restype = ctypes.c_uint16
+        lib.q8o_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.q8o_f16_to_f32.restype = ctypes.c_float
+        lib.q8o_quantize.argtypes = [vp, vp, u64, u64]
+        lib.q8o_matmul.argtypes = [vp, vp, vp, u64, u64, vp, u64]
+        lib.q8o_matmul_sample.argtypes = [vp, vp, vp, u64, u64, vp, u64, vp, vp, u64]
+        lib.q8o_moe.argtypes = [vp, vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64]
+        lib.q8o_moe_sample.argtypes = [vp, vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64,
+                                       vp, vp, u64]
+        for f in (lib.q8o_quantize, lib.q8o_matmul, lib.q8o_matmul_sample, lib.q8o_moe,
+                  lib.q8o_moe_sample):
+            f.restype = ctypes.c_int
+        self.lib = lib
+
+    # -- binary16 ------------------------------------------------------------
+    def f32_to_f16(self, v: float) -> int:
+        return int(self.lib.q8o_f32_to_f16(float(v)))
+
+    def f16_to_f32(self, h: int) -> float:
+        return float(self.lib.q8o_f16_to_f32(int(h)))
+
+    # -- quantiser -------------------------------------------------------------
+    def quantize(self, x: np.ndarray) -> np.ndarray:
+        """x float32 [n_tok, in_dim] -> uint8 [n_tok, in_dim/32*34] canonical blocks."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        n_tok, in_dim = x.shape
+        xq = np.empty((n_tok, in_dim // QK * QBYTES), dtype=np.uint8)
+        rc = self.lib.q8o_quantize(xq.ctypes.data, x.ctypes.data, in_dim, n_tok)
+        if rc != 0:
+            raise ValueError("oracle quantize: bad dims")
+        return xq
+
+    # -- matmul ------------------------------------------------------------------
+    def matmul_q(self, W: np.ndarray, xq: np.ndarray, in_dim: int, out_dim: int, n_tok: int):
+        """Returns (out float32 [n_tok, out_dim], bound float64 [n_tok, out_dim])."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        xq = np.ascontiguousarray(xq, dtype=np.uint8)
+        assert W.nbytes == out_dim * in_dim // QK * QBYTES
+        assert xq.nbytes == n_tok * in_dim // QK * QBYTES
+        out = np.empty((n_tok, out_dim), dtype=np.float32)
+        bound = np.empty((n_tok, out_dim), dtype=np.float64)
+        rc = self.lib.q8o_matmul(out.ctypes.data, bound.ctypes.data, W.ctypes.data, in_dim,
+                                 out_dim, xq.ctypes.data, n_tok)
+        if rc != 0:
+            raise ValueError("oracle matmul: bad dims")
+        return out, bound
+
+    def matmul(self, W: np.ndarray, x: np.ndarray, out_dim: int):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        n_tok, in_dim = x.shape
+        return self.matmul_q(W, self.quantize(x), in_dim, out_dim, n_tok)
+
+    def matmul_sample(self, W, xq, in_dim, out_dim, n_tok, tok, row):
+        tok = np.ascontiguousarray(tok, dtype=np.int64)
+        row = np.ascontiguousarray(row, dtype=np.int64)
+        out = np.empty(tok.size, dtype=np.float32)
+        bound = np.empty(tok.size, dtype=np.float64)
+        rc = self.lib.q8o_matmul_sample(out.ctypes.data, bound.ctypes.data,
+                                        np.ascontiguousarray(W).ctypes.data, in_dim, out_dim,
+                                        np.ascontiguousarray(xq).ctypes.data, n_tok,
+                                        tok.ctypes.data, row.ctypes.data, tok.size)
+        if rc != 0:
+            raise ValueError("oracle matmul_sample: bad arguments")
+        return out, bound
+
+    # -- routed experts ------------------------------------------------------------
+    def moe(self, W_experts, n_expert, expert_stride, ids, in_dim, out_dim, xq, x_per_pair, n_tok):
+        """Returns (out [n_tok*k, out_dim], bound, flag)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        k = ids.size // n_tok if n_tok else 1
+        out = np.empty((n_tok * k, out_dim), dtype=np.float32)
+        bound = np.empty((n_tok * k, out_dim), dtype=np.float64)
+        rc = self.lib.q8o_moe(out.ctypes.data, bound.ctypes.data,
+                              np.ascontiguousarray(W_experts).ctypes.data, n_expert, expert_stride,
+                              ids.ctypes.data, k, in_dim, out_dim,
+                              np.ascontiguousarray(xq).ctypes.data, int(x_per_pair), n_tok)
+        if rc < 0:
+            raise ValueError("oracle moe: bad dims")
+        return out, bound, rc
+
+    def moe_sample(self, W_experts, n_expert, expert_stride, ids, in_dim, out_dim, xq,
+                   x_per_pair, n_tok, pair, row):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        k = ids.size // n_tok
+        pair = np.ascontiguousarray(pair, dtype=np.int64)
+        row = np.ascontiguousarray(row, dtype=np.int64)
+        out = np.empty(pair.size, dtype=np.float32)
+        bound = np.empty(pair.size, dtype=np.float64)
+        rc = self.lib.q8o_moe_sample(out.ctypes.data, bound.ctypes.data,
+                                     np.ascontiguousarray(W_experts).ctypes.data, n_expert,
+                                     expert_stride, ids.ctypes.data, k, in_dim, out_dim,
+                                     np.ascontiguousarray(xq).ctypes.data, int(x_per_pair), n_tok,
+                                     pair.ctypes.data, row.ctypes.data, pair.size)
+        if rc < 0:
+            raise ValueError("oracle moe_sample: bad arguments")
+        return out, bound, rc
+
+
+_oracle = None
+
+
+def get() -> Oracle:
+    """The oracle built from q8_oracle.c (compiled on first use)."""
+    global _oracle
+    with _lock:
+        if _oracle is None:
+            _oracle = Oracle(build())
+    return _oracle
+
+
+def tolerance(bound: np.ndarray) -> np.ndarray:
+    """Allowed |gpu - oracle| per output: 1e-4 * sum_b |d_w d_x isum_b| + 1e-6."""
+    return 1e-4 * bound + 1e-6

@@ -1,0 +1,251 @@
+/*
+ * q8_oracle.c -- plain, slow, obviously correct CPU oracle for the
+ * Q8_0-weight x Q8_0-activation matrix multiply.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code with the CUDA library.
+ *
+ * What it follows (ds4 study guide pages):
+ *   - "Q8_0 quantised matmul" (GPU code walkthrough, trace 3): the operation
+ *     out = W x over Q8_0 weights and Q8_0 activations, with in_dim % 32 == 0
+ *     (32-element blocks), W given as out_dim rows of in_dim weights.
+ *   - "Q8_K quantisation (8-bit)" (model-architecture page, quantisation
+ *     section 1): per block amax = max |x_i|, scale = amax / 127,
+ *     q_i = (int8) roundf(x_i / scale).  The Q8_0 activation quantiser is this
+ *     formula on 32-element blocks with the scale stored as IEEE binary16.
+ *   - "fixed-point dot product" (same page, quantisation section 4): a block's
+ *     contribution is the product of the two blocks' scales and the integer
+ *     dot product of their quants, summed over blocks in fp32.
+ *   - "routed MoE" (GPU code walkthrough, trace 5) and the expert pointer
+ *     array (MoE C notes, section 1): each selected expert is a separate
+ *     weight matrix; only the selected ones are read.
+ *
+ * Readings where the pages are silent (each one also listed in the design notes):
+ *   - block layout: 34 bytes, fp16 d little-endian then int8 q[32] (GGUF Q8_0);
+ *   - x / d is an IEEE fp32 division by the fp32 d (not the fp16-rounded one),
+ *     rounding is roundf (half away from zero), d is stored rounded to binary16
+ *     (to nearest, ties to even, subnormals kept) and the dot uses that stored d;
+ *   - an all-zero block (or one whose fp32 d underflows to 0) stores d = +0 and
+ *     q = 0;
+ *   - accumulation is fp32 in block order b = 0..nb-1, each block adding
+ *     (d_w * d_x) * (float) isum;
+ *   - an expert id outside [0, n_expert) yields a zero output row and raises
+ *     the error flag.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define QK 32
+#define QBYTES 34
+
+/* ---- IEEE-754 binary16 <-> binary32, from the format's definition ---------- */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal: (-1)^s * 2^(e-15) * (1 + f/1024); subnormal (e = 0): 2^-14 * f/1024. */
+uint16_t q8o_f32_to_f16(float value) {
+    uint32_t u;
+    memcpy(&u, &value, 4);
+    uint32_t sign = (u >> 16) & 0x8000u;
+    uint32_t exp32 = (u >> 23) & 0xffu;
+    uint32_t frac32 = u & 0x7fffffu;
+    if (exp32 == 0xffu)                                 /* inf or NaN */
+        return (uint16_t)(sign | 0x7c00u | (frac32 ? 0x200u : 0u));
+    if (exp32 == 0u)                                     /* fp32 zero/subnormal: < 2^-126 -> 0 */
+        return (uint16_t)sign;
+    int e = (int)exp32 - 127;                            /* value = 1.frac * 2^e */
+    if (e > 15)
+        return (uint16_t)(sign | 0x7c00u);               /* overflow -> inf */
+    uint32_t sig = frac32 | 0x800000u;                   /* 24-bit significand */
+    if (e >= -14) {
+        /* normal: keep 10 fraction bits, drop 13, round to nearest even */
+        uint32_t keep = frac32 >> 13;
+        uint32_t rest = frac32 & 0x1fffu;
+        uint32_t h = ((uint32_t)(e + 15) << 10) | keep;
+        if (rest > 0x1000u || (rest == 0x1000u && (keep & 1u)))
+            h += 1u;                                     /* carry may reach inf: correct */
+        return (uint16_t)(sign | h);
+    }
+    /* subnormal result: count in units of 2^-24; value / 2^-24 = sig * 2^(e+1) */
+    int shift = -(e + 1);                                /* >= 14 here */
+    if (shift > 31)
+        return (uint16_t)sign;
+    uint32_t keep = sig >> shift;
+    uint32_t rest = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (keep & 1u)))
+        keep += 1u;                                      /* 0x400 = smallest normal: correct */
+    return (uint16_t)(sign | keep);
+}
+
+float q8o_f16_to_f32(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(1024 + f), e - 25);
+    return s ? -v : v;
+}
+
+/* ---- block access ------------------------------------------------------------ */
+
+static float blk_d(const uint8_t *blk) {
+    return q8o_f16_to_f32((uint16_t)(blk[0] | ((uint16_t)blk[1] << 8)));
+}
+
+static int8_t blk_q(const uint8_t *blk, int i) {
+    return (int8_t)blk[2 + i];
+}
+
+/* ---- activation quantiser ----------------------------------------------------- */
+
+/* One 32-element block of x -> one 34-byte block. */
+void q8o_quantize_block(uint8_t *out, const float *x) {
+    float amax = 0.0f;
+    for (int i = 0; i < QK; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float d = amax / 127.0f;
+    uint16_t dh = 0;
+    if (d != 0.0f) {
+        for (int i = 0; i < QK; ++i)
+            out[2 + i] = (uint8_t)(int8_t)roundf(x[i] / d);
+        dh = q8o_f32_to_f16(d);
+    } else {
+        for (int i = 0; i < QK; ++i) out[2 + i] = 0;
+    }
+    out[0] = (uint8_t)(dh & 0xffu);
+    out[1] = (uint8_t)(dh >> 8);
+}
+
+/* x [n_tok][in_dim] fp32 -> xq [n_tok][in_dim/32] blocks. */
+int q8o_quantize(uint8_t *xq, const float *x, uint64_t in_dim, uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % QK) return -1;
+    uint64_t nb = in_dim / QK;
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint64_t b = 0; b < nb; ++b)
+            q8o_quantize_block(xq + (t * nb + b) * QBYTES, x + t * in_dim + b * QK);
+    return 0;
+}
+
+/* ---- dot product -------------------------------------------------------------- */
+
+/* One output: row w (nb blocks) against activation row a (nb blocks).
+ * Returns the fp32 sum; *bound receives sum_b |d_w d_x isum_b| in double. */
+float q8o_dot_row(const uint8_t *w, const uint8_t *a, uint64_t nb, double *bound) {
+    float acc = 0.0f;
+    double bsum = 0.0;
+    for (uint64_t b = 0; b < nb; ++b) {
+        const uint8_t *wb = w + b * QBYTES;
+        const uint8_t *ab = a + b * QBYTES;
+        int32_t isum = 0;
+        for (int i = 0; i < QK; ++i)
+            isum += (int32_t)blk_q(wb, i) * (int32_t)blk_q(ab, i);
+        float dw = blk_d(wb), dx = blk_d(ab);
+        acc += (dw * dx) * (float)isum;
+        bsum += fabs((double)dw * (double)dx * (double)isum);
+    }
+    if (bound) *bound = bsum;
+    return acc;
+}
+
+/* out[t][o] = sum_b d_w d_x sum_i q_w q_x, W [out_dim][nb] blocks,
+ * xq [n_tok][nb] blocks.  bound (optional) gets the same shape as out. */
+int q8o_matmul(float *out, double *bound, const uint8_t *W, uint64_t in_dim,
+               uint64_t out_dim, const uint8_t *xq, uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % QK) return -1;
+    uint64_t nb = in_dim / QK;
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint64_t o = 0; o < out_dim; ++o) {
+            double bd = 0.0;
+            out[t * out_dim + o] = q8o_dot_row(W + o * nb * QBYTES, xq + t * nb * QBYTES, nb, &bd);
+            if (bound) bound[t * out_dim + o] = bd;
+        }
+    return 0;
+}
+
+/* Selected outputs only: out[s] = (tok[s], row[s]) of the full product. */
+int q8o_matmul_sample(float *out, double *bound, const uint8_t *W, uint64_t in_dim,
+                      uint64_t out_dim, const uint8_t *xq, uint64_t n_tok,
+                      const int64_t *tok, const int64_t *row, uint64_t n_sample) {
+    if (in_dim == 0 || in_dim % QK) return -1;
+    uint64_t nb = in_dim / QK;
+    for (uint64_t s = 0; s < n_sample; ++s) {
+        if (tok[s] < 0 || (uint64_t)tok[s] >= n_tok || row[s] < 0 || (uint64_t)row[s] >= out_dim)
+            return -1;
+        double bd = 0.0;
+        out[s] = q8o_dot_row(W + (uint64_t)row[s] * nb * QBYTES, xq + (uint64_t)tok[s] * nb * QBYTES, nb, &bd);
+        if (bound) bound[s] = bd;
+    }
+    return 0;
+}
+
+/* ---- routed experts ------------------------------------------------------------ */
+
+/* Pairs p = t*k + j select expert e = ids[p]; out[p][o] = W_e[o] . x_row, where
+ * W_e = W_experts + e * expert_stride bytes, and x_row is activation row t
+ * (x_per_pair == 0: xq has n_tok rows) or row p (x_per_pair != 0: n_tok*k rows).
+ * Returns 0, or 1 when some id was out of range (its output row is zero). */
+int q8o_moe(float *out, double *bound, const uint8_t *W_experts, uint32_t n_expert,
+            uint64_t expert_stride, const int32_t *ids, uint32_t k, uint64_t in_dim,
+            uint64_t out_dim, const uint8_t *xq, int x_per_pair, uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % QK || k == 0) return -1;
+    uint64_t nb = in_dim / QK;
+    int flag = 0;
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint32_t j = 0; j < k; ++j) {
+            uint64_t p = t * k + j;
+            int32_t e = ids[p];
+            const uint8_t *xrow = xq + (x_per_pair ? p : t) * nb * QBYTES;
+            for (uint64_t o = 0; o < out_dim; ++o) {
+                double bd = 0.0;
+                float v = 0.0f;
+                if (e < 0 || (uint32_t)e >= n_expert) {
+                    flag = 1;
+                } else {
+                    const uint8_t *w = W_experts + (uint64_t)e * expert_stride + o * nb * QBYTES;
+                    v = q8o_dot_row(w, xrow, nb, &bd);
+                }
+                out[p * out_dim + o] = v;
+                if (bound) bound[p * out_dim + o] = bd;
+            }
+        }
+    return flag;
+}
+
+/* Selected outputs of the routed product: (pair[s], row[s]). */
+int q8o_moe_sample(float *out, double *bound, const uint8_t *W_experts, uint32_t n_expert,
+                   uint64_t expert_stride, const int32_t *ids, uint32_t k, uint64_t in_dim,
+                   uint64_t out_dim, const uint8_t *xq, int x_per_pair, uint64_t n_tok,
+                   const int64_t *pair, const int64_t *row, uint64_t n_sample) {
+    if (in_dim == 0 || in_dim % QK || k == 0) return -1;
+    uint64_t nb = in_dim / QK;
+    int flag = 0;
+    for (uint64_t s = 0; s < n_sample; ++s) {
+        if (pair[s] < 0 || (uint64_t)pair[s] >= n_tok * k || row[s] < 0 || (uint64_t)row[s] >= out_dim)
+            return -1;
+        uint64_t p = (uint64_t)pair[s];
+        int32_t e = ids[p];
+        double bd = 0.0;
+        float v = 0.0f;
+        if (e < 0 || (uint32_t)e >= n_expert) {
+            flag = 1;
+        } else {
+            const uint8_t *xrow = xq + (x_per_pair ? p : p / k) * nb * QBYTES;
+            v = q8o_dot_row(W_experts + (uint64_t)e * expert_stride + (uint64_t)row[s] * nb * QBYTES,
+                            xrow, nb, &bd);
+        }
+        out[s] = v;
+        if (bound) bound[s] = bd;
+    }
+    return flag;
+}

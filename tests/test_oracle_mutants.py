@@ -1,0 +1,69 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin (no GPU).
+
+Each mutant is the oracle's C source with one plausible mistake planted by a
+text substitution, compiled into a temporary directory.  The real oracle is
+never modified.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+MUTANTS = [
+    # quantiser
+    ("reciprocal_multiply", "roundf(x[i] / d)", "roundf(x[i] * (1.0f / d))"),
+    ("round_half_even", "roundf(x[i] / d)", "rintf(x[i] / d)"),
+    ("truncate", "(int8_t)roundf(x[i] / d)", "(int8_t)(x[i] / d)"),
+    ("scale_128", "amax / 127.0f", "amax / 128.0f"),
+    ("signed_max", "float a = fabsf(x[i]);", "float a = x[i];"),
+    ("store_f32_trunc", "dh = q8o_f32_to_f16(d);", "dh = (uint16_t)(q8o_f32_to_f16(d) & 0xfffeu);"),
+    # binary16
+    ("f16_ties_away", "if (rest > 0x1000u || (rest == 0x1000u && (keep & 1u)))", "if (rest >= 0x1000u)"),
+    ("f16_flush_subnormal", "int shift = -(e + 1);", "int shift = 40;"),
+    ("f16_decode_bias", "v = ldexpf((float)(1024 + f), e - 25);", "v = ldexpf((float)(1024 + f), e - 24);"),
+    ("f16_decode_subnormal", "v = ldexpf((float)f, -24);", "v = ldexpf((float)(1024 + f), -25);"),
+    # dot
+    ("drop_last_block", "acc += (dw * dx) * (float)isum;", "if (b + 1 < nb) acc += (dw * dx) * (float)isum;"),
+    ("wrong_index", "(int32_t)blk_q(ab, i)", "(int32_t)blk_q(ab, QK - 1 - i)"),
+    ("wrong_sign", "acc += (dw * dx) * (float)isum;", "acc -= (dw * dx) * (float)isum;"),
+    ("missing_scale", "acc += (dw * dx) * (float)isum;", "acc += dw * (float)isum;"),
+    ("transposed", "out[t * out_dim + o] = q8o_dot_row(W + o * nb * QBYTES, xq + t * nb * QBYTES, nb, &bd);",
+     "out[t * out_dim + o] = q8o_dot_row(W + (o % n_tok) * nb * QBYTES, xq + (t % out_dim) * nb * QBYTES, nb, &bd);"),
+    ("d_byte_order", "(uint16_t)(blk[0] | ((uint16_t)blk[1] << 8))", "(uint16_t)(blk[1] | ((uint16_t)blk[0] << 8))"),
+    ("q_offset", "return (int8_t)blk[2 + i];", "return (int8_t)blk[1 + i];"),
+    # routed experts
+    ("moe_row_choice", "xq + (x_per_pair ? p : t) * nb * QBYTES", "xq + (x_per_pair ? t : p % n_tok) * nb * QBYTES"),
+    ("moe_expert_stride", "W_experts + (uint64_t)e * expert_stride + o * nb * QBYTES", "W_experts + (uint64_t)e * out_dim * nb * QBYTES + o * nb * QBYTES"),
+    ("moe_no_flag", "                    flag = 1;\n                } else {\n                    const uint8_t *w", "                    flag = 0;\n                } else {\n                    const uint8_t *w"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(source, name, old, new):
+    assert source.count(old) >= 1, f"mutation site for {name} not found in the oracle source"
+    mutated = source.replace(old, new)
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, f"mut_{name}.c")
+        lib = os.path.join(d, f"libmut_{name}.so")
+        with open(src, "w") as f:
+            f.write(mutated)
+        oracle.compile_lib(src, lib)
+        m = oracle.Oracle(lib)
+        failed = []
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin(m)
+            except AssertionError:
+                failed.append(pin.__name__)
+            except Exception:  # a crash on the mutant also counts as caught
+                failed.append(pin.__name__ + "(error)")
+        assert failed, f"planted mistake {name!r} passed every pin"
