@@ -1,0 +1,524 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 x Q8_0 matmul on GB300.
+
+One step = one pass of the decode hot path over the decode projection sweep
+workload (attn_q_b shape: W 32768 x 1024 Q8_0, activations fp32 with 1% of
+values scaled x20): for n_tok = 1, 4 and 16, quantise the activations and
+multiply (q8_matmul).  Metric: weight GB/s (34 bytes per 32 weights read per
+call); prefill int8-equivalent TOPS and routed-expert GB/s are reported in
+the same JSON line under "secondary".
+
+Timing: W >= 3 warm-up steps, then exactly K steps replayed as CUDA graphs,
+bracketed by a barrier and a device synchronise, CUDA events on the launching
+stream, max over ranks.  Inputs larger than L2: every call of a step reads its
+own copy of the weights, rotating through copies totalling more than 4x L2.
+SM clocks are sampled with nvidia-smi during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--full]
+
+--impl reference times the CPU oracle (test infrastructure, the only other
+place this file runs it) on the host cores on a bounded sample of the same
+workload.  Under torchrun each rank runs its own replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+QK, QB = 32, 34
+METRIC = "Q8_0 matmul weight GB/s (n_tok≤16) & int8 TOPS (prefill), % of roofline"
+IN_DIM, OUT_DIM, N_TOKS = 1024, 32768, (1, 4, 16)
+W_BYTES = OUT_DIM * IN_DIM // QK * QB
+WORKLOAD = ("decode projection sweep (attn_q_b shape): in_dim=1024, out_dim=32768, n_tok in {1,4,16}; "
+            "Q8_0 weights q~U[-127,127], d~U[1e-3,1e-2] fp16; x~N(0,1) with 1% x20 outliers; seed 0")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--full", action="store_true", help="also measure the long-prefill layer slice")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl")
+    return dist
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="q8clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ peaks and traffic
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash(files=("q8_mma.cu", "q8_common.cuh")) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "q8_quantized_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_hash") != kernel_source_hash(tuple(e.get("files", ("q8_mma.cu", "q8_common.cuh")))):
+            return None
+        return e
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ GPU arm
+def weight_copies(torch, dev, host_w, total_bytes_min):
+    n = max(1, math.ceil(total_bytes_min / host_w.nbytes))
+    t = torch.from_numpy(host_w).to(dev)
+    return [t] + [t.clone() for _ in range(n - 1)]
+
+
+def graph_replays(torch, stream, graphs, steps):
+    """Replay graphs[i % len] for i in range(steps) on `stream`; returns elapsed ms (CUDA events)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_ours(args, rank, world, local, dist):
+    import torch
+    import q8_quantized_matmul_gb300 as q8
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- inputs (seeded, synthetic; weights resident in HBM before timing)
+    Wh = inputs.weights(OUT_DIM, IN_DIM, seed=0)
+    n_calls = len(N_TOKS)
+    copies = weight_copies(torch, dev, Wh, 4 * l2)
+    while len(copies) % n_calls:
+        copies.append(copies[0].clone())
+    xs = {n: torch.from_numpy(inputs.normal((n, IN_DIM), seed=0, p_out=0.01, out_scale=20.0)).to(dev) for n in N_TOKS}
+    outs = {n: torch.empty((n, OUT_DIM), dtype=torch.float32, device=dev) for n in N_TOKS}
+    n_graphs = len(copies) // n_calls
+
+    def call(n, W):
+        rc = q8.q8_matmul(outs[n], W, IN_DIM, OUT_DIM, xs[n], n, stream)
+        if rc:
+            raise q8.Q8Error(rc, "q8_matmul")
+
+    # warm-up eagerly (sizes the scratch, sets kernel attributes), then capture
+    with torch.cuda.stream(stream):
+        for g in range(n_graphs):
+            for c, n in enumerate(N_TOKS):
+                call(n, copies[g * n_calls + c])
+    stream.synchronize()
+    assert q8.q8_last_error(stream) == 0
+    q8.q8_profile_arm(n_graphs * n_calls)
+    graphs = []
+    for g in range(n_graphs):
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            for c, n in enumerate(N_TOKS):
+                call(n, copies[g * n_calls + c])
+        graphs.append(cg)
+    assert q8.q8_profile_used() == n_graphs * n_calls
+
+    graph_replays(torch, stream, graphs, args.warmup)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local if world > 1 else (torch.cuda.current_device())) as clk:
+        ms = graph_replays(torch, stream, graphs, args.steps)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms = max_over_ranks(dist, ms)
+    assert q8.q8_last_error(stream) == 0
+    # per-launch kernel times: the last replay of every graph (all inside the timed region)
+    kern = {n: [] for n in N_TOKS}
+    for g in range(n_graphs):
+        for c, n in enumerate(N_TOKS):
+            kern[n].append(q8.q8_profile_read(g * n_calls + c))
+    q8.q8_profile_arm(0)
+
+    ms_step = ms / args.steps
+    step_bytes = W_BYTES * n_calls
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    tokens_per_s = world * sum(N_TOKS) / (ms_step * 1e-3)
+
+    # algorithmic bytes of the matmul kernel per launch: weights + activation planes + outputs
+    def kbytes(n):
+        npad = (n + 15) // 16 * 16
+        return W_BYTES + npad * IN_DIM + npad * (IN_DIM // QK) * 4 + n * OUT_DIM * 4
+    mean_k = {n: statistics.mean(v) for n, v in kern.items()}
+    tot_bytes = sum(kbytes(n) for n in N_TOKS)
+    tot_ms = sum(mean_k.values())
+    peak, peak_kind = hbm_peak()
+    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
+    tr = committed_traffic("k_mma decode sweep")
+    roofline = {"bound": "hbm", "kernel": "q8::k_mma", "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "algorithmic_bytes_per_launch": round(tot_bytes / n_calls),
+                "per_n": {str(n): {"kernel_us": round(mean_k[n] * 1e3, 2),
+                                   "weight_gbs": round(W_BYTES / (mean_k[n] * 1e-3) / 1e9, 1),
+                                   "frac_of_peak": round(kbytes(n) / (mean_k[n] * 1e-3) / 1e9 / peak, 4)}
+                          for n in N_TOKS}}
+
+    # ---- end to end through the public API with pinned host buffers
+    xh = {n: xs[n].cpu().pin_memory() for n in N_TOKS}
+    oh = {n: torch.empty((n, OUT_DIM), dtype=torch.float32).pin_memory() for n in N_TOKS}
+    xd = {n: torch.empty_like(xs[n]) for n in N_TOKS}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step(i):
+        for c, n in enumerate(N_TOKS):
+            xd[n].copy_(xh[n], non_blocking=True)
+            rc = q8.q8_matmul(outs[n], copies[(i * n_calls + c) % len(copies)], IN_DIM, OUT_DIM, xd[n], n, stream)
+            if rc:
+                raise q8.Q8Error(rc, "q8_matmul")
+            oh[n].copy_(outs[n], non_blocking=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        stream.synchronize()
+        barrier(dist)
+        e0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.steps
+    e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "ms_per_step": round(e2e_ms, 4),
+           "h2d_bytes_per_step": sum(n * IN_DIM * 4 for n in N_TOKS),
+           "d2h_bytes_per_step": sum(n * OUT_DIM * 4 for n in N_TOKS),
+           "path": "q8_matmul via the C ABI, pinned host x -> device, result -> pinned host, eager launches"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {len(copies)} weight copies ({len(copies) * W_BYTES / 2 ** 20:.0f} MiB) "
+                         f"rotated, each call reads its own copy (L2 {l2 / 2 ** 20:.0f} MiB)",
+                   "launch": "CUDA graph replay of the step (3 x [quantise + matmul])",
+                   "tokens_per_s": round(tokens_per_s, 1)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * n_calls * 2,
+        "clocks": clk.summary(),
+    }
+    del copies, graphs
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_secondary:
+        result["secondary"] = secondary(args, torch, q8, dev, stream, l2)
+    return result
+
+
+def timed_eager(torch, stream, fn, iters, warm=2):
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(iters):
+            fn(i)
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def secondary(args, torch, q8, dev, stream, l2):
+    """Other workloads, one line each (kernel timing through the library's event hook)."""
+    out = []
+    tflops, tflops_sus, tkind = tensor_peak()
+    hbm, hkind = hbm_peak()
+
+    def prof_mean(npairs):
+        v = [q8.q8_profile_read(i) for i in range(npairs)]
+        return statistics.mean(v)
+
+    # single matvec (attn_q_a shape)
+    W = inputs.weights(1024, 4096, seed=0)
+    copies = weight_copies(torch, dev, W, 4 * l2)
+    x = torch.from_numpy(inputs.normal((1, 4096), seed=0)).to(dev)
+    o = torch.empty((1, 1024), device=dev)
+    with torch.cuda.stream(stream):
+        for c in copies:
+            q8.q8_matmul(o, c, 4096, 1024, x, 1, stream)
+    stream.synchronize()
+    q8.q8_profile_arm(len(copies))
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=stream):
+        for c in copies:
+            q8.q8_matmul(o, c, 4096, 1024, x, 1, stream)
+    graph_replays(torch, stream, [cg], 3)
+    ms = graph_replays(torch, stream, [cg], 20) / len(copies)
+    kms = prof_mean(len(copies))
+    q8.q8_profile_arm(0)
+    wb = W.nbytes
+    out.append({"workload": "single matvec (attn_q_a shape) in 4096 -> out 1024, n_tok 1",
+                "ms_per_call": round(ms, 5), "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1),
+                "kernel_us": round(kms * 1e3, 2), "kernel_weight_gbs": round(wb / (kms * 1e-3) / 1e9, 1),
+                "kernel_frac_of_hbm_peak": round(wb / (kms * 1e-3) / 1e9 / hbm, 4)})
+    del copies, cg
+
+    # prefill GEMMs (attn_output_a and shared-expert shapes) at n_tok = 512
+    for in_dim, out_dim in ((32768, 1024), (4096, 2048), (2048, 4096)):
+        n = 512
+        W = inputs.weights(out_dim, in_dim, seed=1)
+        copies = weight_copies(torch, dev, W, 2 * l2)
+        x = torch.from_numpy(inputs.normal((n, in_dim), seed=1)).to(dev)
+        o = torch.empty((n, out_dim), device=dev)
+        q8.q8_profile_arm(8)
+        ms = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim, x, n,
+                                                                stream), 8)
+        kms = prof_mean(8)
+        q8.q8_profile_arm(0)
+        ops = 2.0 * in_dim * out_dim * n
+        out.append({"workload": f"prefill GEMM in {in_dim} -> out {out_dim}, n_tok {n}",
+                    "ms_per_call": round(ms, 4), "tops": round(ops / (ms * 1e-3) / 1e12, 2),
+                    "kernel_ms": round(kms, 4), "kernel_tops": round(ops / (kms * 1e-3) / 1e12, 2),
+                    "kernel_frac_of_bf16_peak": round(ops / (kms * 1e-3) / 1e12 / tflops, 4),
+                    "peak_note": f"int8-equivalent ops vs {tkind} dense bf16 tensor peak {tflops} TFLOP/s "
+                                 "(no int8 MMA instruction on sm_103a)"})
+        del copies
+
+    # routed experts: gate/up (x per token) and down (x per pair), 256 experts, 64 tokens, uniform top-6
+    n_exp, n_tok, k = 256, 64, 6
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=0)
+    touched = len(np.unique(ids))
+    idsd = torch.from_numpy(ids).to(dev)
+    for name, in_dim, out_dim, per_pair in (("gate/up", 4096, 2048, 0), ("down", 2048, 4096, 1)):
+        W = torch.from_numpy(inputs.weights(n_exp * out_dim, in_dim, seed=2)).to(dev)
+        stride = out_dim * in_dim // QK * QB
+        x = torch.from_numpy(inputs.normal((n_tok * k if per_pair else n_tok, in_dim), seed=2)).to(dev)
+        o = torch.empty((n_tok * k, out_dim), device=dev)
+        q8.q8_profile_arm(6)
+        ms = timed_eager(torch, stream, lambda i: q8.q8_moe_matmul(o, W, n_exp, stride, idsd, k, in_dim, out_dim, x,
+                                                                    per_pair, n_tok, stream), 6)
+        kms = prof_mean(6)
+        q8.q8_profile_arm(0)
+        wb = touched * stride
+        out.append({"workload": f"routed MoE {name}: 256 experts [{out_dim}x{in_dim}], n_tok 64, uniform top-6 "
+                                f"({touched} experts touched)",
+                    "ms_per_call": round(ms, 4), "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1),
+                    "kernel_ms": round(kms, 4), "kernel_weight_gbs": round(wb / (kms * 1e-3) / 1e9, 1),
+                    "kernel_frac_of_hbm_peak": round(wb / (kms * 1e-3) / 1e9 / hbm, 4)})
+        del W
+    assert q8.q8_last_error(stream) == 0
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+def oracle_step_sample(o, W_rows, xs, rows):
+    """One step of the workload on the first `rows` weight rows with the CPU oracle."""
+    Ws = W_rows[:rows]
+    for n, x in xs.items():
+        xq = o.quantize(x)
+        o.matmul_q(Ws, xq, IN_DIM, rows, n)
+
+
+def cpu_oracle_rate(target_s: float):
+    """Weight GB/s of the oracle on a bounded row sample of the workload (single thread)."""
+    import oracle
+    o = oracle.get()
+    Wh = inputs.weights(OUT_DIM, IN_DIM, seed=0)
+    xs = {n: inputs.normal((n, IN_DIM), seed=0, p_out=0.01, out_scale=20.0) for n in N_TOKS}
+    rows = 256
+    t0 = time.perf_counter()
+    oracle_step_sample(o, Wh, xs, rows)
+    dt = time.perf_counter() - t0
+    rows = int(min(OUT_DIM, max(256, rows * target_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    oracle_step_sample(o, Wh, xs, rows)
+    dt = time.perf_counter() - t0
+    bytes_ = rows * IN_DIM // QK * QB * len(N_TOKS)
+    return {"value": round(bytes_ / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {OUT_DIM} weight rows, n_tok 1, 4, 16 (quantise + matmul), "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    o = oracle.get()
+    Wh = inputs.weights(OUT_DIM, IN_DIM, seed=0)
+    xs = {n: inputs.normal((n, IN_DIM), seed=0, p_out=0.01, out_scale=20.0) for n in N_TOKS}
+    rows = 512
+    t0 = time.perf_counter()
+    oracle_step_sample(o, Wh, xs, rows)
+    per_row = (time.perf_counter() - t0) / rows
+    budget = 120.0 / (args.steps + args.warmup)          # whole run within about two minutes
+    rows = int(min(OUT_DIM, max(64, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_step_sample(o, Wh, xs, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step_sample(o, Wh, xs, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    bytes_ = rows * IN_DIM // QK * QB * len(N_TOKS)
+    v = bytes_ / dt / 1e9
+    sample = (f"each step: first {rows} of {OUT_DIM} weight rows, n_tok 1, 4, 16 (quantise + matmul), "
+              "single-threaded plain C oracle")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        r = run_reference(args, rank, world)
+        if r is not None:
+            print(json.dumps(r))
+        return 0
+    dist = dist_init(world)
+    res = run_ours(args, rank, world, local, dist)
+    if rank == 0:
+        if not args.no_cpu:
+            res["cpu_baseline"] = cpu_oracle_rate(target_s=10.0)
+        print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,184 @@
+/*
+ * q8.h -- C ABI of the GB300 (sm_103a) Q8_0-weight x Q8_0-activation matmul library.
+ *
+ * The operation is the one the ds4 engine's "Q8_0 quantised matmul" entry
+ * (GPU code walkthrough, trace 3, ds4_gpu_matmul_q8_0_tensor) performs:
+ *
+ *     out[t][o] = sum_b  d_w[o][b] * d_x[t][b] * sum_{i<32} q_w[o][b][i] * q_x[t][b][i]
+ *
+ * accumulated in fp32, where W holds out_dim rows of in_dim weights in Q8_0
+ * blocks and the activations are quantised per 32-element block with the
+ * formula printed for the Q8_K quantiser (model-architecture page,
+ * quantisation section 1): d = max|x| / 127, q = roundf(x / d).
+ *
+ * Formats
+ *   Q8_0 block: 34 bytes = fp16 scale d (IEEE binary16, little-endian) then
+ *   int8 q[32].  A row of in_dim values is in_dim/32 consecutive blocks; a
+ *   matrix is its rows back to back (row o = output o).  in_dim % 32 == 0
+ *   (the pages' alignment requirement).
+ *   Activations x: fp32, [n_tok][in_dim], row-major, token-major.
+ *   Outputs out: fp32, [n_tok][out_dim], row-major.
+ *
+ * Conventions (all entry points)
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     an entry point says otherwise.  The library never frees caller memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and return Q8_OK when the work was
+ *     enqueued, or a negative Q8_E* code, in which case nothing was enqueued.
+ *   - Arguments are validated on the host before any launch: null pointers,
+ *     zero or misaligned dimensions and size overflow give Q8_EINVAL; W, x,
+ *     out and xq must be 16-byte aligned, else Q8_EALIGN.  n_tok == 0 or
+ *     out_dim == 0 is valid and does nothing.
+ *   - Errors found on the device (an expert id out of range) never trap:
+ *     the affected output rows are written as zeros and a device error word
+ *     is raised; q8_last_error() reads and clears it.
+ *   - Results are deterministic: the same inputs give the same bits on every
+ *     run (fixed reduction order, no floating-point atomics).
+ *   - The library keeps a per-device grow-only scratch buffer for quantised
+ *     activations and routing tables (the pages' reused aligned Q8 scratch).
+ *     Calls that use scratch must not run concurrently on different streams
+ *     of the same device.  q8_release() frees it.
+ */
+#ifndef Q8_H
+#define Q8_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8_BLOCK 32        /* values per Q8_0 block */
+#define Q8_BLOCK_BYTES 34  /* fp16 d + int8 q[32] */
+
+enum q8_status {
+    Q8_OK = 0,
+    Q8_EINVAL = -1,      /* bad dimension, null pointer, in_dim % 32 != 0, overflow */
+    Q8_EALIGN = -2,      /* a pointer is not 16-byte aligned */
+    Q8_ERANGE = -3,      /* (device) an expert id was outside [0, n_expert) */
+    Q8_ENOMEM = -4,      /* scratch allocation failed */
+    Q8_ECUDA = -5,       /* a CUDA runtime call failed (no device, launch error, ...) */
+    Q8_ETIMEOUT = -6     /* (device) a kernel's bounded wait expired; outputs undefined */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+int q8_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *q8_strerror(int status);
+
+/*
+ * Activation quantiser (model-architecture page, quantisation section 1,
+ * applied to 32-element blocks with the scale stored as binary16).
+ *   xq   out: n_tok * (in_dim/32) Q8_0 blocks, token-major ([n_tok][in_dim/32]).
+ *   x    in:  fp32 [n_tok][in_dim].
+ * Per block: amax = max|x_i| (fp32); d = amax / 127.0f (IEEE division);
+ * if d == 0 every q_i = 0 and the stored d is +0; otherwise
+ * q_i = (int8) roundf(x_i / d) (IEEE division by the fp32 d, halves away from
+ * zero) and the stored d is d rounded to binary16 (nearest, ties to even,
+ * subnormals kept).  Bit-exact: the same bytes as the CPU definition.
+ * NaN/Inf inputs are outside the contract.
+ */
+int q8_quantize_act(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, void *stream);
+
+/*
+ * Q8_0 matmul from fp32 activations (GPU code walkthrough, trace 3:
+ * ds4_gpu_matmul_q8_0_tensor(out, model_map, ..., weight_offset, in_dim,
+ * out_dim, x, n_tok); here W is already a device pointer to the weight rows).
+ *   out  out: fp32 [n_tok][out_dim].
+ *   W    in:  out_dim rows of in_dim/32 Q8_0 blocks (34 bytes each).
+ *   x    in:  fp32 [n_tok][in_dim]; quantised per block into library scratch
+ *             with exactly the q8_quantize_act arithmetic.
+ * n_tok <= 16 runs the weight-streaming decode kernel; larger n_tok the
+ * prefill GEMM.  Both give out[t][o] = sum over blocks, in fp32, of
+ * d_w*d_x*isum with isum the exact int32 block dot; the summation order
+ * differs from a sequential loop only by fp32 rounding.
+ */
+int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
+              const float *x, uint64_t n_tok, void *stream);
+
+/*
+ * Same product from activations already quantised by q8_quantize_act
+ * (xq: [n_tok][in_dim/32] Q8_0 blocks, 16-byte aligned).
+ */
+int q8_matmul_q(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
+                const void *xq, uint64_t n_tok, void *stream);
+
+/*
+ * Routed-expert matmul (GPU code walkthrough, trace 5: the per-expert
+ * projections of ds4_gpu_routed_moe_one_tensor; MoE C notes, section 1: one
+ * weight matrix per expert, only the selected ones are read).  Pairs are
+ * p = t*k + j for token t and slot j; expert e = expert_ids[p].
+ *   out               out: fp32 [n_tok*k][out_dim]; row p = W_e . x_row.
+ *   W_experts         in:  n_expert matrices, expert e at byte offset
+ *                          e*expert_stride_bytes, each out_dim rows of Q8_0 blocks.
+ *   expert_stride_bytes    >= out_dim*(in_dim/32)*34, a multiple of 16.
+ *   expert_ids        in:  int32 [n_tok][k] (device).
+ *   x                 in:  fp32; x_per_pair == 0: [n_tok][in_dim], x_row = row t
+ *                          (gate/up projections); x_per_pair != 0:
+ *                          [n_tok*k][in_dim], x_row = row p (down projection).
+ * Pairs are bucketed by expert on the device (stable in p), each expert's
+ * weights are streamed once for all of its pairs.  An id outside
+ * [0, n_expert) gives a zero row and raises Q8_ERANGE for q8_last_error().
+ */
+int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert,
+                  uint64_t expert_stride_bytes, const int32_t *expert_ids, uint32_t k,
+                  uint64_t in_dim, uint64_t out_dim, const float *x, int x_per_pair,
+                  uint64_t n_tok, void *stream);
+
+/*
+ * Optional load-time repack of Q8_0 rows into split planes (a quant plane
+ * of int8 [rows][in_dim] followed by a scale plane of fp16 [rows][in_dim/32]),
+ * the layout the ROCm MXFP4 work on the pages found fastest (16-byte
+ * aligned value slices with a separate scale array).  Bit-preserving.
+ *   q8_repack_bytes: size of the packed buffer for rows x in_dim.
+ *   q8_repack:       Wp (out, device, q8_repack_bytes bytes) <- W (in, raw rows).
+ *   q8_matmul_packed: as q8_matmul, weights from a q8_repack buffer.
+ */
+uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows);
+int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, void *stream);
+int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_dim,
+                     const float *x, uint64_t n_tok, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word of
+ * the current device: Q8_OK, Q8_ERANGE (an expert id was out of range) or
+ * Q8_ETIMEOUT (a bounded wait inside a kernel expired), or Q8_ECUDA when the
+ * synchronisation itself failed.
+ */
+int q8_last_error(void *stream);
+
+/* Scratch bytes currently held on the current device (0 if none). */
+uint64_t q8_scratch_bytes(void);
+
+/* Frees the scratch of every device (synchronises each first). */
+void q8_release(void);
+
+/*
+ * Kernel timing hook (for benchmarks).  q8_profile_arm(n) creates n pairs of
+ * timing events on the current device (n = 0 destroys them and disarms).
+ * While armed, every call that launches a matmul kernel (q8_matmul,
+ * q8_matmul_q, q8_moe_matmul, q8_matmul_packed) records the next pair, in
+ * round-robin order, on its own stream immediately before and after that
+ * kernel -- also inside CUDA graph capture, where the records become graph
+ * nodes.  q8_profile_used() is the number of pairs recorded since arming;
+ * q8_profile_read(i, &ms) waits for pair i's end event and returns its
+ * elapsed time in milliseconds.  Returns Q8_EINVAL for a pair never recorded.
+ */
+int q8_profile_arm(uint32_t n_pairs);
+uint64_t q8_profile_used(void);
+int q8_profile_read(uint32_t i, float *ms);
+
+/*
+ * Test hook: make the next `count` scratch allocations fail as if the device
+ * were out of memory (they then return Q8_ENOMEM); 0 restores normal
+ * behaviour.  Exists so that the allocation-failure path can be tested
+ * without exhausting a shared GPU.
+ */
+void q8_debug_fail_next_alloc(int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8_H */

@@ -1,0 +1,434 @@
+// q8_api.cu -- the C ABI (include/q8.h): host-side validation, per-device
+// scratch and error word, and dispatch to the kernels.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/q8.h"
+#include "q8_common.cuh"
+#include "q8_kernels.h"
+
+// Device error word (one per device context).  Kernels receive its address.
+__device__ int g_q8_device_error = 0;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr uint32_t MAX_EXPERTS = 16384;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int *err = nullptr;          // device address of g_q8_device_error
+    void *scratch = nullptr;
+    size_t scratch_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[MAX_DEVICES];
+int g_fail_next_alloc = 0;
+
+// Kernel timing hook: event pairs recorded around the main matmul kernel.
+struct Profile {
+    int device = -1;
+    uint32_t n = 0;
+    uint64_t used = 0;
+    cudaEvent_t *ev = nullptr;   // 2*n events
+    uint8_t *recorded = nullptr; // per pair
+} g_prof;
+
+void profile_free() {
+    if (g_prof.ev) {
+        for (uint32_t i = 0; i < 2 * g_prof.n; ++i) cudaEventDestroy(g_prof.ev[i]);
+        delete[] g_prof.ev;
+        delete[] g_prof.recorded;
+    }
+    g_prof = Profile{};
+}
+
+// Launch `launch` between the next pair of timing events when armed.
+template <class F> cudaError_t timed_launch(cudaStream_t st, F launch) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (!g_prof.n || dev != g_prof.device) return launch();
+    const uint32_t i = (uint32_t)(g_prof.used % g_prof.n);
+    cudaError_t e = cudaEventRecord(g_prof.ev[2 * i], st);
+    if (e != cudaSuccess) return e;
+    e = launch();
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(g_prof.ev[2 * i + 1], st);
+    g_prof.recorded[i] = 1;
+    ++g_prof.used;
+    return e;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ECUDA; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device's state, initialised on first use.
+int get_device(DeviceState **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        int sms = 0, major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return Q8_ECUDA;
+        }
+        if (major * 10 + minor != 103) return Q8_ECUDA;   // built for sm_103a only
+        void *err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_q8_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return Q8_ECUDA;
+        }
+        s.num_sms = sms;
+        s.err = static_cast<int *>(err);
+        s.ready = true;
+    }
+    *out = &s;
+    return Q8_OK;
+}
+
+// Grow-only scratch of at least `bytes`.  Growing synchronises the device
+// (cudaFree does), so a call that grows it must not overlap work of another
+// stream that still uses the old buffer -- scratch users are single-stream.
+int reserve_scratch(DeviceState *s, size_t bytes) {
+    if (bytes <= s->scratch_bytes) return Q8_OK;
+    if (g_fail_next_alloc > 0) {
+        --g_fail_next_alloc;
+        return Q8_ENOMEM;
+    }
+    size_t want = bytes + bytes / 4;
+    want = (want + ((size_t)1 << 20) - 1) & ~(((size_t)1 << 20) - 1);
+    if (s->scratch) {
+        cudaFree(s->scratch);
+        s->scratch = nullptr;
+        s->scratch_bytes = 0;
+    }
+    void *p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+        cudaGetLastError();
+        return Q8_ENOMEM;
+    }
+    s->scratch = p;
+    s->scratch_bytes = want;
+    return Q8_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Sub-allocations of the scratch buffer.
+struct Carver {
+    uint8_t *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base(static_cast<uint8_t *>(b)) {}
+    template <class T> T *take(size_t bytes) {
+        T *p = reinterpret_cast<T *>(base + off);
+        off = align256(off + bytes);
+        return p;
+    }
+};
+
+size_t planes_bytes(uint64_t rows, uint64_t in_dim) {
+    return align256(rows * in_dim) + align256(rows * (in_dim / q8::QK) * sizeof(float));
+}
+
+int check_dims(uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % q8::QK) return Q8_EINVAL;
+    if (in_dim > ((uint64_t)1 << 31) || out_dim > ((uint64_t)1 << 31) - 1 || n_tok > ((uint64_t)1 << 31) - 1)
+        return Q8_EINVAL;
+    const uint64_t nb = in_dim / q8::QK;
+    if (out_dim && nb > (((uint64_t)1 << 62) / q8::QB) / out_dim) return Q8_EINVAL;
+    if (n_tok && in_dim > ((uint64_t)1 << 40) / n_tok) return Q8_EINVAL;
+    return Q8_OK;
+}
+
+// out = W x from activation planes already in scratch (n_pad rows).
+int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const int8_t *qx,
+              const float *dx, uint64_t n_tok, cudaStream_t st) {
+    q8::MmaParams p{};
+    p.W = static_cast<const uint8_t *>(W);
+    p.expert_stride = 0;
+    p.in_dim = in_dim;
+    p.out_dim = (uint32_t)out_dim;
+    p.nb = (uint32_t)(in_dim / q8::QK);
+    p.qx = qx;
+    p.dx = dx;
+    p.out = out;
+    p.err = s->err;
+    p.n_tok = (uint32_t)n_tok;
+    p.plan = nullptr;
+    p.row_to_out = nullptr;
+    if (p.nb % 8 == 0) {
+        const uint64_t items = ((out_dim + 15) / 16) * ((n_tok + 63) / 64);
+        const int grid = (int)(items < (uint64_t)s->num_sms ? items : (uint64_t)s->num_sms);
+        return status_of(timed_launch(st, [&] { return q8::launch_mma(p, grid, st); }));
+    }
+    const int hint = (int)((n_tok * out_dim) > (1u << 30) ? (1u << 30) : n_tok * out_dim);
+    return status_of(timed_launch(st, [&] { return q8::launch_generic(p, hint, s->num_sms, st); }));
+}
+
+}  // namespace
+
+extern "C" {
+
+int q8_version(void) { return 10000; }
+
+const char *q8_strerror(int status) {
+    switch (status) {
+        case Q8_OK: return "ok";
+        case Q8_EINVAL: return "invalid argument";
+        case Q8_EALIGN: return "pointer not 16-byte aligned";
+        case Q8_ERANGE: return "expert id out of range";
+        case Q8_ENOMEM: return "scratch allocation failed";
+        case Q8_ECUDA: return "CUDA runtime error";
+        case Q8_ETIMEOUT: return "bounded wait expired inside a kernel";
+        default: return "unknown status";
+    }
+}
+
+int q8_quantize_act(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, void *stream) {
+    int rc = check_dims(in_dim, 1, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0) return Q8_OK;
+    if (!xq || !x) return Q8_EINVAL;
+    if (!aligned16(xq) || !aligned16(x)) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    return status_of(q8::launch_quantize_blocks(static_cast<uint8_t *>(xq), x, n_tok * (in_dim / q8::QK), s->num_sms,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
+                         const void *xq, uint64_t n_tok, void *stream) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W || (!x && !xq)) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(W) || (x && !aligned16(x)) || (xq && !aligned16(xq))) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
+    if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
+    Carver cv(s->scratch);
+    int8_t *qx = cv.take<int8_t>(n_pad * in_dim);
+    float *dx = cv.take<float>(n_pad * (in_dim / q8::QK) * sizeof(float));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = x ? q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st)
+                      : q8::launch_unpack_blocks(qx, dx, static_cast<const uint8_t *>(xq), in_dim, n_pad, n_tok,
+                                                 s->num_sms, st);
+    if (e != cudaSuccess) return Q8_ECUDA;
+    return run_dense(s, out, W, in_dim, out_dim, qx, dx, n_tok, st);
+}
+
+int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x, uint64_t n_tok,
+              void *stream) {
+    if (!x && n_tok) return Q8_EINVAL;
+    return matmul_common(out, W, in_dim, out_dim, x, nullptr, n_tok, stream);
+}
+
+int q8_matmul_q(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const void *xq, uint64_t n_tok,
+                void *stream) {
+    if (!xq && n_tok) return Q8_EINVAL;
+    return matmul_common(out, W, in_dim, out_dim, nullptr, xq, n_tok, stream);
+}
+
+int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t expert_stride_bytes,
+                  const int32_t *expert_ids, uint32_t k, uint64_t in_dim, uint64_t out_dim, const float *x,
+                  int x_per_pair, uint64_t n_tok, void *stream) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_expert == 0 || n_expert > MAX_EXPERTS || k == 0 || k > n_expert) return Q8_EINVAL;
+    const uint64_t nb = in_dim / q8::QK;
+    if (expert_stride_bytes < out_dim * nb * q8::QB) return Q8_EINVAL;
+    if (n_tok * k > ((uint64_t)1 << 31) - 1) return Q8_EINVAL;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W_experts || !expert_ids || !x) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(W_experts) || !aligned16(x) || (expert_stride_bytes & 15u) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
+        return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    const uint64_t n_pairs = n_tok * k;
+    const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
+    const size_t need = align256(n_expert * 4) * 2 + align256(sizeof(q8::PlanHeader) + n_expert * sizeof(q8::Segment)) +
+                        align256(max_rows * 4) * 2 + planes_bytes(max_rows, in_dim);
+    if ((rc = reserve_scratch(s, need))) return rc;
+    Carver cv(s->scratch);
+    int32_t *counts = cv.take<int32_t>(n_expert * 4);
+    int32_t *row0_of = cv.take<int32_t>(n_expert * 4);
+    q8::PlanHeader *plan = cv.take<q8::PlanHeader>(sizeof(q8::PlanHeader) + n_expert * sizeof(q8::Segment));
+    int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
+    int32_t *src_row = cv.take<int32_t>(max_rows * 4);
+    int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
+    float *dx = cv.take<float>(max_rows * nb * sizeof(float));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, counts, row0_of,
+                                     plan, row_to_out, src_row, max_rows, out, s->err, s->num_sms, st);
+    if (e != cudaSuccess) return Q8_ECUDA;
+    e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
+    if (e != cudaSuccess) return Q8_ECUDA;
+    q8::MmaParams p{};
+    p.W = static_cast<const uint8_t *>(W_experts);
+    p.expert_stride = expert_stride_bytes;
+    p.in_dim = in_dim;
+    p.out_dim = (uint32_t)out_dim;
+    p.nb = (uint32_t)nb;
+    p.qx = qx;
+    p.dx = dx;
+    p.out = out;
+    p.err = s->err;
+    p.n_tok = 0;
+    p.plan = plan;
+    p.row_to_out = row_to_out;
+    if (nb % 8 == 0) return status_of(timed_launch(st, [&] { return q8::launch_mma(p, s->num_sms, st); }));
+    const int hint = (int)(max_rows * out_dim > (1u << 30) ? (1u << 30) : max_rows * out_dim);
+    return status_of(timed_launch(st, [&] { return q8::launch_generic(p, hint, s->num_sms, st); }));
+}
+
+uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows) {
+    if (in_dim == 0 || in_dim % q8::QK) return 0;
+    return rows * in_dim + rows * (in_dim / q8::QK) * 2;
+}
+
+int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, void *stream) {
+    int rc = check_dims(in_dim, rows, 1);
+    if (rc) return rc;
+    if (rows == 0) return Q8_OK;
+    if (!Wp || !W) return Q8_EINVAL;
+    if (!aligned16(Wp) || !aligned16(W)) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    return status_of(q8::launch_repack(static_cast<uint8_t *>(Wp), static_cast<const uint8_t *>(W), in_dim, rows,
+                                       s->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_dim, const float *x, uint64_t n_tok,
+                     void *stream) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !Wp || !x) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(Wp) || !aligned16(x)) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
+    if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
+    Carver cv(s->scratch);
+    int8_t *qx = cv.take<int8_t>(n_pad * in_dim);
+    float *dx = cv.take<float>(n_pad * (in_dim / q8::QK) * sizeof(float));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st) != cudaSuccess)
+        return Q8_ECUDA;
+    return status_of(timed_launch(st, [&] {
+        return q8::launch_matmul_packed(out, static_cast<const uint8_t *>(Wp), in_dim, out_dim, qx, dx, n_tok,
+                                        s->num_sms, st);
+    }));
+}
+
+int q8_last_error(void *stream) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    int rc = get_device(&s);
+    if (rc) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    int v = 0, zero = 0;
+    if (cudaMemcpy(&v, s->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(s->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    return v;
+}
+
+uint64_t q8_scratch_bytes(void) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return 0;
+    }
+    return g_dev[dev].scratch_bytes;
+}
+
+void q8_release(void) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    for (int d = 0; d < MAX_DEVICES; ++d) {
+        if (!g_dev[d].scratch) continue;
+        cudaSetDevice(d);
+        cudaDeviceSynchronize();
+        cudaFree(g_dev[d].scratch);
+        g_dev[d].scratch = nullptr;
+        g_dev[d].scratch_bytes = 0;
+    }
+    cudaSetDevice(cur);
+}
+
+int q8_profile_arm(uint32_t n_pairs) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    profile_free();
+    if (n_pairs == 0) return Q8_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    g_prof.ev = new cudaEvent_t[2 * n_pairs];
+    g_prof.recorded = new uint8_t[n_pairs]();
+    for (uint32_t i = 0; i < 2 * n_pairs; ++i) {
+        if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+            cudaGetLastError();
+            for (uint32_t j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+            delete[] g_prof.ev;
+            delete[] g_prof.recorded;
+            g_prof = Profile{};
+            return Q8_ECUDA;
+        }
+    }
+    g_prof.n = n_pairs;
+    g_prof.device = dev;
+    return Q8_OK;
+}
+
+uint64_t q8_profile_used(void) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    return g_prof.used;
+}
+
+int q8_profile_read(uint32_t i, float *ms) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!ms || i >= g_prof.n || !g_prof.recorded[i]) return Q8_EINVAL;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    return Q8_OK;
+}
+
+void q8_debug_fail_next_alloc(int count) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    g_fail_next_alloc = count > 0 ? count : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// q8_kernels.h -- internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q8 {
+
+// Segment table written by the routing kernels (grouped mode) or filled on
+// the host (dense mode: one segment).  Segment s covers activation-plane rows
+// [row0, row0 + count) (padded to a multiple of 16 rows with zero rows) and
+// multiplies them by the weights of `expert`.
+struct Segment {
+    int32_t expert;
+    int32_t row0;
+    int32_t count;
+    int32_t item_start;   // first work item of this segment
+};
+
+struct PlanHeader {      // device-side header before the segment array
+    int32_t n_segments;
+    int32_t n_items;
+    int32_t n_rows;      // activation-plane rows used (multiple of 16)
+    int32_t pad;
+};
+
+struct MmaParams {
+    const uint8_t *W;          // raw Q8_0 rows (dense) or the first expert's rows
+    uint64_t expert_stride;    // bytes between experts
+    uint64_t in_dim;
+    uint32_t out_dim;
+    uint32_t nb;               // in_dim / 32
+    const int8_t *qx;          // activation quant plane [rows][in_dim]
+    const float *dx;           // activation scale plane [rows][nb]
+    float *out;                // [*][out_dim]
+    int *err;                  // device error word
+    // dense mode (plan == nullptr): one segment of n_tok rows, output row = plane row
+    uint32_t n_tok;
+    // grouped mode
+    const PlanHeader *plan;    // header followed by Segment[n_segments]
+    const int32_t *row_to_out; // plane row -> output row (-1: padding)
+};
+
+// Quantiser (q8_quantize.cu)
+cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, int num_sms, cudaStream_t st);
+cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
+                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st);
+cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *xq, uint64_t in_dim, uint64_t n_rows,
+                                 uint64_t n_src, int num_sms, cudaStream_t st);
+
+// Tensor-core (mma.sync int8) matmul over raw Q8_0 rows (q8_mma.cu).
+// Requires nb % 8 == 0, W and expert_stride 16-byte aligned.
+cudaError_t launch_mma(const MmaParams &p, int grid, cudaStream_t st);
+// Any in_dim % 32 == 0 and 2-byte aligned W: one thread per output (slow path).
+cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, cudaStream_t st);
+
+// Routing (q8_moe.cu): buckets pairs by expert and writes the plan.
+//   plan      : PlanHeader + Segment[n_expert]
+//   row_to_out, src_row: int32[max_rows], max_rows = route_max_rows(n_pairs, n_expert)
+//   counts, row0_of: int32[n_expert] scratch
+uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
+cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
+                         uint32_t out_dim, int32_t *counts, int32_t *row0_of, PlanHeader *plan,
+                         int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
+                         int num_sms, cudaStream_t st);
+
+// Repack (q8_repack.cu)
+cudaError_t launch_repack(uint8_t *Wp, const uint8_t *W, uint64_t in_dim, uint64_t rows, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_matmul_packed(float *out, const uint8_t *Wp, uint64_t in_dim, uint64_t out_dim,
+                                 const int8_t *qx, const float *dx, uint64_t n_tok, int num_sms, cudaStream_t st);
+
+}  // namespace q8

@@ -1,0 +1,176 @@
+// q8_moe.cu -- device-side bucketing of (token, slot) pairs by expert.
+//
+// The routed-expert step of the ds4 engine (GPU code walkthrough, trace 5;
+// MoE C notes, section 1) multiplies each selected expert's weights by the
+// rows routed to it, reading only the selected experts.  For a batch of
+// tokens the pairs p = t*k + j are grouped per expert so that every touched
+// expert's weights are streamed once for all of its rows (the grouped GEMM
+// with a per-expert offsets table the pages describe for the packed Metal
+// kernels).  Three small kernels, all deterministic:
+//   1. k_route_count : one CTA per expert counts its pairs; out-of-range ids
+//      get a zero output row and raise Q8_ERANGE (no trap).
+//   2. k_route_plan  : one CTA orders the touched experts by pair count
+//      (largest first, ties by id: the big groups start first, which keeps the
+//      persistent grid balanced under skewed routing), assigns each a
+//      16-row-aligned range of activation-plane rows and a range of work items.
+//   3. k_route_fill  : one CTA per expert lists its pairs in increasing p
+//      (block-wide prefix sums), giving the plane-row -> output-row map and the
+//      plane-row -> input-row map used by the gathering quantiser.
+#include "q8_common.cuh"
+#include "q8_kernels.h"
+
+namespace q8 {
+
+constexpr int ROUTE_THREADS = 512;
+constexpr int TOK_PER_ITEM = 64;   // must match the matmul kernel's tokens per work item
+constexpr int ROWS_PER_ITEM = 16;  // and its weight rows per work item
+
+uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert) {
+    const uint64_t touched = n_pairs < n_expert ? n_pairs : n_expert;
+    return n_pairs + 15 * touched + 16;
+}
+
+__device__ __forceinline__ int block_sum(int v, int *sh) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    int s = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += sh[i];
+    return s;
+}
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_count(const int32_t *__restrict__ ids, uint64_t n_pairs,
+                                                                uint32_t n_expert, int32_t *__restrict__ counts) {
+    __shared__ int sh[32];
+    const int e = blockIdx.x;
+    int cnt = 0;
+    for (uint64_t p = threadIdx.x; p < n_pairs; p += blockDim.x) cnt += (__ldg(ids + p) == e);
+    cnt = block_sum(cnt, sh);
+    if (threadIdx.x == 0) counts[e] = cnt;
+}
+
+// Zero the output rows of pairs whose id is out of range and raise the error word.
+__global__ void __launch_bounds__(256) k_route_bad(const int32_t *__restrict__ ids, uint64_t n_pairs,
+                                                   uint32_t n_expert, uint32_t out_dim, float *__restrict__ out,
+                                                   int *err) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    for (uint64_t p = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_pairs; p += warps) {
+        const int32_t e = __ldg(ids + p);
+        if (e < 0 || (uint32_t)e >= n_expert) {
+            for (uint32_t o = lane; o < out_dim; o += 32) out[p * out_dim + o] = 0.0f;
+            if (lane == 0) raise_error(err, DEV_ERANGE);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
+                                                               uint32_t out_dim, PlanHeader *plan,
+                                                               int32_t *__restrict__ row0_of) {
+    extern __shared__ int32_t sh_plan[];   // order[n_expert] (sorted position -> expert)
+    int32_t *order = sh_plan;
+    __shared__ int n_active_sh;
+    const int n_rb = (int)((out_dim + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
+    if (threadIdx.x == 0) n_active_sh = 0;
+    __syncthreads();
+    // Rank of each touched expert: larger count first, then smaller id.
+    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
+        const int ce = counts[e];
+        if (ce > 0) {
+            int rank = 0;
+            for (uint32_t f = 0; f < n_expert; ++f) {
+                const int cf = counts[f];
+                rank += (cf > ce) || (cf == ce && f < e);
+            }
+            order[rank] = (int32_t)e;   // touched experts take ranks 0..n_active-1
+            atomicAdd(&n_active_sh, 1);
+        }
+        row0_of[e] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Segment *segs = reinterpret_cast<Segment *>(plan + 1);
+        const int n_active = n_active_sh;
+        int row = 0, item = 0;
+        for (int s = 0; s < n_active; ++s) {
+            const int e = order[s];
+            const int ce = counts[e];
+            segs[s].expert = e;
+            segs[s].row0 = row;
+            segs[s].count = ce;
+            segs[s].item_start = item;
+            row0_of[e] = row;
+            row += (ce + 15) & ~15;
+            item += n_rb * ((ce + TOK_PER_ITEM - 1) / TOK_PER_ITEM);
+        }
+        plan->n_segments = n_active;
+        plan->n_items = item;
+        plan->n_rows = row;
+        plan->pad = 0;
+    }
+}
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__restrict__ ids, uint64_t n_pairs,
+                                                               uint32_t k, int x_per_pair,
+                                                               const int32_t *__restrict__ row0_of,
+                                                               int32_t *__restrict__ row_to_out,
+                                                               int32_t *__restrict__ src_row) {
+    __shared__ int warp_tot[ROUTE_THREADS / 32];
+    const int e = blockIdx.x;
+    const int row0 = row0_of[e];
+    if (row0 < 0) return;   // untouched expert (uniform across the CTA)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int base = 0;
+    for (uint64_t p0 = 0; p0 < n_pairs; p0 += blockDim.x) {
+        const uint64_t p = p0 + threadIdx.x;
+        const bool hit = p < n_pairs && __ldg(ids + p) == e;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0) warp_tot[w] = __popc(m);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+            before += (i < w) ? warp_tot[i] : 0;
+            total += warp_tot[i];
+        }
+        if (hit) {
+            const int pos = base + before + __popc(m & ((1u << lane) - 1u));
+            row_to_out[row0 + pos] = (int32_t)p;
+            src_row[row0 + pos] = (int32_t)(x_per_pair ? p : p / k);
+        }
+        base += total;
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
+                         uint32_t out_dim, int32_t *counts, int32_t *row0_of, PlanHeader *plan,
+                         int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
+                         int num_sms, cudaStream_t st) {
+    const uint64_t n_pairs = n_tok * k;
+    cudaError_t e;
+    // Padding rows map to nothing: -1 everywhere first.
+    if ((e = cudaMemsetAsync(row_to_out, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(src_row, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
+    k_route_count<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, n_expert, counts);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    int grid_bad = (int)((n_pairs + 7) / 8);
+    if (grid_bad > num_sms * 4) grid_bad = num_sms * 4;
+    if (grid_bad < 1) grid_bad = 1;
+    k_route_bad<<<grid_bad, 256, 0, st>>>(ids, n_pairs, n_expert, out_dim, out, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t plan_smem = (size_t)n_expert * sizeof(int32_t);
+    if (plan_smem > 48 * 1024) {
+        if ((e = cudaFuncSetAttribute(k_route_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem)) !=
+            cudaSuccess)
+            return e;
+    }
+    k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, plan, row0_of);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_route_fill<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, k, x_per_pair, row0_of, row_to_out, src_row);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

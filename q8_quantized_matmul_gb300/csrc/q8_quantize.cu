@@ -1,0 +1,181 @@
+// q8_quantize.cu -- activation quantiser kernels.
+//
+// The arithmetic is the per-block quantiser of the ds4 pages (model-architecture
+// page, quantisation section 1, printed for Q8_K) applied to 32-element blocks:
+//   amax = max|x_i|,  d = amax / 127 (IEEE fp32 division),
+//   q_i = (int8) roundf(x_i / d) (IEEE division by the fp32 d, halves away from zero),
+//   stored d = binary16(d) (round to nearest even, subnormals kept);
+//   d == 0 (all-zero block, or an fp32 underflow) stores d = +0 and q = 0.
+// The library is built without fast-math, so '/' is the IEEE division and
+// roundf / __float2half_rn are CUDA's correctly specified routines.
+//
+// Thread mapping: four consecutive lanes own one block (eight values each,
+// two 16-byte loads), the block maximum is two xor-shuffles away.  Work is
+// memory bound (4 bytes read per value); grids are sized as a multiple of
+// the SM count and loop over blocks.
+#include "q8_common.cuh"
+#include "q8_kernels.h"
+
+namespace q8 {
+
+struct QuantBlock {
+    int8_t q[8];      // this lane's eight quants
+    uint16_t dh;      // stored binary16 scale (same on the four lanes)
+    float d_stored;   // dh as fp32 (exact)
+};
+
+// x8: this lane's eight values of the block; lanes 4i..4i+3 hold one block.
+__device__ __forceinline__ QuantBlock quantize8(const float (&x8)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x8[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    QuantBlock r;
+    if (d != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = static_cast<int8_t>(static_cast<int>(roundf(__fdiv_rn(x8[i], d))));
+        r.dh = __half_as_ushort(__float2half_rn(d));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = 0;
+        r.dh = 0;
+    }
+    r.d_stored = half_bits_to_float(r.dh);
+    return r;
+}
+
+__device__ __forceinline__ void load8(float (&x8)[8], const float *p) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
+    x8[4] = b.x; x8[5] = b.y; x8[6] = b.z; x8[7] = b.w;
+}
+
+// Canonical 34-byte blocks: xq[blk] for blk in [0, nblk), x read flat.
+__global__ void __launch_bounds__(256) k_quantize_blocks(uint8_t *__restrict__ xq, const float *__restrict__ x,
+                                                         uint64_t nblk) {
+    const uint64_t lane_q = threadIdx.x & 3u;
+    const uint64_t groups_per_cta = blockDim.x / 4;
+    // Whole warps iterate together (the shuffles need all lanes): loop bound is per warp.
+    for (uint64_t base = (uint64_t)blockIdx.x * groups_per_cta; base < nblk; base += (uint64_t)gridDim.x * groups_per_cta) {
+        const uint64_t blk = base + threadIdx.x / 4;
+        const bool live = blk < nblk;
+        float x8[8];
+        if (live) load8(x8, x + blk * QK + lane_q * 8);
+        else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
+        }
+        const QuantBlock r = quantize8(x8);
+        if (live) {
+            uint8_t *o = xq + blk * QB;
+            if (lane_q == 0) *reinterpret_cast<uint16_t *>(o) = r.dh;
+            uint16_t *qo = reinterpret_cast<uint16_t *>(o + 2 + lane_q * 8);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                qo[i] = (uint16_t)((uint8_t)r.q[2 * i]) | (uint16_t)((uint16_t)(uint8_t)r.q[2 * i + 1] << 8);
+        }
+    }
+}
+
+// Split planes for the matmul kernels: qplane [n_rows][in_dim] int8 and
+// dplane [n_rows][nb] fp32 (the stored binary16 scale as fp32).  Output row r
+// is quantised from x row src_row[r] when src_row is given (a negative entry
+// gives a zero row), else from x row r when r < n_src, else it is zero.
+__global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qplane, float *__restrict__ dplane,
+                                                         const float *__restrict__ x, uint64_t in_dim,
+                                                         uint64_t n_rows, const int32_t *__restrict__ src_row,
+                                                         uint64_t n_src) {
+    const uint64_t nb = in_dim / QK;
+    const uint64_t nblk = n_rows * nb;
+    const uint64_t lane_q = threadIdx.x & 3u;
+    const uint64_t groups_per_cta = blockDim.x / 4;
+    for (uint64_t base = (uint64_t)blockIdx.x * groups_per_cta; base < nblk; base += (uint64_t)gridDim.x * groups_per_cta) {
+        const uint64_t blk = base + threadIdx.x / 4;
+        const bool live = blk < nblk;
+        const uint64_t r = live ? blk / nb : 0;
+        const uint64_t b = live ? blk - r * nb : 0;
+        int64_t s = -1;
+        if (live) s = src_row ? (int64_t)src_row[r] : (r < n_src ? (int64_t)r : -1);
+        float x8[8];
+        if (s >= 0) load8(x8, x + (uint64_t)s * in_dim + b * QK + lane_q * 8);
+        else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
+        }
+        const QuantBlock qb = quantize8(x8);
+        if (live) {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
+                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
+            }
+            *reinterpret_cast<uint2 *>(qplane + r * in_dim + b * QK + lane_q * 8) = make_uint2(lo, hi);
+            if (lane_q == 0) dplane[r * nb + b] = qb.d_stored;
+        }
+    }
+}
+
+// Canonical blocks -> split planes (for pre-quantised activations).  One
+// thread per (row, block); rows >= n_src are zero.
+__global__ void __launch_bounds__(256) k_unpack_blocks(int8_t *__restrict__ qplane, float *__restrict__ dplane,
+                                                       const uint8_t *__restrict__ xq, uint64_t in_dim,
+                                                       uint64_t n_rows, uint64_t n_src) {
+    const uint64_t nb = in_dim / QK;
+    const uint64_t nblk = n_rows * nb;
+    for (uint64_t blk = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;
+         blk += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t r = blk / nb, b = blk - r * nb;
+        uint32_t w[8];
+        float d = 0.0f;
+        if (r < n_src) {
+            const uint8_t *p = xq + blk * QB;   // same (row, block) index: xq is [n_src][nb]
+            const uint16_t *p16 = reinterpret_cast<const uint16_t *>(p);
+            d = half_bits_to_float(p16[0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = (uint32_t)p16[1 + 2 * i] | ((uint32_t)p16[2 + 2 * i] << 16);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0;
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(qplane + r * in_dim + b * QK);
+        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dplane[blk] = d;
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+static int grid_for(uint64_t work_items, int per_cta, int num_sms) {
+    uint64_t need = (work_items + per_cta - 1) / per_cta;
+    uint64_t cap = (uint64_t)num_sms * 8;
+    if (need > cap) need = cap;
+    return need ? (int)need : 1;
+}
+
+cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, int num_sms, cudaStream_t st) {
+    if (nblk == 0) return cudaSuccess;
+    k_quantize_blocks<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(xq, x, nblk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
+                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_rows * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *xq, uint64_t in_dim, uint64_t n_rows,
+                                 uint64_t n_src, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_rows * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    k_unpack_blocks<<<grid_for(nblk, 256, num_sms), 256, 0, st>>>(qplane, dplane, xq, in_dim, n_rows, n_src);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

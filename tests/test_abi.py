@@ -1,0 +1,100 @@
+"""The C-ABI library loads and exports every symbol include/q8.h declares, and
+its host-side validation rejects bad arguments before touching a GPU (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q8():
+    from q8_quantized_matmul_gb300 import build
+    build.build()
+    import q8_quantized_matmul_gb300 as m
+    return m
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "q8.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q8_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("q8_quantize_act", "q8_matmul", "q8_moe_matmul"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(q8):
+    lib = ctypes.CDLL(q8.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/q8.h but not exported"
+    assert set(declared_functions()) == set(q8.EXPORTS)
+
+
+def test_version_and_strerror(q8):
+    assert q8.q8_version() >= 10000
+    assert q8.q8_strerror(q8.Q8_ERANGE) == "expert id out of range"
+    assert q8.q8_strerror(12345) == "unknown status"
+
+
+def test_repack_bytes_is_the_same_footprint(q8):
+    assert q8.q8_repack_bytes(4096, 1024) == 1024 * 128 * 34
+    assert q8.q8_repack_bytes(33, 10) == 0
+
+
+# Host validation: fake (never dereferenced) addresses, returns before any CUDA call.
+A = 0x10000  # 16-byte aligned fake address
+B = 0x20000
+
+
+@pytest.mark.parametrize("in_dim", [0, 31, 33, 48])
+def test_bad_in_dim_rejected(q8, in_dim):
+    assert q8.lib.q8_matmul(A, B, in_dim, 8, A, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_quantize_act(A, B, in_dim, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_moe_matmul(A, B, 4, 1 << 20, A, 2, in_dim, 8, A, 0, 3, None) == q8.Q8_EINVAL
+
+
+def test_null_and_misaligned_pointers_rejected(q8):
+    assert q8.lib.q8_matmul(0, B, 64, 8, A, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_matmul(A, 0, 64, 8, A, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_matmul(A + 4, B, 64, 8, A, 1, None) == q8.Q8_EALIGN
+    assert q8.lib.q8_matmul(A, B + 2, 64, 8, A, 1, None) == q8.Q8_EALIGN
+    assert q8.lib.q8_matmul_q(A, B, 64, 8, A + 8, 1, None) == q8.Q8_EALIGN
+    assert q8.lib.q8_quantize_act(A + 1, B, 64, 1, None) == q8.Q8_EALIGN
+
+
+def test_moe_argument_checks(q8):
+    L = q8.lib
+    stride = 8 * 2 * 34  # out 8, in 64 -> 8 rows x 2 blocks
+    assert L.q8_moe_matmul(A, B, 0, stride, A, 1, 64, 8, A, 0, 1, None) == q8.Q8_EINVAL       # no experts
+    assert L.q8_moe_matmul(A, B, 4, stride, A, 5, 64, 8, A, 0, 1, None) == q8.Q8_EINVAL       # k > n_expert
+    assert L.q8_moe_matmul(A, B, 4, stride - 16, A, 2, 64, 8, A, 0, 1, None) == q8.Q8_EINVAL  # stride too small
+    assert L.q8_moe_matmul(A, B, 4, stride + 8, A, 2, 64, 8, A, 0, 1, None) == q8.Q8_EALIGN   # stride % 16
+    assert L.q8_moe_matmul(A, B, 4, stride, A + 2, 2, 64, 8, A, 0, 1, None) == q8.Q8_EALIGN   # ids % 4
+    assert L.q8_moe_matmul(A, B, 1 << 20, stride, A, 2, 64, 8, A, 0, 1, None) == q8.Q8_EINVAL  # too many experts
+
+
+def test_empty_work_is_a_no_op(q8):
+    # n_tok == 0 or out_dim == 0 returns before touching the device
+    assert q8.lib.q8_matmul(A, B, 64, 8, A, 0, None) == q8.Q8_OK
+    assert q8.lib.q8_matmul(A, B, 64, 0, A, 5, None) == q8.Q8_OK
+    assert q8.lib.q8_quantize_act(A, B, 64, 0, None) == q8.Q8_OK
+
+
+def test_overflowing_sizes_rejected(q8):
+    assert q8.lib.q8_matmul(A, B, 1 << 32, 8, A, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_matmul(A, B, 64, 1 << 40, A, 1, None) == q8.Q8_EINVAL
+
+
+def test_no_gpu_means_error_not_crash(q8):
+    """Without a usable sm_103a device the first real call reports Q8_ECUDA."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert q8.lib.q8_matmul(A, B, 64, 8, A, 1, None) == q8.Q8_ECUDA

@@ -1,0 +1,363 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Quantised activations must be bit-exact; matmul outputs must satisfy
+|gpu - oracle| <= 1e-4 * sum_b |d_w d_x isum_b| + 1e-6 element by element.
+Outputs are poisoned with NaN before every call and followed by a NaN guard
+band that must stay untouched, so a kernel that skips rows or writes out of
+bounds fails.
+"""
+import numpy as np
+import pytest
+
+import inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+QK, QB = 32, 34
+GUARD = 64
+
+
+@pytest.fixture(scope="module")
+def q8():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from q8_quantized_matmul_gb300 import build
+    build.build()
+    import q8_quantized_matmul_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+DEV = "cuda:0"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def poisoned(n):
+    return torch.full((n + GUARD,), float("nan"), dtype=torch.float32, device=DEV)
+
+
+def fetch(buf, n, shape):
+    h = buf.cpu().numpy()
+    assert np.all(np.isnan(h[n:])), "guard band after the output was written"
+    return h[:n].reshape(shape)
+
+
+def assert_close(got, ref, bound, what=""):
+    assert not np.any(np.isnan(got)), f"{what}: output element not written (NaN poison survived)"
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    tol = oracle.tolerance(bound)
+    bad = err > tol
+    assert not np.any(bad), (f"{what}: {bad.sum()} outputs out of tolerance, worst err {err.max():.3e} "
+                             f"at {np.unravel_index(np.argmax(err - tol), err.shape)}")
+
+
+def gpu_matmul(q8, W, x, out_dim):
+    n_tok, in_dim = x.shape
+    buf = poisoned(n_tok * out_dim)
+    rc = q8.q8_matmul(buf, W, in_dim, out_dim, x, n_tok)
+    assert rc == 0, q8.q8_strerror(rc)
+    assert q8.q8_last_error() == 0
+    return fetch(buf, n_tok * out_dim, (n_tok, out_dim))
+
+
+# ------------------------------------------------------------------ quantiser
+def _special_x(g, n_tok, in_dim):
+    x = g.standard_normal((n_tok, in_dim)).astype(np.float32)
+    xb = x.reshape(n_tok, -1, QK)
+    nb = xb.shape[1]
+    kinds = g.integers(0, 6, size=(n_tok, nb))
+    for t in range(n_tok):
+        for b in range(nb):
+            k = kinds[t, b]
+            if k == 0:
+                xb[t, b] = 0.0                                              # all-zero block
+            elif k == 1:
+                d = np.float32(2.0 ** g.integers(-20, 4))                   # exact ties (m + 1/2) * d
+                v = (g.integers(0, 126, QK) + 0.5) * np.where(g.random(QK) < .5, -1, 1)
+                v[0] = 127
+                xb[t, b] = (d * v).astype(np.float32)
+            elif k == 2:
+                xb[t, b] *= np.float32(1e-6)                                # subnormal binary16 scale
+            elif k == 3:
+                xb[t, b] *= np.float32(1e-40)                               # scale underflows
+            elif k == 4:
+                xb[t, b] *= np.float32(np.exp(g.uniform(-30, 30)))          # wide magnitudes
+    return x
+
+
+@pytest.mark.parametrize("n_tok,in_dim", [(1, 32), (3, 96), (16, 1024), (37, 4096), (5, 32768)])
+def test_quantize_bit_exact(q8, o, n_tok, in_dim):
+    g = np.random.default_rng(n_tok * 7 + in_dim)
+    for x in (inputs.normal((n_tok, in_dim), seed=n_tok, p_out=0.01), _special_x(g, n_tok, in_dim)):
+        ref = o.quantize(x)
+        xq = torch.full((n_tok * (in_dim // QK) * QB + GUARD,), 0xAB, dtype=torch.uint8, device=DEV)
+        assert q8.q8_quantize_act(xq, dev(x), in_dim, n_tok) == 0
+        h = xq.cpu().numpy()
+        assert np.all(h[-GUARD:] == 0xAB)
+        got = h[:-GUARD].reshape(ref.shape)
+        mism = np.argwhere(got != ref)
+        assert mism.size == 0, f"{len(mism)} bytes differ, first at {mism[:3].tolist()}"
+
+
+def test_quantize_prefill_size_bit_exact(q8, o):
+    x = inputs.normal((512, 32768), seed=0)
+    assert np.array_equal(q8.quantize_act(dev(x)).cpu().numpy(), o.quantize(x))
+
+
+# ------------------------------------------------------------------ dense matmul, small and ragged
+SHAPES = [
+    (256, 16, 1), (512, 100, 3), (1024, 33, 16), (2048, 250, 17), (256, 1000, 64), (768, 77, 65),
+    (4096, 40, 130), (8192, 24, 5), (1280, 131, 200),
+    # in_dim % 256 != 0: rows not 16-byte aligned (slow path)
+    (32, 5, 1), (96, 19, 7), (160, 50, 20), (4000, 8, 2),
+]
+
+
+@pytest.mark.parametrize("in_dim,out_dim,n_tok", SHAPES)
+def test_matmul_parity(q8, o, in_dim, out_dim, n_tok):
+    Wh = inputs.weights(out_dim, in_dim, seed=in_dim + out_dim)
+    xh = inputs.normal((n_tok, in_dim), seed=n_tok, p_out=0.01)
+    ref, bound = o.matmul(Wh, xh, out_dim)
+    got = gpu_matmul(q8, dev(Wh), dev(xh), out_dim)
+    assert_close(got, ref, bound, f"matmul {in_dim}x{out_dim}x{n_tok}")
+
+
+def test_matmul_q_matches_matmul_bitwise(q8, o):
+    in_dim, out_dim, n_tok = 1024, 300, 40
+    W = dev(inputs.weights(out_dim, in_dim, seed=5))
+    x = dev(inputs.normal((n_tok, in_dim), seed=6))
+    a = q8.matmul(W, x, out_dim)
+    b = q8.matmul_q(W, q8.quantize_act(x), in_dim, out_dim)
+    assert torch.equal(a, b)
+
+
+def test_integer_case_exact(q8):
+    """All scales 1.0 and activations that quantise to themselves: exact integer product."""
+    g = np.random.default_rng(3)
+    in_dim, out_dim, n_tok = 512, 64, 20
+    nb = in_dim // QK
+    qw = g.integers(-127, 128, size=(out_dim, nb, QK))
+    Wh = np.empty((out_dim, nb, QB), np.uint8)
+    Wh[..., 0], Wh[..., 1] = 0x00, 0x3C
+    Wh[..., 2:] = qw.astype(np.int8).view(np.uint8)
+    qx = g.integers(-127, 128, size=(n_tok, nb, QK))
+    qx[:, :, 0] = 127                                   # every block's max is 127: d = 1 exactly
+    xh = qx.reshape(n_tok, in_dim).astype(np.float32)
+    got = gpu_matmul(q8, dev(Wh.reshape(out_dim, -1)), dev(xh), out_dim)
+    ref = xh.astype(np.int64) @ qw.reshape(out_dim, in_dim).T
+    assert np.array_equal(got.astype(np.int64), ref)
+
+
+def test_deterministic(q8):
+    in_dim, out_dim, n_tok = 2048, 512, 100
+    W = dev(inputs.weights(out_dim, in_dim, seed=8))
+    x = dev(inputs.normal((n_tok, in_dim), seed=9))
+    a = q8.matmul(W, x, out_dim)
+    for _ in range(3):
+        assert torch.equal(a, q8.matmul(W, x, out_dim))
+
+
+# ------------------------------------------------------------------ the five workloads
+def test_config1_single_matvec(q8, o):
+    Wh = inputs.weights(1024, 4096, seed=0)
+    xh = inputs.normal((1, 4096), seed=0)
+    ref, bound = o.matmul(Wh, xh, 1024)
+    assert_close(gpu_matmul(q8, dev(Wh), dev(xh), 1024), ref, bound, "config 1")
+
+
+@pytest.mark.parametrize("n_tok", [1, 4, 16])
+def test_config2_decode_sweep(q8, o, n_tok):
+    Wh = inputs.weights(32768, 1024, seed=0)
+    xh = inputs.normal((n_tok, 1024), seed=0, p_out=0.01, out_scale=20.0)
+    ref, bound = o.matmul(Wh, xh, 32768)
+    assert_close(gpu_matmul(q8, dev(Wh), dev(xh), 32768), ref, bound, f"config 2 n={n_tok}")
+
+
+def _sampled_check(q8, o, W, x, in_dim, out_dim, n_tok, n_sample=3000, full_tokens=(0,), seed=0):
+    Wd, xd = dev(W), dev(x)
+    got = gpu_matmul(q8, Wd, xd, out_dim)
+    xq = o.quantize(x)
+    g = np.random.default_rng(seed)
+    tok = np.concatenate([g.integers(0, n_tok, n_sample)] + [np.full(out_dim, t) for t in full_tokens])
+    row = np.concatenate([g.integers(0, out_dim, n_sample)] + [np.arange(out_dim) for _ in full_tokens])
+    ref, bound = o.matmul_sample(W, xq, in_dim, out_dim, n_tok, tok, row)
+    assert_close(got[tok, row], ref, bound, f"sampled {in_dim}x{out_dim}x{n_tok}")
+    return got
+
+
+@pytest.mark.parametrize("in_dim,out_dim", [(32768, 1024), (4096, 2048), (2048, 4096)])
+def test_config3_prefill(q8, o, in_dim, out_dim):
+    W = inputs.weights(out_dim, in_dim, seed=1)
+    x = inputs.normal((512, in_dim), seed=1)
+    _sampled_check(q8, o, W, x, in_dim, out_dim, 512, full_tokens=(0, 511))
+
+
+@pytest.mark.parametrize("in_dim,out_dim", [(4096, 1024), (1024, 32768), (32768, 1024), (1024, 4096)])
+def test_config5_dense_layer_slice(q8, o, in_dim, out_dim):
+    W = inputs.weights(out_dim, in_dim, seed=2)
+    x = inputs.normal((4096, in_dim), seed=2)
+    _sampled_check(q8, o, W, x, in_dim, out_dim, 4096, full_tokens=(4095,))
+
+
+# ------------------------------------------------------------------ routed experts
+def gpu_moe(q8, Wd, n_exp, stride, ids, x, x_per_pair, out_dim):
+    n_tok, k = ids.shape
+    buf = poisoned(n_tok * k * out_dim)
+    rc = q8.q8_moe_matmul(buf, Wd, n_exp, stride, dev(ids), k, x.shape[1], out_dim, dev(x), int(x_per_pair), n_tok)
+    assert rc == 0, q8.q8_strerror(rc)
+    return buf, n_tok * k * out_dim
+
+
+def test_moe_small_every_output(q8, o):
+    n_exp, in_dim, out_dim, n_tok, k = 12, 512, 72, 37, 3
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=21)
+    stride = out_dim * in_dim // QK * QB
+    ids = inputs.route_zipf(n_tok, k, n_exp, seed=22)
+    for per_pair in (0, 1):
+        x = inputs.normal((n_tok * k if per_pair else n_tok, in_dim), seed=23 + per_pair)
+        ref, bound, flag = o.moe(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), per_pair, n_tok)
+        buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, per_pair, out_dim)
+        assert q8.q8_last_error() == 0 and flag == 0
+        assert_close(fetch(buf, n, ref.shape), ref, bound, f"moe per_pair={per_pair}")
+
+
+def test_moe_ragged_in_dim_slow_path(q8, o):
+    n_exp, in_dim, out_dim, n_tok, k = 5, 96, 20, 9, 2
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=31)
+    stride = (out_dim * in_dim // QK * QB + 15) // 16 * 16
+    Wpad = np.zeros(n_exp * stride, np.uint8)
+    for e in range(n_exp):
+        Wpad[e * stride:e * stride + out_dim * 3 * QB] = W[e * out_dim:(e + 1) * out_dim].reshape(-1)
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=32)
+    x = inputs.normal((n_tok, in_dim), seed=33)
+    ref, bound, _ = o.moe(Wpad, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok)
+    buf, n = gpu_moe(q8, dev(Wpad), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == 0
+    assert_close(fetch(buf, n, ref.shape), ref, bound, "moe ragged")
+
+
+def test_moe_bad_ids_zero_rows_and_flag(q8, o):
+    n_exp, in_dim, out_dim, n_tok, k = 6, 256, 40, 10, 2
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=41)
+    stride = out_dim * in_dim // QK * QB
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=42)
+    ids[3, 1] = -1
+    ids[7, 0] = 6
+    x = inputs.normal((n_tok, in_dim), seed=43)
+    ref, bound, flag = o.moe(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok)
+    assert flag == 1
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == q8.Q8_ERANGE
+    assert q8.q8_last_error() == 0   # cleared
+    got = fetch(buf, n, ref.shape)
+    assert np.all(got[3 * k + 1] == 0) and np.all(got[7 * k + 0] == 0)
+    assert_close(got, ref, bound, "moe bad ids")
+
+
+def test_moe_k1_identity_equals_dense(q8):
+    n_exp, in_dim, out_dim = 4, 1024, 96
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=51)
+    stride = out_dim * in_dim // QK * QB
+    x = inputs.normal((n_exp, in_dim), seed=52)
+    ids = np.arange(n_exp, dtype=np.int32).reshape(n_exp, 1)
+    Wd = dev(W)
+    moe = q8.moe_matmul(Wd, n_exp, stride, dev(ids), dev(x), False, out_dim)
+    for e in range(n_exp):
+        dense = q8.matmul(Wd[e * out_dim:(e + 1) * out_dim], dev(x[e:e + 1]), out_dim)
+        assert torch.equal(moe[e:e + 1], dense)
+
+
+def _moe_weights(n_exp, out_dim, in_dim, seed):
+    return inputs.weights(n_exp * out_dim, in_dim, seed=seed)
+
+
+def test_config4_routed_moe_gate_and_down(q8, o):
+    n_exp, n_tok, k = 256, 64, 6
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=0)
+    # gate/up: experts [2048 x 4096], x per token
+    W = _moe_weights(n_exp, 2048, 4096, seed=0)
+    stride = 2048 * 128 * QB
+    x = inputs.normal((n_tok, 4096), seed=0)
+    ref, bound, flag = o.moe(W, n_exp, stride, ids, 4096, 2048, o.quantize(x), 0, n_tok)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, 2048)
+    assert q8.q8_last_error() == 0 and flag == 0
+    assert_close(fetch(buf, n, ref.shape), ref, bound, "config 4 gate")
+    del W, buf
+    # down: experts [4096 x 2048], x per pair
+    W = _moe_weights(n_exp, 4096, 2048, seed=1)
+    stride = 4096 * 64 * QB
+    x = inputs.normal((n_tok * k, 2048), seed=1)
+    ref, bound, flag = o.moe(W, n_exp, stride, ids, 2048, 4096, o.quantize(x), 1, n_tok)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 1, 4096)
+    assert q8.q8_last_error() == 0
+    assert_close(fetch(buf, n, ref.shape), ref, bound, "config 4 down")
+
+
+def test_config5_zipf_moe_sampled(q8, o):
+    n_exp, n_tok, k, in_dim, out_dim = 256, 4096, 6, 4096, 2048
+    ids = inputs.route_zipf(n_tok, k, n_exp, s=1.1, seed=0)
+    W = _moe_weights(n_exp, out_dim, in_dim, seed=2)
+    stride = out_dim * (in_dim // QK) * QB
+    x = inputs.normal((n_tok, in_dim), seed=3)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == 0
+    got = fetch(buf, n, (n_tok * k, out_dim))
+    g = np.random.default_rng(5)
+    counts = np.bincount(ids.reshape(-1), minlength=n_exp)
+    hot = int(np.argmax(counts))
+    cold_pairs = np.flatnonzero(np.isin(ids.reshape(-1), np.flatnonzero(counts == counts[counts > 0].min())))[:2]
+    hot_pair = int(np.flatnonzero(ids.reshape(-1) == hot)[-1])
+    pair = np.concatenate([g.integers(0, n_tok * k, 3000), np.full(out_dim, hot_pair),
+                           np.repeat(cold_pairs, out_dim)])
+    row = np.concatenate([g.integers(0, out_dim, 3000), np.arange(out_dim), np.tile(np.arange(out_dim), len(cold_pairs))])
+    ref, bound, flag = o.moe_sample(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok, pair, row)
+    assert flag == 0
+    assert_close(got[pair, row], ref, bound, "config 5 moe")
+    assert not np.any(np.isnan(got)), "some routed output row was never written"
+
+
+# ------------------------------------------------------------------ repack
+def test_repack_layout_and_parity(q8, o):
+    in_dim, out_dim, n_tok = 1024, 200, 13
+    Wh = inputs.weights(out_dim, in_dim, seed=61)
+    Wp = q8.repack(dev(Wh), in_dim, out_dim).cpu().numpy()
+    blk = Wh.reshape(out_dim, -1, QB)
+    assert np.array_equal(Wp[:out_dim * in_dim].reshape(out_dim, -1, QK), blk[..., 2:])
+    assert np.array_equal(Wp[out_dim * in_dim:].reshape(out_dim, -1, 2), blk[..., :2])
+    xh = inputs.normal((n_tok, in_dim), seed=62)
+    ref, bound = o.matmul(Wh, xh, out_dim)
+    got = q8.matmul_packed(dev(Wp), dev(xh), out_dim).cpu().numpy()
+    assert_close(got, ref, bound, "packed")
+
+
+# ------------------------------------------------------------------ error paths and edges
+def test_empty_and_tiny(q8, o):
+    W = dev(inputs.weights(3, 32, seed=71))
+    x = dev(inputs.normal((1, 32), seed=72))
+    out = torch.empty((0, 3), device=DEV)
+    assert q8.q8_matmul(out, W, 32, 3, x, 0) == 0
+    ref, bound = o.matmul(inputs.weights(3, 32, seed=71), inputs.normal((1, 32), seed=72), 3)
+    assert_close(q8.matmul(W, x, 3).cpu().numpy(), ref, bound, "tiny")
+
+
+def test_scratch_alloc_failure_reports_enomem(q8):
+    W = dev(inputs.weights(64, 256, seed=81))
+    x = dev(inputs.normal((8, 256), seed=82))
+    out = torch.empty((8, 64), device=DEV)
+    q8.q8_release()
+    assert q8.q8_scratch_bytes() == 0
+    q8.q8_debug_fail_next_alloc(1)
+    assert q8.q8_matmul(out, W, 256, 64, x, 8) == q8.Q8_ENOMEM
+    assert q8.q8_matmul(out, W, 256, 64, x, 8) == 0
+    assert q8.q8_scratch_bytes() > 0
+    torch.cuda.synchronize()
