@@ -52,11 +52,19 @@ template <class F> cudaError_t timed_launch(cudaStream_t st, F launch) {
     cudaGetDevice(&dev);
     if (!g_prof.n || dev != g_prof.device) return launch();
     const uint32_t i = (uint32_t)(g_prof.used % g_prof.n);
-    cudaError_t e = cudaEventRecord(g_prof.ev[2 * i], st);
+    // Under stream capture a plain record only orders the capture; the
+    // external flag makes it an event-record node of the graph.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        cs = cudaStreamCaptureStatusNone;
+    }
+    const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    cudaError_t e = cudaEventRecordWithFlags(g_prof.ev[2 * i], st, flags);
     if (e != cudaSuccess) return e;
     e = launch();
     if (e != cudaSuccess) return e;
-    e = cudaEventRecord(g_prof.ev[2 * i + 1], st);
+    e = cudaEventRecordWithFlags(g_prof.ev[2 * i + 1], st, flags);
     g_prof.recorded[i] = 1;
     ++g_prof.used;
     return e;
@@ -150,15 +158,54 @@ int check_dims(uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
     return Q8_OK;
 }
 
+// Rows per CTA item for the GEMV: enough items for every SM, at most 512 rows.
+uint32_t gemv_rows_per_item(uint64_t out_dim, int num_sms) {
+    uint64_t r = (out_dim + num_sms - 1) / num_sms;
+    r = (r + 15) & ~(uint64_t)15;
+    if (r < 16) r = 16;
+    if (r > q8::GEMV_MAX_ROWS_PER_ITEM) r = q8::GEMV_MAX_ROWS_PER_ITEM;
+    return (uint32_t)r;
+}
+
+// Warps per 16-row sub-item: split K across warps when the item has few sub-items.
+uint32_t gemv_wpi(uint32_t rows_per_item) {
+    const uint32_t nsub = rows_per_item / 16;
+    uint32_t wpi = 1;
+    while (wpi < 16 && nsub * wpi * 2 <= 16) wpi *= 2;   // 16 warps per CTA
+    return wpi;
+}
+
 // out = W x from activation planes already in scratch (n_pad rows).
 int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const int8_t *qx,
               const float *dx, uint64_t n_tok, cudaStream_t st) {
+    const uint32_t nb = (uint32_t)(in_dim / q8::QK);
+    if (nb % 8 == 0 && n_tok <= 16) {
+        q8::GemvParams g{};
+        g.W = static_cast<const uint8_t *>(W);
+        g.expert_stride = 0;
+        g.in_dim = in_dim;
+        g.out_dim = (uint32_t)out_dim;
+        g.nb = nb;
+        g.qx = qx;
+        g.dx = dx;
+        g.out = out;
+        g.err = s->err;
+        g.n_tok = (uint32_t)n_tok;
+        g.rows_per_item = gemv_rows_per_item(out_dim, s->num_sms);
+        g.wpi = gemv_wpi(g.rows_per_item);
+        g.plan = nullptr;
+        g.row_to_out = nullptr;
+        g.n_expert = 1;
+        const uint64_t items = (out_dim + g.rows_per_item - 1) / g.rows_per_item;
+        const int grid = (int)(items < (uint64_t)s->num_sms ? items : (uint64_t)s->num_sms);
+        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, n_tok > 8, grid, st); }));
+    }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
     p.expert_stride = 0;
     p.in_dim = in_dim;
     p.out_dim = (uint32_t)out_dim;
-    p.nb = (uint32_t)(in_dim / q8::QK);
+    p.nb = nb;
     p.qx = qx;
     p.dx = dx;
     p.out = out;
@@ -261,23 +308,27 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     if ((rc = get_device(&s))) return rc;
     const uint64_t n_pairs = n_tok * k;
     const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
-    const size_t need = align256(n_expert * 4) * 2 + align256(sizeof(q8::PlanHeader) + n_expert * sizeof(q8::Segment)) +
-                        align256(max_rows * 4) * 2 + planes_bytes(max_rows, in_dim);
+    const size_t plan_bytes = q8::route_plan_bytes(n_expert);
+    const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * plan_bytes + align256(max_rows * 4) * 2 +
+                        planes_bytes(max_rows, in_dim);
     if ((rc = reserve_scratch(s, need))) return rc;
     Carver cv(s->scratch);
     int32_t *counts = cv.take<int32_t>(n_expert * 4);
     int32_t *row0_of = cv.take<int32_t>(n_expert * 4);
-    q8::PlanHeader *plan = cv.take<q8::PlanHeader>(sizeof(q8::PlanHeader) + n_expert * sizeof(q8::Segment));
+    uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * plan_bytes);
     int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
     int32_t *src_row = cv.take<int32_t>(max_rows * 4);
     int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
     float *dx = cv.take<float>(max_rows * nb * sizeof(float));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, counts, row0_of,
-                                     plan, row_to_out, src_row, max_rows, out, s->err, s->num_sms, st);
+    uint32_t rows_gemv = (uint32_t)((out_dim + 15) & ~(uint64_t)15);
+    if (rows_gemv > 128) rows_gemv = 128;
+    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_gemv, counts,
+                                     row0_of, plans, row_to_out, src_row, max_rows, out, s->err, s->num_sms, st);
     if (e != cudaSuccess) return Q8_ECUDA;
     e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
     if (e != cudaSuccess) return Q8_ECUDA;
+    auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes); };
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W_experts);
     p.expert_stride = expert_stride_bytes;
@@ -289,11 +340,42 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     p.out = out;
     p.err = s->err;
     p.n_tok = 0;
-    p.plan = plan;
     p.row_to_out = row_to_out;
-    if (nb % 8 == 0) return status_of(timed_launch(st, [&] { return q8::launch_mma(p, s->num_sms, st); }));
-    const int hint = (int)(max_rows * out_dim > (1u << 30) ? (1u << 30) : max_rows * out_dim);
-    return status_of(timed_launch(st, [&] { return q8::launch_generic(p, hint, s->num_sms, st); }));
+    if (nb % 8 != 0) {
+        const int hint = (int)(max_rows * out_dim > (1u << 30) ? (1u << 30) : max_rows * out_dim);
+        return status_of(timed_launch(st, [&] {
+            for (int cls = 0; cls < q8::ROUTE_CLASSES; ++cls) {
+                p.plan = plan_of(cls);
+                cudaError_t e2 = q8::launch_generic(p, hint, s->num_sms, st);
+                if (e2 != cudaSuccess) return e2;
+            }
+            return cudaSuccess;
+        }));
+    }
+    q8::GemvParams g{};
+    g.W = p.W;
+    g.expert_stride = expert_stride_bytes;
+    g.in_dim = in_dim;
+    g.out_dim = (uint32_t)out_dim;
+    g.nb = (uint32_t)nb;
+    g.qx = qx;
+    g.dx = dx;
+    g.out = out;
+    g.err = s->err;
+    g.n_tok = 0;
+    g.rows_per_item = rows_gemv;
+    g.wpi = 1;
+    g.row_to_out = row_to_out;
+    g.n_expert = n_expert;
+    return status_of(timed_launch(st, [&] {
+        g.plan = plan_of(0);
+        cudaError_t e2 = q8::launch_gemv(g, false, s->num_sms, st);
+        if (e2 != cudaSuccess) return e2;
+        g.plan = plan_of(1);
+        if ((e2 = q8::launch_gemv(g, true, s->num_sms, st)) != cudaSuccess) return e2;
+        p.plan = plan_of(2);
+        return q8::launch_mma(p, s->num_sms, st);
+    }));
 }
 
 uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows) {

@@ -54,15 +54,42 @@ cudaError_t launch_mma(const MmaParams &p, int grid, cudaStream_t st);
 // Any in_dim % 32 == 0 and 2-byte aligned W: one thread per output (slow path).
 cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, cudaStream_t st);
 
-// Routing (q8_moe.cu): buckets pairs by expert and writes the plan.
-//   plan      : PlanHeader + Segment[n_expert]
+// Routing (q8_moe.cu): buckets pairs by expert and writes three plans, one per
+// size class of expert group: class 0 = groups of <= 8 rows (int8 GEMV), class 1 =
+// 9..16 rows (fp16 GEMV), class 2 = more than 16 rows (GEMM).  Each plan is a
+// PlanHeader followed by Segment[n_expert]; item numbering follows the kernel that
+// consumes the class (rows_gemv rows x 8 or 16 tokens for the GEMVs,
+// 16 rows x 64 tokens for the GEMM).
 //   row_to_out, src_row: int32[max_rows], max_rows = route_max_rows(n_pairs, n_expert)
 //   counts, row0_of: int32[n_expert] scratch
+constexpr int ROUTE_CLASSES = 3;
 uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
+size_t route_plan_bytes(uint32_t n_expert);
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
-                         uint32_t out_dim, int32_t *counts, int32_t *row0_of, PlanHeader *plan,
+                         uint32_t out_dim, uint32_t rows_gemv, int32_t *counts, int32_t *row0_of, uint8_t *plans,
                          int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
                          int num_sms, cudaStream_t st);
+
+// Weight-streaming GEMV for token groups of <= 8 (int8 MMA) or <= 16 (fp16 MMA) (q8_gemv.cu).
+struct GemvParams {
+    const uint8_t *W;
+    uint64_t expert_stride;
+    uint64_t in_dim;
+    uint32_t out_dim;
+    uint32_t nb;
+    const int8_t *qx;          // activation quant plane [rows][in_dim] (groups padded to 16 rows)
+    const float *dx;           // activation scale plane [rows][nb]
+    float *out;
+    int *err;
+    uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
+    uint32_t rows_per_item;    // multiple of 16, <= 512
+    uint32_t wpi;              // warps per 16-row sub-item (1, 2, 4, 8)
+    const PlanHeader *plan;    // grouped: class plan; nullptr: dense
+    const int32_t *row_to_out;
+    uint32_t n_expert;         // grouped: number of expert matrices
+};
+constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
+cudaError_t launch_gemv(const GemvParams &p, bool f16, int grid, cudaStream_t st);
 
 // Repack (q8_repack.cu)
 cudaError_t launch_repack(uint8_t *Wp, const uint8_t *W, uint64_t in_dim, uint64_t rows, int num_sms,

@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(256) k_generic(const MmaParams p) {
                 if ((uint64_t)segs[mid].row0 <= r) lo = mid;
                 else hi = mid - 1;
             }
+            if (p.plan->n_segments == 0 || r < (uint64_t)segs[lo].row0 ||
+                r >= (uint64_t)segs[lo].row0 + (uint64_t)segs[lo].count)
+                continue;   // row of another plan's segment
             expert = segs[lo].expert;
         }
         const uint8_t *w = p.W + (uint64_t)expert * p.expert_stride + o * (uint64_t)nb * QB;

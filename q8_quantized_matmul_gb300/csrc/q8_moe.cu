@@ -67,13 +67,18 @@ __global__ void __launch_bounds__(256) k_route_bad(const int32_t *__restrict__ i
     }
 }
 
+size_t route_plan_bytes(uint32_t n_expert) {
+    return ((sizeof(PlanHeader) + (size_t)n_expert * sizeof(Segment)) + 255) & ~(size_t)255;
+}
+
+__device__ __forceinline__ int route_class(int count) { return count <= 8 ? 0 : (count <= 16 ? 1 : 2); }
+
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
-                                                               uint32_t out_dim, PlanHeader *plan,
-                                                               int32_t *__restrict__ row0_of) {
+                                                               uint32_t out_dim, uint32_t rows_gemv, uint8_t *plans,
+                                                               size_t plan_stride, int32_t *__restrict__ row0_of) {
     extern __shared__ int32_t sh_plan[];   // order[n_expert] (sorted position -> expert)
     int32_t *order = sh_plan;
     __shared__ int n_active_sh;
-    const int n_rb = (int)((out_dim + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
     if (threadIdx.x == 0) n_active_sh = 0;
     __syncthreads();
     // Rank of each touched expert: larger count first, then smaller id.
@@ -92,24 +97,36 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        Segment *segs = reinterpret_cast<Segment *>(plan + 1);
+        const int n_rb_gemv = (int)((out_dim + rows_gemv - 1) / rows_gemv);
+        const int n_rb_mma = (int)((out_dim + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
+        PlanHeader *hdr[ROUTE_CLASSES];
+        Segment *segs[ROUTE_CLASSES];
+        int nseg[ROUTE_CLASSES] = {0, 0, 0}, nitem[ROUTE_CLASSES] = {0, 0, 0};
+        for (int k = 0; k < ROUTE_CLASSES; ++k) {
+            hdr[k] = reinterpret_cast<PlanHeader *>(plans + k * plan_stride);
+            segs[k] = reinterpret_cast<Segment *>(hdr[k] + 1);
+        }
         const int n_active = n_active_sh;
-        int row = 0, item = 0;
+        int row = 0;
         for (int s = 0; s < n_active; ++s) {
             const int e = order[s];
             const int ce = counts[e];
-            segs[s].expert = e;
-            segs[s].row0 = row;
-            segs[s].count = ce;
-            segs[s].item_start = item;
+            const int k = route_class(ce);
+            Segment &sg = segs[k][nseg[k]++];
+            sg.expert = e;
+            sg.row0 = row;
+            sg.count = ce;
+            sg.item_start = nitem[k];
             row0_of[e] = row;
             row += (ce + 15) & ~15;
-            item += n_rb * ((ce + TOK_PER_ITEM - 1) / TOK_PER_ITEM);
+            nitem[k] += k == 2 ? n_rb_mma * ((ce + TOK_PER_ITEM - 1) / TOK_PER_ITEM) : n_rb_gemv;
         }
-        plan->n_segments = n_active;
-        plan->n_items = item;
-        plan->n_rows = row;
-        plan->pad = 0;
+        for (int k = 0; k < ROUTE_CLASSES; ++k) {
+            hdr[k]->n_segments = nseg[k];
+            hdr[k]->n_items = nitem[k];
+            hdr[k]->n_rows = row;
+            hdr[k]->pad = 0;
+        }
     }
 }
 
@@ -146,7 +163,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__r
 }
 
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
-                         uint32_t out_dim, int32_t *counts, int32_t *row0_of, PlanHeader *plan,
+                         uint32_t out_dim, uint32_t rows_gemv, int32_t *counts, int32_t *row0_of, uint8_t *plans,
                          int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
                          int num_sms, cudaStream_t st) {
     const uint64_t n_pairs = n_tok * k;
@@ -167,7 +184,8 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
             cudaSuccess)
             return e;
     }
-    k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, plan, row0_of);
+    k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, rows_gemv, plans,
+                                                      route_plan_bytes(n_expert), row0_of);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     k_route_fill<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, k, x_per_pair, row0_of, row_to_out, src_row);
     return cudaGetLastError();

@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qp
                                                          const float *__restrict__ x, uint64_t in_dim,
                                                          uint64_t n_rows, const int32_t *__restrict__ src_row,
                                                          uint64_t n_src) {
+    // The matmul that follows only prefetches weights before it waits for this
+    // grid to finish, so it may be scheduled now.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_rows * nb;
     const uint64_t lane_q = threadIdx.x & 3u;

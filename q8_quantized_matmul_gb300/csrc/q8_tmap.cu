@@ -1,0 +1,49 @@
+// q8_tmap.cu -- host helper: tensor maps (TMA descriptors) over raw Q8_0 rows.
+//
+// The driver's cuTensorMapEncodeTiled is reached through the runtime's
+// driver-entry-point query, so the library does not link libcuda directly.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "q8_kernels.h"
+
+namespace q8 {
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool load_encoder() {
+    if (g_encode) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return true;
+}
+}  // namespace
+
+// Rows of raw Q8_0 blocks viewed as 32-bit words: dims {row_bytes/4, rows, n_mat},
+// strides {row_bytes, mat_stride}; box {box_words, box_rows, 1}; no swizzle;
+// out-of-bounds words read as zero.
+bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
+                      uint64_t mat_stride, uint32_t box_words, uint32_t box_rows) {
+    if (!load_encoder()) return false;
+    if (row_bytes % 16 || mat_stride % 16 || (reinterpret_cast<uintptr_t>(W) & 15u)) return false;
+    cuuint64_t dims[3] = {row_bytes / 4, rows, n_mat};
+    cuuint64_t strides[2] = {row_bytes, n_mat > 1 ? mat_stride : rows * row_bytes};
+    cuuint32_t box[3] = {box_words, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(W), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace q8

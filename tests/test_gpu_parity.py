@@ -264,17 +264,33 @@ def test_moe_bad_ids_zero_rows_and_flag(q8, o):
     assert_close(got, ref, bound, "moe bad ids")
 
 
-def test_moe_k1_identity_equals_dense(q8):
+def test_moe_k1_identity_equals_dense(q8, o):
+    """k = 1, token e -> expert e: every routed row equals the dense product of that expert,
+    within the tolerance (the two calls may sum blocks in different fp32 orders)."""
     n_exp, in_dim, out_dim = 4, 1024, 96
     W = inputs.weights(n_exp * out_dim, in_dim, seed=51)
     stride = out_dim * in_dim // QK * QB
     x = inputs.normal((n_exp, in_dim), seed=52)
     ids = np.arange(n_exp, dtype=np.int32).reshape(n_exp, 1)
     Wd = dev(W)
-    moe = q8.moe_matmul(Wd, n_exp, stride, dev(ids), dev(x), False, out_dim)
+    moe = q8.moe_matmul(Wd, n_exp, stride, dev(ids), dev(x), False, out_dim).cpu().numpy()
     for e in range(n_exp):
-        dense = q8.matmul(Wd[e * out_dim:(e + 1) * out_dim], dev(x[e:e + 1]), out_dim)
-        assert torch.equal(moe[e:e + 1], dense)
+        dense = q8.matmul(Wd[e * out_dim:(e + 1) * out_dim], dev(x[e:e + 1]), out_dim).cpu().numpy()
+        ref, bound = o.matmul(W[e * out_dim:(e + 1) * out_dim], x[e:e + 1], out_dim)
+        assert_close(moe[e:e + 1], ref, bound, "moe k=1")
+        assert_close(dense, ref, bound, "dense")
+        assert np.all(np.abs(moe[e:e + 1] - dense) <= 2 * oracle.tolerance(bound))
+
+
+def test_moe_deterministic(q8):
+    n_exp, in_dim, out_dim, n_tok, k = 16, 1024, 256, 40, 4
+    W = dev(inputs.weights(n_exp * out_dim, in_dim, seed=53))
+    stride = out_dim * in_dim // QK * QB
+    ids = dev(inputs.route_zipf(n_tok, k, n_exp, seed=54))
+    x = dev(inputs.normal((n_tok, in_dim), seed=55))
+    a = q8.moe_matmul(W, n_exp, stride, ids, x, False, out_dim)
+    for _ in range(3):
+        assert torch.equal(a, q8.moe_matmul(W, n_exp, stride, ids, x, False, out_dim))
 
 
 def _moe_weights(n_exp, out_dim, in_dim, seed):
