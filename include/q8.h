@@ -58,7 +58,8 @@ enum q8_status {
     Q8_ERANGE = -3,      /* (device) an expert id was outside [0, n_expert) */
     Q8_ENOMEM = -4,      /* scratch allocation failed */
     Q8_ECUDA = -5,       /* a CUDA runtime call failed (no device, launch error, ...) */
-    Q8_ETIMEOUT = -6     /* (device) a kernel's bounded wait expired; outputs undefined */
+    Q8_ETIMEOUT = -6,    /* (device) a kernel's bounded wait expired; outputs undefined */
+    Q8_ESCRATCH = -7     /* the call needs more than the fixed scratch of q8_matmul_noalloc */
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -139,6 +140,36 @@ uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows);
 int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, void *stream);
 int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_dim,
                      const float *x, uint64_t n_tok, void *stream);
+
+/*
+ * q8_matmul without any device allocation.  This entry point has no
+ * counterpart on the pages; it exists for callers that must not allocate
+ * device memory from inside this library: for example an application whose
+ * own pool allocator has reserved the device's memory up front (a cudaMalloc
+ * here would fail or fragment its pool), or a latency-critical decode loop
+ * that cannot afford the device-wide synchronisation and milliseconds that a
+ * first-use cudaMalloc/cudaFree can cost.
+ *
+ * Same arguments, layouts, results and error codes as q8_matmul (the same
+ * kernels run), but the quantised activations live in one fixed array of
+ * Q8_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
+ * library holds that array until the process exits.  The call needs
+ * align256(n_pad*in_dim) + align256(n_pad*(in_dim/32)*4) bytes of it, with
+ * n_pad = n_tok rounded up to a multiple of 16 (for example n_tok <= 16 with
+ * in_dim <= 200000, or n_tok = 512 with in_dim <= 7168); larger calls return
+ * Q8_ESCRATCH and enqueue nothing.  It never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *
+ * The first call on a device looks up the device address of that array
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture.  All calls share the one array and every call
+ * rewrites the part it uses before reading it, so nothing needs clearing; but
+ * calls whose work overlaps on the GPU (different streams without ordering)
+ * race on it and must not be issued.
+ */
+#define Q8_NOALLOC_SCRATCH_BYTES (4u << 20)
+int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
+                      const float *x, uint64_t n_tok, void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device error word of

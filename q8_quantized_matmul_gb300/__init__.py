@@ -19,12 +19,14 @@ LIB_PATH = os.path.join(_PKG, "libq8.so")
 
 QK = 32
 QB = 34
-Q8_OK, Q8_EINVAL, Q8_EALIGN, Q8_ERANGE, Q8_ENOMEM, Q8_ECUDA, Q8_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+Q8_OK, Q8_EINVAL, Q8_EALIGN, Q8_ERANGE, Q8_ENOMEM, Q8_ECUDA, Q8_ETIMEOUT, Q8_ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
+Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 # Every symbol include/q8.h declares.
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
-           "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read")
+           "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
+           "q8_matmul_noalloc")
 
 
 class Q8Error(RuntimeError):
@@ -56,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "q8_profile_arm": ([u32], i32),
         "q8_profile_used": ([], u64),
         "q8_profile_read": ([u32, ctypes.POINTER(ctypes.c_float)], i32),
+        "q8_matmul_noalloc": ([vp, vp, u64, u64, vp, u64, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -106,6 +109,11 @@ def q8_quantize_act(xq, x, in_dim: int, n_tok: int, stream=None) -> int:
 
 def q8_matmul(out, W, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
     return _get().q8_matmul(_p(out), _p(W), in_dim, out_dim, _p(x), n_tok, _s(stream))
+
+
+def q8_matmul_noalloc(out, W, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
+    """q8_matmul with its scratch in the library's fixed device array (no allocation)."""
+    return _get().q8_matmul_noalloc(_p(out), _p(W), in_dim, out_dim, _p(x), n_tok, _s(stream))
 
 
 def q8_matmul_q(out, W, in_dim: int, out_dim: int, xq, n_tok: int, stream=None) -> int:

@@ -224,6 +224,15 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
 
 }  // namespace
 
+namespace q8 {
+// Device address of the current device's error word (nullptr if the device is unusable).
+int *device_error_word() {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    return get_device(&s) ? nullptr : s->err;
+}
+}  // namespace q8
+
 extern "C" {
 
 int q8_version(void) { return 10000; }
@@ -237,6 +246,7 @@ const char *q8_strerror(int status) {
         case Q8_ENOMEM: return "scratch allocation failed";
         case Q8_ECUDA: return "CUDA runtime error";
         case Q8_ETIMEOUT: return "bounded wait expired inside a kernel";
+        case Q8_ESCRATCH: return "call exceeds the fixed scratch of q8_matmul_noalloc";
         default: return "unknown status";
     }
 }

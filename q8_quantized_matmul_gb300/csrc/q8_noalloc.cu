@@ -1,0 +1,141 @@
+// q8_noalloc.cu -- q8_matmul_noalloc: the matmul with its scratch in a fixed
+// device array, for callers that must not allocate device memory through this
+// library (an application whose own pool allocator owns the device's memory,
+// or a decode loop that cannot take the synchronisation and latency of a
+// first-use cudaMalloc).  The pages have no counterpart; the kernels are the
+// ones q8_matmul runs, only the place of the quantised activations differs.
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/q8.h"
+#include "q8_common.cuh"
+#include "q8_kernels.h"
+
+namespace q8 {
+int *device_error_word();   // q8_api.cu
+}
+
+namespace {
+
+// The scratch: quantised activation planes of the current call (int8 plane,
+// then fp32 scale plane).  Every GPU that loads the library holds it until the
+// process exits.  The quantiser writes every byte a call reads (padding rows
+// included) before the matmul reads it, so the array never needs clearing.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[Q8_NOALLOC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+
+struct NoallocDevice {
+    bool ready = false;
+    uint8_t *scratch = nullptr;   // device address of g_noalloc_scratch on that device
+    int num_sms = 0;
+};
+
+std::mutex g_na_mutex;
+NoallocDevice g_na[MAX_DEVICES];
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Once per device, with the device current: the array's device address.
+int noalloc_device(NoallocDevice **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return Q8_ECUDA;
+    }
+    NoallocDevice &d = g_na[dev];
+    if (!d.ready) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return Q8_ECUDA;
+        }
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return Q8_ECUDA;
+        }
+        d.scratch = static_cast<uint8_t *>(ptr);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    *out = &d;
+    return Q8_OK;
+}
+
+}  // namespace
+
+extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
+                                 uint64_t n_tok, void *stream) {
+    // Argument rules of q8_matmul.
+    if (in_dim == 0 || in_dim % q8::QK) return Q8_EINVAL;
+    if (in_dim > ((uint64_t)1 << 31) || out_dim > ((uint64_t)1 << 31) - 1 || n_tok > ((uint64_t)1 << 31) - 1)
+        return Q8_EINVAL;
+    const uint64_t nb = in_dim / q8::QK;
+    if (out_dim && nb > (((uint64_t)1 << 62) / q8::QB) / out_dim) return Q8_EINVAL;
+    if (n_tok && in_dim > ((uint64_t)1 << 40) / n_tok) return Q8_EINVAL;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W || !x) return Q8_EINVAL;
+    const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(out) || !a16(W) || !a16(x)) return Q8_EALIGN;
+    // The planes must fit the fixed array.
+    const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
+    const size_t q_bytes = align256(n_pad * in_dim);
+    const size_t need = q_bytes + align256(n_pad * nb * sizeof(float));
+    if (need > Q8_NOALLOC_SCRATCH_BYTES) return Q8_ESCRATCH;
+
+    std::lock_guard<std::mutex> lk(g_na_mutex);
+    NoallocDevice *d;
+    int rc = noalloc_device(&d);
+    if (rc) return rc;
+    int *err = q8::device_error_word();
+    if (!err) return Q8_ECUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int8_t *qx = reinterpret_cast<int8_t *>(d->scratch);
+    float *dx = reinterpret_cast<float *>(d->scratch + q_bytes);
+    if (q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, d->num_sms, st) != cudaSuccess)
+        return Q8_ECUDA;
+
+    // The same kernel choice as q8_matmul.
+    if (nb % 8 == 0 && n_tok <= 16) {
+        q8::GemvParams g{};
+        g.W = static_cast<const uint8_t *>(W);
+        g.in_dim = in_dim;
+        g.out_dim = (uint32_t)out_dim;
+        g.nb = (uint32_t)nb;
+        g.qx = qx;
+        g.dx = dx;
+        g.out = out;
+        g.err = err;
+        g.n_tok = (uint32_t)n_tok;
+        uint64_t r = (out_dim + d->num_sms - 1) / d->num_sms;
+        r = (r + 15) & ~(uint64_t)15;
+        if (r < 16) r = 16;
+        if (r > q8::GEMV_MAX_ROWS_PER_ITEM) r = q8::GEMV_MAX_ROWS_PER_ITEM;
+        g.rows_per_item = (uint32_t)r;
+        uint32_t wpi = 1;
+        while (wpi < 16 && (g.rows_per_item / 16) * wpi * 2 <= 16) wpi *= 2;
+        g.wpi = wpi;
+        g.n_expert = 1;
+        const uint64_t items = (out_dim + r - 1) / r;
+        const int grid = (int)(items < (uint64_t)d->num_sms ? items : (uint64_t)d->num_sms);
+        return q8::launch_gemv(g, n_tok > 8, grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+    }
+    q8::MmaParams p{};
+    p.W = static_cast<const uint8_t *>(W);
+    p.in_dim = in_dim;
+    p.out_dim = (uint32_t)out_dim;
+    p.nb = (uint32_t)nb;
+    p.qx = qx;
+    p.dx = dx;
+    p.out = out;
+    p.err = err;
+    p.n_tok = (uint32_t)n_tok;
+    if (nb % 8 == 0) {
+        const uint64_t items = ((out_dim + 15) / 16) * ((n_tok + 63) / 64);
+        const int grid = (int)(items < (uint64_t)d->num_sms ? items : (uint64_t)d->num_sms);
+        return q8::launch_mma(p, grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+    }
+    const uint64_t hint = n_tok * out_dim > (1u << 30) ? (1u << 30) : n_tok * out_dim;
+    return q8::launch_generic(p, (int)hint, d->num_sms, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+}
