@@ -179,6 +179,10 @@ int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uint64_t out_d
  */
 int q8_last_error(void *stream);
 
+/* Name of the last CUDA runtime error behind a Q8_ECUDA return ("cudaSuccess"
+ * if none yet); for diagnostics. */
+const char *q8_last_cuda_error(void);
+
 /* Scratch bytes currently held on the current device (0 if none). */
 uint64_t q8_scratch_bytes(void);
 

@@ -26,12 +26,13 @@ Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
-           "q8_matmul_noalloc")
+           "q8_matmul_noalloc", "q8_last_cuda_error")
 
 
 class Q8Error(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {_get().q8_strerror(status).decode()} ({status})")
+        detail = f" [{_get().q8_last_cuda_error().decode()}]" if status == Q8_ECUDA else ""
+        super().__init__(f"{what}: {_get().q8_strerror(status).decode()} ({status}){detail}")
         self.status = status
 
 
@@ -59,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "q8_profile_used": ([], u64),
         "q8_profile_read": ([u32, ctypes.POINTER(ctypes.c_float)], i32),
         "q8_matmul_noalloc": ([vp, vp, u64, u64, vp, u64, vp], i32),
+        "q8_last_cuda_error": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -167,6 +169,10 @@ def q8_profile_read(i: int) -> float:
     ms = ctypes.c_float(0.0)
     _check(_get().q8_profile_read(i, ctypes.byref(ms)), "q8_profile_read")
     return ms.value
+
+
+def q8_last_cuda_error() -> str:
+    return _get().q8_last_cuda_error().decode()
 
 
 def q8_strerror(status: int) -> str:

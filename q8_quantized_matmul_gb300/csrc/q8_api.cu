@@ -70,7 +70,13 @@ template <class F> cudaError_t timed_launch(cudaStream_t st, F launch) {
     return e;
 }
 
-int status_of(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ECUDA; }
+cudaError_t g_last_cuda_error = cudaSuccess;   // for q8_last_cuda_error()
+
+int status_of(cudaError_t e) {
+    if (e == cudaSuccess) return Q8_OK;
+    g_last_cuda_error = e;
+    return Q8_ECUDA;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -222,6 +228,61 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
     return status_of(timed_launch(st, [&] { return q8::launch_generic(p, hint, s->num_sms, st); }));
 }
 
+// Prefill (n_tok > 16, even number of blocks per row): tcgen05 GEMM on fp16
+// operands.  Weights are expanded to an fp16 plane with block-major scales,
+// activations quantised straight into the fp16 operand; K is split when the
+// output tiles do not fill the GPU.
+int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
+           const void *xq, uint64_t n_tok, cudaStream_t st) {
+    const uint64_t nb = in_dim / q8::QK;
+    const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
+    const uint64_t n_ld = (n_tok + 255) & ~(uint64_t)255;
+    const uint64_t tiles = (m_ld / 128) * (n_ld / 256);
+    uint64_t ksplit = 1;
+    if (tiles < (uint64_t)s->num_sms) {
+        ksplit = (uint64_t)s->num_sms / tiles;
+        const uint64_t max_split = nb / 16 > 0 ? nb / 16 : 1;   // keep >= 16 blocks per split
+        if (ksplit > max_split) ksplit = max_split;
+        if (ksplit < 1) ksplit = 1;
+    }
+    uint64_t kb_per = (nb + ksplit - 1) / ksplit;
+    kb_per = (kb_per + 1) & ~(uint64_t)1;
+    ksplit = (nb + kb_per - 1) / kb_per;
+    const size_t need = align256(out_dim * in_dim * 2) + align256(nb * m_ld * 4) + align256(n_ld * in_dim * 2) +
+                        align256(nb * n_ld * 4) + (ksplit > 1 ? align256(ksplit * n_tok * out_dim * 4) : 0);
+    int rc = reserve_scratch(s, need);
+    if (rc) return rc;
+    Carver cv(s->scratch);
+    __half *a16 = cv.take<__half>(out_dim * in_dim * 2);
+    float *dwT = cv.take<float>(nb * m_ld * 4);
+    __half *b16 = cv.take<__half>(n_ld * in_dim * 2);
+    float *dxT = cv.take<float>(nb * n_ld * 4);
+    float *partial = ksplit > 1 ? cv.take<float>(ksplit * n_tok * out_dim * 4) : nullptr;
+    if ((rc = status_of(q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W), (uint32_t)out_dim,
+                                             (uint32_t)nb, (uint32_t)m_ld, s->num_sms, st))))
+        return rc;
+    cudaError_t e = x ? q8::launch_quantize_f16t(b16, dxT, x, in_dim, n_tok, n_ld, s->num_sms, st)
+                      : q8::launch_unpack_f16t(b16, dxT, static_cast<const uint8_t *>(xq), in_dim, n_tok, n_ld,
+                                               s->num_sms, st);
+    if ((rc = status_of(e))) return rc;
+    q8::TcParams p{};
+    p.M = (int)out_dim;
+    p.N = (int)n_tok;
+    p.nb = (int)nb;
+    p.ksplit = (int)ksplit;
+    p.kb_per = (int)kb_per;
+    p.dxT = dxT;
+    p.dwT = dwT;
+    p.n_ld = n_ld;
+    p.m_ld = m_ld;
+    p.out = out;
+    p.partial = partial;
+    p.err = s->err;
+    const uint64_t units = tiles * ksplit;
+    const int grid = (int)(units < (uint64_t)s->num_sms ? units : (uint64_t)s->num_sms);
+    return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, b16, n_ld, grid, st); }));
+}
+
 }  // namespace
 
 namespace q8 {
@@ -274,12 +335,14 @@ static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t ou
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t nb = in_dim / q8::QK;
+    if (n_tok > 16 && nb % 2 == 0) return run_tc(s, out, W, in_dim, out_dim, x, xq, n_tok, st);
     const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
     if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
     Carver cv(s->scratch);
     int8_t *qx = cv.take<int8_t>(n_pad * in_dim);
-    float *dx = cv.take<float>(n_pad * (in_dim / q8::QK) * sizeof(float));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *dx = cv.take<float>(n_pad * nb * sizeof(float));
     cudaError_t e = x ? q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st)
                       : q8::launch_unpack_blocks(qx, dx, static_cast<const uint8_t *>(xq), in_dim, n_pad, n_tok,
                                                  s->num_sms, st);
@@ -516,6 +579,11 @@ int q8_profile_read(uint32_t i, float *ms) {
         return Q8_ECUDA;
     }
     return Q8_OK;
+}
+
+const char *q8_last_cuda_error(void) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    return cudaGetErrorName(g_last_cuda_error);
 }
 
 void q8_debug_fail_next_alloc(int count) {

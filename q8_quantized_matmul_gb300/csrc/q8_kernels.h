@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace q8 {
@@ -90,6 +91,33 @@ struct GemvParams {
 };
 constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
 cudaError_t launch_gemv(const GemvParams &p, bool f16, int grid, cudaStream_t st);
+
+// Prefill GEMM on tcgen05 (q8_tc.cu).  Weights as an fp16 plane [M][K] (from
+// launch_tc_expand) with block-major scales dwT[nb][m_ld]; activations as an
+// fp16 plane [n_ld rows][K] with block-major scales dxT[nb][n_ld]
+// (launch_quantize_f16t / launch_unpack_f16t).  m_ld % 128 == 0, n_ld % 256 == 0,
+// nb even.  With ksplit > 1, partial[ksplit][N][M] holds the K-split sums.
+struct TcParams {
+    int M;                 // weight rows (out_dim)
+    int N;                 // tokens
+    int nb;                // blocks per row
+    int ksplit;            // K splits
+    int kb_per;            // blocks per split (even)
+    const float *dxT;
+    const float *dwT;
+    uint64_t n_ld, m_ld;
+    float *out;            // [N][M]
+    float *partial;        // [ksplit][N][M] or nullptr
+    int *err;
+};
+cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
+                             int num_sms, cudaStream_t st);
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
+                           cudaStream_t st);
+cudaError_t launch_quantize_f16t(__half *q16, float *dxT, const float *x, uint64_t in_dim, uint64_t n_tok,
+                                 uint64_t n_ld, int num_sms, cudaStream_t st);
+cudaError_t launch_unpack_f16t(__half *q16, float *dxT, const uint8_t *xq, uint64_t in_dim, uint64_t n_tok,
+                               uint64_t n_ld, int num_sms, cudaStream_t st);
 
 // Repack (q8_repack.cu)
 cudaError_t launch_repack(uint8_t *Wp, const uint8_t *W, uint64_t in_dim, uint64_t rows, int num_sms,

@@ -151,6 +151,72 @@ __global__ void __launch_bounds__(256) k_unpack_blocks(int8_t *__restrict__ qpla
     }
 }
 
+// Prefill operand: fp16 quant plane q16 [n_ld][in_dim] (exact integers) and
+// block-major scales dxT [nb][n_ld]; rows n_tok..n_ld-1 are zero.  Same
+// arithmetic as the other quantiser kernels.
+__global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
+                                                       const float *__restrict__ x, uint64_t in_dim, uint64_t n_tok,
+                                                       uint64_t n_ld) {
+    const uint64_t nb = in_dim / QK;
+    const uint64_t nblk = n_ld * nb;
+    const uint64_t lane_q = threadIdx.x & 3u;
+    const uint64_t groups_per_cta = blockDim.x / 4;
+    for (uint64_t base = (uint64_t)blockIdx.x * groups_per_cta; base < nblk; base += (uint64_t)gridDim.x * groups_per_cta) {
+        const uint64_t blk = base + threadIdx.x / 4;
+        const bool live = blk < nblk;
+        const uint64_t r = live ? blk / nb : 0;
+        const uint64_t b = live ? blk - r * nb : 0;
+        float x8[8];
+        if (live && r < n_tok) load8(x8, x + r * in_dim + b * QK + lane_q * 8);
+        else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
+        }
+        const QuantBlock qb = quantize8(x8);
+        if (live) {
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                h[i] = (uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i])) |
+                       ((uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i + 1])) << 16);
+            *reinterpret_cast<uint4 *>(q16 + r * in_dim + b * QK + lane_q * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+            if (lane_q == 0) dxT[b * n_ld + r] = qb.d_stored;
+        }
+    }
+}
+
+// Canonical blocks [n_tok][nb] -> the prefill operand (as k_quantize_f16t).
+__global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
+                                                     const uint8_t *__restrict__ xq, uint64_t in_dim, uint64_t n_tok,
+                                                     uint64_t n_ld) {
+    const uint64_t nb = in_dim / QK;
+    const uint64_t nblk = n_ld * nb;
+    for (uint64_t blk = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;
+         blk += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t r = blk / nb, b = blk - r * nb;
+        uint4 *dst = reinterpret_cast<uint4 *>(q16 + r * in_dim + b * QK);
+        if (r < n_tok) {
+            const uint16_t *p16 = reinterpret_cast<const uint16_t *>(xq + blk * QB);
+            dxT[b * n_ld + r] = half_bits_to_float(p16[0]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t two = p16[1 + c * 4 + e];
+                    o[e] = (uint32_t)__half_as_ushort(__int2half_rn((int)(int8_t)(two & 0xff))) |
+                           ((uint32_t)__half_as_ushort(__int2half_rn((int)(int8_t)(two >> 8))) << 16);
+                }
+                dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            dxT[b * n_ld + r] = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 static int grid_for(uint64_t work_items, int per_cta, int num_sms) {
     uint64_t need = (work_items + per_cta - 1) / per_cta;
@@ -170,6 +236,22 @@ cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
     k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_f16t(__half *q16, float *dxT, const float *x, uint64_t in_dim, uint64_t n_tok,
+                                 uint64_t n_ld, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_ld * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    k_quantize_f16t<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(q16, dxT, x, in_dim, n_tok, n_ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_f16t(__half *q16, float *dxT, const uint8_t *xq, uint64_t in_dim, uint64_t n_tok,
+                               uint64_t n_ld, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_ld * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    k_unpack_f16t<<<grid_for(nblk, 256, num_sms), 256, 0, st>>>(q16, dxT, xq, in_dim, n_tok, n_ld);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,413 @@
+// q8_tc.cu -- prefill GEMM on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// out[t][o] = sum_b d_w[o][b] d_x[t][b] isum_b[t][o] (ds4 pages: the Q8_0 matmul
+// of the GPU code walkthrough, trace 3; fixed-point block dot of the
+// model-architecture page, quantisation section 4; the pages route n_tok >= 2
+// prefill to a tensor-core tier, concepts page section 4m).
+//
+// sm_103a has no int8 tcgen05.mma (ptxas rejects kind::i8 for it), so the int8
+// arithmetic runs exactly on kind::f16: quants |q| <= 127 are exact in fp16,
+// every product is an integer below 2^14 and a block's 32-product sum is below
+// 2^24, exact in the fp32 accumulator.  The scales differ per 32-value block,
+// so each block gets its own accumulator: two UMMAs (K = 16 each) write a fresh
+// 128 x 256 fp32 tile into one of two TMEM slots, and eight epilogue warps read
+// it back (tcgen05.ld) and fold it into fp32 registers as
+// acc[o][t] += isum * d_x[t] * d_w[o] (packed f32x2 multiply and FMA).  That
+// epilogue costs two fp32 operations per output per block, 1/16 of the MMA's
+// multiply-adds, and the fp32 pipe, not the tensor pipe, sets the ceiling
+// (about half the fp16 tensor rate).
+//
+// Warp roles (320 threads, one persistent CTA per SM):
+//   warp 0  TMA producer: per stage of K = 64 (two blocks) the fp16 weight tile
+//           (128 x 64, 128-byte swizzle), the fp16 activation tile (256 x 64,
+//           128-byte swizzle), and the two blocks' scales (1-D bulk copies).
+//   warp 1  allocates TMEM (512 columns) and issues the UMMAs from one thread;
+//           tcgen05.commit signals "slot full" and, per stage, "stage consumed".
+//   2..9    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the 256
+//           columns; arrives "slot empty" after reading, "stage empty" after
+//           using the stage's scales.
+// Work units are (128-row tile, 256-token tile, K split); with fewer tiles than
+// SMs, K is split and the partial sums are added by a second kernel in a fixed
+// order (deterministic).  Every wait is bounded.
+#include <cuda.h>
+
+#include "q8_common.cuh"
+#include "q8_kernels.h"
+
+namespace q8 {
+
+namespace tc {
+constexpr int BM = 128;                                // weight rows per tile (UMMA M)
+constexpr int BN = 256;                                // tokens per tile (UMMA N)
+constexpr int BK = 64;                                 // K elements per stage (two blocks)
+constexpr int NSTAGE = 4;
+constexpr int A_BYTES = BM * BK * 2;                   // 16384
+constexpr int B_BYTES = BN * BK * 2;                   // 32768
+constexpr int DX_BYTES = 2 * BN * 4;                   // 2048
+constexpr int DW_BYTES = 2 * BM * 4;                   // 1024
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + DX_BYTES + DW_BYTES;   // 51 KiB, 1 KiB aligned
+constexpr int NUM_EPI = 8;                             // epilogue warps: 2 per TMEM lane quarter
+constexpr int EPI_COLS = BN / (NUM_EPI / 4);          // 128 columns per epilogue warp
+constexpr int NTHREADS = (2 + NUM_EPI) * 32;
+constexpr uint32_t TMEM_COLS = 512;                    // two 256-column accumulator slots
+constexpr int NBAR = 2 * NSTAGE + 4 + 1;               // full, empty, tfull[2], tempty[2], done
+constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + 1024 + NBAR * 8 + 16;
+static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+}  // namespace tc
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major tile with 128-byte swizzle, rows 128
+// bytes apart, 8-row groups 1024 bytes apart (the layout a 128-byte-swizzled
+// TMA box of 64 fp16 per row produces).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                            // leading byte offset (unused with swizzle)
+    d |= (uint64_t)(1024u >> 4) << 32;                 // stride byte offset: 8-row group
+    d |= (uint64_t)1 << 46;                            // descriptor version
+    d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: fp32 accumulate, fp16 A and B, both K-major, N x M.
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// (a0, a1) += (v0, v1) * (x0, x1) * (w, w), accumulator pair in one 64-bit register.
+__device__ __forceinline__ void tc_fold(uint64_t &acc, uint32_t v0, uint32_t v1, float x0, float x1, uint64_t ww) {
+    asm("{\n\t.reg .b64 v, x, t;\n\tmov.b64 v, {%1, %2};\n\tmov.b64 x, {%3, %4};\n\t"
+        "mul.rn.f32x2 t, v, x;\n\t"
+        "fma.rn.f32x2 %0, t, %5, %0;\n\t}"
+        : "+l"(acc)
+        : "r"(v0), "r"(v1), "f"(x0), "f"(x1), "l"(ww));
+}
+
+__device__ __forceinline__ uint64_t tc_pair(float w) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(w));
+    return r;
+}
+
+struct TcUnit {
+    int mt, nt, kb0, kb1;
+};
+
+__device__ __forceinline__ bool tc_unit(const TcParams &p, int u, TcUnit &w) {
+    const int m_tiles = (p.M + tc::BM - 1) / tc::BM;
+    const int n_tiles = (p.N + tc::BN - 1) / tc::BN;
+    const int units = m_tiles * n_tiles * p.ksplit;
+    if (u >= units) return false;
+    w.mt = u % m_tiles;                 // consecutive units share the activation tile
+    const int r = u / m_tiles;
+    w.nt = r % n_tiles;
+    const int ks = r / n_tiles;
+    w.kb0 = ks * p.kb_per;
+    w.kb1 = min(p.nb, w.kb0 + p.kb_per);
+    return true;
+}
+
+__global__ void __launch_bounds__(tc::NTHREADS, 1)
+    k_tc_gemm(const TcParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base_s = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + (((base_s + 1023u) & ~1023u) - base_s);      // 1 KiB aligned stages
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * STAGE_BYTES);
+    uint64_t *full = bars, *empty = bars + NSTAGE;
+    uint64_t *tfull = bars + 2 * NSTAGE, *tempty = tfull + 2, *done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + NUM_EPI);   // MMA commit + every epilogue warp
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], NUM_EPI);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {   // TMEM allocation (whole warp)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t fills[NSTAGE] = {0, 0, 0, 0};
+            TcUnit w;
+            for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
+                const int m0 = w.mt * BM, n0 = w.nt * BN;
+                for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+                    if (mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
+                        uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
+                        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                        tma_load_2d(st, &tmA, kb * QK, m0, &full[stage]);
+                        tma_load_2d(st + A_BYTES, &tmB, kb * QK, n0, &full[stage]);
+                        float *dxs = reinterpret_cast<float *>(st + A_BYTES + B_BYTES);
+                        float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+                        bulk_g2s(dxs, p.dxT + (size_t)kb * p.n_ld + n0, BN * 4, &full[stage]);
+                        bulk_g2s(dxs + BN, p.dxT + (size_t)(kb + 1) * p.n_ld + n0, BN * 4, &full[stage]);
+                        bulk_g2s(dws, p.dwT + (size_t)kb * p.m_ld + m0, BM * 4, &full[stage]);
+                        bulk_g2s(dws + BM, p.dwT + (size_t)(kb + 1) * p.m_ld + m0, BM * 4, &full[stage]);
+                        ++fills[stage];
+                    }
+                    if (++stage == NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < NSTAGE; ++s)
+                if (fills[s]) mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.err, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc(BM, BN);
+            uint32_t stage = 0, phase = 0, blk = 0;
+            TcUnit w;
+            for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
+                for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+                    mbar_wait(&full[stage], phase, p.err, abort_flag);
+                    tc_fence_after();
+                    const uint32_t a_s = smem_addr(smem + (size_t)stage * STAGE_BYTES);
+                    const uint32_t b_s = a_s + A_BYTES;
+                    for (int j = 0; j < 2; ++j, ++blk) {
+                        const uint32_t slot = blk & 1u;
+                        mbar_wait(&tempty[slot], ((blk >> 1) & 1u) ^ 1u, p.err, abort_flag);
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + slot * BN;
+#pragma unroll
+                        for (int k16 = 0; k16 < 2; ++k16) {
+                            const uint32_t koff = (uint32_t)(2 * j + k16) * 32u;   // 16 fp16 = 32 bytes
+                            tc_mma_f16(d_tmem, sw128_desc(a_s + koff), sw128_desc(b_s + koff), idesc, k16);
+                        }
+                        tc_commit(&tfull[slot]);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            tc_commit(done);                          // all MMAs issued by this thread
+            mbar_wait(done, 0, p.err, nullptr);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int h = (warp - 2) >> 2;                // column half
+        const int m = q * 32 + lane;                  // row within the tile
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint32_t stage = 0, phase = 0, blk = 0;
+        TcUnit w;
+        for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
+            uint64_t acc[EPI_COLS / 2];   // this warp's columns as fp32 pairs
+#pragma unroll
+            for (int i = 0; i < EPI_COLS / 2; ++i) acc[i] = 0ull;
+            for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+                const uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
+                // the scales arrive with the stage (the MMA warp waited on the same barrier)
+                mbar_wait(&full[stage], phase, p.err, abort_flag);
+                const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
+                const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+                for (int j = 0; j < 2; ++j, ++blk) {
+                    const uint32_t slot = blk & 1u;
+                    mbar_wait(&tfull[slot], (blk >> 1) & 1u, p.err, abort_flag);
+                    tc_fence_after();
+                    const uint64_t ww = tc_pair(dws[j * BM + m]);
+                    const float *dxj = dxs + j * BN + h * EPI_COLS;
+                    const uint32_t col0 = lane_addr + slot * BN + h * EPI_COLS;
+                    // 16-column chunks, the next chunk's TMEM load in flight while
+                    // the current one is folded in
+                    uint32_t v[2][16];
+                    tc_ld16(col0, v[0]);
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS / 16; ++c) {
+                        tc_wait_ld();
+                        if (c + 1 < EPI_COLS / 16) tc_ld16(col0 + (c + 1) * 16, v[(c + 1) & 1]);
+                        const float4 *x4 = reinterpret_cast<const float4 *>(dxj + c * 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 x = x4[i];
+                            tc_fold(acc[c * 8 + 2 * i], v[c & 1][4 * i], v[c & 1][4 * i + 1], x.x, x.y, ww);
+                            tc_fold(acc[c * 8 + 2 * i + 1], v[c & 1][4 * i + 2], v[c & 1][4 * i + 3], x.z, x.w, ww);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[slot]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == NSTAGE) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // ---- write this unit's rows x this warp's tokens
+            const int row = w.mt * BM + m;
+            const int tok0 = w.nt * BN + h * EPI_COLS;
+            const int ks = w.kb0 / p.kb_per;
+            float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
+            if (row < p.M) {
+#pragma unroll
+                for (int i = 0; i < EPI_COLS / 2; ++i) {
+                    const int t = tok0 + 2 * i;
+                    const float lo = __uint_as_float((uint32_t)acc[i]);
+                    const float hi = __uint_as_float((uint32_t)(acc[i] >> 32));
+                    if (t < p.N) dst[(size_t)t * p.M + row] = lo;
+                    if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = hi;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// K-split partials -> out, adding the splits in order.
+__global__ void __launch_bounds__(256) k_tc_reduce(float *__restrict__ out, const float *__restrict__ partial,
+                                                   uint64_t n, int ksplit) {
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        float s = partial[i];
+        for (int k = 1; k < ksplit; ++k) s += partial[(uint64_t)k * n + i];
+        out[i] = s;
+    }
+}
+
+// Raw Q8_0 rows -> fp16 quant plane [rows][in_dim] (exact) and block-major
+// scales dwT[b][m_ld] (fp32 of the stored binary16 scale).  One thread per block,
+// rows fastest so the scale writes are coalesced.
+__global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, float *__restrict__ dwT,
+                                                   const uint8_t *__restrict__ W, uint32_t rows, uint32_t nb,
+                                                   uint32_t m_ld) {
+    const uint64_t total = (uint64_t)rows * nb;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t b = (uint32_t)(i / rows), r = (uint32_t)(i - (uint64_t)b * rows);
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(W + ((uint64_t)r * nb + b) * QB);
+        dwT[(uint64_t)b * m_ld + r] = half_bits_to_float(src[0]);
+        uint4 *dst = reinterpret_cast<uint4 *>(a16 + (uint64_t)r * nb * QK + (uint64_t)b * QK);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint16_t two = src[1 + c * 4 + e];   // quants 8c+2e, 8c+2e+1
+                const __half lo = __int2half_rn((int)(int8_t)(two & 0xff));
+                const __half hi = __int2half_rn((int)(int8_t)(two >> 8));
+                o[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            }
+            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                     uint32_t box_rows);
+
+cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
+                             int num_sms, cudaStream_t st) {
+    const uint64_t total = (uint64_t)rows * nb;
+    if (!total) return cudaSuccess;
+    uint64_t grid = (total + 255) / 256;
+    if (grid > (uint64_t)num_sms * 16) grid = (uint64_t)num_sms * 16;
+    k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
+                           cudaStream_t st) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    alignas(64) CUtensorMap tmA, tmB;
+    const uint64_t K = (uint64_t)p.nb * QK;
+    if (!encode_f16_tmap(&tmA, a16, K, (uint64_t)p.M, tc::BK, tc::BM)) return cudaErrorInvalidValue;
+    if (!encode_f16_tmap(&tmB, b16, K, n_rows_b, tc::BK, tc::BN)) return cudaErrorInvalidValue;
+    k_tc_gemm<<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.ksplit == 1) return e;
+    const uint64_t n = (uint64_t)p.N * p.M;
+    uint64_t g = (n + 255) / 256;
+    if (g > 4096) g = 4096;
+    k_tc_reduce<<<(int)g, 256, 0, st>>>(p.out, p.partial, n, p.ksplit);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

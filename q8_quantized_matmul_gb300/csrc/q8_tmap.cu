@@ -46,4 +46,20 @@ bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint6
     return r == CUDA_SUCCESS;
 }
 
+// Row-major fp16 matrix [rows][cols] with a 128-byte-swizzled box of
+// box_cols (64) x box_rows: the canonical K-major operand layout of tcgen05.
+bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                     uint32_t box_rows) {
+    if (!load_encoder()) return false;
+    if ((cols * 2) % 16 || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace q8

@@ -65,7 +65,7 @@ def gpu_matmul(q8, W, x, out_dim):
     n_tok, in_dim = x.shape
     buf = poisoned(n_tok * out_dim)
     rc = q8.q8_matmul(buf, W, in_dim, out_dim, x, n_tok)
-    assert rc == 0, q8.q8_strerror(rc)
+    assert rc == 0, f"{q8.q8_strerror(rc)} {q8.q8_last_cuda_error()}"
     assert q8.q8_last_error() == 0
     return fetch(buf, n_tok * out_dim, (n_tok, out_dim))
 
