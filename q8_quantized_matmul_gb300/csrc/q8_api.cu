@@ -164,23 +164,6 @@ int check_dims(uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
     return Q8_OK;
 }
 
-// Rows per CTA item for the GEMV: enough items for every SM, at most 512 rows.
-uint32_t gemv_rows_per_item(uint64_t out_dim, int num_sms) {
-    uint64_t r = (out_dim + num_sms - 1) / num_sms;
-    r = (r + 15) & ~(uint64_t)15;
-    if (r < 16) r = 16;
-    if (r > q8::GEMV_MAX_ROWS_PER_ITEM) r = q8::GEMV_MAX_ROWS_PER_ITEM;
-    return (uint32_t)r;
-}
-
-// Warps per 16-row sub-item: split K across warps when the item has few sub-items.
-uint32_t gemv_wpi(uint32_t rows_per_item) {
-    const uint32_t nsub = rows_per_item / 16;
-    uint32_t wpi = 1;
-    while (wpi < 16 && nsub * wpi * 2 <= 16) wpi *= 2;   // 16 warps per CTA
-    return wpi;
-}
-
 // out = W x from activation planes already in scratch (n_pad rows).
 int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const int8_t *qx,
               const float *dx, uint64_t n_tok, cudaStream_t st) {
@@ -197,14 +180,12 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.out = out;
         g.err = s->err;
         g.n_tok = (uint32_t)n_tok;
-        g.rows_per_item = gemv_rows_per_item(out_dim, s->num_sms);
-        g.wpi = gemv_wpi(g.rows_per_item);
+        g.n_items = q8::gemv_dense_items(out_dim, s->num_sms);
         g.plan = nullptr;
         g.row_to_out = nullptr;
         g.n_expert = 1;
-        const uint64_t items = (out_dim + g.rows_per_item - 1) / g.rows_per_item;
-        const int grid = (int)(items < (uint64_t)s->num_sms ? items : (uint64_t)s->num_sms);
-        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, n_tok > 8, grid, st); }));
+        const int grid = (int)(g.n_items < (uint32_t)s->num_sms ? g.n_items : (uint32_t)s->num_sms);
+        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st); }));
     }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
@@ -437,15 +418,14 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     g.err = s->err;
     g.n_tok = 0;
     g.rows_per_item = rows_gemv;
-    g.wpi = 1;
     g.row_to_out = row_to_out;
     g.n_expert = n_expert;
     return status_of(timed_launch(st, [&] {
         g.plan = plan_of(0);
-        cudaError_t e2 = q8::launch_gemv(g, false, s->num_sms, st);
+        cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
         if (e2 != cudaSuccess) return e2;
         g.plan = plan_of(1);
-        if ((e2 = q8::launch_gemv(g, true, s->num_sms, st)) != cudaSuccess) return e2;
+        if ((e2 = q8::launch_gemv(g, 2, s->num_sms, st)) != cudaSuccess) return e2;
         p.plan = plan_of(2);
         return q8::launch_mma(p, s->num_sms, st);
     }));

@@ -89,6 +89,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     }
 }
 
+// After an abort: wait, until the global-timer deadline t_end at the latest, for
+// a phase whose copies may still be in flight, so that no bulk copy lands after
+// the CTA has exited.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t t_end) {
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() > t_end) return;
+}
+
 // ---------------------------------------------------------------- bulk copy (TMA, 1-D)
 // Global -> shared, completion counted on `bar` in bytes.  src and dst must be
 // 16-byte aligned and bytes a multiple of 16.

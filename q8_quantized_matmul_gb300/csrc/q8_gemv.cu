@@ -9,41 +9,44 @@
 // enough weight bytes in flight and to spend few instructions per byte.
 //
 // Layout of the work
-//   * A CTA item is (segment, token group, row range).  A token group is up to
-//     NT*8 tokens (NT = 1 or 2 N tiles of the MMA); its activation fragments are
-//     staged once into shared memory in MMA-fragment order (converted to fp16,
-//     exact for int8), so a warp reads one block's fragment with one 16-byte
-//     load per lane and N tile.
-//   * The row range is cut into 16-row sub-items (the MMA M dimension).  Each of
-//     the 16 warps owns whole sub-items and streams their weight rows through its
-//     own two-slot ring: one tiled TMA copy (cp.async.bulk.tensor) per slot of
-//     16 rows x 8 blocks, over a tensor map that views the raw rows as 32-bit
-//     words with a 76-word box, so rows land 304 bytes apart (an odd multiple of
-//     16 bytes: the fragment loads are bank-conflict free).  The box's last 32
-//     bytes per row belong to the next slot and are not used; words past the end
-//     of a row and rows past out_dim are filled with zeros by the TMA.  When the
-//     rows are too few for the warps, WPI warps split a sub-item's blocks and add
-//     their partial sums through shared memory in a fixed order.
-//   * Per block: the weight fragment (rows g and g+8, two 4-byte groups of
-//     quants per lane) comes from 32-bit shared loads.  The sum over a block's 32
-//     products does not depend on their order, so each lane may take any fixed
-//     set of quant positions as long as the activation fragment uses the same
-//     one: odd blocks (quants 4-byte aligned) use the natural MMA order; even
-//     blocks (quants at 2 mod 4) give lanes 0-2 two aligned words each and lane
-//     3 one aligned word plus the four edge bytes joined by one byte permute,
-//     and the staged activations are permuted to match.  The quants are converted
-//     to fp16 (exact: |q| <= 127), and two mma.sync m16n8k16 f16 per N tile give
-//     the block dot (16 rows x 8 tokens x 32 values) in fp32, exact because
-//     every product is an integer below 2^14 and every block sum below 2^24.
-//     It is then scaled by d_w*d_x and added in fp32 with packed f32x2
-//     instructions.  fp16 rather than int8 MMA: on GB300 mma.sync runs int8 at
-//     251 and fp16 at 942 MAC per SM per clock (measured); the 8-token N tile
-//     costs 8 or 16 MACs per weight, which int8 cannot deliver at the HBM rate.
-//   * Memory-level parallelism: the ring is small, so at the start of an item
-//     each warp also issues TMA L2 prefetches for all of its remaining slots;
-//     HBM then sees the item's whole request at once and the ring refills from
-//     L2 at low latency.
-//   * Launched with programmatic stream serialisation: the weight prefetch starts
+//   * A CTA item is (segment, token group, row range).  The row range is cut into
+//     16-row sub-items; the weights of an item stream through shared memory as
+//     slots of 16 rows x 8 blocks, one tiled TMA copy (cp.async.bulk.tensor) per
+//     slot over a tensor map that views the raw rows as 32-bit words with a
+//     76-word box, so rows land 304 bytes apart (an odd multiple of 16 bytes:
+//     the fragment loads below are bank-conflict free).  The box's last 32 bytes
+//     per row belong to the next slot and are not used; words past the end of a
+//     row and rows past out_dim are filled with zeros by the TMA.
+//   * Warp specialisation.  One producer warp walks the CTA's slot sequence
+//     (items in order; within an item, K-slot major and sub-items inner) and
+//     issues every copy into a CTA-wide ring of 32 slots (152 KB in flight),
+//     reusing a slot once its consumer has released it.  TMA issue stalls while
+//     the SM's copy queue drains at the HBM rate, so only this warp ever waits
+//     there.  Sixteen consumer warps own the sub-items (G = 16 / wpi groups,
+//     sub-item s in group s mod G) and, when an item has fewer than 16
+//     sub-items, wpi warps split its K slots and add their partial sums
+//     through shared memory in a fixed order.  Consecutive slots of the
+//     sequence belong to different warps, so the ring drains in arrival order.
+//   * The token group's activations are staged once per K chunk by the consumer
+//     warps, in the order the mode's inner loop reads them.
+//   * Modes.  Mode 0 (at most 2 tokens): dp4a.  A lane owns one block column j
+//     of the slot and four of its rows; it reads the block's 9 words, aligns the
+//     quants with one byte permute per word and forms the int32 block dot with
+//     8 dp4a per token; the 8 block columns of a row are added by shuffles at
+//     the end.  Modes 1 and 2 (8 or 16 tokens): mma.sync m16n8k16 in fp16 on the
+//     exact int8 values, one or two 8-token N tiles.  The weight fragment (rows
+//     g and g+8, two 4-byte groups of quants per lane) comes from 32-bit shared
+//     loads.  The sum over a block's 32 products does not depend on their order,
+//     so each lane may take any fixed set of quant positions as long as the
+//     activation fragment uses the same one: odd blocks (quants 4-byte aligned)
+//     use the natural MMA order; even blocks (quants at 2 mod 4) give lanes 0-2
+//     two aligned words each and lane 3 one aligned word plus the four edge
+//     bytes joined by one byte permute, and the staged activations are permuted
+//     to match.  fp32 accumulation of each block dot is exact (products below
+//     2^14, block sums below 2^24); it is then scaled by d_w*d_x and added in
+//     fp32 with packed f32x2 instructions.  fp16 rather than int8 MMA: on GB300
+//     mma.sync runs int8 at 251 and fp16 at 942 MAC per SM per clock (measured).
+//   * Launched with programmatic stream serialisation: the weight stream starts
 //     before the preceding quantiser kernel has finished; activations are read
 //     only after griddepcontrol.wait.
 #include <cuda.h>
@@ -54,22 +57,36 @@
 namespace q8 {
 
 namespace gv {
-constexpr int NW = 16;                   // warps per CTA
-constexpr int NTHREADS = NW * 32;
-constexpr int ROWS = 16;                 // rows per sub-item
-constexpr int KC = 8;                    // blocks per weight slot
-constexpr int BOX_WORDS = (KC * QB + 32) / 4;   // 76 words per row of a slot
-constexpr int SROW = BOX_WORDS * 4;      // 304 bytes: 19 x 16, an odd multiple of 16
-constexpr int SLOT = ROWS * SROW;        // 4864 bytes
-constexpr int NSLOT = 2;                 // ring depth per warp
-constexpr int SUBMAX = 2;                // sub-items per warp per CTA item
-constexpr int ACT_BYTES = 48 * 1024;     // activation fragments per chunk
-constexpr int KA_MAX = ACT_BYTES / (32 * 16);  // blocks per chunk with one N tile (96)
-constexpr int DX_FLOATS = KA_MAX * 16;   // scales of a chunk: [block][16 tokens]
-constexpr int RING_BYTES = NW * NSLOT * SLOT;
-constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + NW * NSLOT * 8 + 64;
+constexpr int NCW = 16;                          // consumer warps
+constexpr int PRODUCER = NCW;                    // warp index of the TMA producer
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int CONSUMER_THREADS = NCW * 32;
+constexpr int ROWS = 16;                         // rows per sub-item
+constexpr int KC = 8;                            // blocks per weight slot
+constexpr int BOX_WORDS = (KC * QB + 32) / 4;    // 76 words per row of a slot
+constexpr int SROW = BOX_WORDS * 4;              // 304 bytes: 19 x 16, an odd multiple of 16
+constexpr int SLOT = ROWS * SROW;                // 4864 bytes
+constexpr int NSLOT = 32;                        // CTA ring depth
+constexpr int SUBMAX = 512 / (NCW * 16);         // sub-items per warp per CTA item
+constexpr int ACT_BYTES = 40 * 1024;             // staged activations per chunk
+constexpr int DX_FLOATS = 1280;                  // staged activation scales per chunk
+constexpr int RING_BYTES = NSLOT * SLOT;
+constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + 2 * NSLOT * 8 + NSLOT * 4 + 16;
+constexpr int BAR_CONSUMERS = 1;                 // named barrier of the consumer warps
 static_assert(SMEM <= 227 * 1024, "shared memory");
-static_assert(SUBMAX * NW * ROWS >= GEMV_MAX_ROWS_PER_ITEM, "rows per item");
+static_assert(NSLOT >= 32, "one producer lane per slot of a batch");
+static_assert(SUBMAX * NCW * ROWS >= GEMV_MAX_ROWS_PER_ITEM, "rows per item");
+// Modes: 0 = dp4a, up to 2 tokens; 1 = fp16 MMA, one 8-token N tile; 2 = two N tiles.
+template <int MODE> struct Mode {
+    static constexpr int TOKG = MODE == 0 ? 2 : MODE * 8;          // tokens per group
+    static constexpr int NT = MODE == 0 ? 1 : MODE;                // MMA N tiles
+    static constexpr int ACT_BLOCK = MODE == 0 ? 80 : MODE * 512;   // staged activation bytes per block
+    static constexpr int DXW = MODE == 0 ? 2 : 16;                  // staged scales per block
+    static constexpr int KA = (ACT_BYTES / ACT_BLOCK) / KC * KC;    // blocks per chunk (512, 80, 40)
+    static constexpr int NACC = MODE == 0 ? 8 : NT * 4;             // fp32 results per lane and sub-item
+    static_assert(KA * DXW <= DX_FLOATS, "scale buffer");
+    static_assert(NCW * SUBMAX * NACC * 32 * 4 <= ACT_BYTES, "split-K buffer");
+};
 }  // namespace gv
 
 __device__ __forceinline__ uint32_t lds32g(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
@@ -132,42 +149,41 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Bring a box of the tensor into L2 without a shared-memory destination.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
+// dp4a mode: the four rows of a sub-item that lane group rb (lanes 8rb..8rb+7,
+// one weight block each) reads in step i.  The sets {0,3,4,7} and {1,2,5,6} (and
+// the same plus 8) put the 32 lanes' word addresses, block starts 34j bytes
+// apart at a row pitch of 76 words, in 32 different banks.
+__device__ __forceinline__ int dp4a_row(int rb, int i) {
+    return (i >> 1) * 8 + (rb >> 1) * 4 + ((i & 1) ? 1 + (rb & 1) : 3 * (rb & 1));
+}
 
 // Item decoding.  Returns false past the last item.
 struct GItem {
     int expert;
     int xrow0;      // first activation-plane row of the token group
-    int ntok;       // tokens in the group (<= NT*8)
+    int ntok;       // tokens in the group
     int tok0;       // index of the first token within its segment
     uint32_t r0;    // first weight row
     uint32_t nrows;
 };
 
-template <int NT>
+template <int TOKG>
 __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it) {
-    constexpr int TOKG = NT * 8;
     if (!p.plan) {
-        const uint32_t n_items = (p.out_dim + p.rows_per_item - 1) / p.rows_per_item;
-        if ((uint32_t)i >= n_items) return false;
+        // dense: n_items contiguous ranges of whole sub-items, sizes differing by at most one
+        if ((uint32_t)i >= p.n_items) return false;
+        const uint32_t nsub_all = (p.out_dim + gv::ROWS - 1) / gv::ROWS;
+        const uint32_t s0 = (uint32_t)(((uint64_t)i * nsub_all) / p.n_items);
+        const uint32_t s1 = (uint32_t)(((uint64_t)(i + 1) * nsub_all) / p.n_items);
         it.expert = 0;
         it.xrow0 = 0;
         it.ntok = (int)p.n_tok;
         it.tok0 = 0;
-        it.r0 = (uint32_t)i * p.rows_per_item;
-        it.nrows = min(p.rows_per_item, p.out_dim - it.r0);
+        it.r0 = s0 * gv::ROWS;
+        it.nrows = min((s1 - s0) * gv::ROWS, p.out_dim - it.r0);
         return true;
     }
     if (i >= p.plan->n_items) return false;
@@ -191,250 +207,456 @@ __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it)
     return true;
 }
 
+// Bounded wait until the producer has armed round r of a slot.
+__device__ __forceinline__ bool wait_armed(volatile uint32_t *armed, uint32_t r, int *err, volatile int *abort) {
+    if (*armed == r) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (*armed == r) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+                raise_error(err, DEV_ETIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Warps per sub-item for an item of nsub sub-items and nk K slots: the largest
+// power of two that keeps every consumer warp on at most one sub-item group.
+__device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
+    uint32_t wpi = 1;
+    while (nsub * wpi * 2 <= (uint32_t)gv::NCW && wpi * 2 <= nk) wpi *= 2;
+    return wpi;
+}
+
+// The producer warp: every slot of every item of this CTA, in order, 32 at a
+// time (lane l issues slot base + l).  One thread issuing alone is limited to
+// about one tiled copy per 170 ns, well below the HBM rate; 32 lanes are not.
+// After arming a slot's full barrier for round r (its use number) the lane
+// publishes r in armed[slot].  Consumers of different warps take different
+// slots and copies land out of order, so a warp may come to round r + 1 of a
+// slot while round r has not landed; its parity wait would then see the
+// previous phase as complete.  Waiting for armed[slot] == r first rules that
+// out.  Returns the number of slots planned.
+template <int TOKG>
+__device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorMap *tmap, uint8_t *ring, uint64_t *full,
+                                            uint64_t *empty, volatile uint32_t *armed, volatile int *abort_flag,
+                                            int lane) {
+    using namespace gv;
+    const uint32_t nk = (p.nb + KC - 1) / KC;
+    uint32_t seqbase = 0;
+    GItem it;
+    for (int item_i = blockIdx.x; gemv_item<TOKG>(p, item_i, it); item_i += gridDim.x) {
+        const uint32_t nsub = (it.nrows + ROWS - 1) / ROWS;
+        const uint32_t total = nk * nsub;
+        for (uint32_t base = 0; base < total; base += 32) {
+            const uint32_t idx = base + (uint32_t)lane;
+            if (idx < total) {
+                const uint32_t seq = seqbase + idx, slot = seq % NSLOT;
+                const uint32_t kk = idx / nsub, sub = idx - kk * nsub;
+                if (mbar_wait(&empty[slot], ((seq / NSLOT) & 1u) ^ 1u, p.err, abort_flag)) {
+                    mbar_arrive_expect_tx(&full[slot], SLOT);
+                    tma_load_3d(ring + (size_t)slot * SLOT, tmap, (int)(kk * (KC * QB / 4)),
+                                (int)(it.r0 + sub * ROWS), it.expert, &full[slot]);
+                    __threadfence_block();
+                    armed[slot] = seq / NSLOT;
+                }
+            }
+            __syncwarp();
+        }
+        seqbase += total;
+    }
+    return seqbase;
+}
+
+// Stage one K chunk [kb0, kb0 + ka) of the token group's activations (consumer
+// threads only).  All global loads of a thread are issued before any is used:
+// under a saturated HBM stream each round trip costs a microsecond or more.
+template <int MODE>
+__device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it, uint32_t kb0, uint32_t ka,
+                                            uint8_t *act, float *dxs) {
+    using namespace gv;
+    using M = Mode<MODE>;
+    constexpr int NT = M::NT;
+    const uint32_t nb = p.nb;
+    if (MODE == 0) {
+        // [block][token][8 words], 80 bytes per block.  The words are arranged to
+        // meet the weight words of the block where they lie in the row:
+        //   odd block (quants word-aligned, q0..q31 in words 1..8 of the read):
+        //     A[0] = X[7], A[k] = X[k-1]
+        //   even block (quants at 2 mod 4, words 1..7 hold q2..q29, the edge word
+        //   holds q0, q1, q30, q31):  A[0] = [x0, x1, x30, x31], A[k] = x[4k-2 .. 4k+1]
+        for (uint32_t e = threadIdx.x; e < ka * 2; e += CONSUMER_THREADS) {
+            const uint32_t b = e >> 1, t = e & 1;
+            uint32_t X[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            float d = 0.0f;
+            if (t < (uint32_t)it.ntok) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.qx + (uint64_t)(it.xrow0 + t) * p.in_dim +
+                                                                   (uint64_t)(kb0 + b) * QK);
+                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                d = __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b);
+                X[0] = v0.x; X[1] = v0.y; X[2] = v0.z; X[3] = v0.w;
+                X[4] = v1.x; X[5] = v1.y; X[6] = v1.z; X[7] = v1.w;
+            }
+            uint32_t A[8];
+            if ((kb0 + b) & 1u) {
+                A[0] = X[7];
+#pragma unroll
+                for (int k = 1; k < 8; ++k) A[k] = X[k - 1];
+            } else {
+                A[0] = __byte_perm(X[0], X[7], 0x7610);
+#pragma unroll
+                for (int k = 1; k < 8; ++k) A[k] = funnel16(X[k - 1], X[k]);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(act + (size_t)b * M::ACT_BLOCK + t * 32);
+            dst[0] = make_uint4(A[0], A[1], A[2], A[3]);
+            dst[1] = make_uint4(A[4], A[5], A[6], A[7]);
+            dxs[e] = d;
+        }
+    } else {
+        // MMA B fragments, fp16: [block][N tile][lane][16 bytes].  The planes hold
+        // 16-row-padded token groups, so rows past ntok read zeros.
+        // Words of the activation block a lane's fragment is built from:
+        //   odd block: words c, 4+c;  even block: x[4c+2..4c+5] from words c, c+1 and
+        //   x[4c+18..4c+21] from words c+4, c+5 (c < 3); lane 3: x[14..17] from words 3, 4
+        //   and [x0, x1, x30, x31] from words 0, 7.
+        constexpr int R = (M::KA * 32 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+        uint32_t wv[R][NT][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+            if (e < ka * 32) {
+                const uint32_t b = e >> 5, l = e & 31, lg = l >> 2, lc = l & 3;
+                const bool even = ((kb0 + b) & 1u) == 0;
+                const uint32_t i1 = even ? lc + 1 : 4 + lc;
+                const uint32_t i2 = lc < 3 ? lc + 4 : 0u;
+                const uint32_t i3 = lc < 3 ? lc + 5 : 7u;
+                const int8_t *xr = p.qx + (uint64_t)(it.xrow0 + lg) * p.in_dim + (uint64_t)(kb0 + b) * QK;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
+                    wv[r][t][0] = __ldg(xt + lc);
+                    wv[r][t][1] = __ldg(xt + i1);
+                    wv[r][t][2] = __ldg(xt + i2);
+                    wv[r][t][3] = __ldg(xt + i3);
+                }
+            }
+        }
+        constexpr int RD = (M::KA * 16 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+        float dv[RD];
+#pragma unroll
+        for (int r = 0; r < RD; ++r) {
+            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+            const uint32_t b = e >> 4, t = e & 15;
+            dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8)) ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b) : 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+            if (e < ka * 32) {
+                const uint32_t b = e >> 5, l = e & 31, lc = l & 3;
+                const bool even = ((kb0 + b) & 1u) == 0;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    uint32_t f0, f1;
+                    if (!even) {
+                        f0 = wv[r][t][0];
+                        f1 = wv[r][t][1];
+                    } else {
+                        f0 = funnel16(wv[r][t][0], wv[r][t][1]);
+                        f1 = lc < 3 ? funnel16(wv[r][t][2], wv[r][t][3]) : __byte_perm(wv[r][t][2], wv[r][t][3], 0x7610);
+                    }
+                    uint4 h;
+                    s8x4_to_h2x2(f0, h.x, h.y);   // MMA over the first 16 quants: b0, b1
+                    s8x4_to_h2x2(f1, h.z, h.w);   // MMA over the second 16 quants
+                    *reinterpret_cast<uint4 *>(act + (size_t)b * M::ACT_BLOCK + (size_t)t * 512 + (size_t)l * 16) = h;
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RD; ++r) {
+            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+            if (e < ka * 16) dxs[e] = dv[r];
+        }
+    }
+}
+
+// dp4a mode, one slot: lane = (row group rb, block column j).  Each row's
+// block dot is 8 dp4a over the weight words as they lie in shared memory, the
+// activation words having been arranged to match; one byte permute forms the
+// edge word (odd block: word 8; even block: q0, q1, q30, q31).
+__device__ __forceinline__ void slot_dp4a(const uint8_t *sbase, const uint8_t *act, const float *dxs, uint32_t bl0,
+                                          int lane, float (&acc)[8], bool two_tokens) {
+    using namespace gv;
+    const int j = lane & 7, rb = lane >> 3;
+    const uint32_t bl = bl0 + (uint32_t)j;
+    const uint4 *xa = reinterpret_cast<const uint4 *>(act + (size_t)bl * Mode<0>::ACT_BLOCK);
+    const uint4 x00 = xa[0], x01 = xa[1];
+    const uint32_t A0[8] = {x00.x, x00.y, x00.z, x00.w, x01.x, x01.y, x01.z, x01.w};
+    uint32_t A1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (two_tokens) {
+        const uint4 x10 = xa[2], x11 = xa[3];
+        A1[0] = x10.x; A1[1] = x10.y; A1[2] = x10.z; A1[3] = x10.w;
+        A1[4] = x11.x; A1[5] = x11.y; A1[6] = x11.z; A1[7] = x11.w;
+    }
+    const float dx0 = dxs[bl * 2], dx1 = dxs[bl * 2 + 1];
+    // block j starts at byte 34j of the row: word-aligned when j is even, else at 2 mod 4
+    const uint32_t sel = (j & 1) ? 0x7654u : 0x5432u;
+    const int wbase = (34 * j) >> 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t *wr = reinterpret_cast<const uint32_t *>(sbase + dp4a_row(rb, i) * SROW) + wbase;
+        uint32_t W[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) W[k] = wr[k];
+        const uint32_t dbits = (j & 1) ? (W[0] >> 16) : (W[0] & 0xffffu);
+        const float dw = half_bits_to_float((uint16_t)dbits);
+        const uint32_t edge = __byte_perm(W[0], W[8], sel);
+        int s0 = __dp4a((int)edge, (int)A0[0], 0), s1 = 0;
+        if (two_tokens) s1 = __dp4a((int)edge, (int)A1[0], 0);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) {
+            s0 = __dp4a((int)W[k], (int)A0[k], s0);
+            if (two_tokens) s1 = __dp4a((int)W[k], (int)A1[k], s1);
+        }
+        acc[i] = fmaf((float)s0, dw * dx0, acc[i]);
+        if (two_tokens) acc[4 + i] = fmaf((float)s1, dw * dx1, acc[4 + i]);
+    }
+}
+
+// MMA modes, one slot: 16 rows x 8 blocks x NT*8 tokens.
 template <int NT>
+__device__ __forceinline__ void slot_mma(const uint8_t *sbase, const uint8_t *act, const float *dxs, uint32_t bl0,
+                                         int lane, uint64_t (&acc)[NT][2]) {
+    using namespace gv;
+    constexpr int ACT_BLOCK = NT * 512;
+    const int g = lane >> 2, c = lane & 3;
+    const uint8_t *r0base = sbase + g * SROW;
+    const uint8_t *abase = act + (size_t)bl0 * ACT_BLOCK + (size_t)lane * 16;
+    const float *dbase = dxs + bl0 * 16 + 2 * c;
+#pragma unroll
+    for (uint32_t jp = 0; jp < KC / 2; ++jp) {
+        const uint8_t *e0 = r0base + jp * (2 * QB);   // even block, row g
+        const uint8_t *e8 = e0 + 8 * SROW;            // even block, row g+8
+        uint32_t w[2][4];   // [block][row g lo, row g+8 lo, row g hi, row g+8 hi]
+        {
+            const uint32_t sel = c < 3 ? 0x3210u : 0x5432u;
+            w[0][0] = lds32g(e0 + even_off_a(c));
+            w[0][1] = lds32g(e8 + even_off_a(c));
+            w[0][2] = __byte_perm(lds32g(e0 + even_off_b(c)), lds32g(e0 + 32), sel);
+            w[0][3] = __byte_perm(lds32g(e8 + even_off_b(c)), lds32g(e8 + 32), sel);
+        }
+        w[1][0] = lds32g(e0 + QB + 2 + 4 * c);
+        w[1][1] = lds32g(e8 + QB + 2 + 4 * c);
+        w[1][2] = lds32g(e0 + QB + 18 + 4 * c);
+        w[1][3] = lds32g(e8 + QB + 18 + 4 * c);
+        uint64_t dw0[2], dw8[2];
+        dw0[0] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e0)));
+        dw8[0] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e8)));
+        dw0[1] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e0 + QB)));
+        dw8[1] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e8 + QB)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t bo = 2 * jp + h;                // block within the slot
+            uint32_t h0l, h0h, h1l, h1h, h2l, h2h, h3l, h3h;
+            s8x4_to_h2x2(w[h][0], h0l, h0h);     // row g,   first 16 quants
+            s8x4_to_h2x2(w[h][1], h1l, h1h);     // row g+8, first 16 quants
+            s8x4_to_h2x2(w[h][2], h2l, h2h);     // row g,   second 16 quants
+            s8x4_to_h2x2(w[h][3], h3l, h3h);     // row g+8, second 16 quants
+            const uint8_t *af = abase + (size_t)bo * ACT_BLOCK;   // + t * 512: N tile t
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint64_t dx01 = *reinterpret_cast<const uint64_t *>(dbase + bo * 16 + t * 8);
+                const uint4 b4 = *reinterpret_cast<const uint4 *>(af + t * 512);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16_16816(d, h0l, h1l, h0h, h1h, b4.x, b4.y);
+                mma_f16_16816(d, h2l, h3l, h2h, h3h, b4.z, b4.w);
+                scale_acc64(acc[t][0], d[0], d[1], dx01, dw0[h]);
+                scale_acc64(acc[t][1], d[2], d[3], dx01, dw8[h]);
+            }
+        }
+    }
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, const __grid_constant__ CUtensorMap tmap) {
     using namespace gv;
-    constexpr int AFR = NT * 16;                    // activation fragment bytes per lane per block (fp16)
-    constexpr int KA = (ACT_BYTES / (32 * AFR)) / KC * KC;   // blocks per activation chunk (96 or 48)
+    using M = Mode<MODE>;
+    constexpr int NT = M::NT;
+    constexpr int KA = M::KA;
+    constexpr int NACC = M::NACC;
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint8_t *act = smem + RING_BYTES;
     float *dxs = reinterpret_cast<float *>(act + ACT_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(dxs + DX_FLOATS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + NW * NSLOT);
+    uint64_t *full = reinterpret_cast<uint64_t *>(dxs + DX_FLOATS);
+    uint64_t *empty = full + NSLOT;
+    volatile uint32_t *armed = reinterpret_cast<volatile uint32_t *>(empty + NSLOT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(armed + NSLOT);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            armed[s] = 0xffffffffu;
+        }
+        fence_mbar_init();
     }
-    if (lane == 0)
-        for (int s = 0; s < NSLOT; ++s) mbar_init(&bars[warp * NSLOT + s], 1);
-    fence_mbar_init();
     __syncthreads();
 
+    if (warp == PRODUCER) {
+        const uint32_t planned = produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane);
+        // After a timed-out wait: let the copies still in flight land (with one
+        // overall time limit) before the CTA's shared memory goes away.
+        if (*abort_flag && lane == 0) {
+            const uint64_t t_end = global_timer_ns() + WAIT_LIMIT_NS;
+            const uint32_t first = planned > (uint32_t)NSLOT ? planned - NSLOT : 0u;
+            for (uint32_t q = first; q < planned; ++q) mbar_drain(&full[q % NSLOT], (q / NSLOT) & 1u, t_end);
+        }
+        return;
+    }
+
     const uint32_t nb = p.nb;
-    const uint32_t nslots_row = (nb + KC - 1) / KC;          // weight slots per row
+    const uint32_t nk = (nb + KC - 1) / KC;
     const int kachunks = (int)((nb + KA - 1) / KA);
-    uint8_t *myring = ring + (size_t)warp * NSLOT * SLOT;
-    uint64_t *mybar = bars + warp * NSLOT;
+    uint32_t seqbase = 0;
     bool waited_dep = false;
-    uint32_t qbase = 0;      // this warp's slots issued over all items (ring position and phase)
 
     for (int item_i = blockIdx.x;; item_i += gridDim.x) {
         GItem it;
-        if (!gemv_item<NT>(p, item_i, it)) break;
-        const int nsub = (int)((it.nrows + ROWS - 1) / ROWS);
-        int wpi = (int)p.wpi;
-        while (wpi > 1 && nsub * wpi > NW) wpi >>= 1;
-        const int slice = warp % wpi;                        // this warp's K slice
-        const int lane_group = warp / wpi;                   // which sub-item stream
-        const int ngroups = NW / wpi;
-        int my_nsub = 0;
-        for (int s = lane_group; s < nsub; s += ngroups) ++my_nsub;
-        if (my_nsub > SUBMAX) my_nsub = SUBMAX;              // the host keeps nsub <= ngroups*SUBMAX
-
-        // This warp streams, for k = slice, slice+wpi, ... (its K slice) and for
-        // each of its sub-items, one 16-row x KC-block slot.  Slot sequence
-        // number q (k-major, sub-items inner); the ring position and mbarrier
-        // phase come from the warp's running count gq = qbase + q.
-        const uint32_t my_k = (nslots_row > (uint32_t)slice) ? (nslots_row - slice + wpi - 1) / wpi : 0;
-        const uint32_t total = (uint32_t)my_nsub * my_k;
-        auto issue = [&](uint32_t q) {
-            if (lane == 0) {
-                const uint32_t kk = q / (uint32_t)my_nsub;
-                const int sub = (int)(q - kk * (uint32_t)my_nsub);
-                const uint32_t kslot = (uint32_t)slice + kk * (uint32_t)wpi;
-                const uint32_t gq = qbase + q;
-                const int slot = (int)(gq % NSLOT);
-                const uint32_t rs = it.r0 + (uint32_t)(lane_group + sub * ngroups) * ROWS;
-                mbar_arrive_expect_tx(&mybar[slot], SLOT);
-                tma_load_3d(myring + slot * SLOT, &tmap, (int)(kslot * (KC * QB / 4)), (int)rs, it.expert,
-                            &mybar[slot]);
-            }
-        };
-
-        uint64_t acc[SUBMAX][NT][2];   // packed fp32 pairs: [row g | row g+8] x tokens (2c, 2c+1)
-#pragma unroll
-        for (int s = 0; s < SUBMAX; ++s)
-#pragma unroll
-            for (int t = 0; t < NT; ++t) acc[s][t][0] = acc[s][t][1] = 0ull;
-
-        for (uint32_t q0 = 0; q0 < total && q0 < NSLOT; ++q0) issue(q0);
-        // The shared-memory ring holds only NSLOT slots per warp; ask L2 for all
-        // of this warp's remaining slots now, so that HBM sees the whole item's
-        // bytes at once and the ring refills from L2.
-        if (lane == 0) {
-            for (uint32_t q = NSLOT; q < total; ++q) {
-                const uint32_t kq = q / (uint32_t)my_nsub;
-                const int sub = (int)(q - kq * (uint32_t)my_nsub);
-                const uint32_t kslot = (uint32_t)slice + kq * (uint32_t)wpi;
-                const uint32_t rs = it.r0 + (uint32_t)(lane_group + sub * ngroups) * ROWS;
-                tma_prefetch_l2_3d(&tmap, (int)(kslot * (KC * QB / 4)), (int)rs, it.expert);
-            }
-        }
+        if (!gemv_item<M::TOKG>(p, item_i, it)) break;
+        const uint32_t nsub = (it.nrows + ROWS - 1) / ROWS;
+        const uint32_t wpi = item_wpi(nsub, nk);
+        const uint32_t ngroups = (uint32_t)NCW / wpi;
+        const uint32_t slice = (uint32_t)warp % wpi, grp = (uint32_t)warp / wpi;
         if (!waited_dep) {
             grid_dep_wait();      // activations are written by the preceding kernel
             waited_dep = true;
         }
 
-        uint32_t kk = 0;
+        float accf[SUBMAX][NACC];
+        uint64_t acc[SUBMAX][NT][2];
+#pragma unroll
+        for (int s2 = 0; s2 < SUBMAX; ++s2) {
+#pragma unroll
+            for (int e = 0; e < NACC; ++e) accf[s2][e] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[s2][t][0] = acc[s2][t][1] = 0ull;
+        }
+
+        uint32_t kk = slice;
         for (int ch = 0; ch < kachunks; ++ch) {
             const uint32_t kb0 = (uint32_t)ch * KA;
             const uint32_t ka = min((uint32_t)KA, nb - kb0);
-            // ---- stage this chunk's activation fragments (all warps), then sync
-            __syncthreads();
-            for (uint32_t e = threadIdx.x; e < ka * 32; e += NTHREADS) {
-                const uint32_t b = e >> 5, l = e & 31;
-                const uint32_t lg = l >> 2, lc = l & 3;
-                const bool even = ((kb0 + b) & 1u) == 0;
-                const int8_t *xr = p.qx + (uint64_t)(it.xrow0 + lg) * p.in_dim + (uint64_t)(kb0 + b) * QK;
-                uint4 *dst = reinterpret_cast<uint4 *>(act + ((size_t)b * 32 + l) * AFR);
-                // words of the activation block this lane's fragment is built from
-                //   odd block: words c, 4+c;  even block: x[4c+2..4c+5] from words c, c+1 and
-                //   x[4c+18..4c+21] from words c+4, c+5 (c < 3); lane 3: x[14..17] from words 3, 4
-                //   and [x0, x1, x30, x31] from words 0, 7.
-                const uint32_t i0 = even ? lc : lc;
-                const uint32_t i1 = even ? lc + 1 : 4 + lc;
-                const uint32_t i2 = lc < 3 ? lc + 4 : 0u;
-                const uint32_t i3 = lc < 3 ? lc + 5 : 7u;
+            named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);   // previous chunk or item done with act
+            stage_chunk<MODE>(p, it, kb0, ka, act, dxs);
+            named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
+            for (; kk < nk; kk += wpi) {
+                const uint32_t kb = kk * KC;
+                if (kb >= kb0 + ka) break;                     // belongs to the next chunk
+                const uint32_t bl0 = kb - kb0;
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
-                    const uint32_t w0 = __ldg(xt + i0), w1 = __ldg(xt + i1);
-                    uint32_t f0, f1;
-                    if (!even) {
-                        f0 = w0;
-                        f1 = w1;
-                    } else {
-                        const uint32_t w2 = __ldg(xt + i2), w3 = __ldg(xt + i3);
-                        f0 = funnel16(w0, w1);
-                        f1 = lc < 3 ? funnel16(w2, w3) : __byte_perm(w2, w3, 0x7610);
-                    }
-                    uint4 h;
-                    s8x4_to_h2x2(f0, h.x, h.y);   // MMA over the first quant group: b0, b1
-                    s8x4_to_h2x2(f1, h.z, h.w);   // MMA over the second quant group
-                    dst[t] = h;
-                }
-            }
-            for (uint32_t e = threadIdx.x; e < ka * 16; e += NTHREADS) {
-                const uint32_t b = e >> 4, t = e & 15;
-                dxs[e] = (t < (uint32_t)(NT * 8)) ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b) : 0.0f;
-            }
-            __syncthreads();
-            // ---- consume this warp's slots whose K lies in the chunk
-            for (; kk < my_k; ++kk) {
-                const uint32_t kb = ((uint32_t)slice + kk * (uint32_t)wpi) * KC;
-                if (kb >= kb0 + ka) break;                        // belongs to the next chunk
-#pragma unroll
-                for (int s = 0; s < SUBMAX; ++s) {
-                    if (s < my_nsub) {
-                        const uint32_t q = kk * (uint32_t)my_nsub + s;
-                        const uint32_t gq = qbase + q;
-                        const int slot = (int)(gq % NSLOT);
-                        mbar_wait(&mybar[slot], (gq / NSLOT) & 1u, p.err, abort_flag);
-                        const uint8_t *r0base = myring + slot * SLOT + g * SROW;
-                        const uint32_t bl0 = kb - kb0;                    // first block of the slot in the chunk
-                        const uint8_t *abase = act + ((size_t)bl0 * 32 + lane) * AFR;
-                        const float *dbase = dxs + bl0 * 16 + 2 * c;
-                        // Every slot holds KC = 8 blocks (nb % 8 == 0): 4 pairs.
-#pragma unroll
-                        for (uint32_t jp = 0; jp < KC / 2; ++jp) {
-                            const uint8_t *e0 = r0base + jp * (2 * QB);   // even block, row g
-                            const uint8_t *e8 = e0 + 8 * SROW;            // even block, row g+8
-                            uint32_t w[2][4];   // [block][row g lo, row g+8 lo, row g hi, row g+8 hi]
-                            {
-                                const uint32_t sel = c < 3 ? 0x3210u : 0x5432u;
-                                w[0][0] = lds32g(e0 + even_off_a(c));
-                                w[0][1] = lds32g(e8 + even_off_a(c));
-                                w[0][2] = __byte_perm(lds32g(e0 + even_off_b(c)), lds32g(e0 + 32), sel);
-                                w[0][3] = __byte_perm(lds32g(e8 + even_off_b(c)), lds32g(e8 + 32), sel);
-                            }
-                            w[1][0] = lds32g(e0 + QB + 2 + 4 * c);
-                            w[1][1] = lds32g(e8 + QB + 2 + 4 * c);
-                            w[1][2] = lds32g(e0 + QB + 18 + 4 * c);
-                            w[1][3] = lds32g(e8 + QB + 18 + 4 * c);
-                            uint64_t dw0[2], dw8[2];
-                            dw0[0] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e0)));
-                            dw8[0] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e8)));
-                            dw0[1] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e0 + QB)));
-                            dw8[1] = pack_same(half_bits_to_float(*reinterpret_cast<const uint16_t *>(e8 + QB)));
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const uint32_t bo = 2 * jp + h;                // block within the slot
-                                uint32_t h0l, h0h, h1l, h1h, h2l, h2h, h3l, h3h;
-                                s8x4_to_h2x2(w[h][0], h0l, h0h);     // row g,   first group
-                                s8x4_to_h2x2(w[h][1], h1l, h1h);     // row g+8, first group
-                                s8x4_to_h2x2(w[h][2], h2l, h2h);     // row g,   second group
-                                s8x4_to_h2x2(w[h][3], h3l, h3h);     // row g+8, second group
-                                const uint4 *af = reinterpret_cast<const uint4 *>(abase + (size_t)bo * 32 * AFR);
-#pragma unroll
-                                for (int t = 0; t < NT; ++t) {
-                                    const uint64_t dx01 = *reinterpret_cast<const uint64_t *>(dbase + bo * 16 + t * 8);
-                                    const uint4 b4 = af[t];
-                                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                                    mma_f16_16816(d, h0l, h1l, h0h, h1h, b4.x, b4.y);
-                                    mma_f16_16816(d, h2l, h3l, h2h, h3h, b4.z, b4.w);
-                                    scale_acc64(acc[s][t][0], d[0], d[1], dx01, dw0[h]);
-                                    scale_acc64(acc[s][t][1], d[2], d[3], dx01, dw8[h]);
-                                }
-                            }
+                for (int s2 = 0; s2 < SUBMAX; ++s2) {
+                    const uint32_t sub = grp + (uint32_t)s2 * ngroups;
+                    if (sub < nsub) {
+                        const uint32_t seq = seqbase + kk * nsub + sub;
+                        const uint32_t slot = seq % NSLOT;
+                        if (wait_armed(&armed[slot], seq / NSLOT, p.err, abort_flag))
+                            mbar_wait(&full[slot], (seq / NSLOT) & 1u, p.err, abort_flag);
+                        const uint8_t *sbase = ring + (size_t)slot * SLOT;
+                        if (MODE == 0) {
+                            float (&a8)[8] = *reinterpret_cast<float (*)[8]>(&accf[s2][0]);
+                            slot_dp4a(sbase, act, dxs, bl0, lane, a8, it.ntok > 1);
+                        } else {
+                            slot_mma<NT>(sbase, act, dxs, bl0, lane, acc[s2]);
                         }
-                        // slot consumed: refill it with the slot NSLOT ahead
                         __syncwarp();
-                        fence_proxy_async_smem();
-                        if (q + NSLOT < total) issue(q + NSLOT);
+                        if (lane == 0) mbar_arrive(&empty[slot]);
                     }
                 }
             }
         }
-        qbase += total;
+        seqbase += nk * nsub;
 
-        // ---- split-K partials (wpi > 1): add in slice order through shared memory
-        float accf[SUBMAX][NT][4];
+        if (MODE != 0) {
 #pragma unroll
-        for (int s = 0; s < SUBMAX; ++s)
+            for (int s2 = 0; s2 < SUBMAX; ++s2)
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                accf[s][t][0] = lo_of(acc[s][t][0]);
-                accf[s][t][1] = hi_of(acc[s][t][0]);
-                accf[s][t][2] = lo_of(acc[s][t][1]);
-                accf[s][t][3] = hi_of(acc[s][t][1]);
-            }
+                for (int t = 0; t < NT; ++t) {
+                    accf[s2][t * 4 + 0] = lo_of(acc[s2][t][0]);
+                    accf[s2][t * 4 + 1] = hi_of(acc[s2][t][0]);
+                    accf[s2][t * 4 + 2] = lo_of(acc[s2][t][1]);
+                    accf[s2][t * 4 + 3] = hi_of(acc[s2][t][1]);
+                }
+        }
+        // ---- split-K partials (wpi > 1): added in slice order through shared memory
         if (wpi > 1) {
-            __syncthreads();   // activation buffer reused for the partials
+            named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);   // act is reused for the partials
             float *red = reinterpret_cast<float *>(act);
             if (slice > 0) {
 #pragma unroll
-                for (int s = 0; s < SUBMAX; ++s)
+                for (int s2 = 0; s2 < SUBMAX; ++s2)
 #pragma unroll
-                    for (int t = 0; t < NT; ++t)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            red[(((warp * SUBMAX + s) * NT + t) * 4 + e) * 32 + lane] = accf[s][t][e];
+                    for (int e = 0; e < NACC; ++e) red[((warp * SUBMAX + s2) * NACC + e) * 32 + lane] = accf[s2][e];
             }
-            __syncthreads();
+            named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
             if (slice == 0) {
-                for (int k = 1; k < wpi; ++k) {
-                    const int w2 = warp + k;
+                for (uint32_t k = 1; k < wpi; ++k) {
+                    const int w2 = warp + (int)k;
 #pragma unroll
-                    for (int s = 0; s < SUBMAX; ++s)
+                    for (int s2 = 0; s2 < SUBMAX; ++s2)
 #pragma unroll
-                        for (int t = 0; t < NT; ++t)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                accf[s][t][e] += red[(((w2 * SUBMAX + s) * NT + t) * 4 + e) * 32 + lane];
+                        for (int e = 0; e < NACC; ++e) accf[s2][e] += red[((w2 * SUBMAX + s2) * NACC + e) * 32 + lane];
                 }
             }
         }
         // ---- outputs
-        if (slice == 0) {
+        if (MODE == 0) {
+            // add the 8 block columns of each row (lanes differing in bits 0-2)
 #pragma unroll
-            for (int s = 0; s < SUBMAX; ++s) {
-                if (s < my_nsub) {
-                    const uint32_t rs = it.r0 + (uint32_t)(lane_group + s * ngroups) * ROWS;
+            for (int s2 = 0; s2 < SUBMAX; ++s2)
+#pragma unroll
+                for (int e = 0; e < NACC; ++e) {
+                    float v = accf[s2][e];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    accf[s2][e] = v;
+                }
+            if (slice == 0 && (lane & 7) == 0) {
+                const int rb = lane >> 3;
+#pragma unroll
+                for (int s2 = 0; s2 < SUBMAX; ++s2) {
+                    const uint32_t sub = grp + (uint32_t)s2 * ngroups;
+                    if (sub < nsub) {
+                        const uint32_t rs = it.r0 + sub * ROWS;
+#pragma unroll
+                        for (int e = 0; e < NACC; ++e) {
+                            const int tok = e >> 2;
+                            const uint32_t row = rs + (uint32_t)dp4a_row(rb, e & 3);
+                            if (tok < it.ntok && row < it.r0 + it.nrows) {
+                                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok]
+                                                            : (int64_t)(it.tok0 + tok);
+                                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + row] = accf[s2][e];
+                            }
+                        }
+                    }
+                }
+            }
+        } else if (slice == 0) {
+            const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+            for (int s2 = 0; s2 < SUBMAX; ++s2) {
+                const uint32_t sub = grp + (uint32_t)s2 * ngroups;
+                if (sub < nsub) {
+                    const uint32_t rs = it.r0 + sub * ROWS;
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -444,14 +666,13 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                             if (tok < it.ntok && row < it.r0 + it.nrows) {
                                 const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok]
                                                             : (int64_t)(it.tok0 + tok);
-                                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + row] = accf[s][t][e];
+                                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + row] = accf[s2][t * 4 + e];
                             }
                         }
                     }
                 }
             }
         }
-        __syncthreads();   // item boundary: activation buffer reuse
     }
     if (!waited_dep) grid_dep_wait();
 }
@@ -459,13 +680,14 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
                       uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
-cudaError_t launch_gemv(const GemvParams &p, bool two_tiles, int grid, cudaStream_t st) {
-    static bool attr_done[2] = {false, false};
-    const void *fn = two_tiles ? (const void *)k_gemv<2> : (const void *)k_gemv<1>;
-    if (!attr_done[two_tiles]) {
+cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st) {
+    static bool attr_done[3] = {false, false, false};
+    if (mode < 0 || mode > 2) return cudaErrorInvalidValue;
+    const void *fn = mode == 0 ? (const void *)k_gemv<0> : (mode == 1 ? (const void *)k_gemv<1> : (const void *)k_gemv<2>);
+    if (!attr_done[mode]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gv::SMEM);
         if (e != cudaSuccess) return e;
-        attr_done[two_tiles] = true;
+        attr_done[mode] = true;
     }
     alignas(64) CUtensorMap tmap;
     const uint64_t row_bytes = (uint64_t)p.nb * QB;

@@ -71,7 +71,8 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
                          int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
                          int num_sms, cudaStream_t st);
 
-// Weight-streaming GEMV for token groups of <= 8 (int8 MMA) or <= 16 (fp16 MMA) (q8_gemv.cu).
+// Weight-streaming GEMV (q8_gemv.cu).  Modes: 0 = dp4a, token groups of <= 2;
+// 1 = fp16 MMA, one 8-token N tile; 2 = two N tiles (<= 16 tokens).
 struct GemvParams {
     const uint8_t *W;
     uint64_t expert_stride;
@@ -83,14 +84,24 @@ struct GemvParams {
     float *out;
     int *err;
     uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
-    uint32_t rows_per_item;    // multiple of 16, <= 512
-    uint32_t wpi;              // warps per 16-row sub-item (1, 2, 4, 8)
+    uint32_t rows_per_item;    // grouped: rows per item, multiple of 16, <= 512
+    uint32_t n_items;          // dense: items (contiguous runs of 16-row sub-items, <= 32 each)
     const PlanHeader *plan;    // grouped: class plan; nullptr: dense
     const int32_t *row_to_out;
     uint32_t n_expert;         // grouped: number of expert matrices
 };
 constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
-cudaError_t launch_gemv(const GemvParams &p, bool f16, int grid, cudaStream_t st);
+cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st);
+inline int gemv_mode(uint64_t n_tok) { return n_tok <= 2 ? 0 : (n_tok <= 8 ? 1 : 2); }
+// Dense items: one per SM while there are enough 16-row sub-items, each at most
+// GEMV_MAX_ROWS_PER_ITEM rows.
+inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
+    const uint64_t nsub = (out_dim + 15) / 16;
+    const uint64_t per = GEMV_MAX_ROWS_PER_ITEM / 16;
+    uint64_t items = nsub < (uint64_t)num_sms ? nsub : (uint64_t)num_sms;
+    if (items * per < nsub) items = (nsub + per - 1) / per;
+    return (uint32_t)items;
+}
 
 // Prefill GEMM on tcgen05 (q8_tc.cu).  Weights as an fp16 plane [M][K] (from
 // launch_tc_expand) with block-major scales dwT[nb][m_ld]; activations as an

@@ -108,18 +108,10 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
         g.out = out;
         g.err = err;
         g.n_tok = (uint32_t)n_tok;
-        uint64_t r = (out_dim + d->num_sms - 1) / d->num_sms;
-        r = (r + 15) & ~(uint64_t)15;
-        if (r < 16) r = 16;
-        if (r > q8::GEMV_MAX_ROWS_PER_ITEM) r = q8::GEMV_MAX_ROWS_PER_ITEM;
-        g.rows_per_item = (uint32_t)r;
-        uint32_t wpi = 1;
-        while (wpi < 16 && (g.rows_per_item / 16) * wpi * 2 <= 16) wpi *= 2;
-        g.wpi = wpi;
+        g.n_items = q8::gemv_dense_items(out_dim, d->num_sms);
         g.n_expert = 1;
-        const uint64_t items = (out_dim + r - 1) / r;
-        const int grid = (int)(items < (uint64_t)d->num_sms ? items : (uint64_t)d->num_sms);
-        return q8::launch_gemv(g, n_tok > 8, grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+        const int grid = (int)(g.n_items < (uint32_t)d->num_sms ? g.n_items : (uint32_t)d->num_sms);
+        return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
     }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
