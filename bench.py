@@ -173,7 +173,10 @@ def tensor_peak():
         return 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_hash(files=("q8_mma.cu", "q8_common.cuh")) -> str:
+GEMV_FILES = ("q8_gemv.cu", "q8_common.cuh", "q8_quant.cuh", "q8_kernels.h")
+
+
+def kernel_source_hash(files=GEMV_FILES) -> str:
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "q8_quantized_matmul_gb300", "csrc", f), "rb") as fh:
@@ -187,7 +190,7 @@ def committed_traffic(kernel: str):
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
         e = d[kernel]
-        if e.get("source_hash") != kernel_source_hash(tuple(e.get("files", ("q8_mma.cu", "q8_common.cuh")))):
+        if e.get("source_hash") != kernel_source_hash(tuple(e.get("files", GEMV_FILES))):
             return None
         return e
     except (OSError, KeyError, ValueError):
@@ -254,14 +257,8 @@ def run_ours(args, rank, world, local, dist):
                     call(n, copies[g * n_calls + c])
             gs.append(cg)
         return gs
-    q8.q8_profile_arm(0)
     graphs = capture()                       # the step as the bench times it
-    q8.q8_profile_arm(n_graphs * n_calls)
-    graphs_ev = capture()                    # the same step with timing events around each matmul kernel
-    assert q8.q8_profile_used() == n_graphs * n_calls
-
     graph_replays(torch, stream, graphs, max(args.warmup, n_graphs))   # every graph runs at least once
-    graph_replays(torch, stream, graphs_ev, n_graphs)
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(local if world > 1 else (torch.cuda.current_device())) as clk:
@@ -269,39 +266,52 @@ def run_ours(args, rank, world, local, dist):
     torch.cuda.synchronize(dev)
     barrier(dist)
     ms = max_over_ranks(dist, ms)
-    # kernel times: a second timed loop of the instrumented step; the events of
-    # the last replay of every graph are read
-    graph_replays(torch, stream, graphs_ev, max(args.steps, n_graphs))
     assert q8.q8_last_error(stream) == 0
-    kern = {n: [] for n in N_TOKS}
-    for g in range(n_graphs):
-        for c, n in enumerate(N_TOKS):
-            kern[n].append(q8.q8_profile_read(g * n_calls + c))
-    q8.q8_profile_arm(0)
+
+    # Kernel-level timing: per token count, a graph of back-to-back calls, each on
+    # its own weight copy, replayed; per-call time = replay time / calls.  For
+    # n_tok <= 8 a call is one GEMV launch (it quantises the activations itself);
+    # for n_tok = 16 it is the quantiser kernel plus the GEMV behind it (PDL).
+    per_call = {}
+    for n in N_TOKS:
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            for c in copies:
+                call(n, c)
+        graph_replays(torch, stream, [cg], 2)
+        reps = 8
+        per_call[n] = graph_replays(torch, stream, [cg], reps) / (reps * len(copies))
+        del cg
+    assert q8.q8_last_error(stream) == 0
 
     ms_step = ms / args.steps
     step_bytes = W_BYTES * n_calls
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     tokens_per_s = world * sum(N_TOKS) / (ms_step * 1e-3)
 
-    # algorithmic bytes of the matmul kernel per launch: weights + activation planes + outputs
+    # algorithmic bytes of one call: weights, fp32 activations, fp32 outputs, and
+    # for 16 tokens the activation planes written by the quantiser and read back
     def kbytes(n):
-        npad = (n + 15) // 16 * 16
-        return W_BYTES + npad * IN_DIM + npad * (IN_DIM // QK) * 4 + n * OUT_DIM * 4
-    mean_k = {n: statistics.mean(v) for n, v in kern.items()}
+        b = W_BYTES + n * IN_DIM * 4 + n * OUT_DIM * 4
+        if n > 8:
+            npad = (n + 15) // 16 * 16
+            b += 2 * (npad * IN_DIM + npad * (IN_DIM // QK) * 4)
+        return b
     tot_bytes = sum(kbytes(n) for n in N_TOKS)
-    tot_ms = sum(mean_k.values())
+    tot_ms = sum(per_call.values())
     peak, peak_kind = hbm_peak()
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
-    tr = committed_traffic("k_mma decode sweep")
-    roofline = {"bound": "hbm", "kernel": "q8::k_mma", "achieved": round(achieved, 1), "peak": peak,
+    tr = committed_traffic("k_gemv decode sweep")
+    roofline = {"bound": "hbm", "kernel": "q8::k_gemv", "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "algorithmic_bytes_per_launch": round(tot_bytes / n_calls),
-                "per_n": {str(n): {"kernel_us": round(mean_k[n] * 1e3, 2),
-                                   "weight_gbs": round(W_BYTES / (mean_k[n] * 1e-3) / 1e9, 1),
-                                   "frac_of_peak": round(kbytes(n) / (mean_k[n] * 1e-3) / 1e9 / peak, 4)}
+                "timing": "graph of back-to-back calls per token count, CUDA events around the replays",
+                "per_n": {str(n): {"us_per_call": round(per_call[n] * 1e3, 2),
+                                   "launches_per_call": 1 if n <= 8 else 2,
+                                   "weight_gbs": round(W_BYTES / (per_call[n] * 1e-3) / 1e9, 1),
+                                   "frac_of_peak": round(kbytes(n) / (per_call[n] * 1e-3) / 1e9 / peak, 4)}
                           for n in N_TOKS}}
 
     # ---- end to end through the public API with pinned host buffers
@@ -341,14 +351,15 @@ def run_ours(args, rank, world, local, dist):
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {len(copies)} weight copies ({len(copies) * W_BYTES / 2 ** 20:.0f} MiB) "
                          f"rotated, each call reads its own copy (L2 {l2 / 2 ** 20:.0f} MiB)",
-                   "launch": "CUDA graph replay of the step (3 x [quantise + matmul])",
+                   "launch": "CUDA graph replay of the step (n_tok 1 and 4: one fused GEMV kernel each; "
+                             "n_tok 16: quantiser + GEMV)",
                    "tokens_per_s": round(tokens_per_s, 1)},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * n_calls * 2,
+        "gpu_launches": args.steps * sum(1 if n <= 8 else 2 for n in N_TOKS),
         "clocks": clk.summary(),
     }
-    del copies, graphs, graphs_ev
+    del copies, graphs
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_secondary:
         result["secondary"] = secondary(args, torch, q8, dev, stream, l2)
@@ -387,20 +398,18 @@ def secondary(args, torch, q8, dev, stream, l2):
         for c in copies:
             q8.q8_matmul(o, c, 4096, 1024, x, 1, stream)
     stream.synchronize()
-    q8.q8_profile_arm(len(copies))
     cg = torch.cuda.CUDAGraph()
     with torch.cuda.graph(cg, stream=stream):
         for c in copies:
             q8.q8_matmul(o, c, 4096, 1024, x, 1, stream)
     graph_replays(torch, stream, [cg], 3)
-    ms = graph_replays(torch, stream, [cg], 20) / len(copies)
-    kms = prof_mean(len(copies))
-    q8.q8_profile_arm(0)
+    ms = graph_replays(torch, stream, [cg], 20) / (20 * len(copies))
     wb = W.nbytes
     out.append({"workload": "single matvec (attn_q_a shape) in 4096 -> out 1024, n_tok 1",
                 "ms_per_call": round(ms, 5), "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1),
-                "kernel_us": round(kms * 1e3, 2), "kernel_weight_gbs": round(wb / (kms * 1e-3) / 1e9, 1),
-                "kernel_frac_of_hbm_peak": round(wb / (kms * 1e-3) / 1e9 / hbm, 4)})
+                "launches_per_call": 1,
+                "frac_of_hbm_peak": round(wb / (ms * 1e-3) / 1e9 / hbm, 4),
+                "timing": "graph of back-to-back calls, each on its own weight copy"})
     del copies, cg
 
     # prefill GEMMs (attn_output_a and shared-expert shapes) at n_tok = 512

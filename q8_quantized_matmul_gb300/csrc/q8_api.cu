@@ -164,9 +164,10 @@ int check_dims(uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
     return Q8_OK;
 }
 
-// out = W x from activation planes already in scratch (n_pad rows).
+// out = W x from activation planes already in scratch (n_pad rows), or, with
+// x_fused given, from the fp32 rows quantised inside the GEMV.
 int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const int8_t *qx,
-              const float *dx, uint64_t n_tok, cudaStream_t st) {
+              const float *dx, const float *x_fused, uint64_t n_tok, cudaStream_t st) {
     const uint32_t nb = (uint32_t)(in_dim / q8::QK);
     if (nb % 8 == 0 && n_tok <= 16) {
         q8::GemvParams g{};
@@ -177,6 +178,7 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.nb = nb;
         g.qx = qx;
         g.dx = dx;
+        g.x = x_fused;
         g.out = out;
         g.err = s->err;
         g.n_tok = (uint32_t)n_tok;
@@ -185,7 +187,7 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.row_to_out = nullptr;
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)s->num_sms ? g.n_items : (uint32_t)s->num_sms);
-        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st); }));
+        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), x_fused == nullptr, grid, st); }));
     }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
@@ -319,6 +321,9 @@ static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t ou
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t nb = in_dim / q8::QK;
     if (n_tok > 16 && nb % 2 == 0) return run_tc(s, out, W, in_dim, out_dim, x, xq, n_tok, st);
+    // small activations: one kernel, the GEMV quantises them itself
+    if (x && nb % 8 == 0 && q8::gemv_fuses_quantiser(n_tok, nb))
+        return run_dense(s, out, W, in_dim, out_dim, nullptr, nullptr, x, n_tok, st);
     const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
     if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
     Carver cv(s->scratch);
@@ -328,7 +333,7 @@ static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t ou
                       : q8::launch_unpack_blocks(qx, dx, static_cast<const uint8_t *>(xq), in_dim, n_pad, n_tok,
                                                  s->num_sms, st);
     if (e != cudaSuccess) return Q8_ECUDA;
-    return run_dense(s, out, W, in_dim, out_dim, qx, dx, n_tok, st);
+    return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st);
 }
 
 int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x, uint64_t n_tok,
@@ -422,10 +427,10 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     g.n_expert = n_expert;
     return status_of(timed_launch(st, [&] {
         g.plan = plan_of(0);
-        cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
+        cudaError_t e2 = q8::launch_gemv(g, 1, true, s->num_sms, st);
         if (e2 != cudaSuccess) return e2;
         g.plan = plan_of(1);
-        if ((e2 = q8::launch_gemv(g, 2, s->num_sms, st)) != cudaSuccess) return e2;
+        if ((e2 = q8::launch_gemv(g, 2, true, s->num_sms, st)) != cudaSuccess) return e2;
         p.plan = plan_of(2);
         return q8::launch_mma(p, s->num_sms, st);
     }));

@@ -46,18 +46,23 @@
 //     2^14, block sums below 2^24); it is then scaled by d_w*d_x and added in
 //     fp32 with packed f32x2 instructions.  fp16 rather than int8 MMA: on GB300
 //     mma.sync runs int8 at 251 and fp16 at 942 MAC per SM per clock (measured).
-//   * Launched with programmatic stream serialisation: the weight stream starts
-//     before the preceding quantiser kernel has finished; activations are read
-//     only after griddepcontrol.wait.
+//   * Small activations (at most 1024 token-block pairs per CTA) are quantised
+//     by the consumer warps themselves from the fp32 rows, with the quantiser
+//     kernels' arithmetic: one kernel per call, launched in stream order.
+//     Otherwise the quantiser kernel writes activation planes first and this
+//     kernel is launched behind it with programmatic stream serialisation: the
+//     weight stream starts while the quantiser runs (it writes nothing the
+//     weights depend on), activations are read only after griddepcontrol.wait.
 #include <cuda.h>
 
 #include "q8_common.cuh"
 #include "q8_kernels.h"
+#include "q8_quant.cuh"
 
 namespace q8 {
 
 namespace gv {
-constexpr int NCW = 16;                          // consumer warps
+constexpr int NCW = 14;                          // consumer warps (15 warps: 128 registers each)
 constexpr int PRODUCER = NCW;                    // warp index of the TMA producer
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr int CONSUMER_THREADS = NCW * 32;
@@ -67,11 +72,12 @@ constexpr int BOX_WORDS = (KC * QB + 32) / 4;    // 76 words per row of a slot
 constexpr int SROW = BOX_WORDS * 4;              // 304 bytes: 19 x 16, an odd multiple of 16
 constexpr int SLOT = ROWS * SROW;                // 4864 bytes
 constexpr int NSLOT = 32;                        // CTA ring depth
-constexpr int SUBMAX = 512 / (NCW * 16);         // sub-items per warp per CTA item
+constexpr int SUBMAX = (512 + NCW * 16 - 1) / (NCW * 16);   // sub-items per warp per CTA item
 constexpr int ACT_BYTES = 40 * 1024;             // staged activations per chunk
 constexpr int DX_FLOATS = 1280;                  // staged activation scales per chunk
 constexpr int RING_BYTES = NSLOT * SLOT;
-constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + 2 * NSLOT * 8 + NSLOT * 4 + 16;
+constexpr int QT_BYTES = 20736;                  // fused quantiser: natural-order quants of a chunk
+constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + QT_BYTES + 2 * NSLOT * 8 + NSLOT * 4 + 16;
 constexpr int BAR_CONSUMERS = 1;                 // named barrier of the consumer warps
 static_assert(SMEM <= 227 * 1024, "shared memory");
 static_assert(NSLOT >= 32, "one producer lane per slot of a batch");
@@ -85,7 +91,9 @@ template <int MODE> struct Mode {
     static constexpr int KA = (ACT_BYTES / ACT_BLOCK) / KC * KC;    // blocks per chunk (512, 80, 40)
     static constexpr int NACC = MODE == 0 ? 8 : NT * 4;             // fp32 results per lane and sub-item
     static_assert(KA * DXW <= DX_FLOATS, "scale buffer");
-    static_assert(NCW * SUBMAX * NACC * 32 * 4 <= ACT_BYTES, "split-K buffer");
+    static_assert(NCW * NACC * 32 * 4 <= ACT_BYTES, "split-K buffer");
+    static constexpr int QT_STRIDE = KA * QK + 16;                  // fused: bytes per token row of a chunk
+    static_assert(MODE == 0 || TOKG * QT_STRIDE <= QT_BYTES, "fused quantiser buffer");
 };
 }  // namespace gv
 
@@ -225,10 +233,11 @@ __device__ __forceinline__ bool wait_armed(volatile uint32_t *armed, uint32_t r,
 }
 
 // Warps per sub-item for an item of nsub sub-items and nk K slots: the largest
-// power of two that keeps every consumer warp on at most one sub-item group.
+// power of two dividing the consumer count with every sub-item on its own
+// group of wpi warps (so with wpi > 1 each warp holds one sub-item).
 __device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
     uint32_t wpi = 1;
-    while (nsub * wpi * 2 <= (uint32_t)gv::NCW && wpi * 2 <= nk) wpi *= 2;
+    while (gv::NCW % (wpi * 2) == 0 && nsub * wpi * 2 <= (uint32_t)gv::NCW && wpi * 2 <= nk) wpi *= 2;
     return wpi;
 }
 
@@ -384,6 +393,99 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
     }
 }
 
+// Fused quantiser (dense path, x given): the CTA quantises tokens 0..TOKG-1 of
+// chunk [kb0, kb0 + ka) from the fp32 rows itself, with the arithmetic of the
+// quantiser kernels (four lanes per block), and writes the mode's layout.
+// Rows past n_tok are quantised from zeros (q = 0, d = 0).  Loads are issued
+// two rounds at a time before they are used.
+template <int MODE>
+__device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GItem &it, uint32_t kb0, uint32_t ka,
+                                                  uint8_t *act, float *dxs, uint8_t *qtmp) {
+    using namespace gv;
+    using M = Mode<MODE>;
+    constexpr uint32_t TOKQ = M::TOKG;
+    constexpr uint32_t GROUPS = CONSUMER_THREADS / 4;
+    const uint32_t lane_q = threadIdx.x & 3u;
+    const uint32_t npair = ka * TOKQ;                     // (token, block) pairs, token-major
+    const uint32_t rounds = (npair + GROUPS - 1) / GROUPS;
+    for (uint32_t r0 = 0; r0 < rounds; r0 += 2) {
+        float xv[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
+            const uint32_t t = pr / ka, b = pr - t * ka;
+            if (pr < npair && t < (uint32_t)it.ntok)
+                load8(xv[h], p.x + (uint64_t)t * p.in_dim + (uint64_t)(kb0 + b) * QK + lane_q * 8);
+            else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) xv[h][i] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
+            const uint32_t t = pr / ka, b = pr - t * ka;
+            const QuantBlock qb = quantize8(xv[h]);   // all lanes: the block maximum is shuffled
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
+                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
+            }
+            if (MODE == 0) {
+                // lane q holds words X[2q] = lo, X[2q+1] = hi; arrange as in stage_chunk
+                const uint32_t nbw = __shfl_sync(0xffffffffu, lo, (threadIdx.x & ~3u) | ((lane_q + 1) & 3u));
+                if (pr < npair && r0 + h < rounds) {
+                    uint32_t *dst = reinterpret_cast<uint32_t *>(act + (size_t)b * M::ACT_BLOCK + t * 32);
+                    if ((kb0 + b) & 1u) {
+                        dst[2 * lane_q + 1] = lo;
+                        dst[(2 * lane_q + 2) & 7u] = hi;
+                    } else {
+                        dst[2 * lane_q + 1] = funnel16(lo, hi);
+                        if (lane_q < 3) dst[2 * lane_q + 2] = funnel16(hi, nbw);
+                        else dst[0] = __byte_perm(nbw, hi, 0x7610);
+                    }
+                    if (lane_q == 0) dxs[b * 2 + t] = qb.d_stored;
+                }
+            } else {
+                if (pr < npair && r0 + h < rounds) {
+                    *reinterpret_cast<uint2 *>(qtmp + (size_t)t * M::QT_STRIDE + (size_t)b * QK + lane_q * 8) =
+                        make_uint2(lo, hi);
+                    if (lane_q == 0) dxs[b * 16 + t] = qb.d_stored;
+                }
+            }
+        }
+    }
+    if (MODE == 0) return;
+    named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
+    // natural-order quants -> MMA B fragments, as stage_chunk does from the planes
+    constexpr int NT = M::NT;
+    for (uint32_t e = threadIdx.x; e < ka * 32; e += CONSUMER_THREADS) {
+        const uint32_t b = e >> 5, l = e & 31, lg = l >> 2, lc = l & 3;
+        const bool even = ((kb0 + b) & 1u) == 0;
+        const uint32_t i1 = even ? lc + 1 : 4 + lc;
+        const uint32_t i2 = lc < 3 ? lc + 4 : 0u;
+        const uint32_t i3 = lc < 3 ? lc + 5 : 7u;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t *xt = reinterpret_cast<const uint32_t *>(qtmp + (size_t)(lg + 8 * t) * M::QT_STRIDE +
+                                                                    (size_t)b * QK);
+            uint32_t f0, f1;
+            if (!even) {
+                f0 = xt[lc];
+                f1 = xt[i1];
+            } else {
+                f0 = funnel16(xt[lc], xt[i1]);
+                f1 = lc < 3 ? funnel16(xt[i2], xt[i3]) : __byte_perm(xt[i2], xt[i3], 0x7610);
+            }
+            uint4 hh;
+            s8x4_to_h2x2(f0, hh.x, hh.y);
+            s8x4_to_h2x2(f1, hh.z, hh.w);
+            *reinterpret_cast<uint4 *>(act + (size_t)b * M::ACT_BLOCK + (size_t)t * 512 + (size_t)l * 16) = hh;
+        }
+    }
+}
+
 // dp4a mode, one slot: lane = (row group rb, block column j).  Each row's
 // block dot is 8 dp4a over the weight words as they lie in shared memory, the
 // activation words having been arranged to match; one byte permute forms the
@@ -493,7 +595,8 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     uint8_t *ring = smem;
     uint8_t *act = smem + RING_BYTES;
     float *dxs = reinterpret_cast<float *>(act + ACT_BYTES);
-    uint64_t *full = reinterpret_cast<uint64_t *>(dxs + DX_FLOATS);
+    uint8_t *qtmp = reinterpret_cast<uint8_t *>(dxs + DX_FLOATS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(qtmp + QT_BYTES);
     uint64_t *empty = full + NSLOT;
     volatile uint32_t *armed = reinterpret_cast<volatile uint32_t *>(empty + NSLOT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(armed + NSLOT);
@@ -556,7 +659,8 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             const uint32_t kb0 = (uint32_t)ch * KA;
             const uint32_t ka = min((uint32_t)KA, nb - kb0);
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);   // previous chunk or item done with act
-            stage_chunk<MODE>(p, it, kb0, ka, act, dxs);
+            if (p.x) stage_chunk_fused<MODE>(p, it, kb0, ka, act, dxs, qtmp);
+            else stage_chunk<MODE>(p, it, kb0, ka, act, dxs);
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
             for (; kk < nk; kk += wpi) {
                 const uint32_t kb = kk * KC;
@@ -596,24 +700,21 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                     accf[s2][t * 4 + 3] = hi_of(acc[s2][t][1]);
                 }
         }
-        // ---- split-K partials (wpi > 1): added in slice order through shared memory
+        // ---- split-K partials (wpi > 1, one sub-item per warp): added in slice
+        // order through shared memory
         if (wpi > 1) {
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);   // act is reused for the partials
             float *red = reinterpret_cast<float *>(act);
             if (slice > 0) {
 #pragma unroll
-                for (int s2 = 0; s2 < SUBMAX; ++s2)
-#pragma unroll
-                    for (int e = 0; e < NACC; ++e) red[((warp * SUBMAX + s2) * NACC + e) * 32 + lane] = accf[s2][e];
+                for (int e = 0; e < NACC; ++e) red[(warp * NACC + e) * 32 + lane] = accf[0][e];
             }
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
             if (slice == 0) {
                 for (uint32_t k = 1; k < wpi; ++k) {
                     const int w2 = warp + (int)k;
 #pragma unroll
-                    for (int s2 = 0; s2 < SUBMAX; ++s2)
-#pragma unroll
-                        for (int e = 0; e < NACC; ++e) accf[s2][e] += red[((w2 * SUBMAX + s2) * NACC + e) * 32 + lane];
+                    for (int e = 0; e < NACC; ++e) accf[0][e] += red[(w2 * NACC + e) * 32 + lane];
                 }
             }
         }
@@ -680,7 +781,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
                       uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
-cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st) {
+cudaError_t launch_gemv(const GemvParams &p, int mode, bool after_quantiser, int grid, cudaStream_t st) {
     static bool attr_done[3] = {false, false, false};
     if (mode < 0 || mode > 2) return cudaErrorInvalidValue;
     const void *fn = mode == 0 ? (const void *)k_gemv<0> : (mode == 1 ? (const void *)k_gemv<1> : (const void *)k_gemv<2>);
@@ -704,7 +805,7 @@ cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_quantiser ? 1 : 0;
     GemvParams pp = p;
     void *args[] = {&pp, &tmap};
     return cudaLaunchKernelExC(&cfg, fn, args);

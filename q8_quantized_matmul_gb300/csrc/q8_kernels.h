@@ -81,6 +81,7 @@ struct GemvParams {
     uint32_t nb;
     const int8_t *qx;          // activation quant plane [rows][in_dim] (groups padded to 16 rows)
     const float *dx;           // activation scale plane [rows][nb]
+    const float *x;            // dense only: fp32 rows [n_tok][in_dim] quantised in the kernel (qx, dx unused)
     float *out;
     int *err;
     uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
@@ -91,8 +92,19 @@ struct GemvParams {
     uint32_t n_expert;         // grouped: number of expert matrices
 };
 constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
-cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st);
+// after_quantiser: launched with programmatic stream serialisation behind this
+// library's quantiser kernel (the weights stream while it runs; activations are
+// read after griddepcontrol.wait).  Otherwise an ordinary launch.
+cudaError_t launch_gemv(const GemvParams &p, int mode, bool after_quantiser, int grid, cudaStream_t st);
 inline int gemv_mode(uint64_t n_tok) { return n_tok <= 2 ? 0 : (n_tok <= 8 ? 1 : 2); }
+// The dense GEMV quantises the activations itself when each CTA's share of that
+// work stays small: at most 8 tokens and 1024 (token, block) pairs with the
+// mode's token count.  (At 16 tokens the in-kernel quantiser delays the first
+// MMA by more than the separate quantiser kernel costs.)
+inline bool gemv_fuses_quantiser(uint64_t n_tok, uint64_t nb) {
+    const uint64_t tok = n_tok <= 2 ? 2 : 8;
+    return n_tok <= 8 && tok * nb <= 1024;
+}
 // Dense items: one per SM while there are enough 16-row sub-items, each at most
 // GEMV_MAX_ROWS_PER_ITEM rows.
 inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {

@@ -141,6 +141,22 @@ def test_matmul_q_matches_matmul_bitwise(q8, o):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("n_tok,in_dim,out_dim", [(1, 256, 100), (2, 1024, 333), (3, 512, 64), (8, 1024, 1000),
+                                                   (8, 4096, 150), (5, 2048, 4100), (1, 16384, 40), (2, 8192, 77)])
+def test_fused_quantiser_matches_planes_bitwise(q8, n_tok, in_dim, out_dim):
+    """Small dense calls quantise inside the GEMV; q8_matmul_q feeds the same GEMV
+    from quantiser-kernel output.  Any difference in a quant or a scale (ties,
+    subnormal and underflowing scales included) changes the result bits."""
+    g = np.random.default_rng(in_dim + n_tok)
+    W = dev(inputs.weights(out_dim, in_dim, seed=11))
+    # special blocks reach binary16 overflow (inf scales, inf/nan outputs): compare bit patterns
+    for xh in (inputs.normal((n_tok, in_dim), seed=n_tok, p_out=0.01), _special_x(g, n_tok, in_dim)):
+        x = dev(xh)
+        a = q8.matmul(W, x, out_dim)
+        b = q8.matmul_q(W, q8.quantize_act(x), in_dim, out_dim)
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_integer_case_exact(q8):
     """All scales 1.0 and activations that quantise to themselves: exact integer product."""
     g = np.random.default_rng(3)
@@ -368,12 +384,16 @@ def test_empty_and_tiny(q8, o):
 
 def test_scratch_alloc_failure_reports_enomem(q8):
     W = dev(inputs.weights(64, 256, seed=81))
-    x = dev(inputs.normal((8, 256), seed=82))
-    out = torch.empty((8, 64), device=DEV)
+    x = dev(inputs.normal((20, 256), seed=82))
+    out = torch.empty((20, 64), device=DEV)
     q8.q8_release()
     assert q8.q8_scratch_bytes() == 0
-    q8.q8_debug_fail_next_alloc(1)
-    assert q8.q8_matmul(out, W, 256, 64, x, 8) == q8.Q8_ENOMEM
+    # a small decode call quantises inside the GEMV and needs no scratch
     assert q8.q8_matmul(out, W, 256, 64, x, 8) == 0
+    assert q8.q8_scratch_bytes() == 0
+    # 20 tokens take the tensor-core path, whose operands live in scratch
+    q8.q8_debug_fail_next_alloc(1)
+    assert q8.q8_matmul(out, W, 256, 64, x, 20) == q8.Q8_ENOMEM
+    assert q8.q8_matmul(out, W, 256, 64, x, 20) == 0
     assert q8.q8_scratch_bytes() > 0
     torch.cuda.synchronize()
