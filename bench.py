@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--full", action="store_true", help="also measure the long-prefill layer slice")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=("decode1", "decode16", "prefill", "moe"),
+    ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "moe"),
                     help="run one workload's call a few times without timing (for ncu captures)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -526,8 +526,8 @@ def profile_case(case: str):
     import q8_quantized_matmul_gb300 as q8
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if case in ("decode1", "decode16"):
-        n = 1 if case == "decode1" else 16
+    if case in ("decode1", "decode4", "decode16"):
+        n = int(case[len("decode"):])
         W = torch.from_numpy(inputs.weights(OUT_DIM, IN_DIM, seed=0)).to(dev)
         x = torch.from_numpy(inputs.normal((n, IN_DIM), seed=0, p_out=0.01, out_scale=20.0)).to(dev)
         fn = lambda: q8.matmul(W, x, OUT_DIM)

@@ -187,7 +187,8 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.row_to_out = nullptr;
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)s->num_sms ? g.n_items : (uint32_t)s->num_sms);
-        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), x_fused == nullptr, grid, st); }));
+        g.weights_early = x_fused ? 0 : 1;   // planes: the preceding kernel is the quantiser
+        return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st); }));
     }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
@@ -423,14 +424,15 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     g.err = s->err;
     g.n_tok = 0;
     g.rows_per_item = rows_gemv;
+    g.weights_early = 1;   // behind the quantiser, then behind the previous class's GEMV
     g.row_to_out = row_to_out;
     g.n_expert = n_expert;
     return status_of(timed_launch(st, [&] {
         g.plan = plan_of(0);
-        cudaError_t e2 = q8::launch_gemv(g, 1, true, s->num_sms, st);
+        cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
         if (e2 != cudaSuccess) return e2;
         g.plan = plan_of(1);
-        if ((e2 = q8::launch_gemv(g, 2, true, s->num_sms, st)) != cudaSuccess) return e2;
+        if ((e2 = q8::launch_gemv(g, 2, s->num_sms, st)) != cudaSuccess) return e2;
         p.plan = plan_of(2);
         return q8::launch_mma(p, s->num_sms, st);
     }));

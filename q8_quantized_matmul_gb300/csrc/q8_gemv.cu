@@ -46,13 +46,18 @@
 //     2^14, block sums below 2^24); it is then scaled by d_w*d_x and added in
 //     fp32 with packed f32x2 instructions.  fp16 rather than int8 MMA: on GB300
 //     mma.sync runs int8 at 251 and fp16 at 942 MAC per SM per clock (measured).
-//   * Small activations (at most 1024 token-block pairs per CTA) are quantised
-//     by the consumer warps themselves from the fp32 rows, with the quantiser
-//     kernels' arithmetic: one kernel per call, launched in stream order.
-//     Otherwise the quantiser kernel writes activation planes first and this
-//     kernel is launched behind it with programmatic stream serialisation: the
-//     weight stream starts while the quantiser runs (it writes nothing the
-//     weights depend on), activations are read only after griddepcontrol.wait.
+//   * Small activations (at most 8 tokens, 1024 token-block pairs per CTA) are
+//     quantised by the consumer warps themselves from the fp32 rows, with the
+//     quantiser kernels' arithmetic: one kernel per call.  Otherwise the
+//     quantiser kernel writes activation planes first.
+//   * Launched with programmatic stream serialisation, so the launch and the
+//     barrier set-up overlap the end of the preceding kernel.  Nothing written
+//     by an earlier kernel is read before griddepcontrol.wait, except the
+//     weights when the kernel runs behind this library's quantiser (which
+//     triggers early and writes nothing they depend on): then the weight
+//     stream starts while it runs.  This kernel does not trigger early: measured
+//     on GB300, an early trigger sped up runs of equal calls but slowed a
+//     mixed decode step (a fused call followed by quantiser + GEMV) by 10 %.
 #include <cuda.h>
 
 #include "q8_common.cuh"
@@ -602,19 +607,23 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     volatile int *abort_flag = reinterpret_cast<volatile int *>(armed + NSLOT);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        *abort_flag = 0;
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-        for (int s = 0; s < NSLOT; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-            armed[s] = 0xffffffffu;
+    // one thread per ring slot initialises its barriers (one thread doing all 64
+    // delays the first copy by about a microsecond)
+    if (threadIdx.x < NSLOT) {
+        const int s = threadIdx.x;
+        if (s == 0) {
+            *abort_flag = 0;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
         }
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+        armed[s] = 0xffffffffu;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == PRODUCER) {
+        if (!p.weights_early) grid_dep_wait();
         const uint32_t planned = produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane);
         // After a timed-out wait: let the copies still in flight land (with one
         // overall time limit) before the CTA's shared memory goes away.
@@ -781,7 +790,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
                       uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
-cudaError_t launch_gemv(const GemvParams &p, int mode, bool after_quantiser, int grid, cudaStream_t st) {
+cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st) {
     static bool attr_done[3] = {false, false, false};
     if (mode < 0 || mode > 2) return cudaErrorInvalidValue;
     const void *fn = mode == 0 ? (const void *)k_gemv<0> : (mode == 1 ? (const void *)k_gemv<1> : (const void *)k_gemv<2>);
@@ -805,7 +814,7 @@ cudaError_t launch_gemv(const GemvParams &p, int mode, bool after_quantiser, int
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = after_quantiser ? 1 : 0;
+    cfg.numAttrs = 1;
     GemvParams pp = p;
     void *args[] = {&pp, &tmap};
     return cudaLaunchKernelExC(&cfg, fn, args);

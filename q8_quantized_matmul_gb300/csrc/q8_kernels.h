@@ -82,6 +82,8 @@ struct GemvParams {
     const int8_t *qx;          // activation quant plane [rows][in_dim] (groups padded to 16 rows)
     const float *dx;           // activation scale plane [rows][nb]
     const float *x;            // dense only: fp32 rows [n_tok][in_dim] quantised in the kernel (qx, dx unused)
+    int weights_early;         // 1: launched behind this library's quantiser, which writes nothing the
+                               //    weights depend on: the weight stream starts before griddepcontrol.wait
     float *out;
     int *err;
     uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
@@ -92,10 +94,8 @@ struct GemvParams {
     uint32_t n_expert;         // grouped: number of expert matrices
 };
 constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
-// after_quantiser: launched with programmatic stream serialisation behind this
-// library's quantiser kernel (the weights stream while it runs; activations are
-// read after griddepcontrol.wait).  Otherwise an ordinary launch.
-cudaError_t launch_gemv(const GemvParams &p, int mode, bool after_quantiser, int grid, cudaStream_t st);
+// Launched with programmatic stream serialisation; see GemvParams::weights_early.
+cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st);
 inline int gemv_mode(uint64_t n_tok) { return n_tok <= 2 ? 0 : (n_tok <= 8 ? 1 : 2); }
 // The dense GEMV quantises the activations itself when each CTA's share of that
 // work stays small: at most 8 tokens and 1024 (token, block) pairs with the

@@ -111,7 +111,8 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
             g.n_items = q8::gemv_dense_items(out_dim, d->num_sms);
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)d->num_sms ? g.n_items : (uint32_t)d->num_sms);
-        return q8::launch_gemv(g, q8::gemv_mode(n_tok), true, grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+        g.weights_early = 1;   // the preceding kernel is the quantiser
+        return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
     }
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
