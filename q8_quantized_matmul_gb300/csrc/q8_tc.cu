@@ -349,29 +349,55 @@ __global__ void __launch_bounds__(256) k_tc_reduce(float *__restrict__ out, cons
 }
 
 // Raw Q8_0 rows -> fp16 quant plane [rows][in_dim] (exact) and block-major
-// scales dwT[b][m_ld] (fp32 of the stored binary16 scale).  One thread per block,
-// rows fastest so the scale writes are coalesced.
+// scales dwT[b][m_ld] (fp32 of the stored binary16 scale).  A CTA converts tiles
+// of 8 rows x 32 blocks: warp w takes row r0 + w and lane l block b0 + l, so a
+// warp reads 32 consecutive 34-byte blocks (1088 contiguous bytes) and writes
+// 32 consecutive 64-byte runs; the scales go through shared memory and leave
+// as 32-byte runs of dwT.
+__device__ __forceinline__ void s8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    // bias each byte to unsigned, place it under the fp16 exponent of 1024, subtract 1024 + 128
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, float *__restrict__ dwT,
                                                    const uint8_t *__restrict__ W, uint32_t rows, uint32_t nb,
                                                    uint32_t m_ld) {
-    const uint64_t total = (uint64_t)rows * nb;
-    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (uint64_t)gridDim.x * blockDim.x) {
-        const uint32_t b = (uint32_t)(i / rows), r = (uint32_t)(i - (uint64_t)b * rows);
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(W + ((uint64_t)r * nb + b) * QB);
-        dwT[(uint64_t)b * m_ld + r] = half_bits_to_float(src[0]);
-        uint4 *dst = reinterpret_cast<uint4 *>(a16 + (uint64_t)r * nb * QK + (uint64_t)b * QK);
+    __shared__ float ds[8][33];
+    const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const uint32_t tiles_r = (rows + 7) / 8, tiles_b = (nb + 31) / 32;
+    const uint64_t tiles = (uint64_t)tiles_r * tiles_b;
+    for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const uint32_t tb = (uint32_t)(tile % tiles_b), tr = (uint32_t)(tile / tiles_b);
+        const uint32_t r = tr * 8 + w, b = tb * 32 + l;
+        if (r < rows && b < nb) {
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(W + ((uint64_t)r * nb + b) * QB);
+            uint16_t h[17];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[4];
+            for (int i = 0; i < 17; ++i) h[i] = __ldg(src + i);
+            ds[w][l] = half_bits_to_float(h[0]);
+            uint4 *dst = reinterpret_cast<uint4 *>(a16 + (uint64_t)r * nb * QK + (uint64_t)b * QK);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint16_t two = src[1 + c * 4 + e];   // quants 8c+2e, 8c+2e+1
-                const __half lo = __int2half_rn((int)(int8_t)(two & 0xff));
-                const __half hi = __int2half_rn((int)(int8_t)(two >> 8));
-                o[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t word = (uint32_t)h[1 + 4 * c + 2 * e] | ((uint32_t)h[2 + 4 * c + 2 * e] << 16);
+                    s8x4_to_half2x2(word, o[2 * e], o[2 * e + 1]);
+                }
+                dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        __syncthreads();
+        {
+            const uint32_t bb = threadIdx.x >> 3, rr = threadIdx.x & 7;   // 32 blocks x 8 rows
+            const uint32_t r2 = tr * 8 + rr, b2 = tb * 32 + bb;
+            if (r2 < rows && b2 < nb) dwT[(uint64_t)b2 * m_ld + r2] = ds[rr][bb];
+        }
+        __syncthreads();
     }
 }
 
@@ -380,10 +406,9 @@ bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t
 
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
                              int num_sms, cudaStream_t st) {
-    const uint64_t total = (uint64_t)rows * nb;
-    if (!total) return cudaSuccess;
-    uint64_t grid = (total + 255) / 256;
-    if (grid > (uint64_t)num_sms * 16) grid = (uint64_t)num_sms * 16;
+    const uint64_t tiles = (uint64_t)((rows + 7) / 8) * ((nb + 31) / 32);
+    if (!tiles) return cudaSuccess;
+    const uint64_t grid = tiles < (uint64_t)num_sms * 8 ? tiles : (uint64_t)num_sms * 8;
     k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld);
     return cudaGetLastError();
 }
