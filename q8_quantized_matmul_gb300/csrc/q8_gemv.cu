@@ -22,10 +22,10 @@
 //     issues every copy into a CTA-wide ring of 32 slots (152 KB in flight),
 //     reusing a slot once its consumer has released it.  TMA issue stalls while
 //     the SM's copy queue drains at the HBM rate, so only this warp ever waits
-//     there.  Sixteen consumer warps own the sub-items (G = 16 / wpi groups,
-//     sub-item s in group s mod G) and, when an item has fewer than 16
-//     sub-items, wpi warps split its K slots and add their partial sums
-//     through shared memory in a fixed order.  Consecutive slots of the
+//     there.  Fourteen consumer warps own the sub-items (G = 14 / wpi groups,
+//     sub-item s in group s mod G) and, when an item has fewer than 14
+//     sub-items, wpi warps (2, 7 or 14) split its K slots and add their
+//     partial sums through shared memory in a fixed order.  Consecutive slots of the
 //     sequence belong to different warps, so the ring drains in arrival order.
 //   * The token group's activations are staged once per K chunk by the consumer
 //     warps, in the order the mode's inner loop reads them.
@@ -238,11 +238,13 @@ __device__ __forceinline__ bool wait_armed(volatile uint32_t *armed, uint32_t r,
 }
 
 // Warps per sub-item for an item of nsub sub-items and nk K slots: the largest
-// power of two dividing the consumer count with every sub-item on its own
-// group of wpi warps (so with wpi > 1 each warp holds one sub-item).
+// divisor of the consumer count (1, 2, 7, 14) that keeps every sub-item on its
+// own group of wpi warps, with a K slot for each warp (so with wpi > 1 each warp
+// holds one sub-item).  A single 16-row sub-item is split over all 14 warps.
 __device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
     uint32_t wpi = 1;
-    while (gv::NCW % (wpi * 2) == 0 && nsub * wpi * 2 <= (uint32_t)gv::NCW && wpi * 2 <= nk) wpi *= 2;
+    for (uint32_t d = 2; d <= (uint32_t)gv::NCW; ++d)
+        if (gv::NCW % d == 0 && nsub * d <= (uint32_t)gv::NCW && d <= nk) wpi = d;
     return wpi;
 }
 
