@@ -183,6 +183,7 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.err = s->err;
         g.n_tok = (uint32_t)n_tok;
         g.n_items = q8::gemv_dense_items(out_dim, s->num_sms);
+        q8::gemv_dense_split(out_dim, g.n_items, g.sub_base, g.sub_rem);
         g.plan = nullptr;
         g.row_to_out = nullptr;
         g.n_expert = 1;

@@ -186,11 +186,13 @@ struct GItem {
 template <int TOKG>
 __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it) {
     if (!p.plan) {
-        // dense: n_items contiguous ranges of whole sub-items, sizes differing by at most one
+        // dense: n_items contiguous ranges of whole sub-items, sizes differing by at
+        // most one (the split is computed on the host: a 64-bit division here
+        // would delay the first weight copy)
         if ((uint32_t)i >= p.n_items) return false;
-        const uint32_t nsub_all = (p.out_dim + gv::ROWS - 1) / gv::ROWS;
-        const uint32_t s0 = (uint32_t)(((uint64_t)i * nsub_all) / p.n_items);
-        const uint32_t s1 = (uint32_t)(((uint64_t)(i + 1) * nsub_all) / p.n_items);
+        const uint32_t ui = (uint32_t)i;
+        const uint32_t s0 = ui * p.sub_base + min(ui, p.sub_rem);
+        const uint32_t s1 = s0 + p.sub_base + (ui < p.sub_rem ? 1u : 0u);
         it.expert = 0;
         it.xrow0 = 0;
         it.ntok = (int)p.n_tok;
@@ -403,8 +405,8 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
 // Fused quantiser (dense path, x given): the CTA quantises tokens 0..TOKG-1 of
 // chunk [kb0, kb0 + ka) from the fp32 rows itself, with the arithmetic of the
 // quantiser kernels (four lanes per block), and writes the mode's layout.
-// Rows past n_tok are quantised from zeros (q = 0, d = 0).  Loads are issued
-// two rounds at a time before they are used.
+// Only the group's real tokens are quantised; padding tokens get zero
+// fragments and scales.  Loads are issued three rounds at a time before use.
 template <int MODE>
 __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GItem &it, uint32_t kb0, uint32_t ka,
                                                   uint8_t *act, float *dxs, uint8_t *qtmp) {
@@ -413,15 +415,20 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
     constexpr uint32_t TOKQ = M::TOKG;
     constexpr uint32_t GROUPS = CONSUMER_THREADS / 4;
     const uint32_t lane_q = threadIdx.x & 3u;
-    const uint32_t npair = ka * TOKQ;                     // (token, block) pairs, token-major
+    const uint32_t ntok = (uint32_t)it.ntok;              // <= TOKQ
+    const uint32_t npair = ka * ntok;                     // (token, block) pairs, token-major
     const uint32_t rounds = (npair + GROUPS - 1) / GROUPS;
-    for (uint32_t r0 = 0; r0 < rounds; r0 += 2) {
-        float xv[2][8];
+    constexpr int RB = 3;                                 // rounds whose loads are in flight together
+    if (MODE != 0)   // padding tokens: zero scales (their fragments are zero, see below)
+        for (uint32_t e = threadIdx.x; e < ka * 16; e += CONSUMER_THREADS)
+            if ((e & 15u) >= ntok) dxs[e] = 0.0f;
+    for (uint32_t r0 = 0; r0 < rounds; r0 += RB) {
+        float xv[RB][8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < RB; ++h) {
             const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
             const uint32_t t = pr / ka, b = pr - t * ka;
-            if (pr < npair && t < (uint32_t)it.ntok)
+            if (pr < npair)
                 load8(xv[h], p.x + (uint64_t)t * p.in_dim + (uint64_t)(kb0 + b) * QK + lane_q * 8);
             else {
 #pragma unroll
@@ -429,7 +436,7 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
             }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < RB; ++h) {
             const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
             const uint32_t t = pr / ka, b = pr - t * ka;
             const QuantBlock qb = quantize8(xv[h]);   // all lanes: the block maximum is shuffled
@@ -478,7 +485,10 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
             const uint32_t *xt = reinterpret_cast<const uint32_t *>(qtmp + (size_t)(lg + 8 * t) * M::QT_STRIDE +
                                                                     (size_t)b * QK);
             uint32_t f0, f1;
-            if (!even) {
+            if (lg + 8 * t >= ntok) {   // padding token: not quantised, zero fragment
+                f0 = 0;
+                f1 = 0;
+            } else if (!even) {
                 f0 = xt[lc];
                 f1 = xt[i1];
             } else {

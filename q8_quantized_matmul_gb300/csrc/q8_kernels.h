@@ -89,6 +89,8 @@ struct GemvParams {
     uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
     uint32_t rows_per_item;    // grouped: rows per item, multiple of 16, <= 512
     uint32_t n_items;          // dense: items (contiguous runs of 16-row sub-items, <= 32 each)
+    uint32_t sub_base;         // dense: every item has sub_base sub-items, the first sub_rem one more
+    uint32_t sub_rem;
     const PlanHeader *plan;    // grouped: class plan; nullptr: dense
     const int32_t *row_to_out;
     uint32_t n_expert;         // grouped: number of expert matrices
@@ -107,6 +109,11 @@ inline bool gemv_fuses_quantiser(uint64_t n_tok, uint64_t nb) {
 }
 // Dense items: one per SM while there are enough 16-row sub-items, each at most
 // GEMV_MAX_ROWS_PER_ITEM rows.
+inline void gemv_dense_split(uint64_t out_dim, uint32_t n_items, uint32_t &base, uint32_t &rem) {
+    const uint64_t nsub = (out_dim + 15) / 16;
+    base = (uint32_t)(nsub / n_items);
+    rem = (uint32_t)(nsub % n_items);
+}
 inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
     const uint64_t nsub = (out_dim + 15) / 16;
     const uint64_t per = GEMV_MAX_ROWS_PER_ITEM / 16;

@@ -109,6 +109,7 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
         g.err = err;
         g.n_tok = (uint32_t)n_tok;
             g.n_items = q8::gemv_dense_items(out_dim, d->num_sms);
+        q8::gemv_dense_split(out_dim, g.n_items, g.sub_base, g.sub_rem);
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)d->num_sms ? g.n_items : (uint32_t)d->num_sms);
         g.weights_early = 1;   // the preceding kernel is the quantiser
