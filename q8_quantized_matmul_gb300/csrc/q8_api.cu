@@ -221,8 +221,8 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
            const void *xq, uint64_t n_tok, cudaStream_t st) {
     const uint64_t nb = in_dim / q8::QK;
     const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
-    const uint64_t n_ld = (n_tok + 255) & ~(uint64_t)255;
-    const uint64_t tiles = (m_ld / 128) * (n_ld / 256);
+    const uint64_t n_ld = (n_tok + 127) & ~(uint64_t)127;
+    const uint64_t tiles = (m_ld / 128) * (n_ld / 128);
     uint64_t ksplit = 1;
     if (tiles < (uint64_t)s->num_sms) {
         ksplit = (uint64_t)s->num_sms / tiles;

@@ -125,7 +125,7 @@ inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
 // Prefill GEMM on tcgen05 (q8_tc.cu).  Weights as an fp16 plane [M][K] (from
 // launch_tc_expand) with block-major scales dwT[nb][m_ld]; activations as an
 // fp16 plane [n_ld rows][K] with block-major scales dxT[nb][n_ld]
-// (launch_quantize_f16t / launch_unpack_f16t).  m_ld % 128 == 0, n_ld % 256 == 0,
+// (launch_quantize_f16t / launch_unpack_f16t).  m_ld % 128 == 0, n_ld % 128 == 0,
 // nb even.  With ksplit > 1, partial[ksplit][N][M] holds the K-split sums.
 struct TcParams {
     int M;                 // weight rows (out_dim)

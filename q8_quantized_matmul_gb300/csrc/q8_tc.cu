@@ -10,8 +10,9 @@
 // every product is an integer below 2^14 and a block's 32-product sum is below
 // 2^24, exact in the fp32 accumulator.  The scales differ per 32-value block,
 // so each block gets its own accumulator: two UMMAs (K = 16 each) write a fresh
-// 128 x 256 fp32 tile into one of two TMEM slots, and eight epilogue warps read
-// it back (tcgen05.ld) and fold it into fp32 registers as
+// 128 x 128 fp32 tile into one of four TMEM slots, and eight epilogue warps read
+// it back (tcgen05.ld, a warp's 64 columns in one batch and one wait) and fold
+// it into fp32 registers as
 // acc[o][t] += isum * d_x[t] * d_w[o] (packed f32x2 multiply and FMA).  That
 // epilogue costs two fp32 operations per output per block, 1/16 of the MMA's
 // multiply-adds, and the fp32 pipe, not the tensor pipe, sets the ceiling
@@ -19,14 +20,15 @@
 //
 // Warp roles (320 threads, one persistent CTA per SM):
 //   warp 0  TMA producer: per stage of K = 64 (two blocks) the fp16 weight tile
-//           (128 x 64, 128-byte swizzle), the fp16 activation tile (256 x 64,
-//           128-byte swizzle), and the two blocks' scales (1-D bulk copies).
+//           (128 x 64, 128-byte swizzle), the fp16 activation tile (128 x 64,
+//           128-byte swizzle), and the two blocks' scales (1-D bulk copies);
+//           six stages.
 //   warp 1  allocates TMEM (512 columns) and issues the UMMAs from one thread;
 //           tcgen05.commit signals "slot full" and, per stage, "stage consumed".
-//   2..9    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the 256
+//   2..9    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the 128
 //           columns; arrives "slot empty" after reading, "stage empty" after
 //           using the stage's scales.
-// Work units are (128-row tile, 256-token tile, K split); with fewer tiles than
+// Work units are (128-row tile, 128-token tile, K split); with fewer tiles than
 // SMs, K is split and the partial sums are added by a second kernel in a fixed
 // order (deterministic).  Every wait is bounded.
 #include <cuda.h>
@@ -38,21 +40,23 @@ namespace q8 {
 
 namespace tc {
 constexpr int BM = 128;                                // weight rows per tile (UMMA M)
-constexpr int BN = 256;                                // tokens per tile (UMMA N)
+constexpr int BN = 128;                                // tokens per tile (UMMA N)
 constexpr int BK = 64;                                 // K elements per stage (two blocks)
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 6;
 constexpr int A_BYTES = BM * BK * 2;                   // 16384
-constexpr int B_BYTES = BN * BK * 2;                   // 32768
-constexpr int DX_BYTES = 2 * BN * 4;                   // 2048
+constexpr int B_BYTES = BN * BK * 2;                   // 16384
+constexpr int DX_BYTES = 2 * BN * 4;                   // 1024
 constexpr int DW_BYTES = 2 * BM * 4;                   // 1024
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + DX_BYTES + DW_BYTES;   // 51 KiB, 1 KiB aligned
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + DX_BYTES + DW_BYTES;   // 34 KiB, 1 KiB aligned
 constexpr int NUM_EPI = 8;                             // epilogue warps: 2 per TMEM lane quarter
-constexpr int EPI_COLS = BN / (NUM_EPI / 4);          // 128 columns per epilogue warp
+constexpr int EPI_COLS = BN / (NUM_EPI / 4);          // 64 columns per epilogue warp
 constexpr int NTHREADS = (2 + NUM_EPI) * 32;
-constexpr uint32_t TMEM_COLS = 512;                    // two 256-column accumulator slots
-constexpr int NBAR = 2 * NSTAGE + 4 + 1;               // full, empty, tfull[2], tempty[2], done
+constexpr int NSLOT_T = 4;                             // TMEM accumulator slots of BN columns
+constexpr uint32_t TMEM_COLS = NSLOT_T * BN;           // 512
+constexpr int NBAR = 2 * NSTAGE + 2 * NSLOT_T + 1;     // full, empty, tfull, tempty, done
 constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + 1024 + NBAR * 8 + 16;
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+static_assert(SMEM <= 227 * 1024, "shared memory");
 }  // namespace tc
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     uint8_t *smem = smem_raw + (((base_s + 1023u) & ~1023u) - base_s);      // 1 KiB aligned stages
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * STAGE_BYTES);
     uint64_t *full = bars, *empty = bars + NSTAGE;
-    uint64_t *tfull = bars + 2 * NSTAGE, *tempty = tfull + 2, *done = tempty + 2;
+    uint64_t *tfull = bars + 2 * NSTAGE, *tempty = tfull + NSLOT_T, *done = tempty + NSLOT_T;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1 + NUM_EPI);   // MMA commit + every epilogue warp
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSLOT_T; ++s) {
             mbar_init(&tfull[s], 1);
             mbar_init(&tempty[s], NUM_EPI);
         }
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            uint32_t fills[NSTAGE] = {0, 0, 0, 0};
+            uint32_t fills[NSTAGE] = {};
             TcUnit w;
             for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
                 const int m0 = w.mt * BM, n0 = w.nt * BN;
@@ -239,8 +243,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     const uint32_t a_s = smem_addr(smem + (size_t)stage * STAGE_BYTES);
                     const uint32_t b_s = a_s + A_BYTES;
                     for (int j = 0; j < 2; ++j, ++blk) {
-                        const uint32_t slot = blk & 1u;
-                        mbar_wait(&tempty[slot], ((blk >> 1) & 1u) ^ 1u, p.err, abort_flag);
+                        const uint32_t slot = blk % NSLOT_T;
+                        mbar_wait(&tempty[slot], ((blk / NSLOT_T) & 1u) ^ 1u, p.err, abort_flag);
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + slot * BN;
 #pragma unroll
@@ -279,26 +283,25 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                 const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
                 const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
                 for (int j = 0; j < 2; ++j, ++blk) {
-                    const uint32_t slot = blk & 1u;
-                    mbar_wait(&tfull[slot], (blk >> 1) & 1u, p.err, abort_flag);
+                    const uint32_t slot = blk % NSLOT_T;
+                    mbar_wait(&tfull[slot], (blk / NSLOT_T) & 1u, p.err, abort_flag);
                     tc_fence_after();
                     const uint64_t ww = tc_pair(dws[j * BM + m]);
                     const float *dxj = dxs + j * BN + h * EPI_COLS;
                     const uint32_t col0 = lane_addr + slot * BN + h * EPI_COLS;
-                    // 16-column chunks, the next chunk's TMEM load in flight while
-                    // the current one is folded in
-                    uint32_t v[2][16];
-                    tc_ld16(col0, v[0]);
+                    // the block's columns in one batch of TMEM loads and one wait
+                    uint32_t v[EPI_COLS / 16][16];
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS / 16; ++c) tc_ld16(col0 + c * 16, v[c]);
+                    tc_wait_ld();
 #pragma unroll
                     for (int c = 0; c < EPI_COLS / 16; ++c) {
-                        tc_wait_ld();
-                        if (c + 1 < EPI_COLS / 16) tc_ld16(col0 + (c + 1) * 16, v[(c + 1) & 1]);
                         const float4 *x4 = reinterpret_cast<const float4 *>(dxj + c * 16);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const float4 x = x4[i];
-                            tc_fold(acc[c * 8 + 2 * i], v[c & 1][4 * i], v[c & 1][4 * i + 1], x.x, x.y, ww);
-                            tc_fold(acc[c * 8 + 2 * i + 1], v[c & 1][4 * i + 2], v[c & 1][4 * i + 3], x.z, x.w, ww);
+                            tc_fold(acc[c * 8 + 2 * i], v[c][4 * i], v[c][4 * i + 1], x.x, x.y, ww);
+                            tc_fold(acc[c * 8 + 2 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3], x.z, x.w, ww);
                         }
                     }
                     tc_fence_before();
