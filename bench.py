@@ -14,7 +14,7 @@ stream, max over ranks.  Inputs larger than L2: every call of a step reads its
 own copy of the weights, rotating through copies totalling more than 4x L2.
 SM clocks are sampled with nvidia-smi during the timed region.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--full]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (test infrastructure, the only other
 place this file runs it) on the host cores on a bounded sample of the same
@@ -56,7 +56,6 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--full", action="store_true", help="also measure the long-prefill layer slice")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "moe"),
@@ -456,6 +455,44 @@ def secondary(args, torch, q8, dev, stream, l2):
                     "kernel_frac_of_hbm_peak": round(wb / (kms * 1e-3) / 1e9 / hbm, 4)})
         del W
     assert q8.q8_last_error(stream) == 0
+    torch.cuda.empty_cache()
+
+    # long prefill layer slice: 4096 tokens through q_a, q_b, output_a, output_b, then routed
+    # gate/up and down over 256 experts with Zipf(1.1) top-6 routing
+    n = 4096
+    rows = []
+    total_ops, total_ms = 0.0, 0.0
+    for in_dim, out_dim in ((4096, 1024), (1024, 32768), (32768, 1024), (1024, 4096)):
+        W = torch.from_numpy(inputs.weights(out_dim, in_dim, seed=3)).to(dev)
+        x = torch.from_numpy(inputs.normal((n, in_dim), seed=3)).to(dev)
+        o = torch.empty((n, out_dim), device=dev)
+        ms = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, W, in_dim, out_dim, x, n, stream), 3, warm=1)
+        ops = 2.0 * in_dim * out_dim * n
+        total_ops += ops
+        total_ms += ms
+        rows.append(f"{in_dim}->{out_dim}: {ms:.3f} ms, {ops / (ms * 1e-3) / 1e12:.0f} TOPS")
+        del W, x, o
+    ids = torch.from_numpy(inputs.route_zipf(n, 6, 256, s=1.1, seed=0)).to(dev)
+    for name, in_dim, out_dim, per_pair in (("gate/up", 4096, 2048, 0), ("down", 2048, 4096, 1)):
+        W = torch.from_numpy(inputs.weights(256 * out_dim, in_dim, seed=2)).to(dev)
+        stride = out_dim * in_dim // QK * QB
+        x = torch.from_numpy(inputs.normal((n * 6 if per_pair else n, in_dim), seed=2)).to(dev)
+        o = torch.empty((n * 6, out_dim), device=dev)
+        ms = timed_eager(torch, stream, lambda i: q8.q8_moe_matmul(o, W, 256, stride, ids, 6, in_dim, out_dim, x,
+                                                                    per_pair, n, stream), 3, warm=1)
+        ops = 2.0 * in_dim * out_dim * n * 6
+        total_ops += ops
+        total_ms += ms
+        rows.append(f"MoE {name}: {ms:.3f} ms, {ops / (ms * 1e-3) / 1e12:.0f} TOPS")
+        del W, x, o
+    assert q8.q8_last_error(stream) == 0
+    out.append({"workload": "long prefill layer slice, n_tok 4096: q_a 4096->1024, q_b 1024->32768, "
+                            "output_a 32768->1024, output_b 1024->4096, routed gate/up and down over 256 experts "
+                            "(Zipf(1.1) top-6)",
+                "ms_per_slice": round(total_ms, 3), "tops": round(total_ops / (total_ms * 1e-3) / 1e12, 1),
+                "frac_of_bf16_peak": round(total_ops / (total_ms * 1e-3) / 1e12 / tflops, 4),
+                "per_call": rows,
+                "timing": "eager calls (quantise + expand + GEMM each), CUDA events, mean of 3"})
     torch.cuda.empty_cache()
     return out
 

@@ -433,9 +433,7 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
         cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
         if (e2 != cudaSuccess) return e2;
         g.plan = plan_of(1);
-        if ((e2 = q8::launch_gemv(g, 2, s->num_sms, st)) != cudaSuccess) return e2;
-        p.plan = plan_of(2);
-        return q8::launch_mma(p, s->num_sms, st);
+        return q8::launch_gemv(g, 2, s->num_sms, st);
     }));
 }
 

@@ -55,15 +55,15 @@ cudaError_t launch_mma(const MmaParams &p, int grid, cudaStream_t st);
 // Any in_dim % 32 == 0 and 2-byte aligned W: one thread per output (slow path).
 cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, cudaStream_t st);
 
-// Routing (q8_moe.cu): buckets pairs by expert and writes three plans, one per
-// size class of expert group: class 0 = groups of <= 8 rows (int8 GEMV), class 1 =
-// 9..16 rows (fp16 GEMV), class 2 = more than 16 rows (GEMM).  Each plan is a
-// PlanHeader followed by Segment[n_expert]; item numbering follows the kernel that
-// consumes the class (rows_gemv rows x 8 or 16 tokens for the GEMVs,
-// 16 rows x 64 tokens for the GEMM).
+// Routing (q8_moe.cu): buckets pairs by expert and writes two plans, one per
+// size class of expert group: class 0 = groups of <= 8 rows (GEMV, one 8-token
+// MMA tile), class 1 = more rows (GEMV, 16-token groups: a group of 300 rows is 19
+// token groups, each streaming the expert's weights, which stay in L2 while the
+// groups run side by side).  Each plan is a PlanHeader followed by
+// Segment[n_expert]; items are rows_gemv rows x one token group.
 //   row_to_out, src_row: int32[max_rows], max_rows = route_max_rows(n_pairs, n_expert)
 //   counts, row0_of: int32[n_expert] scratch
-constexpr int ROUTE_CLASSES = 3;
+constexpr int ROUTE_CLASSES = 2;
 uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
 size_t route_plan_bytes(uint32_t n_expert);
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,

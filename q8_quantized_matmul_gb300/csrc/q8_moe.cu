@@ -22,8 +22,6 @@
 namespace q8 {
 
 constexpr int ROUTE_THREADS = 512;
-constexpr int TOK_PER_ITEM = 64;   // must match the matmul kernel's tokens per work item
-constexpr int ROWS_PER_ITEM = 16;  // and its weight rows per work item
 
 uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert) {
     const uint64_t touched = n_pairs < n_expert ? n_pairs : n_expert;
@@ -71,7 +69,8 @@ size_t route_plan_bytes(uint32_t n_expert) {
     return ((sizeof(PlanHeader) + (size_t)n_expert * sizeof(Segment)) + 255) & ~(size_t)255;
 }
 
-__device__ __forceinline__ int route_class(int count) { return count <= 8 ? 0 : (count <= 16 ? 1 : 2); }
+__device__ __forceinline__ int route_class(int count) { return count <= 8 ? 0 : 1; }
+__device__ __forceinline__ int route_class_tokens(int cls) { return cls == 0 ? 8 : 16; }   // GEMV token group
 
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
                                                                uint32_t out_dim, uint32_t rows_gemv, uint8_t *plans,
@@ -98,10 +97,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
     __syncthreads();
     if (threadIdx.x == 0) {
         const int n_rb_gemv = (int)((out_dim + rows_gemv - 1) / rows_gemv);
-        const int n_rb_mma = (int)((out_dim + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
         PlanHeader *hdr[ROUTE_CLASSES];
         Segment *segs[ROUTE_CLASSES];
-        int nseg[ROUTE_CLASSES] = {0, 0, 0}, nitem[ROUTE_CLASSES] = {0, 0, 0};
+        int nseg[ROUTE_CLASSES] = {}, nitem[ROUTE_CLASSES] = {};
         for (int k = 0; k < ROUTE_CLASSES; ++k) {
             hdr[k] = reinterpret_cast<PlanHeader *>(plans + k * plan_stride);
             segs[k] = reinterpret_cast<Segment *>(hdr[k] + 1);
@@ -119,7 +117,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
             sg.item_start = nitem[k];
             row0_of[e] = row;
             row += (ce + 15) & ~15;
-            nitem[k] += k == 2 ? n_rb_mma * ((ce + TOK_PER_ITEM - 1) / TOK_PER_ITEM) : n_rb_gemv;
+            const int tg = route_class_tokens(k);
+            nitem[k] += n_rb_gemv * ((ce + tg - 1) / tg);
         }
         for (int k = 0; k < ROUTE_CLASSES; ++k) {
             hdr[k]->n_segments = nseg[k];
