@@ -265,7 +265,7 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     p.err = s->err;
     const uint64_t units = tiles * ksplit;
     const int grid = (int)(units < (uint64_t)s->num_sms ? units : (uint64_t)s->num_sms);
-    return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, b16, n_ld, grid, st); }));
+    return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, out_dim, b16, n_ld, grid, st); }));
 }
 
 }  // namespace
@@ -370,8 +370,23 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     const uint64_t n_pairs = n_tok * k;
     const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
     const size_t plan_bytes = q8::route_plan_bytes(n_expert);
+    // Tensor-core class: at most tc_cap experts of more than MOE_TC_MIN_ROWS rows,
+    // their weights expanded to fp16 slots of slot_rows rows.
+    const uint64_t slot_rows = (out_dim + 127) & ~(uint64_t)127;
+    uint64_t tc_cap = 0;
+    if (nb % 8 == 0 && n_pairs >= q8::MOE_TC_MIN_PAIRS) {
+        tc_cap = n_pairs / (q8::MOE_TC_MIN_ROWS + 1);
+        if (tc_cap > n_expert) tc_cap = n_expert;
+        const uint64_t by_budget = q8::MOE_TC_BUDGET / (slot_rows * in_dim * 2);
+        if (tc_cap > by_budget) tc_cap = by_budget;
+    }
+    uint64_t tc_rows = max_rows < n_pairs + 15 * tc_cap + 16 ? max_rows : n_pairs + 15 * tc_cap + 16;
+    const uint64_t tc_ld = ((tc_rows + 127) & ~(uint64_t)127) + 128;   // a tile may start at the last row
+    const size_t tc_bytes = tc_cap ? align256(tc_cap * slot_rows * in_dim * 2) + align256(nb * tc_cap * slot_rows * 4) +
+                                         align256(tc_ld * in_dim * 2) + align256(nb * tc_ld * 4)
+                                   : 0;
     const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * plan_bytes + align256(max_rows * 4) * 2 +
-                        planes_bytes(max_rows, in_dim);
+                        planes_bytes(max_rows, in_dim) + tc_bytes;
     if ((rc = reserve_scratch(s, need))) return rc;
     Carver cv(s->scratch);
     int32_t *counts = cv.take<int32_t>(n_expert * 4);
@@ -381,15 +396,29 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     int32_t *src_row = cv.take<int32_t>(max_rows * 4);
     int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
     float *dx = cv.take<float>(max_rows * nb * sizeof(float));
+    __half *a16 = tc_cap ? cv.take<__half>(tc_cap * slot_rows * in_dim * 2) : nullptr;
+    float *dwT = tc_cap ? cv.take<float>(nb * tc_cap * slot_rows * 4) : nullptr;
+    __half *b16 = tc_cap ? cv.take<__half>(tc_ld * in_dim * 2) : nullptr;
+    float *dxT = tc_cap ? cv.take<float>(nb * tc_ld * 4) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t rows_gemv = (uint32_t)((out_dim + 15) & ~(uint64_t)15);
     if (rows_gemv > 128) rows_gemv = 128;
-    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_gemv, counts,
-                                     row0_of, plans, row_to_out, src_row, max_rows, out, s->err, s->num_sms, st);
-    if (e != cudaSuccess) return Q8_ECUDA;
-    e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
+    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_gemv,
+                                     (uint32_t)tc_cap, counts, row0_of, plans, row_to_out, src_row, max_rows, out,
+                                     s->err, s->num_sms, st);
     if (e != cudaSuccess) return Q8_ECUDA;
     auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes); };
+    if (tc_cap) {
+        e = q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W_experts), (uint32_t)out_dim, (uint32_t)nb,
+                                 (uint32_t)(tc_cap * slot_rows), s->num_sms, st, plan_of(2), expert_stride_bytes,
+                                 (uint32_t)slot_rows, (uint32_t)tc_cap);
+        if (e != cudaSuccess) return Q8_ECUDA;
+        e = q8::launch_quantize_planes_tc(qx, dx, b16, dxT, tc_ld, plan_of(2), x, in_dim, max_rows, src_row,
+                                          s->num_sms, st);
+    } else {
+        e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
+    }
+    if (e != cudaSuccess) return Q8_ECUDA;
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W_experts);
     p.expert_stride = expert_stride_bytes;
@@ -402,10 +431,10 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     p.err = s->err;
     p.n_tok = 0;
     p.row_to_out = row_to_out;
-    if (nb % 8 != 0) {
+    if (nb % 8 != 0) {   // no tensor-core class here (tc_cap == 0)
         const int hint = (int)(max_rows * out_dim > (1u << 30) ? (1u << 30) : max_rows * out_dim);
         return status_of(timed_launch(st, [&] {
-            for (int cls = 0; cls < q8::ROUTE_CLASSES; ++cls) {
+            for (int cls = 0; cls < q8::ROUTE_GEMV_CLASSES; ++cls) {
                 p.plan = plan_of(cls);
                 cudaError_t e2 = q8::launch_generic(p, hint, s->num_sms, st);
                 if (e2 != cudaSuccess) return e2;
@@ -425,10 +454,30 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     g.err = s->err;
     g.n_tok = 0;
     g.rows_per_item = rows_gemv;
-    g.weights_early = 1;   // behind the quantiser, then behind the previous class's GEMV
+    g.weights_early = 1;   // behind the quantiser or the grouped GEMM, then behind the previous class's GEMV
     g.row_to_out = row_to_out;
     g.n_expert = n_expert;
+    q8::TcParams tp{};
+    tp.M = (int)out_dim;
+    tp.N = 0;
+    tp.nb = (int)nb;
+    tp.ksplit = 1;
+    tp.kb_per = (int)nb;
+    tp.dxT = dxT;
+    tp.dwT = dwT;
+    tp.n_ld = tc_ld;
+    tp.m_ld = tc_cap * slot_rows;
+    tp.out = out;
+    tp.partial = nullptr;
+    tp.err = s->err;
+    tp.plan = plan_of(2);
+    tp.row_to_out = row_to_out;
+    tp.slot_rows = (int)slot_rows;
     return status_of(timed_launch(st, [&] {
+        if (tc_cap) {
+            cudaError_t e2 = q8::launch_tc_gemm(tp, a16, tc_cap * slot_rows, b16, tc_ld, s->num_sms, st);
+            if (e2 != cudaSuccess) return e2;
+        }
         g.plan = plan_of(0);
         cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
         if (e2 != cudaSuccess) return e2;

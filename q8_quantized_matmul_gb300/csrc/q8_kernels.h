@@ -22,7 +22,7 @@ struct PlanHeader {      // device-side header before the segment array
     int32_t n_segments;
     int32_t n_items;
     int32_t n_rows;      // activation-plane rows used (multiple of 16)
-    int32_t pad;
+    int32_t row_end;     // end of this class's rows (the tensor-core class holds rows [0, row_end))
 };
 
 struct MmaParams {
@@ -46,6 +46,11 @@ struct MmaParams {
 cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
                                    const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st);
+// As launch_quantize_planes, except that rows [0, tc_plan->row_end) go to the
+// tensor-core operand instead: fp16 quants q16[r][in_dim], scales dxT[b][n_ld].
+cudaError_t launch_quantize_planes_tc(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
+                                      const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_rows,
+                                      const int32_t *src_row, int num_sms, cudaStream_t st);
 cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *xq, uint64_t in_dim, uint64_t n_rows,
                                  uint64_t n_src, int num_sms, cudaStream_t st);
 
@@ -55,21 +60,29 @@ cudaError_t launch_mma(const MmaParams &p, int grid, cudaStream_t st);
 // Any in_dim % 32 == 0 and 2-byte aligned W: one thread per output (slow path).
 cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, cudaStream_t st);
 
-// Routing (q8_moe.cu): buckets pairs by expert and writes two plans, one per
+// Routing (q8_moe.cu): buckets pairs by expert and writes three plans, one per
 // size class of expert group: class 0 = groups of <= 8 rows (GEMV, one 8-token
 // MMA tile), class 1 = more rows (GEMV, 16-token groups: a group of 300 rows is 19
 // token groups, each streaming the expert's weights, which stay in L2 while the
-// groups run side by side).  Each plan is a PlanHeader followed by
-// Segment[n_expert]; items are rows_gemv rows x one token group.
+// groups run side by side), class 2 = the largest groups, more than
+// MOE_TC_MIN_ROWS rows each, at most tc_cap of them (tcgen05 GEMM on the
+// expert's weights expanded to fp16; items are 128-row x 128-token tiles).
+// Experts are taken largest first, so the class-2 groups own plane rows
+// [0, row_end).  Each plan is a PlanHeader followed by Segment[n_expert];
+// GEMV items are rows_gemv rows x one token group.
 //   row_to_out, src_row: int32[max_rows], max_rows = route_max_rows(n_pairs, n_expert)
 //   counts, row0_of: int32[n_expert] scratch
-constexpr int ROUTE_CLASSES = 2;
+constexpr int ROUTE_CLASSES = 3;
+constexpr int ROUTE_GEMV_CLASSES = 2;          // classes 0 and 1 run on the GEMV
+constexpr int MOE_TC_MIN_ROWS = 64;            // class 2 takes groups of more rows than this
+constexpr uint64_t MOE_TC_MIN_PAIRS = 1024;    // ... in batches of at least this many pairs
+constexpr uint64_t MOE_TC_BUDGET = 2ull << 30; // bytes of expanded fp16 expert weights per call
 uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
 size_t route_plan_bytes(uint32_t n_expert);
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
-                         uint32_t out_dim, uint32_t rows_gemv, int32_t *counts, int32_t *row0_of, uint8_t *plans,
-                         int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
-                         int num_sms, cudaStream_t st);
+                         uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap, int32_t *counts, int32_t *row0_of,
+                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out,
+                         int *err, int num_sms, cudaStream_t st);
 
 // Weight-streaming GEMV (q8_gemv.cu).  Modes: 0 = dp4a, token groups of <= 2;
 // 1 = fp16 MMA, one 8-token N tile; 2 = two N tiles (<= 16 tokens).
@@ -139,11 +152,23 @@ struct TcParams {
     float *out;            // [N][M]
     float *partial;        // [ksplit][N][M] or nullptr
     int *err;
+    // grouped (routed experts, plan != nullptr): the units of the class-2 plan.
+    // Segment s multiplies expert slot s (a16 rows [s * slot_rows, s * slot_rows + M))
+    // by plane rows [row0, row0 + count) and writes output row row_to_out[plane row].
+    // N, ksplit and kb_per are unused (no K split).
+    const PlanHeader *plan;
+    const int32_t *row_to_out;
+    int slot_rows;         // multiple of 128
 };
+// Expands rows x nb Q8_0 blocks of W into a16 / dwT.  With plan != nullptr it
+// expands every segment's expert (W + expert * expert_stride) into slot s,
+// a16 rows and dwT columns from s * slot_rows; n_slots_max bounds the grid.
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
-                             int num_sms, cudaStream_t st);
-cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
-                           cudaStream_t st);
+                             int num_sms, cudaStream_t st, const PlanHeader *plan = nullptr,
+                             uint64_t expert_stride = 0, uint32_t slot_rows = 0, uint32_t n_slots_max = 1);
+// n_rows_a / n_rows_b: rows of the a16 / b16 planes (the tensor maps' extents).
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, uint64_t n_rows_a, const __half *b16,
+                           uint64_t n_rows_b, int grid, cudaStream_t st);
 cudaError_t launch_quantize_f16t(__half *q16, float *dxT, const float *x, uint64_t in_dim, uint64_t n_tok,
                                  uint64_t n_ld, int num_sms, cudaStream_t st);
 cudaError_t launch_unpack_f16t(__half *q16, float *dxT, const uint8_t *xq, uint64_t in_dim, uint64_t n_tok,

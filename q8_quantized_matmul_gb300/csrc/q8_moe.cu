@@ -11,8 +11,9 @@
 //      get a zero output row and raise Q8_ERANGE (no trap).
 //   2. k_route_plan  : one CTA orders the touched experts by pair count
 //      (largest first, ties by id: the big groups start first, which keeps the
-//      persistent grid balanced under skewed routing), assigns each a
-//      16-row-aligned range of activation-plane rows and a range of work items.
+//      persistent grid balanced under skewed routing), gives each a size class,
+//      a 16-row-aligned range of activation-plane rows and a range of work
+//      items of its class.
 //   3. k_route_fill  : one CTA per expert lists its pairs in increasing p
 //      (block-wide prefix sums), giving the plane-row -> output-row map and the
 //      plane-row -> input-row map used by the gathering quantiser.
@@ -69,12 +70,12 @@ size_t route_plan_bytes(uint32_t n_expert) {
     return ((sizeof(PlanHeader) + (size_t)n_expert * sizeof(Segment)) + 255) & ~(size_t)255;
 }
 
-__device__ __forceinline__ int route_class(int count) { return count <= 8 ? 0 : 1; }
 __device__ __forceinline__ int route_class_tokens(int cls) { return cls == 0 ? 8 : 16; }   // GEMV token group
 
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
-                                                               uint32_t out_dim, uint32_t rows_gemv, uint8_t *plans,
-                                                               size_t plan_stride, int32_t *__restrict__ row0_of) {
+                                                               uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap,
+                                                               uint8_t *plans, size_t plan_stride,
+                                                               int32_t *__restrict__ row0_of) {
     extern __shared__ int32_t sh_plan[];   // order[n_expert] (sorted position -> expert)
     int32_t *order = sh_plan;
     __shared__ int n_active_sh;
@@ -97,9 +98,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
     __syncthreads();
     if (threadIdx.x == 0) {
         const int n_rb_gemv = (int)((out_dim + rows_gemv - 1) / rows_gemv);
+        const int m_tiles_tc = (int)((out_dim + 127) / 128);
         PlanHeader *hdr[ROUTE_CLASSES];
         Segment *segs[ROUTE_CLASSES];
-        int nseg[ROUTE_CLASSES] = {}, nitem[ROUTE_CLASSES] = {};
+        int nseg[ROUTE_CLASSES] = {}, nitem[ROUTE_CLASSES] = {}, rend[ROUTE_CLASSES] = {};
         for (int k = 0; k < ROUTE_CLASSES; ++k) {
             hdr[k] = reinterpret_cast<PlanHeader *>(plans + k * plan_stride);
             segs[k] = reinterpret_cast<Segment *>(hdr[k] + 1);
@@ -109,7 +111,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
         for (int s = 0; s < n_active; ++s) {
             const int e = order[s];
             const int ce = counts[e];
-            const int k = route_class(ce);
+            // counts only fall along the order, so class 2 is a prefix of it
+            const int k = (ce > MOE_TC_MIN_ROWS && nseg[2] < (int)tc_cap) ? 2 : (ce <= 8 ? 0 : 1);
             Segment &sg = segs[k][nseg[k]++];
             sg.expert = e;
             sg.row0 = row;
@@ -117,14 +120,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
             sg.item_start = nitem[k];
             row0_of[e] = row;
             row += (ce + 15) & ~15;
-            const int tg = route_class_tokens(k);
-            nitem[k] += n_rb_gemv * ((ce + tg - 1) / tg);
+            rend[k] = row;
+            if (k == 2) {
+                nitem[k] += m_tiles_tc * ((ce + 127) / 128);
+            } else {
+                const int tg = route_class_tokens(k);
+                nitem[k] += n_rb_gemv * ((ce + tg - 1) / tg);
+            }
         }
         for (int k = 0; k < ROUTE_CLASSES; ++k) {
             hdr[k]->n_segments = nseg[k];
             hdr[k]->n_items = nitem[k];
             hdr[k]->n_rows = row;
-            hdr[k]->pad = 0;
+            hdr[k]->row_end = rend[k];
         }
     }
 }
@@ -162,9 +170,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__r
 }
 
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
-                         uint32_t out_dim, uint32_t rows_gemv, int32_t *counts, int32_t *row0_of, uint8_t *plans,
-                         int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out, int *err,
-                         int num_sms, cudaStream_t st) {
+                         uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap, int32_t *counts, int32_t *row0_of,
+                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out,
+                         int *err, int num_sms, cudaStream_t st) {
     const uint64_t n_pairs = n_tok * k;
     cudaError_t e;
     // Padding rows map to nothing: -1 everywhere first.
@@ -183,7 +191,7 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
             cudaSuccess)
             return e;
     }
-    k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, rows_gemv, plans,
+    k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, rows_gemv, tc_cap, plans,
                                                       route_plan_bytes(n_expert), row0_of);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     k_route_fill<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, k, x_per_pair, row0_of, row_to_out, src_row);

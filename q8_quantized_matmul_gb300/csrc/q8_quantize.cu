@@ -43,13 +43,28 @@ __global__ void __launch_bounds__(256) k_quantize_blocks(uint8_t *__restrict__ x
 // dplane [n_rows][nb] fp32 (the stored binary16 scale as fp32).  Output row r
 // is quantised from x row src_row[r] when src_row is given (a negative entry
 // gives a zero row), else from x row r when r < n_src, else it is zero.
+// With TC, rows [0, tc_plan->row_end) are written to the tensor-core operand
+// (fp16 quants q16[r][in_dim], scales dxT[b][n_ld]) instead of the planes.
+__device__ __forceinline__ void store_f16_quants(__half *dst, const QuantBlock &qb) {
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        h[i] = (uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i])) |
+               ((uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+template <bool TC>
 __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qplane, float *__restrict__ dplane,
                                                          const float *__restrict__ x, uint64_t in_dim,
                                                          uint64_t n_rows, const int32_t *__restrict__ src_row,
-                                                         uint64_t n_src) {
+                                                         uint64_t n_src, __half *__restrict__ q16,
+                                                         float *__restrict__ dxT, uint64_t n_ld,
+                                                         const PlanHeader *tc_plan) {
     // The matmul that follows only prefetches weights before it waits for this
     // grid to finish, so it may be scheduled now.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint64_t tc_rows = TC ? (uint64_t)tc_plan->row_end : 0;
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_rows * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -68,7 +83,10 @@ __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qp
             for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
         }
         const QuantBlock qb = quantize8(x8);
-        if (live) {
+        if (TC && live && r < tc_rows) {
+            store_f16_quants(q16 + r * in_dim + b * QK + lane_q * 8, qb);
+            if (lane_q == 0) dxT[b * n_ld + r] = qb.d_stored;
+        } else if (live) {
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -133,12 +151,7 @@ __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16,
         }
         const QuantBlock qb = quantize8(x8);
         if (live) {
-            uint32_t h[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                h[i] = (uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i])) |
-                       ((uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i + 1])) << 16);
-            *reinterpret_cast<uint4 *>(q16 + r * in_dim + b * QK + lane_q * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+            store_f16_quants(q16 + r * in_dim + b * QK + lane_q * 8, qb);
             if (lane_q == 0) dxT[b * n_ld + r] = qb.d_stored;
         }
     }
@@ -194,7 +207,18 @@ cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x
                                    const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
-    k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
+    k_quantize_planes<false><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row,
+                                                                         n_src, nullptr, nullptr, 0, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_planes_tc(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
+                                      const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_rows,
+                                      const int32_t *src_row, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_rows * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    k_quantize_planes<true><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row,
+                                                                        0, q16, dxT, n_ld, tc_plan);
     return cudaGetLastError();
 }
 

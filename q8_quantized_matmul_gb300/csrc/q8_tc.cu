@@ -144,9 +144,12 @@ __device__ __forceinline__ uint64_t tc_pair(float w) {
 
 struct TcUnit {
     int mt, nt, kb0, kb1;
+    int a_row, b_row;   // first a16 / b16 plane row of the tile (also the dwT / dxT column)
+    int n_valid;        // grouped: tokens of the tile that belong to the segment
 };
 
-__device__ __forceinline__ bool tc_unit(const TcParams &p, int u, TcUnit &w) {
+// Dense: units are (128-row tile, 128-token tile, K split).
+__device__ __forceinline__ bool tc_unit_dense(const TcParams &p, int u, TcUnit &w) {
     const int m_tiles = (p.M + tc::BM - 1) / tc::BM;
     const int n_tiles = (p.N + tc::BN - 1) / tc::BN;
     const int units = m_tiles * n_tiles * p.ksplit;
@@ -157,12 +160,49 @@ __device__ __forceinline__ bool tc_unit(const TcParams &p, int u, TcUnit &w) {
     const int ks = r / n_tiles;
     w.kb0 = ks * p.kb_per;
     w.kb1 = min(p.nb, w.kb0 + p.kb_per);
+    w.a_row = w.mt * tc::BM;
+    w.b_row = w.nt * tc::BN;
+    w.n_valid = tc::BN;
     return true;
 }
 
+// Grouped: the plan's segments in order, each m_tiles x ceil(count / 128)
+// units from item_start on (weight tile fastest).  Units only grow along a
+// CTA's loop, so the segment cursor only moves forward.
+__device__ __forceinline__ bool tc_unit_grouped(const TcParams &p, int u, TcUnit &w, int &seg) {
+    const PlanHeader *h = p.plan;
+    if (u >= h->n_items) return false;
+    const Segment *sg = reinterpret_cast<const Segment *>(h + 1);
+    const int nseg = h->n_segments;
+    while (seg + 1 < nseg && sg[seg + 1].item_start <= u) ++seg;
+    const int m_tiles = (p.M + tc::BM - 1) / tc::BM;
+    const int v = u - sg[seg].item_start;
+    w.mt = v % m_tiles;
+    w.nt = v / m_tiles;
+    w.kb0 = 0;
+    w.kb1 = p.nb;
+    w.a_row = seg * p.slot_rows + w.mt * tc::BM;
+    w.b_row = sg[seg].row0 + w.nt * tc::BN;
+    w.n_valid = min(tc::BN, sg[seg].count - w.nt * tc::BN);
+    return true;
+}
+
+template <bool G>
+__device__ __forceinline__ bool tc_unit(const TcParams &p, int u, TcUnit &w, int &seg) {
+    if constexpr (G) return tc_unit_grouped(p, u, w, seg);
+    else return tc_unit_dense(p, u, w);
+}
+
+template <bool G>
 __global__ void __launch_bounds__(tc::NTHREADS, 1)
     k_tc_gemm(const TcParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
     using namespace tc;
+    if constexpr (G) {
+        // The GEMV launched behind this grid waits for it before it reads or
+        // writes anything this grid touches; let it take the SMs this grid frees.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (p.plan->n_items == 0) return;
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_s = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((base_s + 1023u) & ~1023u) - base_s);      // 1 KiB aligned stages
@@ -205,8 +245,9 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t fills[NSTAGE] = {};
             TcUnit w;
-            for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
-                const int m0 = w.mt * BM, n0 = w.nt * BN;
+            int seg = 0;
+            for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
+                const int m0 = w.a_row, n0 = w.b_row;
                 for (int kb = w.kb0; kb < w.kb1; kb += 2) {
                     if (mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
                         uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
@@ -236,7 +277,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             const uint32_t idesc = tc_idesc(BM, BN);
             uint32_t stage = 0, phase = 0, blk = 0;
             TcUnit w;
-            for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
+            int seg = 0;
+            for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
                 for (int kb = w.kb0; kb < w.kb1; kb += 2) {
                     mbar_wait(&full[stage], phase, p.err, abort_flag);
                     tc_fence_after();
@@ -272,7 +314,8 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t stage = 0, phase = 0, blk = 0;
         TcUnit w;
-        for (int u = blockIdx.x; tc_unit(p, u, w); u += gridDim.x) {
+        int seg = 0;
+        for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
             uint64_t acc[EPI_COLS / 2];   // this warp's columns as fp32 pairs
 #pragma unroll
             for (int i = 0; i < EPI_COLS / 2; ++i) acc[i] = 0ull;
@@ -317,17 +360,31 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             }
             // ---- write this unit's rows x this warp's tokens
             const int row = w.mt * BM + m;
-            const int tok0 = w.nt * BN + h * EPI_COLS;
-            const int ks = w.kb0 / p.kb_per;
-            float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
-            if (row < p.M) {
+            const int tok0 = h * EPI_COLS;            // within the tile
+            if constexpr (G) {
+                if (row < p.M) {
 #pragma unroll
-                for (int i = 0; i < EPI_COLS / 2; ++i) {
-                    const int t = tok0 + 2 * i;
-                    const float lo = __uint_as_float((uint32_t)acc[i]);
-                    const float hi = __uint_as_float((uint32_t)(acc[i] >> 32));
-                    if (t < p.N) dst[(size_t)t * p.M + row] = lo;
-                    if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = hi;
+                    for (int i = 0; i < EPI_COLS / 2; ++i) {
+                        const int t = tok0 + 2 * i;
+                        if (t < w.n_valid)
+                            p.out[(size_t)p.row_to_out[w.b_row + t] * p.M + row] = __uint_as_float((uint32_t)acc[i]);
+                        if (t + 1 < w.n_valid)
+                            p.out[(size_t)p.row_to_out[w.b_row + t + 1] * p.M + row] =
+                                __uint_as_float((uint32_t)(acc[i] >> 32));
+                    }
+                }
+            } else {
+                const int ks = w.kb0 / p.kb_per;
+                float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
+                if (row < p.M) {
+#pragma unroll
+                    for (int i = 0; i < EPI_COLS / 2; ++i) {
+                        const int t = w.b_row + tok0 + 2 * i;
+                        const float lo = __uint_as_float((uint32_t)acc[i]);
+                        const float hi = __uint_as_float((uint32_t)(acc[i] >> 32));
+                        if (t < p.N) dst[(size_t)t * p.M + row] = lo;
+                        if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = hi;
+                    }
                 }
             }
         }
@@ -368,21 +425,29 @@ __device__ __forceinline__ void s8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32
 
 __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, float *__restrict__ dwT,
                                                    const uint8_t *__restrict__ W, uint32_t rows, uint32_t nb,
-                                                   uint32_t m_ld) {
+                                                   uint32_t m_ld, const PlanHeader *plan, uint64_t expert_stride,
+                                                   uint32_t slot_rows) {
     __shared__ float ds[8][33];
     const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const uint32_t tiles_r = (rows + 7) / 8, tiles_b = (nb + 31) / 32;
-    const uint64_t tiles = (uint64_t)tiles_r * tiles_b;
+    const uint64_t tiles_slot = (uint64_t)tiles_r * tiles_b;
+    const uint32_t n_slots = plan ? (uint32_t)plan->n_segments : 1u;
+    const Segment *segs = plan ? reinterpret_cast<const Segment *>(plan + 1) : nullptr;
+    const uint64_t tiles = tiles_slot * n_slots;
     for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const uint32_t tb = (uint32_t)(tile % tiles_b), tr = (uint32_t)(tile / tiles_b);
+        const uint32_t slot = (uint32_t)(tile / tiles_slot);
+        const uint64_t ts = tile - (uint64_t)slot * tiles_slot;
+        const uint32_t tb = (uint32_t)(ts % tiles_b), tr = (uint32_t)(ts / tiles_b);
+        const uint8_t *Ws = plan ? W + (uint64_t)segs[slot].expert * expert_stride : W;
+        const uint64_t row_base = (uint64_t)slot * slot_rows;   // first a16 row / dwT column of the slot
         const uint32_t r = tr * 8 + w, b = tb * 32 + l;
         if (r < rows && b < nb) {
-            const uint16_t *src = reinterpret_cast<const uint16_t *>(W + ((uint64_t)r * nb + b) * QB);
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(Ws + ((uint64_t)r * nb + b) * QB);
             uint16_t h[17];
 #pragma unroll
             for (int i = 0; i < 17; ++i) h[i] = __ldg(src + i);
             ds[w][l] = half_bits_to_float(h[0]);
-            uint4 *dst = reinterpret_cast<uint4 *>(a16 + (uint64_t)r * nb * QK + (uint64_t)b * QK);
+            uint4 *dst = reinterpret_cast<uint4 *>(a16 + (row_base + r) * nb * QK + (uint64_t)b * QK);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[4];
@@ -398,7 +463,7 @@ __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, flo
         {
             const uint32_t bb = threadIdx.x >> 3, rr = threadIdx.x & 7;   // 32 blocks x 8 rows
             const uint32_t r2 = tr * 8 + rr, b2 = tb * 32 + bb;
-            if (r2 < rows && b2 < nb) dwT[(uint64_t)b2 * m_ld + r2] = ds[rr][bb];
+            if (r2 < rows && b2 < nb) dwT[(uint64_t)b2 * m_ld + row_base + r2] = ds[rr][bb];
         }
         __syncthreads();
     }
@@ -408,27 +473,36 @@ bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t
                      uint32_t box_rows);
 
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
-                             int num_sms, cudaStream_t st) {
-    const uint64_t tiles = (uint64_t)((rows + 7) / 8) * ((nb + 31) / 32);
+                             int num_sms, cudaStream_t st, const PlanHeader *plan, uint64_t expert_stride,
+                             uint32_t slot_rows, uint32_t n_slots_max) {
+    const uint64_t tiles = (uint64_t)((rows + 7) / 8) * ((nb + 31) / 32) * n_slots_max;
     if (!tiles) return cudaSuccess;
     const uint64_t grid = tiles < (uint64_t)num_sms * 8 ? tiles : (uint64_t)num_sms * 8;
-    k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld);
+    k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld, plan, expert_stride, slot_rows);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
-                           cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM);
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, uint64_t n_rows_a, const __half *b16,
+                           uint64_t n_rows_b, int grid, cudaStream_t st) {
+    const bool grouped = p.plan != nullptr;
+    static bool attr_done[2] = {false, false};
+    if (!attr_done[grouped]) {
+        cudaError_t e = grouped ? cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)tc::SMEM)
+                                : cudaFuncSetAttribute(k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)tc::SMEM);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        attr_done[grouped] = true;
     }
     alignas(64) CUtensorMap tmA, tmB;
     const uint64_t K = (uint64_t)p.nb * QK;
-    if (!encode_f16_tmap(&tmA, a16, K, (uint64_t)p.M, tc::BK, tc::BM)) return cudaErrorInvalidValue;
+    if (!encode_f16_tmap(&tmA, a16, K, n_rows_a, tc::BK, tc::BM)) return cudaErrorInvalidValue;
     if (!encode_f16_tmap(&tmB, b16, K, n_rows_b, tc::BK, tc::BN)) return cudaErrorInvalidValue;
-    k_tc_gemm<<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
+    if (grouped) {
+        k_tc_gemm<true><<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
+        return cudaGetLastError();
+    }
+    k_tc_gemm<false><<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.ksplit == 1) return e;
     const uint64_t n = (uint64_t)p.N * p.M;

@@ -358,6 +358,82 @@ def test_config5_zipf_moe_sampled(q8, o):
     assert not np.any(np.isnan(got)), "some routed output row was never written"
 
 
+def _ids_with_counts(counts, k, seed):
+    """int32 [n_pairs / k, k]: expert e appears counts[e] times, in a seeded random order."""
+    flat = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    assert flat.size % k == 0
+    flat = np.random.default_rng(seed).permutation(flat).astype(np.int32)
+    return flat.reshape(-1, k)
+
+
+# Groups around the tensor-core class's edges: 64 rows stays on the GEMV, 65 is
+# the smallest tensor-core group, 127 / 128 / 129 straddle one 128-token tile,
+# 300 spans three; the small groups take the two GEMV classes.
+TC_COUNTS = [65, 127, 128, 129, 200, 300, 1, 2, 3, 5, 8, 9, 16, 17, 33, 64]
+
+
+@pytest.mark.parametrize("in_dim,out_dim", [(256, 200), (2048, 136)])
+def test_moe_tensor_core_class_every_output(q8, o, in_dim, out_dim):
+    """Batches of >= 1024 pairs send groups of more than 64 rows to the grouped tcgen05
+    GEMM; every output of every class is checked, and a second call must agree bit for bit."""
+    n_exp, k = len(TC_COUNTS), 3
+    ids = _ids_with_counts(TC_COUNTS, k, seed=81)
+    n_tok = ids.shape[0]
+    assert n_tok * k >= 1024
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=82)
+    stride = out_dim * in_dim // QK * QB
+    Wd = dev(W)
+    for per_pair in (0, 1):
+        x = inputs.normal((n_tok * k if per_pair else n_tok, in_dim), seed=83 + per_pair, p_out=0.01)
+        ref, bound, flag = o.moe(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), per_pair, n_tok)
+        assert flag == 0
+        buf, n = gpu_moe(q8, Wd, n_exp, stride, ids, x, per_pair, out_dim)
+        assert q8.q8_last_error() == 0
+        got = fetch(buf, n, ref.shape)
+        assert_close(got, ref, bound, f"moe tensor-core class per_pair={per_pair}")
+        buf2, _ = gpu_moe(q8, Wd, n_exp, stride, ids, x, per_pair, out_dim)
+        assert np.array_equal(fetch(buf2, n, ref.shape), got)
+
+
+def test_moe_tensor_core_class_empty(q8, o):
+    """A batch large enough for the tensor-core class, but no group of more than 64 rows."""
+    n_exp, n_tok, k, in_dim, out_dim = 64, 512, 2, 256, 72
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=84)
+    assert np.bincount(ids.reshape(-1), minlength=n_exp).max() <= 64
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=85)
+    stride = out_dim * in_dim // QK * QB
+    x = inputs.normal((n_tok, in_dim), seed=86)
+    ref, bound, _ = o.moe(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == 0
+    assert_close(fetch(buf, n, ref.shape), ref, bound, "moe without tensor-core groups")
+
+
+def test_moe_tensor_core_budget_overflow_sampled(q8, o):
+    """Experts of 4096 x 16384 expand to 128 MiB of fp16 each, so the 2 GiB budget takes 16
+    of the 20 qualifying groups (ties by id: experts 0..15); 16..19 stay on the GEMV.
+    Whole output rows of the first and last tensor-core experts and of every overflow
+    expert are checked, plus random elements."""
+    n_exp, k, in_dim, out_dim, per = 20, 1, 16384, 4096, 70
+    ids = _ids_with_counts([per] * n_exp, k, seed=87)
+    n_tok = ids.shape[0]
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=88)
+    stride = out_dim * (in_dim // QK) * QB
+    x = inputs.normal((n_tok, in_dim), seed=89)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == 0
+    got = fetch(buf, n, (n_tok * k, out_dim))
+    flat = ids.reshape(-1)
+    whole = [int(np.flatnonzero(flat == e)[j]) for e, j in ((0, 0), (15, -1), (16, 0), (17, 5), (18, 33), (19, -1))]
+    g = np.random.default_rng(90)
+    pair = np.concatenate([g.integers(0, n_tok * k, 2000), np.repeat(whole, out_dim)])
+    row = np.concatenate([g.integers(0, out_dim, 2000), np.tile(np.arange(out_dim), len(whole))])
+    ref, bound, flag = o.moe_sample(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok, pair, row)
+    assert flag == 0
+    assert_close(got[pair, row], ref, bound, "moe budget overflow")
+    assert not np.any(np.isnan(got)), "some routed output row was never written"
+
+
 # ------------------------------------------------------------------ repack
 def test_repack_layout_and_parity(q8, o):
     in_dim, out_dim, n_tok = 1024, 200, 13
