@@ -265,7 +265,7 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     p.err = s->err;
     const uint64_t units = tiles * ksplit;
     const int grid = (int)(units < (uint64_t)s->num_sms ? units : (uint64_t)s->num_sms);
-    return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, out_dim, b16, n_ld, grid, st); }));
+    return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, b16, n_ld, grid, st); }));
 }
 
 }  // namespace
@@ -370,21 +370,16 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     const uint64_t n_pairs = n_tok * k;
     const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
     const size_t plan_bytes = q8::route_plan_bytes(n_expert);
-    // Tensor-core class: at most tc_cap experts of more than MOE_TC_MIN_ROWS rows,
-    // their weights expanded to fp16 slots of slot_rows rows.
-    const uint64_t slot_rows = (out_dim + 127) & ~(uint64_t)127;
+    // Tensor-core class: experts of more than MOE_TC_MIN_ROWS rows, read as raw
+    // Q8_0 rows by the grouped GEMM; their activation rows go to the fp16 operand.
     uint64_t tc_cap = 0;
     if (nb % 8 == 0 && n_pairs >= q8::MOE_TC_MIN_PAIRS) {
         tc_cap = n_pairs / (q8::MOE_TC_MIN_ROWS + 1);
         if (tc_cap > n_expert) tc_cap = n_expert;
-        const uint64_t by_budget = q8::MOE_TC_BUDGET / (slot_rows * in_dim * 2);
-        if (tc_cap > by_budget) tc_cap = by_budget;
     }
-    uint64_t tc_rows = max_rows < n_pairs + 15 * tc_cap + 16 ? max_rows : n_pairs + 15 * tc_cap + 16;
+    const uint64_t tc_rows = max_rows < n_pairs + 15 * tc_cap + 16 ? max_rows : n_pairs + 15 * tc_cap + 16;
     const uint64_t tc_ld = ((tc_rows + 127) & ~(uint64_t)127) + 128;   // a tile may start at the last row
-    const size_t tc_bytes = tc_cap ? align256(tc_cap * slot_rows * in_dim * 2) + align256(nb * tc_cap * slot_rows * 4) +
-                                         align256(tc_ld * in_dim * 2) + align256(nb * tc_ld * 4)
-                                   : 0;
+    const size_t tc_bytes = tc_cap ? align256(tc_ld * in_dim * 2) + align256(nb * tc_ld * 4) : 0;
     const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * plan_bytes + align256(max_rows * 4) * 2 +
                         planes_bytes(max_rows, in_dim) + tc_bytes;
     if ((rc = reserve_scratch(s, need))) return rc;
@@ -396,8 +391,6 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     int32_t *src_row = cv.take<int32_t>(max_rows * 4);
     int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
     float *dx = cv.take<float>(max_rows * nb * sizeof(float));
-    __half *a16 = tc_cap ? cv.take<__half>(tc_cap * slot_rows * in_dim * 2) : nullptr;
-    float *dwT = tc_cap ? cv.take<float>(nb * tc_cap * slot_rows * 4) : nullptr;
     __half *b16 = tc_cap ? cv.take<__half>(tc_ld * in_dim * 2) : nullptr;
     float *dxT = tc_cap ? cv.take<float>(nb * tc_ld * 4) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -409,10 +402,6 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     if (e != cudaSuccess) return Q8_ECUDA;
     auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes); };
     if (tc_cap) {
-        e = q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W_experts), (uint32_t)out_dim, (uint32_t)nb,
-                                 (uint32_t)(tc_cap * slot_rows), s->num_sms, st, plan_of(2), expert_stride_bytes,
-                                 (uint32_t)slot_rows, (uint32_t)tc_cap);
-        if (e != cudaSuccess) return Q8_ECUDA;
         e = q8::launch_quantize_planes_tc(qx, dx, b16, dxT, tc_ld, plan_of(2), x, in_dim, max_rows, src_row,
                                           s->num_sms, st);
     } else {
@@ -464,18 +453,18 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     tp.ksplit = 1;
     tp.kb_per = (int)nb;
     tp.dxT = dxT;
-    tp.dwT = dwT;
+    tp.dwT = nullptr;
     tp.n_ld = tc_ld;
-    tp.m_ld = tc_cap * slot_rows;
+    tp.m_ld = 0;
     tp.out = out;
     tp.partial = nullptr;
     tp.err = s->err;
     tp.plan = plan_of(2);
     tp.row_to_out = row_to_out;
-    tp.slot_rows = (int)slot_rows;
     return status_of(timed_launch(st, [&] {
         if (tc_cap) {
-            cudaError_t e2 = q8::launch_tc_gemm(tp, a16, tc_cap * slot_rows, b16, tc_ld, s->num_sms, st);
+            cudaError_t e2 = q8::launch_tc_gemm_raw(tp, static_cast<const uint8_t *>(W_experts), n_expert,
+                                                    expert_stride_bytes, b16, tc_ld, s->num_sms, st);
             if (e2 != cudaSuccess) return e2;
         }
         g.plan = plan_of(0);

@@ -62,11 +62,11 @@ cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, 
 
 // Routing (q8_moe.cu): buckets pairs by expert and writes three plans, one per
 // size class of expert group: class 0 = groups of <= 8 rows (GEMV, one 8-token
-// MMA tile), class 1 = more rows (GEMV, 16-token groups: a group of 300 rows is 19
+// MMA tile), class 1 = more rows (GEMV, 16-token groups: a group of 60 rows is 4
 // token groups, each streaming the expert's weights, which stay in L2 while the
-// groups run side by side), class 2 = the largest groups, more than
-// MOE_TC_MIN_ROWS rows each, at most tc_cap of them (tcgen05 GEMM on the
-// expert's weights expanded to fp16; items are 128-row x 128-token tiles).
+// groups run side by side), class 2 = groups of more than MOE_TC_MIN_ROWS rows,
+// at most tc_cap of them (the grouped tcgen05 GEMM on raw Q8_0 expert rows;
+// items are 128-row x 128-token tiles).
 // Experts are taken largest first, so the class-2 groups own plane rows
 // [0, row_end).  Each plan is a PlanHeader followed by Segment[n_expert];
 // GEMV items are rows_gemv rows x one token group.
@@ -74,9 +74,8 @@ cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, 
 //   counts, row0_of: int32[n_expert] scratch
 constexpr int ROUTE_CLASSES = 3;
 constexpr int ROUTE_GEMV_CLASSES = 2;          // classes 0 and 1 run on the GEMV
-constexpr int MOE_TC_MIN_ROWS = 64;            // class 2 takes groups of more rows than this
+constexpr int MOE_TC_MIN_ROWS = 16;            // class 2 takes groups of more rows than this
 constexpr uint64_t MOE_TC_MIN_PAIRS = 1024;    // ... in batches of at least this many pairs
-constexpr uint64_t MOE_TC_BUDGET = 2ull << 30; // bytes of expanded fp16 expert weights per call
 uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
 size_t route_plan_bytes(uint32_t n_expert);
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
@@ -152,23 +151,24 @@ struct TcParams {
     float *out;            // [N][M]
     float *partial;        // [ksplit][N][M] or nullptr
     int *err;
-    // grouped (routed experts, plan != nullptr): the units of the class-2 plan.
-    // Segment s multiplies expert slot s (a16 rows [s * slot_rows, s * slot_rows + M))
-    // by plane rows [row0, row0 + count) and writes output row row_to_out[plane row].
-    // N, ksplit and kb_per are unused (no K split).
+    // grouped (routed experts, plan != nullptr; raw weights only): the units of
+    // the class-2 plan.  Segment s multiplies its expert's rows by plane rows
+    // [row0, row0 + count) and writes output row row_to_out[plane row].  N,
+    // ksplit and kb_per are unused (no K split).
     const PlanHeader *plan;
     const int32_t *row_to_out;
-    int slot_rows;         // multiple of 128
 };
-// Expands rows x nb Q8_0 blocks of W into a16 / dwT.  With plan != nullptr it
-// expands every segment's expert (W + expert * expert_stride) into slot s,
-// a16 rows and dwT columns from s * slot_rows; n_slots_max bounds the grid.
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
-                             int num_sms, cudaStream_t st, const PlanHeader *plan = nullptr,
-                             uint64_t expert_stride = 0, uint32_t slot_rows = 0, uint32_t n_slots_max = 1);
-// n_rows_a / n_rows_b: rows of the a16 / b16 planes (the tensor maps' extents).
-cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, uint64_t n_rows_a, const __half *b16,
-                           uint64_t n_rows_b, int grid, cudaStream_t st);
+                             int num_sms, cudaStream_t st);
+// n_rows_b: rows of the b16 plane (the tensor map's extent).  Dense only.
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
+                           cudaStream_t st);
+// The same GEMM with the weights read as raw Q8_0 rows (n_mat matrices of M rows,
+// mat_stride bytes apart; grouped units take the segment's expert) and converted
+// to fp16 in shared memory: no a16 / dwT planes.  nb % 8 == 0 and, dense,
+// kb_per % 8 == 0; W and mat_stride 16-byte aligned.
+cudaError_t launch_tc_gemm_raw(const TcParams &p, const uint8_t *W, uint64_t n_mat, uint64_t mat_stride,
+                               const __half *b16, uint64_t n_rows_b, int grid, cudaStream_t st);
 cudaError_t launch_quantize_f16t(__half *q16, float *dxT, const float *x, uint64_t in_dim, uint64_t n_tok,
                                  uint64_t n_ld, int num_sms, cudaStream_t st);
 cudaError_t launch_unpack_f16t(__half *q16, float *dxT, const uint8_t *xq, uint64_t in_dim, uint64_t n_tok,

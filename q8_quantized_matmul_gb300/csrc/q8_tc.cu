@@ -18,19 +18,26 @@
 // multiply-adds, and the fp32 pipe, not the tensor pipe, sets the ceiling
 // (about half the fp16 tensor rate).
 //
-// Warp roles (320 threads, one persistent CTA per SM):
-//   warp 0  TMA producer: per stage of K = 64 (two blocks) the fp16 weight tile
-//           (128 x 64, 128-byte swizzle), the fp16 activation tile (128 x 64,
-//           128-byte swizzle), and the two blocks' scales (1-D bulk copies);
-//           six stages.
+// Warp roles (one persistent CTA per SM):
+//   warp 0  TMA producer: per stage of K = 64 (two blocks) the fp16 activation
+//           tile (128 x 64, 128-byte swizzle) and its two blocks' scales (1-D
+//           bulk copies); with fp16 weights also the weight tile and scales
+//           (six stages), with raw weights one copy of 8 raw Q8_0 blocks x 128
+//           rows per four stages into a ring of two (four stages).
 //   warp 1  allocates TMEM (512 columns) and issues the UMMAs from one thread;
 //           tcgen05.commit signals "slot full" and, per stage, "stage consumed".
 //   2..9    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the 128
 //           columns; arrives "slot empty" after reading, "stage empty" after
 //           using the stage's scales.
-// Work units are (128-row tile, 128-token tile, K split); with fewer tiles than
-// SMs, K is split and the partial sums are added by a second kernel in a fixed
-// order (deterministic).  Every wait is bounded.
+//   10, 11  raw weights only: converters.  Each stage's weight tile is written
+//           from the raw copy as exact fp16 in the layout the fp16 tensor map
+//           gives, with the weight scales beside it, then handed to the tensor
+//           core (proxy fence + the stage's "full" barrier).
+// Dense work units are (128-row tile, 128-token tile, K split); with fewer tiles
+// than SMs, K is split and the partial sums are added by a second kernel in a
+// fixed order (deterministic).  Grouped units (routed experts) come from the
+// routing plan: (expert group, 128-row tile, 128-token tile), output rows
+// scattered through the plane-row -> output-row map.  Every wait is bounded.
 #include <cuda.h>
 
 #include "q8_common.cuh"
@@ -42,21 +49,34 @@ namespace tc {
 constexpr int BM = 128;                                // weight rows per tile (UMMA M)
 constexpr int BN = 128;                                // tokens per tile (UMMA N)
 constexpr int BK = 64;                                 // K elements per stage (two blocks)
-constexpr int NSTAGE = 6;
 constexpr int A_BYTES = BM * BK * 2;                   // 16384
 constexpr int B_BYTES = BN * BK * 2;                   // 16384
 constexpr int DX_BYTES = 2 * BN * 4;                   // 1024
 constexpr int DW_BYTES = 2 * BM * 4;                   // 1024
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + DX_BYTES + DW_BYTES;   // 34 KiB, 1 KiB aligned
 constexpr int NUM_EPI = 8;                             // epilogue warps: 2 per TMEM lane quarter
-constexpr int EPI_COLS = BN / (NUM_EPI / 4);          // 64 columns per epilogue warp
-constexpr int NTHREADS = (2 + NUM_EPI) * 32;
 constexpr int NSLOT_T = 4;                             // TMEM accumulator slots of BN columns
 constexpr uint32_t TMEM_COLS = NSLOT_T * BN;           // 512
-constexpr int NBAR = 2 * NSTAGE + 2 * NSLOT_T + 1;     // full, empty, tfull, tempty, done
-constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + 1024 + NBAR * 8 + 16;
-static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-static_assert(SMEM <= 227 * 1024, "shared memory");
+// Raw-weight variant: the A operand arrives as raw Q8_0 rows, 8 blocks (272
+// bytes, 68 words) x 128 rows per copy, and converter warps write the fp16
+// tile and the weight scales of each stage.
+constexpr int RAW_KB = 8;                              // blocks per raw copy (K = 256)
+constexpr int RAW_WORDS = RAW_KB * QB / 4;             // 68
+constexpr int RAW_BYTES = BM * RAW_WORDS * 4;          // 34816 = 34 KiB
+constexpr int NRAW = 2;                                // raw copies in flight
+constexpr int NCONV = 2;                               // converter warps
+static_assert(STAGE_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stage alignment");
+
+template <bool RAW> struct Cfg {
+    static constexpr int NSTAGE = RAW ? 4 : 6;
+    static constexpr int NTHREADS = (2 + NUM_EPI + (RAW ? NCONV : 0)) * 32;
+    static constexpr int NRAWS = RAW ? NRAW : 0;
+    // full, empty, tfull, tempty, done, raw full, raw empty
+    static constexpr int NBAR = 2 * NSTAGE + 2 * NSLOT_T + 1 + 2 * NRAWS;
+    static constexpr size_t SMEM =
+        (size_t)NSTAGE * STAGE_BYTES + (size_t)NRAWS * RAW_BYTES + 1024 + NBAR * 8 + 16;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 }  // namespace tc
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -67,6 +87,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -142,10 +173,23 @@ __device__ __forceinline__ uint64_t tc_pair(float w) {
     return r;
 }
 
+// Four int8 -> two half2 (exact): bias each byte to unsigned, place it under the
+// fp16 exponent of 1024, subtract 1024 + 128.
+__device__ __forceinline__ void s8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 struct TcUnit {
     int mt, nt, kb0, kb1;
-    int a_row, b_row;   // first a16 / b16 plane row of the tile (also the dwT / dxT column)
+    int a_row, b_row;   // first weight row (in the expert) / b16 plane row of the tile,
+                        // also the dwT / dxT column
     int n_valid;        // grouped: tokens of the tile that belong to the segment
+    int expert;         // grouped: expert matrix of the tile
+    int ncols;          // UMMA N of the tile: 128, or 64 / 32 for a group's short last tile
 };
 
 // Dense: units are (128-row tile, 128-token tile, K split).
@@ -163,12 +207,14 @@ __device__ __forceinline__ bool tc_unit_dense(const TcParams &p, int u, TcUnit &
     w.a_row = w.mt * tc::BM;
     w.b_row = w.nt * tc::BN;
     w.n_valid = tc::BN;
+    w.expert = 0;
+    w.ncols = tc::BN;
     return true;
 }
 
 // Grouped: the plan's segments in order, each m_tiles x ceil(count / 128)
-// units from item_start on (weight tile fastest).  Units only grow along a
-// CTA's loop, so the segment cursor only moves forward.
+// units from item_start on (weight tile fastest), on the segment's expert.
+// Units only grow along a CTA's loop, so the segment cursor only moves forward.
 __device__ __forceinline__ bool tc_unit_grouped(const TcParams &p, int u, TcUnit &w, int &seg) {
     const PlanHeader *h = p.plan;
     if (u >= h->n_items) return false;
@@ -181,9 +227,11 @@ __device__ __forceinline__ bool tc_unit_grouped(const TcParams &p, int u, TcUnit
     w.nt = v / m_tiles;
     w.kb0 = 0;
     w.kb1 = p.nb;
-    w.a_row = seg * p.slot_rows + w.mt * tc::BM;
+    w.a_row = w.mt * tc::BM;
     w.b_row = sg[seg].row0 + w.nt * tc::BN;
     w.n_valid = min(tc::BN, sg[seg].count - w.nt * tc::BN);
+    w.expert = sg[seg].expert;
+    w.ncols = w.n_valid > 64 ? 128 : (w.n_valid > 32 ? 64 : 32);
     return true;
 }
 
@@ -193,10 +241,138 @@ __device__ __forceinline__ bool tc_unit(const TcParams &p, int u, TcUnit &w, int
     else return tc_unit_dense(p, u, w);
 }
 
-template <bool G>
-__global__ void __launch_bounds__(tc::NTHREADS, 1)
+// One stage's share of a raw copy (blocks 2J, 2J + 1 of the copy's 8) for rows
+// ct and ct + 64: fp16 quants into the stage's A tile in the 128-byte-swizzled
+// K-major layout (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8), the
+// layout the fp16 tensor map writes), scales into dws[j][r].  The 68 bytes of a
+// row's block pair start at word r * 68 + 17 J: five aligned 16-byte loads from
+// word r * 68 + (17 J & ~3) cover them, and rows 8 apart fall in different
+// bank groups.
+template <int J>
+__device__ __forceinline__ void tc_convert(const uint8_t *raw, uint8_t *a16, float *dws, int ct) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = ct + rr * 64;
+        const uint4 *src = reinterpret_cast<const uint4 *>(raw) + (r * tc::RAW_WORDS + ((17 * J) & ~3)) / 4;
+        uint32_t w[20];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const uint4 v = src[i];
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        constexpr int o = (17 * J) & 3;   // word offset of the pair inside the loaded words
+        uint8_t *row = a16 + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t q0, q1;
+            if (c < 4) {   // block 2J: quants at byte 2 of the pair
+                q0 = funnel16(w[o + 2 * c], w[o + 2 * c + 1]);
+                q1 = funnel16(w[o + 2 * c + 1], w[o + 2 * c + 2]);
+            } else {       // block 2J + 1: quants at byte 36 (word 9)
+                q0 = w[o + 9 + 2 * (c - 4)];
+                q1 = w[o + 10 + 2 * (c - 4)];
+            }
+            uint32_t h0, h1, h2, h3;
+            s8x4_to_half2x2(q0, h0, h1);
+            s8x4_to_half2x2(q1, h2, h3);
+            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = make_uint4(h0, h1, h2, h3);
+        }
+        dws[r] = half_bits_to_float((uint16_t)(w[o] & 0xffffu));
+        dws[tc::BM + r] = half_bits_to_float((uint16_t)(w[o + 8] >> 16));
+    }
+}
+
+// Epilogue warp state: stage ring and TMEM slot counters, carried across units.
+struct TcEpi {
+    uint8_t *smem;
+    uint64_t *full, *empty, *tfull, *tempty;
+    volatile int *abort_flag;
+    uint32_t lane_addr;   // TMEM address of this warp's lane quarter
+    int m, h, lane;       // tile row, column half, lane
+    uint32_t stage, phase, blk;
+};
+
+// One unit of an epilogue warp: NCW = columns of this warp (half the unit's N).
+// Per block, the warp's columns leave TMEM in one batch of x16 loads and are
+// folded into acc as isum * d_x[t] * d_w[o]; then the unit's outputs are stored.
+template <int NCW, bool G, int NSTAGE>
+__device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit &w, TcEpi &e) {
+    using namespace tc;
+    uint64_t acc[NCW / 2];   // fp32 pairs
+#pragma unroll
+    for (int i = 0; i < NCW / 2; ++i) acc[i] = 0ull;
+    for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+        const uint8_t *st = e.smem + (size_t)e.stage * STAGE_BYTES;
+        // the scales arrive with the stage (the MMA warp waited on the same barrier)
+        mbar_wait(&e.full[e.stage], e.phase, p.err, e.abort_flag);
+        const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
+        const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+        for (int j = 0; j < 2; ++j, ++e.blk) {
+            const uint32_t slot = e.blk % NSLOT_T;
+            mbar_wait(&e.tfull[slot], (e.blk / NSLOT_T) & 1u, p.err, e.abort_flag);
+            tc_fence_after();
+            const uint64_t ww = tc_pair(dws[j * BM + e.m]);
+            const float *dxj = dxs + j * BN + e.h * NCW;
+            const uint32_t col0 = e.lane_addr + slot * BN + e.h * NCW;
+            uint32_t v[NCW / 16][16];
+#pragma unroll
+            for (int c = 0; c < NCW / 16; ++c) tc_ld16(col0 + c * 16, v[c]);
+            tc_wait_ld();
+#pragma unroll
+            for (int c = 0; c < NCW / 16; ++c) {
+                const float4 *x4 = reinterpret_cast<const float4 *>(dxj + c * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 x = x4[i];
+                    tc_fold(acc[c * 8 + 2 * i], v[c][4 * i], v[c][4 * i + 1], x.x, x.y, ww);
+                    tc_fold(acc[c * 8 + 2 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3], x.z, x.w, ww);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (e.lane == 0) mbar_arrive(&e.tempty[slot]);
+        }
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(&e.empty[e.stage]);
+        if (++e.stage == NSTAGE) {
+            e.stage = 0;
+            e.phase ^= 1u;
+        }
+    }
+    // ---- this unit's rows x this warp's tokens
+    const int row = w.mt * BM + e.m;
+    const int tok0 = e.h * NCW;                       // within the tile
+    if (row >= p.M) return;
+    if constexpr (G) {
+#pragma unroll
+        for (int i = 0; i < NCW / 2; ++i) {
+            const int t = tok0 + 2 * i;
+            if (t < w.n_valid)
+                p.out[(size_t)p.row_to_out[w.b_row + t] * p.M + row] = __uint_as_float((uint32_t)acc[i]);
+            if (t + 1 < w.n_valid)
+                p.out[(size_t)p.row_to_out[w.b_row + t + 1] * p.M + row] = __uint_as_float((uint32_t)(acc[i] >> 32));
+        }
+    } else {
+        const int ks = w.kb0 / p.kb_per;
+        float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
+#pragma unroll
+        for (int i = 0; i < NCW / 2; ++i) {
+            const int t = w.b_row + tok0 + 2 * i;
+            if (t < p.N) dst[(size_t)t * p.M + row] = __uint_as_float((uint32_t)acc[i]);
+            if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = __uint_as_float((uint32_t)(acc[i] >> 32));
+        }
+    }
+}
+
+template <bool G, bool RAW>
+__global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
     k_tc_gemm(const TcParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
     using namespace tc;
+    constexpr int NSTAGE = Cfg<RAW>::NSTAGE;
+    constexpr int NBAR = Cfg<RAW>::NBAR;
     if constexpr (G) {
         // The GEMV launched behind this grid waits for it before it reads or
         // writes anything this grid touches; let it take the SMs this grid frees.
@@ -206,23 +382,29 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_s = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((base_s + 1023u) & ~1023u) - base_s);      // 1 KiB aligned stages
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * STAGE_BYTES);
+    uint8_t *raw_s = smem + (size_t)NSTAGE * STAGE_BYTES;                     // raw copies (RAW only)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw_s + (size_t)Cfg<RAW>::NRAWS * RAW_BYTES);
     uint64_t *full = bars, *empty = bars + NSTAGE;
     uint64_t *tfull = bars + 2 * NSTAGE, *tempty = tfull + NSLOT_T, *done = tempty + NSLOT_T;
+    uint64_t *raw_full = done + 1, *raw_empty = raw_full + Cfg<RAW>::NRAWS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + NUM_EPI);   // MMA commit + every epilogue warp
+            mbar_init(&full[s], RAW ? 1 + NCONV : 1);   // producer (+ every converter warp)
+            mbar_init(&empty[s], 1 + NUM_EPI);           // MMA commit + every epilogue warp
         }
         for (int s = 0; s < NSLOT_T; ++s) {
             mbar_init(&tfull[s], 1);
             mbar_init(&tempty[s], NUM_EPI);
         }
         mbar_init(done, 1);
+        for (int s = 0; s < Cfg<RAW>::NRAWS; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], NCONV);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -242,24 +424,43 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
+            uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
             uint32_t fills[NSTAGE] = {};
+            uint32_t rfills[NRAW] = {};
             TcUnit w;
             int seg = 0;
             for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
                 const int m0 = w.a_row, n0 = w.b_row;
                 for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+                    if constexpr (RAW) {
+                        if ((kb - w.kb0) % RAW_KB == 0) {   // next raw copy: 8 blocks x 128 rows
+                            if (mbar_wait(&raw_empty[rs], rph ^ 1u, p.err, abort_flag)) {
+                                mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
+                                tma_load_3d(raw_s + (size_t)rs * RAW_BYTES, &tmA, (kb / RAW_KB) * RAW_WORDS, m0,
+                                            w.expert, &raw_full[rs]);
+                                ++rfills[rs];
+                            }
+                            if (++rs == NRAW) {
+                                rs = 0;
+                                rph ^= 1u;
+                            }
+                        }
+                    }
                     if (mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
                         uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
-                        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                        tma_load_2d(st, &tmA, kb * QK, m0, &full[stage]);
-                        tma_load_2d(st + A_BYTES, &tmB, kb * QK, n0, &full[stage]);
                         float *dxs = reinterpret_cast<float *>(st + A_BYTES + B_BYTES);
-                        float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+                        if constexpr (RAW) {
+                            mbar_arrive_expect_tx(&full[stage], B_BYTES + DX_BYTES);
+                        } else {
+                            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                            tma_load_2d(st, &tmA, kb * QK, m0, &full[stage]);
+                            float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+                            bulk_g2s(dws, p.dwT + (size_t)kb * p.m_ld + m0, BM * 4, &full[stage]);
+                            bulk_g2s(dws + BM, p.dwT + (size_t)(kb + 1) * p.m_ld + m0, BM * 4, &full[stage]);
+                        }
+                        tma_load_2d(st + A_BYTES, &tmB, kb * QK, n0, &full[stage]);
                         bulk_g2s(dxs, p.dxT + (size_t)kb * p.n_ld + n0, BN * 4, &full[stage]);
                         bulk_g2s(dxs + BN, p.dxT + (size_t)(kb + 1) * p.n_ld + n0, BN * 4, &full[stage]);
-                        bulk_g2s(dws, p.dwT + (size_t)kb * p.m_ld + m0, BM * 4, &full[stage]);
-                        bulk_g2s(dws + BM, p.dwT + (size_t)(kb + 1) * p.m_ld + m0, BM * 4, &full[stage]);
                         ++fills[stage];
                     }
                     if (++stage == NSTAGE) {
@@ -268,17 +469,23 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
                     }
                 }
             }
-            for (int s = 0; s < NSTAGE; ++s)
-                if (fills[s]) mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.err, nullptr);
+            if (*abort_flag) {
+                // let every copy this thread issued land before the CTA exits
+                const uint64_t t_end = global_timer_ns() + 1000000ull;
+                for (int s = 0; s < NSTAGE; ++s)
+                    if (fills[s]) mbar_drain(&full[s], (fills[s] - 1u) & 1u, t_end);
+                for (int s = 0; s < NRAW; ++s)
+                    if (rfills[s]) mbar_drain(&raw_full[s], (rfills[s] - 1u) & 1u, t_end);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = tc_idesc(BM, BN);
             uint32_t stage = 0, phase = 0, blk = 0;
             TcUnit w;
             int seg = 0;
             for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
+                const uint32_t idesc = tc_idesc(BM, w.ncols);
                 for (int kb = w.kb0; kb < w.kb1; kb += 2) {
                     mbar_wait(&full[stage], phase, p.err, abort_flag);
                     tc_fence_after();
@@ -306,85 +513,54 @@ __global__ void __launch_bounds__(tc::NTHREADS, 1)
             tc_commit(done);                          // all MMAs issued by this thread
             mbar_wait(done, 0, p.err, nullptr);
         }
-    } else {
+    } else if (warp < 2 + NUM_EPI) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;                // column half
         const int m = q * 32 + lane;                  // row within the tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-        uint32_t stage = 0, phase = 0, blk = 0;
+        TcEpi e{smem, full, empty, tfull, tempty, abort_flag, lane_addr, m, h, lane, 0u, 0u, 0u};
         TcUnit w;
         int seg = 0;
         for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
-            uint64_t acc[EPI_COLS / 2];   // this warp's columns as fp32 pairs
+            if (w.ncols == 128) tc_epilogue_unit<64, G, NSTAGE>(p, w, e);
+            else if (w.ncols == 64) tc_epilogue_unit<32, G, NSTAGE>(p, w, e);
+            else tc_epilogue_unit<16, G, NSTAGE>(p, w, e);
+        }
+    } else if constexpr (RAW) {
+        // ------------------------------------------------ converters: raw copy -> fp16 A tile + scales
+        const int ct = threadIdx.x - (2 + NUM_EPI) * 32;   // 0 .. 63
+        uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
+        TcUnit w;
+        int seg = 0;
+        for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
+            for (int kg = w.kb0; kg < w.kb1; kg += RAW_KB) {
+                const bool raw_ok = mbar_wait(&raw_full[rs], rph, p.err, abort_flag);
+                const uint8_t *raw = raw_s + (size_t)rs * RAW_BYTES;
 #pragma unroll
-            for (int i = 0; i < EPI_COLS / 2; ++i) acc[i] = 0ull;
-            for (int kb = w.kb0; kb < w.kb1; kb += 2) {
-                const uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
-                // the scales arrive with the stage (the MMA warp waited on the same barrier)
-                mbar_wait(&full[stage], phase, p.err, abort_flag);
-                const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
-                const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
-                for (int j = 0; j < 2; ++j, ++blk) {
-                    const uint32_t slot = blk % NSLOT_T;
-                    mbar_wait(&tfull[slot], (blk / NSLOT_T) & 1u, p.err, abort_flag);
-                    tc_fence_after();
-                    const uint64_t ww = tc_pair(dws[j * BM + m]);
-                    const float *dxj = dxs + j * BN + h * EPI_COLS;
-                    const uint32_t col0 = lane_addr + slot * BN + h * EPI_COLS;
-                    // the block's columns in one batch of TMEM loads and one wait
-                    uint32_t v[EPI_COLS / 16][16];
-#pragma unroll
-                    for (int c = 0; c < EPI_COLS / 16; ++c) tc_ld16(col0 + c * 16, v[c]);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < EPI_COLS / 16; ++c) {
-                        const float4 *x4 = reinterpret_cast<const float4 *>(dxj + c * 16);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float4 x = x4[i];
-                            tc_fold(acc[c * 8 + 2 * i], v[c][4 * i], v[c][4 * i + 1], x.x, x.y, ww);
-                            tc_fold(acc[c * 8 + 2 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3], x.z, x.w, ww);
-                        }
+                for (int J = 0; J < RAW_KB / 2; ++J) {
+                    const bool ok = mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag) && raw_ok;
+                    if (ok) {
+                        uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
+                        float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
+                        if (J == 0) tc_convert<0>(raw, st, dws, ct);
+                        else if (J == 1) tc_convert<1>(raw, st, dws, ct);
+                        else if (J == 2) tc_convert<2>(raw, st, dws, ct);
+                        else tc_convert<3>(raw, st, dws, ct);
+                        fence_async_smem();
                     }
-                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[slot]);
+                    if (ok && lane == 0) mbar_arrive(&full[stage]);
+                    if (++stage == NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == NSTAGE) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            // ---- write this unit's rows x this warp's tokens
-            const int row = w.mt * BM + m;
-            const int tok0 = h * EPI_COLS;            // within the tile
-            if constexpr (G) {
-                if (row < p.M) {
-#pragma unroll
-                    for (int i = 0; i < EPI_COLS / 2; ++i) {
-                        const int t = tok0 + 2 * i;
-                        if (t < w.n_valid)
-                            p.out[(size_t)p.row_to_out[w.b_row + t] * p.M + row] = __uint_as_float((uint32_t)acc[i]);
-                        if (t + 1 < w.n_valid)
-                            p.out[(size_t)p.row_to_out[w.b_row + t + 1] * p.M + row] =
-                                __uint_as_float((uint32_t)(acc[i] >> 32));
-                    }
-                }
-            } else {
-                const int ks = w.kb0 / p.kb_per;
-                float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
-                if (row < p.M) {
-#pragma unroll
-                    for (int i = 0; i < EPI_COLS / 2; ++i) {
-                        const int t = w.b_row + tok0 + 2 * i;
-                        const float lo = __uint_as_float((uint32_t)acc[i]);
-                        const float hi = __uint_as_float((uint32_t)(acc[i] >> 32));
-                        if (t < p.N) dst[(size_t)t * p.M + row] = lo;
-                        if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = hi;
-                    }
+                if (raw_ok && lane == 0) mbar_arrive(&raw_empty[rs]);
+                if (++rs == NRAW) {
+                    rs = 0;
+                    rph ^= 1u;
                 }
             }
         }
@@ -414,40 +590,24 @@ __global__ void __launch_bounds__(256) k_tc_reduce(float *__restrict__ out, cons
 // warp reads 32 consecutive 34-byte blocks (1088 contiguous bytes) and writes
 // 32 consecutive 64-byte runs; the scales go through shared memory and leave
 // as 32-byte runs of dwT.
-__device__ __forceinline__ void s8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    // bias each byte to unsigned, place it under the fp16 exponent of 1024, subtract 1024 + 128
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
 
 __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, float *__restrict__ dwT,
                                                    const uint8_t *__restrict__ W, uint32_t rows, uint32_t nb,
-                                                   uint32_t m_ld, const PlanHeader *plan, uint64_t expert_stride,
-                                                   uint32_t slot_rows) {
+                                                   uint32_t m_ld) {
     __shared__ float ds[8][33];
     const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const uint32_t tiles_r = (rows + 7) / 8, tiles_b = (nb + 31) / 32;
-    const uint64_t tiles_slot = (uint64_t)tiles_r * tiles_b;
-    const uint32_t n_slots = plan ? (uint32_t)plan->n_segments : 1u;
-    const Segment *segs = plan ? reinterpret_cast<const Segment *>(plan + 1) : nullptr;
-    const uint64_t tiles = tiles_slot * n_slots;
+    const uint64_t tiles = (uint64_t)tiles_r * tiles_b;
     for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const uint32_t slot = (uint32_t)(tile / tiles_slot);
-        const uint64_t ts = tile - (uint64_t)slot * tiles_slot;
-        const uint32_t tb = (uint32_t)(ts % tiles_b), tr = (uint32_t)(ts / tiles_b);
-        const uint8_t *Ws = plan ? W + (uint64_t)segs[slot].expert * expert_stride : W;
-        const uint64_t row_base = (uint64_t)slot * slot_rows;   // first a16 row / dwT column of the slot
+        const uint32_t tb = (uint32_t)(tile % tiles_b), tr = (uint32_t)(tile / tiles_b);
         const uint32_t r = tr * 8 + w, b = tb * 32 + l;
         if (r < rows && b < nb) {
-            const uint16_t *src = reinterpret_cast<const uint16_t *>(Ws + ((uint64_t)r * nb + b) * QB);
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(W + ((uint64_t)r * nb + b) * QB);
             uint16_t h[17];
 #pragma unroll
             for (int i = 0; i < 17; ++i) h[i] = __ldg(src + i);
             ds[w][l] = half_bits_to_float(h[0]);
-            uint4 *dst = reinterpret_cast<uint4 *>(a16 + (row_base + r) * nb * QK + (uint64_t)b * QK);
+            uint4 *dst = reinterpret_cast<uint4 *>(a16 + (uint64_t)r * nb * QK + (uint64_t)b * QK);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[4];
@@ -463,7 +623,7 @@ __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, flo
         {
             const uint32_t bb = threadIdx.x >> 3, rr = threadIdx.x & 7;   // 32 blocks x 8 rows
             const uint32_t r2 = tr * 8 + rr, b2 = tb * 32 + bb;
-            if (r2 < rows && b2 < nb) dwT[(uint64_t)b2 * m_ld + row_base + r2] = ds[rr][bb];
+            if (r2 < rows && b2 < nb) dwT[(uint64_t)b2 * m_ld + r2] = ds[rr][bb];
         }
         __syncthreads();
     }
@@ -471,45 +631,58 @@ __global__ void __launch_bounds__(256) k_tc_expand(__half *__restrict__ a16, flo
 
 bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                      uint32_t box_rows);
+bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
+                      uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
-                             int num_sms, cudaStream_t st, const PlanHeader *plan, uint64_t expert_stride,
-                             uint32_t slot_rows, uint32_t n_slots_max) {
-    const uint64_t tiles = (uint64_t)((rows + 7) / 8) * ((nb + 31) / 32) * n_slots_max;
+                             int num_sms, cudaStream_t st) {
+    const uint64_t tiles = (uint64_t)((rows + 7) / 8) * ((nb + 31) / 32);
     if (!tiles) return cudaSuccess;
     const uint64_t grid = tiles < (uint64_t)num_sms * 8 ? tiles : (uint64_t)num_sms * 8;
-    k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld, plan, expert_stride, slot_rows);
+    k_tc_expand<<<(int)grid, 256, 0, st>>>(a16, dwT, W, rows, nb, m_ld);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, uint64_t n_rows_a, const __half *b16,
-                           uint64_t n_rows_b, int grid, cudaStream_t st) {
-    const bool grouped = p.plan != nullptr;
-    static bool attr_done[2] = {false, false};
-    if (!attr_done[grouped]) {
-        cudaError_t e = grouped ? cudaFuncSetAttribute(k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       (int)tc::SMEM)
-                                : cudaFuncSetAttribute(k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       (int)tc::SMEM);
+template <bool G, bool RAW>
+static cudaError_t launch_tc_variant(const TcParams &p, const CUtensorMap &tmA, const CUtensorMap &tmB, int grid,
+                                     cudaStream_t st) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<G, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)tc::Cfg<RAW>::SMEM);
         if (e != cudaSuccess) return e;
-        attr_done[grouped] = true;
+        attr_done = true;
     }
-    alignas(64) CUtensorMap tmA, tmB;
-    const uint64_t K = (uint64_t)p.nb * QK;
-    if (!encode_f16_tmap(&tmA, a16, K, n_rows_a, tc::BK, tc::BM)) return cudaErrorInvalidValue;
-    if (!encode_f16_tmap(&tmB, b16, K, n_rows_b, tc::BK, tc::BN)) return cudaErrorInvalidValue;
-    if (grouped) {
-        k_tc_gemm<true><<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
-        return cudaGetLastError();
-    }
-    k_tc_gemm<false><<<grid, tc::NTHREADS, tc::SMEM, st>>>(p, tmA, tmB);
+    k_tc_gemm<G, RAW><<<grid, tc::Cfg<RAW>::NTHREADS, tc::Cfg<RAW>::SMEM, st>>>(p, tmA, tmB);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.ksplit == 1) return e;
+    if (e != cudaSuccess || G || p.ksplit == 1) return e;
     const uint64_t n = (uint64_t)p.N * p.M;
     uint64_t g = (n + 255) / 256;
     if (g > 4096) g = 4096;
     k_tc_reduce<<<(int)g, 256, 0, st>>>(p.out, p.partial, n, p.ksplit);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const TcParams &p, const __half *a16, const __half *b16, uint64_t n_rows_b, int grid,
+                           cudaStream_t st) {
+    if (p.plan) return cudaErrorInvalidValue;   // grouped units read raw weights
+    alignas(64) CUtensorMap tmA, tmB;
+    const uint64_t K = (uint64_t)p.nb * QK;
+    if (!encode_f16_tmap(&tmA, a16, K, (uint64_t)p.M, tc::BK, tc::BM)) return cudaErrorInvalidValue;
+    if (!encode_f16_tmap(&tmB, b16, K, n_rows_b, tc::BK, tc::BN)) return cudaErrorInvalidValue;
+    return launch_tc_variant<false, false>(p, tmA, tmB, grid, st);
+}
+
+cudaError_t launch_tc_gemm_raw(const TcParams &p, const uint8_t *W, uint64_t n_mat, uint64_t mat_stride,
+                               const __half *b16, uint64_t n_rows_b, int grid, cudaStream_t st) {
+    if (p.nb % tc::RAW_KB || (!p.plan && p.kb_per % tc::RAW_KB)) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap tmA, tmB;
+    const uint64_t K = (uint64_t)p.nb * QK;
+    if (!encode_rows_tmap(&tmA, W, (uint64_t)p.nb * QB, (uint64_t)p.M, n_mat, mat_stride, tc::RAW_WORDS, tc::BM))
+        return cudaErrorInvalidValue;
+    if (!encode_f16_tmap(&tmB, b16, K, n_rows_b, tc::BK, tc::BN)) return cudaErrorInvalidValue;
+    return p.plan ? launch_tc_variant<true, true>(p, tmA, tmB, grid, st)
+                  : launch_tc_variant<false, true>(p, tmA, tmB, grid, st);
 }
 
 }  // namespace q8

@@ -366,15 +366,16 @@ def _ids_with_counts(counts, k, seed):
     return flat.reshape(-1, k)
 
 
-# Groups around the tensor-core class's edges: 64 rows stays on the GEMV, 65 is
-# the smallest tensor-core group, 127 / 128 / 129 straddle one 128-token tile,
-# 300 spans three; the small groups take the two GEMV classes.
-TC_COUNTS = [65, 127, 128, 129, 200, 300, 1, 2, 3, 5, 8, 9, 16, 17, 33, 64]
+# Groups around the class edges: 1-8 rows run on the GEMV in one 8-token tile,
+# 9-16 in 16-token groups, larger groups on the grouped tcgen05 GEMM, whose
+# last tile of a group is 32, 64 or 128 tokens wide: 17 / 32 / 33 / 64 / 65
+# straddle those widths, 127 / 128 / 129 one full tile, 300 spans three.
+TC_COUNTS = [65, 127, 128, 129, 200, 300, 1, 2, 3, 5, 8, 9, 16, 17, 33, 64, 32, 1]
 
 
 @pytest.mark.parametrize("in_dim,out_dim", [(256, 200), (2048, 136)])
 def test_moe_tensor_core_class_every_output(q8, o, in_dim, out_dim):
-    """Batches of >= 1024 pairs send groups of more than 64 rows to the grouped tcgen05
+    """Batches of >= 1024 pairs send groups of more than 16 rows to the grouped tcgen05
     GEMM; every output of every class is checked, and a second call must agree bit for bit."""
     n_exp, k = len(TC_COUNTS), 3
     ids = _ids_with_counts(TC_COUNTS, k, seed=81)
@@ -396,10 +397,10 @@ def test_moe_tensor_core_class_every_output(q8, o, in_dim, out_dim):
 
 
 def test_moe_tensor_core_class_empty(q8, o):
-    """A batch large enough for the tensor-core class, but no group of more than 64 rows."""
-    n_exp, n_tok, k, in_dim, out_dim = 64, 512, 2, 256, 72
+    """A batch large enough for the tensor-core class, but no group of more than 16 rows."""
+    n_exp, n_tok, k, in_dim, out_dim = 256, 512, 2, 256, 72
     ids = inputs.route_uniform(n_tok, k, n_exp, seed=84)
-    assert np.bincount(ids.reshape(-1), minlength=n_exp).max() <= 64
+    assert np.bincount(ids.reshape(-1), minlength=n_exp).max() <= 16
     W = inputs.weights(n_exp * out_dim, in_dim, seed=85)
     stride = out_dim * in_dim // QK * QB
     x = inputs.normal((n_tok, in_dim), seed=86)
@@ -409,11 +410,10 @@ def test_moe_tensor_core_class_empty(q8, o):
     assert_close(fetch(buf, n, ref.shape), ref, bound, "moe without tensor-core groups")
 
 
-def test_moe_tensor_core_budget_overflow_sampled(q8, o):
-    """Experts of 4096 x 16384 expand to 128 MiB of fp16 each, so the 2 GiB budget takes 16
-    of the 20 qualifying groups (ties by id: experts 0..15); 16..19 stay on the GEMV.
-    Whole output rows of the first and last tensor-core experts and of every overflow
-    expert are checked, plus random elements."""
+def test_moe_tensor_core_large_experts_sampled(q8, o):
+    """Twenty experts of 4096 x 16384 with 70 rows each, all on the grouped tcgen05 GEMM
+    (32 weight tiles per expert, 64 raw copies of 8 blocks per tile).  Whole output rows of
+    six experts are checked, plus random elements."""
     n_exp, k, in_dim, out_dim, per = 20, 1, 16384, 4096, 70
     ids = _ids_with_counts([per] * n_exp, k, seed=87)
     n_tok = ids.shape[0]
@@ -430,7 +430,7 @@ def test_moe_tensor_core_budget_overflow_sampled(q8, o):
     row = np.concatenate([g.integers(0, out_dim, 2000), np.tile(np.arange(out_dim), len(whole))])
     ref, bound, flag = o.moe_sample(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok, pair, row)
     assert flag == 0
-    assert_close(got[pair, row], ref, bound, "moe budget overflow")
+    assert_close(got[pair, row], ref, bound, "moe large experts")
     assert not np.any(np.isnan(got)), "some routed output row was never written"
 
 
