@@ -214,12 +214,18 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
 }
 
 // Prefill (n_tok > 16, even number of blocks per row): tcgen05 GEMM on fp16
-// operands.  Weights are expanded to an fp16 plane with block-major scales,
-// activations quantised straight into the fp16 operand; K is split when the
-// output tiles do not fill the GPU.
+// operands, activations quantised straight into the fp16 operand; K is split
+// when the output tiles do not fill the GPU.  Up to TC_RAW_MAX_TOKENS tokens
+// (and in_dim / 32 a multiple of 8) the GEMM reads the raw Q8_0 rows and
+// converts them in shared memory; beyond that the weights are first expanded
+// to an fp16 plane with block-major scales (the in-kernel conversion costs
+// about 12 % of the GEMM, the expansion a fixed pass over the weights).
+constexpr uint64_t TC_RAW_MAX_TOKENS = 640;
 int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
            const void *xq, uint64_t n_tok, cudaStream_t st) {
     const uint64_t nb = in_dim / q8::QK;
+    const bool raw = nb % 8 == 0 && n_tok <= TC_RAW_MAX_TOKENS;   // raw Q8_0 rows, no fp16 plane
+    const uint64_t kb_align = raw ? 8 : 2;
     const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
     const uint64_t n_ld = (n_tok + 127) & ~(uint64_t)127;
     const uint64_t tiles = (m_ld / 128) * (n_ld / 128);
@@ -231,20 +237,21 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
         if (ksplit < 1) ksplit = 1;
     }
     uint64_t kb_per = (nb + ksplit - 1) / ksplit;
-    kb_per = (kb_per + 1) & ~(uint64_t)1;
+    kb_per = (kb_per + kb_align - 1) / kb_align * kb_align;
     ksplit = (nb + kb_per - 1) / kb_per;
-    const size_t need = align256(out_dim * in_dim * 2) + align256(nb * m_ld * 4) + align256(n_ld * in_dim * 2) +
-                        align256(nb * n_ld * 4) + (ksplit > 1 ? align256(ksplit * n_tok * out_dim * 4) : 0);
+    const size_t need = (raw ? 0 : align256(out_dim * in_dim * 2) + align256(nb * m_ld * 4)) +
+                        align256(n_ld * in_dim * 2) + align256(nb * n_ld * 4) +
+                        (ksplit > 1 ? align256(ksplit * n_tok * out_dim * 4) : 0);
     int rc = reserve_scratch(s, need);
     if (rc) return rc;
     Carver cv(s->scratch);
-    __half *a16 = cv.take<__half>(out_dim * in_dim * 2);
-    float *dwT = cv.take<float>(nb * m_ld * 4);
+    __half *a16 = raw ? nullptr : cv.take<__half>(out_dim * in_dim * 2);
+    float *dwT = raw ? nullptr : cv.take<float>(nb * m_ld * 4);
     __half *b16 = cv.take<__half>(n_ld * in_dim * 2);
     float *dxT = cv.take<float>(nb * n_ld * 4);
     float *partial = ksplit > 1 ? cv.take<float>(ksplit * n_tok * out_dim * 4) : nullptr;
-    if ((rc = status_of(q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W), (uint32_t)out_dim,
-                                             (uint32_t)nb, (uint32_t)m_ld, s->num_sms, st))))
+    if (!raw && (rc = status_of(q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W), (uint32_t)out_dim,
+                                                     (uint32_t)nb, (uint32_t)m_ld, s->num_sms, st))))
         return rc;
     cudaError_t e = x ? q8::launch_quantize_f16t(b16, dxT, x, in_dim, n_tok, n_ld, s->num_sms, st)
                       : q8::launch_unpack_f16t(b16, dxT, static_cast<const uint8_t *>(xq), in_dim, n_tok, n_ld,
@@ -265,6 +272,10 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     p.err = s->err;
     const uint64_t units = tiles * ksplit;
     const int grid = (int)(units < (uint64_t)s->num_sms ? units : (uint64_t)s->num_sms);
+    if (raw)
+        return status_of(timed_launch(st, [&] {
+            return q8::launch_tc_gemm_raw(p, static_cast<const uint8_t *>(W), 1, 0, b16, n_ld, grid, st);
+        }));
     return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, b16, n_ld, grid, st); }));
 }
 

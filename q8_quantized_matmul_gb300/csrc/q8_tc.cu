@@ -69,7 +69,11 @@ static_assert(STAGE_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stage alignment
 
 template <bool RAW> struct Cfg {
     static constexpr int NSTAGE = RAW ? 4 : 6;
-    static constexpr int NTHREADS = (2 + NUM_EPI + (RAW ? NCONV : 0)) * 32;
+    // MMA issuers: the issuing thread shares its scheduler with two folding
+    // epilogue warps and slows down while they fold; with fp16 weights a second
+    // issuer on another scheduler takes every other stage.
+    static constexpr int NMMA = RAW ? 1 : 2;
+    static constexpr int NTHREADS = (2 + NUM_EPI + (RAW ? NCONV : 0) + (NMMA - 1)) * 32;
     static constexpr int NRAWS = RAW ? NRAW : 0;
     // full, empty, tfull, tempty, done, raw full, raw empty
     static constexpr int NBAR = 2 * NSTAGE + 2 * NSLOT_T + 1 + 2 * NRAWS;
@@ -182,6 +186,9 @@ __device__ __forceinline__ void s8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
+
+// A predicate the whole warp agrees on (lane 0's value).
+__device__ __forceinline__ bool warp_all(bool v) { return __shfl_sync(0xffffffffu, (int)v, 0) != 0; }
 
 struct TcUnit {
     int mt, nt, kb0, kb1;
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
             mbar_init(&tfull[s], 1);
             mbar_init(&tempty[s], NUM_EPI);
         }
-        mbar_init(done, 1);
+        mbar_init(done, Cfg<RAW>::NMMA);
         for (int s = 0; s < Cfg<RAW>::NRAWS; ++s) {
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], NCONV);
@@ -423,30 +430,36 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
-            uint32_t fills[NSTAGE] = {};
-            uint32_t rfills[NRAW] = {};
-            TcUnit w;
-            int seg = 0;
-            for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
-                const int m0 = w.a_row, n0 = w.b_row;
-                for (int kb = w.kb0; kb < w.kb1; kb += 2) {
-                    if constexpr (RAW) {
-                        if ((kb - w.kb0) % RAW_KB == 0) {   // next raw copy: 8 blocks x 128 rows
-                            if (mbar_wait(&raw_empty[rs], rph ^ 1u, p.err, abort_flag)) {
+        // The whole warp walks the loop and waits (lane 0 issues): a warp with
+        // one lane looping and 31 parked at the final barrier slows the other
+        // warps of its scheduler.
+        uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
+        uint32_t fills[NSTAGE] = {};
+        uint32_t rfills[NRAW] = {};
+        TcUnit w;
+        int seg = 0;
+        for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
+            const int m0 = w.a_row, n0 = w.b_row;
+            for (int kb = w.kb0; kb < w.kb1; kb += 2) {
+                if constexpr (RAW) {
+                    if ((kb - w.kb0) % RAW_KB == 0) {   // next raw copy: 8 blocks x 128 rows
+                        if (warp_all(mbar_wait(&raw_empty[rs], rph ^ 1u, p.err, abort_flag))) {
+                            if (lane == 0) {
                                 mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
                                 tma_load_3d(raw_s + (size_t)rs * RAW_BYTES, &tmA, (kb / RAW_KB) * RAW_WORDS, m0,
                                             w.expert, &raw_full[rs]);
-                                ++rfills[rs];
                             }
-                            if (++rs == NRAW) {
-                                rs = 0;
-                                rph ^= 1u;
-                            }
+                            ++rfills[rs];
+                        }
+                        __syncwarp();
+                        if (++rs == NRAW) {
+                            rs = 0;
+                            rph ^= 1u;
                         }
                     }
-                    if (mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
+                }
+                if (warp_all(mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag))) {
+                    if (lane == 0) {
                         uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
                         float *dxs = reinterpret_cast<float *>(st + A_BYTES + B_BYTES);
                         if constexpr (RAW) {
@@ -461,40 +474,53 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                         tma_load_2d(st + A_BYTES, &tmB, kb * QK, n0, &full[stage]);
                         bulk_g2s(dxs, p.dxT + (size_t)kb * p.n_ld + n0, BN * 4, &full[stage]);
                         bulk_g2s(dxs + BN, p.dxT + (size_t)(kb + 1) * p.n_ld + n0, BN * 4, &full[stage]);
-                        ++fills[stage];
                     }
+                    ++fills[stage];
+                }
+                __syncwarp();
+                if (++stage == NSTAGE) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (*abort_flag && lane == 0) {
+            // let every copy this warp issued land before the CTA exits
+            const uint64_t t_end = global_timer_ns() + 1000000ull;
+            for (int s = 0; s < NSTAGE; ++s)
+                if (fills[s]) mbar_drain(&full[s], (fills[s] - 1u) & 1u, t_end);
+            for (int s = 0; s < NRAW; ++s)
+                if (rfills[s]) mbar_drain(&raw_full[s], (rfills[s] - 1u) & 1u, t_end);
+        }
+        __syncwarp();
+    } else if (warp == 1 || (Cfg<RAW>::NMMA > 1 && warp == 2 + NUM_EPI)) {
+        // ------------------------------------------------ MMA issuers (stage s: issuer s % NMMA)
+        // whole warp in the loop and the waits, lane 0 issues
+        constexpr uint32_t NMMA = Cfg<RAW>::NMMA;
+        const uint32_t which = warp == 1 ? 0u : 1u;
+        uint32_t stage = 0, phase = 0, blk = 0, ks = 0;
+        TcUnit w;
+        int seg = 0;
+        for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
+            const uint32_t idesc = tc_idesc(BM, w.ncols);
+            for (int kb = w.kb0; kb < w.kb1; kb += 2, ++ks) {
+                if (ks % NMMA != which) {   // the other issuer's stage
+                    blk += 2;
                     if (++stage == NSTAGE) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    continue;
                 }
-            }
-            if (*abort_flag) {
-                // let every copy this thread issued land before the CTA exits
-                const uint64_t t_end = global_timer_ns() + 1000000ull;
-                for (int s = 0; s < NSTAGE; ++s)
-                    if (fills[s]) mbar_drain(&full[s], (fills[s] - 1u) & 1u, t_end);
-                for (int s = 0; s < NRAW; ++s)
-                    if (rfills[s]) mbar_drain(&raw_full[s], (rfills[s] - 1u) & 1u, t_end);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, blk = 0;
-            TcUnit w;
-            int seg = 0;
-            for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
-                const uint32_t idesc = tc_idesc(BM, w.ncols);
-                for (int kb = w.kb0; kb < w.kb1; kb += 2) {
-                    mbar_wait(&full[stage], phase, p.err, abort_flag);
+                mbar_wait(&full[stage], phase, p.err, abort_flag);
+                tc_fence_after();
+                const uint32_t a_s = smem_addr(smem + (size_t)stage * STAGE_BYTES);
+                const uint32_t b_s = a_s + A_BYTES;
+                for (int j = 0; j < 2; ++j, ++blk) {
+                    const uint32_t slot = blk % NSLOT_T;
+                    mbar_wait(&tempty[slot], ((blk / NSLOT_T) & 1u) ^ 1u, p.err, abort_flag);
                     tc_fence_after();
-                    const uint32_t a_s = smem_addr(smem + (size_t)stage * STAGE_BYTES);
-                    const uint32_t b_s = a_s + A_BYTES;
-                    for (int j = 0; j < 2; ++j, ++blk) {
-                        const uint32_t slot = blk % NSLOT_T;
-                        mbar_wait(&tempty[slot], ((blk / NSLOT_T) & 1u) ^ 1u, p.err, abort_flag);
-                        tc_fence_after();
+                    if (lane == 0) {
                         const uint32_t d_tmem = tmem_base + slot * BN;
 #pragma unroll
                         for (int k16 = 0; k16 < 2; ++k16) {
@@ -503,16 +529,19 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                         }
                         tc_commit(&tfull[slot]);
                     }
-                    tc_commit(&empty[stage]);
-                    if (++stage == NSTAGE) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    __syncwarp();
+                }
+                if (lane == 0) tc_commit(&empty[stage]);
+                __syncwarp();
+                if (++stage == NSTAGE) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            tc_commit(done);                          // all MMAs issued by this thread
-            mbar_wait(done, 0, p.err, nullptr);
         }
+        if (lane == 0) tc_commit(done);               // all MMAs issued by this thread
+        __syncwarp();
+        mbar_wait(done, 0, p.err, nullptr);
     } else if (warp < 2 + NUM_EPI) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp

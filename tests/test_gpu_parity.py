@@ -118,6 +118,8 @@ def test_quantize_prefill_size_bit_exact(q8, o):
 SHAPES = [
     (256, 16, 1), (512, 100, 3), (1024, 33, 16), (2048, 250, 17), (256, 1000, 64), (768, 77, 65),
     (4096, 40, 130), (8192, 24, 5), (1280, 131, 200),
+    # prefill with nb % 8 != 0: weights expanded to an fp16 plane instead of read raw
+    (2112, 130, 150),
     # in_dim % 256 != 0: rows not 16-byte aligned (slow path)
     (32, 5, 1), (96, 19, 7), (160, 50, 20), (4000, 8, 2),
 ]
