@@ -58,7 +58,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "moe"),
+    ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "prefill_long", "moe",
+                                               "moe_zipf", "moe_zipf_small"),
                     help="run one workload's call a few times without timing (for ncu captures)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -578,11 +579,21 @@ def profile_case(case: str):
         W = torch.from_numpy(inputs.weights(1024, 32768, seed=1)).to(dev)
         x = torch.from_numpy(inputs.normal((512, 32768), seed=1)).to(dev)
         fn = lambda: q8.matmul(W, x, 1024)
-    else:
+    elif case == "prefill_long":   # long-prefill shape: the weights go through the fp16 plane
+        W = torch.from_numpy(inputs.weights(32768, 1024, seed=3)).to(dev)
+        x = torch.from_numpy(inputs.normal((4096, 1024), seed=3)).to(dev)
+        fn = lambda: q8.matmul(W, x, 32768)
+    elif case == "moe":
         ids = torch.from_numpy(inputs.route_uniform(64, 6, 256, seed=0)).to(dev)
         W = torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=2)).to(dev)
         x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
         fn = lambda: q8.moe_matmul(W, 256, 2048 * 128 * QB, ids, x, False, 2048)
+    else:   # routed gate/up with Zipf(1.1) top-6: the layer slice's (moe_zipf) or 1024 tokens over 64 experts
+        n, ne = (4096, 256) if case == "moe_zipf" else (1024, 64)
+        ids = torch.from_numpy(inputs.route_zipf(n, 6, ne, s=1.1, seed=0)).to(dev)
+        W = torch.from_numpy(inputs.weights(ne * 2048, 4096, seed=2)).to(dev)
+        x = torch.from_numpy(inputs.normal((n, 4096), seed=2)).to(dev)
+        fn = lambda: q8.moe_matmul(W, ne, 2048 * 128 * QB, ids, x, False, 2048)
     for _ in range(5):
         fn()
     torch.cuda.synchronize()
