@@ -637,6 +637,10 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     if (warp == PRODUCER) {
         if (!p.weights_early) grid_dep_wait();
         const uint32_t planned = produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane);
+        // Every weight copy of this CTA is issued: a kernel launched behind this one
+        // with programmatic serialisation may take the SMs freed from here on (its
+        // reads of anything this grid writes wait in griddepcontrol.wait).
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // After a timed-out wait: let the copies still in flight land (with one
         // overall time limit) before the CTA's shared memory goes away.
         if (*abort_flag && lane == 0) {
