@@ -391,8 +391,9 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     const uint64_t tc_rows = max_rows < n_pairs + 15 * tc_cap + 16 ? max_rows : n_pairs + 15 * tc_cap + 16;
     const uint64_t tc_ld = ((tc_rows + 127) & ~(uint64_t)127) + 128;   // a tile may start at the last row
     const size_t tc_bytes = tc_cap ? align256(tc_ld * in_dim * 2) + align256(nb * tc_ld * 4) : 0;
+    const bool gemv_path = nb % 8 == 0;   // routed GEMV / tensor-core kernels (else the generic kernel)
     const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * plan_bytes + align256(max_rows * 4) * 2 +
-                        planes_bytes(max_rows, in_dim) + tc_bytes;
+                        (gemv_path ? align256(n_pairs * 4) : 0) + planes_bytes(max_rows, in_dim) + tc_bytes;
     if ((rc = reserve_scratch(s, need))) return rc;
     Carver cv(s->scratch);
     int32_t *counts = cv.take<int32_t>(n_expert * 4);
@@ -400,6 +401,7 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * plan_bytes);
     int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
     int32_t *src_row = cv.take<int32_t>(max_rows * 4);
+    int32_t *dst_row = gemv_path ? cv.take<int32_t>(n_pairs * 4) : nullptr;
     int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
     float *dx = cv.take<float>(max_rows * nb * sizeof(float));
     __half *b16 = tc_cap ? cv.take<__half>(tc_ld * in_dim * 2) : nullptr;
@@ -408,16 +410,18 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     uint32_t rows_gemv = (uint32_t)((out_dim + 15) & ~(uint64_t)15);
     if (rows_gemv > 128) rows_gemv = 128;
     cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_gemv,
-                                     (uint32_t)tc_cap, counts, row0_of, plans, row_to_out, src_row, max_rows, out,
-                                     s->err, s->num_sms, st);
+                                     (uint32_t)tc_cap, counts, row0_of, plans, row_to_out, src_row, dst_row, max_rows,
+                                     out, s->err, s->num_sms, st);
     if (e != cudaSuccess) return Q8_ECUDA;
     auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes); };
-    if (tc_cap) {
-        e = q8::launch_quantize_planes_tc(qx, dx, b16, dxT, tc_ld, plan_of(2), x, in_dim, max_rows, src_row,
-                                          s->num_sms, st);
-    } else {
+    // The GEMV and tensor-core kernels read only the real rows: the quantiser walks
+    // the pairs and leaves the padding rows unwritten.  The generic kernel gets
+    // zero padding rows.
+    if (gemv_path)
+        e = q8::launch_quantize_pairs(qx, dx, b16, dxT, tc_ld, tc_cap ? plan_of(2) : nullptr, x, in_dim, n_pairs, k,
+                                      x_per_pair, dst_row, s->num_sms, st);
+    else
         e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
-    }
     if (e != cudaSuccess) return Q8_ECUDA;
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W_experts);

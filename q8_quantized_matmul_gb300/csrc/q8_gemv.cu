@@ -335,8 +335,9 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
             dxs[e] = d;
         }
     } else {
-        // MMA B fragments, fp16: [block][N tile][lane][16 bytes].  The planes hold
-        // 16-row-padded token groups, so rows past ntok read zeros.
+        // MMA B fragments, fp16: [block][N tile][lane][16 bytes].  Rows past the
+        // group's ntok are not read (routed planes leave their padding rows
+        // unwritten): their fragments and scales are zero.
         // Words of the activation block a lane's fragment is built from:
         //   odd block: words c, 4+c;  even block: x[4c+2..4c+5] from words c, c+1 and
         //   x[4c+18..4c+21] from words c+4, c+5 (c < 3); lane 3: x[14..17] from words 3, 4
@@ -355,11 +356,15 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
                 const int8_t *xr = p.qx + (uint64_t)(it.xrow0 + lg) * p.in_dim + (uint64_t)(kb0 + b) * QK;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
-                    wv[r][t][0] = __ldg(xt + lc);
-                    wv[r][t][1] = __ldg(xt + i1);
-                    wv[r][t][2] = __ldg(xt + i2);
-                    wv[r][t][3] = __ldg(xt + i3);
+                    if (lg + 8u * (uint32_t)t < (uint32_t)it.ntok) {
+                        const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
+                        wv[r][t][0] = __ldg(xt + lc);
+                        wv[r][t][1] = __ldg(xt + i1);
+                        wv[r][t][2] = __ldg(xt + i2);
+                        wv[r][t][3] = __ldg(xt + i3);
+                    } else {
+                        wv[r][t][0] = wv[r][t][1] = wv[r][t][2] = wv[r][t][3] = 0u;
+                    }
                 }
             }
         }
@@ -369,7 +374,9 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
         for (int r = 0; r < RD; ++r) {
             const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
             const uint32_t b = e >> 4, t = e & 15;
-            dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8)) ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b) : 0.0f;
+            dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8) && t < (uint32_t)it.ntok)
+                        ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b)
+                        : 0.0f;
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {

@@ -46,11 +46,13 @@ struct MmaParams {
 cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
                                    const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st);
-// As launch_quantize_planes, except that rows [0, tc_plan->row_end) go to the
-// tensor-core operand instead: fp16 quants q16[r][in_dim], scales dxT[b][n_ld].
-cudaError_t launch_quantize_planes_tc(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
-                                      const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_rows,
-                                      const int32_t *src_row, int num_sms, cudaStream_t st);
+// Routed pairs straight to their plane rows: pair p (activation row p, or p / k
+// when x holds one row per token) goes to plane row dst_row[p]; padding rows are
+// not written.  With tc_plan, rows [0, tc_plan->row_end) go to the tensor-core
+// operand instead: fp16 quants q16[r][in_dim], scales dxT[b][n_ld].
+cudaError_t launch_quantize_pairs(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
+                                  const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_pairs,
+                                  uint32_t k, int x_per_pair, const int32_t *dst_row, int num_sms, cudaStream_t st);
 cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *xq, uint64_t in_dim, uint64_t n_rows,
                                  uint64_t n_src, int num_sms, cudaStream_t st);
 
@@ -71,6 +73,7 @@ cudaError_t launch_generic(const MmaParams &p, int max_items_hint, int num_sms, 
 // [0, row_end).  Each plan is a PlanHeader followed by Segment[n_expert];
 // GEMV items are rows_gemv rows x one token group.
 //   row_to_out, src_row: int32[max_rows], max_rows = route_max_rows(n_pairs, n_expert)
+//   dst_row (optional): int32[n_pairs], pair -> plane row (-1: bad id)
 //   counts, row0_of: int32[n_expert] scratch
 constexpr int ROUTE_CLASSES = 3;
 constexpr int ROUTE_GEMV_CLASSES = 2;          // classes 0 and 1 run on the GEMV
@@ -80,8 +83,8 @@ uint64_t route_max_rows(uint64_t n_pairs, uint64_t n_expert);
 size_t route_plan_bytes(uint32_t n_expert);
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
                          uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap, int32_t *counts, int32_t *row0_of,
-                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out,
-                         int *err, int num_sms, cudaStream_t st);
+                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, int32_t *dst_row, uint64_t max_rows,
+                         float *out, int *err, int num_sms, cudaStream_t st);
 
 // Weight-streaming GEMV (q8_gemv.cu).  Modes: 0 = dp4a, token groups of <= 2;
 // 1 = fp16 MMA, one 8-token N tile; 2 = two N tiles (<= 16 tokens).

@@ -72,67 +72,157 @@ size_t route_plan_bytes(uint32_t n_expert) {
 
 __device__ __forceinline__ int route_class_tokens(int cls) { return cls == 0 ? 8 : 16; }   // GEMV token group
 
+// Block-wide exclusive scan of (a, b) pairs, one pair per thread; returns the
+// totals through *ta / *tb.  sh: 2 * (blockDim.x / 32) ints.
+__device__ __forceinline__ void block_scan2(int &a, int &b, int *sh, int *ta, int *tb) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int ia = a, ib = b;   // inclusive within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+            ia += xa;
+            ib += xb;
+        }
+    }
+    __syncthreads();
+    if (lane == 31) {
+        sh[w] = ia;
+        sh[nw + w] = ib;
+    }
+    __syncthreads();
+    int oa = 0, ob = 0, sa = 0, sb = 0;
+    for (int i = 0; i < nw; ++i) {
+        if (i < w) {
+            oa += sh[i];
+            ob += sh[nw + i];
+        }
+        sa += sh[i];
+        sb += sh[nw + i];
+    }
+    a = oa + ia - a;
+    b = ob + ib - b;
+    *ta = sa;
+    *tb = sb;
+}
+
+// One CTA.  Touched experts ordered by count (descending, ties by id); in that
+// order the classes are contiguous: [0, n2) tensor-core class, [n2, n_gt8)
+// class 1, the rest class 0.  Rows and items are exclusive scans over the order.
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
                                                                uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap,
                                                                uint8_t *plans, size_t plan_stride,
                                                                int32_t *__restrict__ row0_of) {
-    extern __shared__ int32_t sh_plan[];   // order[n_expert] (sorted position -> expert)
-    int32_t *order = sh_plan;
-    __shared__ int n_active_sh;
-    if (threadIdx.x == 0) n_active_sh = 0;
-    __syncthreads();
-    // Rank of each touched expert: larger count first, then smaller id.
+    extern __shared__ int32_t sh_plan[];   // cnt[n_expert], order[n_expert]
+    int32_t *cnt = sh_plan;
+    int32_t *order = sh_plan + n_expert;
+    __shared__ int tot_sh[3];              // touched, > MOE_TC_MIN_ROWS, > 8
+    __shared__ int scan_sh[2 * (ROUTE_THREADS / 32)];
+    __shared__ int mark_sh[4];             // item / row scans at the class starts n2 and n_gt8
+    if (threadIdx.x < 3) tot_sh[threadIdx.x] = 0;
     for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
-        const int ce = counts[e];
-        if (ce > 0) {
-            int rank = 0;
-            for (uint32_t f = 0; f < n_expert; ++f) {
-                const int cf = counts[f];
-                rank += (cf > ce) || (cf == ce && f < e);
-            }
-            order[rank] = (int32_t)e;   // touched experts take ranks 0..n_active-1
-            atomicAdd(&n_active_sh, 1);
-        }
+        cnt[e] = counts[e];
         row0_of[e] = -1;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const int n_rb_gemv = (int)((out_dim + rows_gemv - 1) / rows_gemv);
-        const int m_tiles_tc = (int)((out_dim + 127) / 128);
-        PlanHeader *hdr[ROUTE_CLASSES];
-        Segment *segs[ROUTE_CLASSES];
-        int nseg[ROUTE_CLASSES] = {}, nitem[ROUTE_CLASSES] = {}, rend[ROUTE_CLASSES] = {};
-        for (int k = 0; k < ROUTE_CLASSES; ++k) {
-            hdr[k] = reinterpret_cast<PlanHeader *>(plans + k * plan_stride);
-            segs[k] = reinterpret_cast<Segment *>(hdr[k] + 1);
-        }
-        const int n_active = n_active_sh;
-        int row = 0;
-        for (int s = 0; s < n_active; ++s) {
-            const int e = order[s];
-            const int ce = counts[e];
-            // counts only fall along the order, so class 2 is a prefix of it
-            const int k = (ce > MOE_TC_MIN_ROWS && nseg[2] < (int)tc_cap) ? 2 : (ce <= 8 ? 0 : 1);
-            Segment &sg = segs[k][nseg[k]++];
-            sg.expert = e;
-            sg.row0 = row;
-            sg.count = ce;
-            sg.item_start = nitem[k];
-            row0_of[e] = row;
-            row += (ce + 15) & ~15;
-            rend[k] = row;
-            if (k == 2) {
-                nitem[k] += m_tiles_tc * ((ce + 127) / 128);
-            } else {
-                const int tg = route_class_tokens(k);
-                nitem[k] += n_rb_gemv * ((ce + tg - 1) / tg);
+    int my_active = 0, my_gt_t = 0, my_gt8 = 0;
+    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
+        const int ce = cnt[e];
+        if (ce > 0) {
+            int rank = 0;
+            for (uint32_t f = 0; f < n_expert; ++f) {
+                const int cf = cnt[f];
+                rank += (cf > ce) || (cf == ce && f < e);
             }
+            order[rank] = (int32_t)e;   // touched experts take ranks 0..n_active-1
+            ++my_active;
+            my_gt_t += ce > MOE_TC_MIN_ROWS;
+            my_gt8 += ce > 8;
         }
+    }
+    if (my_active) {
+        atomicAdd(&tot_sh[0], my_active);
+        atomicAdd(&tot_sh[1], my_gt_t);
+        atomicAdd(&tot_sh[2], my_gt8);
+    }
+    __syncthreads();
+    const int n_active = tot_sh[0];
+    const int n2 = min(tot_sh[1], (int)tc_cap);
+    const int n_gt8 = tot_sh[2];
+    const int n_rb_gemv = (int)((out_dim + rows_gemv - 1) / rows_gemv);
+    const int m_tiles_tc = (int)((out_dim + 127) / 128);
+    auto cls_of = [&](int sp) { return sp < n2 ? 2 : (sp < n_gt8 ? 1 : 0); };
+    auto items_of = [&](int sp, int ce) {
+        const int k = cls_of(sp);
+        if (k == 2) return m_tiles_tc * ((ce + 127) / 128);
+        const int tg = route_class_tokens(k);
+        return n_rb_gemv * ((ce + tg - 1) / tg);
+    };
+    // each thread owns a contiguous chunk of sorted positions
+    const int chunk = (n_active + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int s0 = min(n_active, (int)threadIdx.x * chunk), s1 = min(n_active, s0 + chunk);
+    int rows = 0, items = 0;
+    for (int sp = s0; sp < s1; ++sp) {
+        const int ce = cnt[order[sp]];
+        rows += (ce + 15) & ~15;
+        items += items_of(sp, ce);
+    }
+    int rows_total, items_total;
+    block_scan2(rows, items, scan_sh, &rows_total, &items_total);
+    // scans at the class starts (n2: class 1 starts; n_gt8: class 0 starts)
+    if (threadIdx.x < 4) mark_sh[threadIdx.x] = -1;
+    __syncthreads();
+    {
+        int r = rows, it = items;
+        for (int sp = s0; sp <= s1; ++sp) {
+            if (sp == n2 && sp <= n_active) {
+                mark_sh[0] = it;
+                mark_sh[1] = r;
+            }
+            if (sp == n_gt8 && sp <= n_active) {
+                mark_sh[2] = it;
+                mark_sh[3] = r;
+            }
+            if (sp == s1) break;
+            const int ce = cnt[order[sp]];
+            r += (ce + 15) & ~15;
+            it += items_of(sp, ce);
+        }
+    }
+    __syncthreads();
+    // positions past every chunk (empty trailing classes) take the totals
+    const int it_at_n2 = mark_sh[0] >= 0 ? mark_sh[0] : items_total, row_at_n2 = mark_sh[1] >= 0 ? mark_sh[1] : rows_total;
+    const int it_at_8 = mark_sh[2] >= 0 ? mark_sh[2] : items_total, row_at_8 = mark_sh[3] >= 0 ? mark_sh[3] : rows_total;
+    Segment *segs[ROUTE_CLASSES];
+    for (int k = 0; k < ROUTE_CLASSES; ++k)
+        segs[k] = reinterpret_cast<Segment *>(reinterpret_cast<PlanHeader *>(plans + k * plan_stride) + 1);
+    {
+        int r = rows, it = items;
+        for (int sp = s0; sp < s1; ++sp) {
+            const int e = order[sp], ce = cnt[e];
+            const int k = cls_of(sp);
+            const int cstart = k == 2 ? 0 : (k == 1 ? n2 : n_gt8);
+            const int ibase = k == 2 ? 0 : (k == 1 ? it_at_n2 : it_at_8);
+            Segment &sg = segs[k][sp - cstart];
+            sg.expert = e;
+            sg.row0 = r;
+            sg.count = ce;
+            sg.item_start = it - ibase;
+            row0_of[e] = r;
+            r += (ce + 15) & ~15;
+            it += items_of(sp, ce);
+        }
+    }
+    if (threadIdx.x == 0) {
+        const int nseg[3] = {n_active - n_gt8, n_gt8 - n2, n2};
+        const int nitem[3] = {items_total - it_at_8, it_at_8 - it_at_n2, it_at_n2};
+        const int rend[3] = {n_active > n_gt8 ? rows_total : 0, n_gt8 > n2 ? row_at_8 : 0, n2 > 0 ? row_at_n2 : 0};
         for (int k = 0; k < ROUTE_CLASSES; ++k) {
-            hdr[k]->n_segments = nseg[k];
-            hdr[k]->n_items = nitem[k];
-            hdr[k]->n_rows = row;
-            hdr[k]->row_end = rend[k];
+            PlanHeader *h = reinterpret_cast<PlanHeader *>(plans + k * plan_stride);
+            h->n_segments = nseg[k];
+            h->n_items = nitem[k];
+            h->n_rows = rows_total;
+            h->row_end = rend[k];
         }
     }
 }
@@ -141,7 +231,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__r
                                                                uint32_t k, int x_per_pair,
                                                                const int32_t *__restrict__ row0_of,
                                                                int32_t *__restrict__ row_to_out,
-                                                               int32_t *__restrict__ src_row) {
+                                                               int32_t *__restrict__ src_row,
+                                                               int32_t *__restrict__ dst_row) {
     __shared__ int warp_tot[ROUTE_THREADS / 32];
     const int e = blockIdx.x;
     const int row0 = row0_of[e];
@@ -163,6 +254,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__r
             const int pos = base + before + __popc(m & ((1u << lane) - 1u));
             row_to_out[row0 + pos] = (int32_t)p;
             src_row[row0 + pos] = (int32_t)(x_per_pair ? p : p / k);
+            if (dst_row) dst_row[p] = row0 + pos;
         }
         base += total;
         __syncthreads();
@@ -171,13 +263,14 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__r
 
 cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert, int x_per_pair,
                          uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap, int32_t *counts, int32_t *row0_of,
-                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, uint64_t max_rows, float *out,
-                         int *err, int num_sms, cudaStream_t st) {
+                         uint8_t *plans, int32_t *row_to_out, int32_t *src_row, int32_t *dst_row, uint64_t max_rows,
+                         float *out, int *err, int num_sms, cudaStream_t st) {
     const uint64_t n_pairs = n_tok * k;
     cudaError_t e;
-    // Padding rows map to nothing: -1 everywhere first.
+    // Padding rows map to nothing, pairs with a bad id to no row: -1 everywhere first.
     if ((e = cudaMemsetAsync(row_to_out, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(src_row, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
+    if (dst_row && (e = cudaMemsetAsync(dst_row, 0xff, n_pairs * sizeof(int32_t), st)) != cudaSuccess) return e;
     k_route_count<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, n_expert, counts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     int grid_bad = (int)((n_pairs + 7) / 8);
@@ -185,7 +278,7 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
     if (grid_bad < 1) grid_bad = 1;
     k_route_bad<<<grid_bad, 256, 0, st>>>(ids, n_pairs, n_expert, out_dim, out, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t plan_smem = (size_t)n_expert * sizeof(int32_t);
+    const size_t plan_smem = 2 * (size_t)n_expert * sizeof(int32_t);
     if (plan_smem > 48 * 1024) {
         if ((e = cudaFuncSetAttribute(k_route_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem)) !=
             cudaSuccess)
@@ -194,7 +287,8 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
     k_route_plan<<<1, ROUTE_THREADS, plan_smem, st>>>(counts, n_expert, out_dim, rows_gemv, tc_cap, plans,
                                                       route_plan_bytes(n_expert), row0_of);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_route_fill<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, k, x_per_pair, row0_of, row_to_out, src_row);
+    k_route_fill<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, k, x_per_pair, row0_of, row_to_out, src_row,
+                                                       dst_row);
     return cudaGetLastError();
 }
 

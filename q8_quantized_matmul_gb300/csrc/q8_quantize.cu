@@ -43,8 +43,6 @@ __global__ void __launch_bounds__(256) k_quantize_blocks(uint8_t *__restrict__ x
 // dplane [n_rows][nb] fp32 (the stored binary16 scale as fp32).  Output row r
 // is quantised from x row src_row[r] when src_row is given (a negative entry
 // gives a zero row), else from x row r when r < n_src, else it is zero.
-// With TC, rows [0, tc_plan->row_end) are written to the tensor-core operand
-// (fp16 quants q16[r][in_dim], scales dxT[b][n_ld]) instead of the planes.
 __device__ __forceinline__ void store_f16_quants(__half *dst, const QuantBlock &qb) {
     uint32_t h[4];
 #pragma unroll
@@ -54,17 +52,13 @@ __device__ __forceinline__ void store_f16_quants(__half *dst, const QuantBlock &
     *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-template <bool TC>
 __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qplane, float *__restrict__ dplane,
                                                          const float *__restrict__ x, uint64_t in_dim,
                                                          uint64_t n_rows, const int32_t *__restrict__ src_row,
-                                                         uint64_t n_src, __half *__restrict__ q16,
-                                                         float *__restrict__ dxT, uint64_t n_ld,
-                                                         const PlanHeader *tc_plan) {
+                                                         uint64_t n_src) {
     // The matmul that follows only prefetches weights before it waits for this
     // grid to finish, so it may be scheduled now.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const uint64_t tc_rows = TC ? (uint64_t)tc_plan->row_end : 0;
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_rows * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -83,10 +77,7 @@ __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qp
             for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
         }
         const QuantBlock qb = quantize8(x8);
-        if (TC && live && r < tc_rows) {
-            store_f16_quants(q16 + r * in_dim + b * QK + lane_q * 8, qb);
-            if (lane_q == 0) dxT[b * n_ld + r] = qb.d_stored;
-        } else if (live) {
+        if (live) {
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -95,6 +86,54 @@ __global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qp
             }
             *reinterpret_cast<uint2 *>(qplane + r * in_dim + b * QK + lane_q * 8) = make_uint2(lo, hi);
             if (lane_q == 0) dplane[r * nb + b] = qb.d_stored;
+        }
+    }
+}
+
+// Routed pairs -> plane rows (see launch_quantize_pairs).  Same arithmetic and
+// thread mapping as k_quantize_planes, over the pairs instead of the plane rows.
+template <bool TC>
+__global__ void __launch_bounds__(256) k_quantize_pairs(int8_t *__restrict__ qplane, float *__restrict__ dplane,
+                                                        const float *__restrict__ x, uint64_t in_dim,
+                                                        uint64_t n_pairs, uint32_t k, int x_per_pair,
+                                                        const int32_t *__restrict__ dst_row,
+                                                        __half *__restrict__ q16, float *__restrict__ dxT,
+                                                        uint64_t n_ld, const PlanHeader *tc_plan) {
+    // The matmul that follows only prefetches weights before it waits for this
+    // grid to finish, so it may be scheduled now.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint64_t tc_rows = TC ? (uint64_t)tc_plan->row_end : 0;
+    const uint64_t nb = in_dim / QK;
+    const uint64_t nblk = n_pairs * nb;
+    const uint64_t lane_q = threadIdx.x & 3u;
+    const uint64_t groups_per_cta = blockDim.x / 4;
+    for (uint64_t base = (uint64_t)blockIdx.x * groups_per_cta; base < nblk; base += (uint64_t)gridDim.x * groups_per_cta) {
+        const uint64_t blk = base + threadIdx.x / 4;
+        const bool live = blk < nblk;
+        const uint64_t pr = live ? blk / nb : 0;
+        const uint64_t b = live ? blk - pr * nb : 0;
+        const int64_t r = live ? (int64_t)dst_row[pr] : -1;
+        float x8[8];
+        if (r >= 0) load8(x8, x + (x_per_pair ? pr : pr / k) * in_dim + b * QK + lane_q * 8);
+        else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x8[i] = 0.0f;
+        }
+        const QuantBlock qb = quantize8(x8);
+        if (r < 0) continue;   // bad id: no row (all lanes of the block agree)
+        const uint64_t ru = (uint64_t)r;
+        if (TC && ru < tc_rows) {
+            store_f16_quants(q16 + ru * in_dim + b * QK + lane_q * 8, qb);
+            if (lane_q == 0) dxT[b * n_ld + ru] = qb.d_stored;
+        } else {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
+                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
+            }
+            *reinterpret_cast<uint2 *>(qplane + ru * in_dim + b * QK + lane_q * 8) = make_uint2(lo, hi);
+            if (lane_q == 0) dplane[ru * nb + b] = qb.d_stored;
         }
     }
 }
@@ -207,18 +246,7 @@ cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x
                                    const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
-    k_quantize_planes<false><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row,
-                                                                         n_src, nullptr, nullptr, 0, nullptr);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quantize_planes_tc(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
-                                      const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_rows,
-                                      const int32_t *src_row, int num_sms, cudaStream_t st) {
-    const uint64_t nblk = n_rows * (in_dim / QK);
-    if (nblk == 0) return cudaSuccess;
-    k_quantize_planes<true><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row,
-                                                                        0, q16, dxT, n_ld, tc_plan);
+    k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
     return cudaGetLastError();
 }
 
@@ -243,6 +271,22 @@ cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *x
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
     k_unpack_blocks<<<grid_for(nblk, 256, num_sms), 256, 0, st>>>(qplane, dplane, xq, in_dim, n_rows, n_src);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_pairs(int8_t *qplane, float *dplane, __half *q16, float *dxT, uint64_t n_ld,
+                                  const PlanHeader *tc_plan, const float *x, uint64_t in_dim, uint64_t n_pairs,
+                                  uint32_t k, int x_per_pair, const int32_t *dst_row, int num_sms, cudaStream_t st) {
+    const uint64_t nblk = n_pairs * (in_dim / QK);
+    if (nblk == 0) return cudaSuccess;
+    if (tc_plan)
+        k_quantize_pairs<true><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_pairs, k,
+                                                                           x_per_pair, dst_row, q16, dxT, n_ld,
+                                                                           tc_plan);
+    else
+        k_quantize_pairs<false><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_pairs, k,
+                                                                            x_per_pair, dst_row, nullptr, nullptr,
+                                                                            0, nullptr);
     return cudaGetLastError();
 }
 
