@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(256) k_unpack_blocks(int8_t *__restrict__ qpla
 __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
                                                        const float *__restrict__ x, uint64_t in_dim, uint64_t n_tok,
                                                        uint64_t n_ld) {
+    // The GEMM behind reads these planes only after its griddepcontrol.wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -200,6 +202,8 @@ __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16,
 __global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
                                                      const uint8_t *__restrict__ xq, uint64_t in_dim, uint64_t n_tok,
                                                      uint64_t n_ld) {
+    // The GEMM behind reads these planes only after its griddepcontrol.wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     for (uint64_t blk = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;

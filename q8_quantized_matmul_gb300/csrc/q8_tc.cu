@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
         uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
         uint32_t fills[NSTAGE] = {};
         uint32_t rfills[NRAW] = {};
+        bool dep_waited = false;
         TcUnit w;
         int seg = 0;
         for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
@@ -470,6 +471,12 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                             float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
                             bulk_g2s(dws, p.dwT + (size_t)kb * p.m_ld + m0, BM * 4, &full[stage]);
                             bulk_g2s(dws + BM, p.dwT + (size_t)(kb + 1) * p.m_ld + m0, BM * 4, &full[stage]);
+                        }
+                        if (!dep_waited) {
+                            // the activations come from the kernel just before this one (launched
+                            // with programmatic serialisation); the weights and the plan are older
+                            asm volatile("griddepcontrol.wait;" ::: "memory");
+                            dep_waited = true;
                         }
                         tma_load_2d(st + A_BYTES, &tmB, kb * QK, n0, &full[stage]);
                         bulk_g2s(dxs, p.dxT + (size_t)kb * p.n_ld + n0, BN * 4, &full[stage]);
@@ -682,8 +689,18 @@ static cudaError_t launch_tc_variant(const TcParams &p, const CUtensorMap &tmA, 
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    k_tc_gemm<G, RAW><<<grid, tc::Cfg<RAW>::NTHREADS, tc::Cfg<RAW>::SMEM, st>>>(p, tmA, tmB);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(tc::Cfg<RAW>::NTHREADS);
+    cfg.dynamicSmemBytes = tc::Cfg<RAW>::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_tc_gemm<G, RAW>, p, tmA, tmB);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || G || p.ksplit == 1) return e;
     const uint64_t n = (uint64_t)p.N * p.M;
     uint64_t g = (n + 255) / 256;

@@ -412,6 +412,23 @@ def test_moe_tensor_core_class_empty(q8, o):
     assert_close(fetch(buf, n, ref.shape), ref, bound, "moe without tensor-core groups")
 
 
+def test_moe_many_experts_every_output(q8, o):
+    """12000 experts: the routing plan's shared-memory arrays (96 KB) need the opt-in
+    limit; Zipf routing over 1600 pairs gives tensor-core, 16-token and 8-token groups."""
+    n_exp, n_tok, k, in_dim, out_dim = 12000, 200, 8, 256, 24
+    ids = inputs.route_zipf(n_tok, k, n_exp, s=1.1, seed=91)
+    counts = np.bincount(ids.reshape(-1), minlength=n_exp)
+    assert counts.max() > 16 and np.any((counts > 8) & (counts <= 16)) and np.any((counts > 0) & (counts <= 8))
+    W = inputs.weights(n_exp * out_dim, in_dim, seed=92)
+    stride = out_dim * in_dim // QK * QB
+    x = inputs.normal((n_tok, in_dim), seed=93)
+    ref, bound, flag = o.moe(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 0, n_tok)
+    assert flag == 0
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 0, out_dim)
+    assert q8.q8_last_error() == 0
+    assert_close(fetch(buf, n, ref.shape), ref, bound, "moe 12000 experts")
+
+
 def test_moe_tensor_core_large_experts_sampled(q8, o):
     """Twenty experts of 4096 x 16384 with 70 rows each, all on the grouped tcgen05 GEMM
     (32 weight tiles per expert, 64 raw copies of 8 blocks per tile).  Whole output rows of
