@@ -134,8 +134,10 @@ def test_matmul_parity(q8, o, in_dim, out_dim, n_tok):
     assert_close(got, ref, bound, f"matmul {in_dim}x{out_dim}x{n_tok}")
 
 
-def test_matmul_q_matches_matmul_bitwise(q8, o):
-    in_dim, out_dim, n_tok = 1024, 300, 40
+@pytest.mark.parametrize("in_dim,out_dim,n_tok", [(1024, 300, 40), (1024, 200, 700), (2048, 70, 12)])
+def test_matmul_q_matches_matmul_bitwise(q8, o, in_dim, out_dim, n_tok):
+    """Pre-quantised activations give the same bits as fp32 ones: prefill with raw weights
+    (40 tokens), with the fp16 weight plane (700 tokens), and the 9-16-token GEMV."""
     W = dev(inputs.weights(out_dim, in_dim, seed=5))
     x = dev(inputs.normal((n_tok, in_dim), seed=6))
     a = q8.matmul(W, x, out_dim)
