@@ -7,8 +7,9 @@
 // expert's weights are streamed once for all of its rows (the grouped GEMM
 // with a per-expert offsets table the pages describe for the packed Metal
 // kernels).  Three small kernels, all deterministic:
-//   1. k_route_count : one CTA per expert counts its pairs; out-of-range ids
-//      get a zero output row and raise Q8_ERANGE (no trap).
+//   1. k_route_count : one CTA per expert counts its pairs; one more gives
+//      out-of-range ids a zero output row and raises Q8_ERANGE (no trap); all
+//      of them reset the row maps.
 //   2. k_route_plan  : one CTA orders the touched experts by pair count
 //      (largest first, ties by id: the big groups start first, which keeps the
 //      persistent grid balanced under skewed routing), gives each a size class,
@@ -41,29 +42,46 @@ __device__ __forceinline__ int block_sum(int v, int *sh) {
     return s;
 }
 
+// CTA e < n_expert counts expert e's pairs.  CTA n_expert zeroes the output rows
+// of pairs whose id is out of range and raises the error word.  Every CTA also
+// takes a share of setting the plane-row and pair maps to -1 (padding / no row),
+// which the fill kernel then overwrites for the real rows.
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_count(const int32_t *__restrict__ ids, uint64_t n_pairs,
-                                                                uint32_t n_expert, int32_t *__restrict__ counts) {
+                                                                uint32_t n_expert, int32_t *__restrict__ counts,
+                                                                uint32_t out_dim, float *__restrict__ out, int *err,
+                                                                int32_t *__restrict__ row_to_out,
+                                                                int32_t *__restrict__ src_row, uint64_t max_rows,
+                                                                int32_t *__restrict__ dst_row) {
     __shared__ int sh[32];
-    const int e = blockIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < max_rows; i += nthr) {
+        row_to_out[i] = -1;
+        src_row[i] = -1;
+    }
+    if (dst_row)
+        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_pairs; i += nthr) dst_row[i] = -1;
+    const uint32_t e = blockIdx.x;
+    if (e == n_expert) {
+        // each warp reads 32 consecutive ids; the (rare) bad pairs are zeroed by the whole warp
+        const int lane = threadIdx.x & 31;
+        const uint64_t nwarp = blockDim.x >> 5;
+        for (uint64_t p0 = (uint64_t)(threadIdx.x >> 5) * 32; p0 < n_pairs; p0 += nwarp * 32) {
+            const uint64_t p = p0 + lane;
+            const int32_t id = p < n_pairs ? __ldg(ids + p) : 0;
+            unsigned bad = __ballot_sync(0xffffffffu, p < n_pairs && (id < 0 || (uint32_t)id >= n_expert));
+            while (bad) {
+                const uint64_t pb = p0 + (uint64_t)(__ffs(bad) - 1);
+                bad &= bad - 1u;
+                for (uint32_t o = lane; o < out_dim; o += 32) out[pb * out_dim + o] = 0.0f;
+                if (lane == 0) raise_error(err, DEV_ERANGE);
+            }
+        }
+        return;
+    }
     int cnt = 0;
-    for (uint64_t p = threadIdx.x; p < n_pairs; p += blockDim.x) cnt += (__ldg(ids + p) == e);
+    for (uint64_t p = threadIdx.x; p < n_pairs; p += blockDim.x) cnt += (__ldg(ids + p) == (int32_t)e);
     cnt = block_sum(cnt, sh);
     if (threadIdx.x == 0) counts[e] = cnt;
-}
-
-// Zero the output rows of pairs whose id is out of range and raise the error word.
-__global__ void __launch_bounds__(256) k_route_bad(const int32_t *__restrict__ ids, uint64_t n_pairs,
-                                                   uint32_t n_expert, uint32_t out_dim, float *__restrict__ out,
-                                                   int *err) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
-    for (uint64_t p = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_pairs; p += warps) {
-        const int32_t e = __ldg(ids + p);
-        if (e < 0 || (uint32_t)e >= n_expert) {
-            for (uint32_t o = lane; o < out_dim; o += 32) out[p * out_dim + o] = 0.0f;
-            if (lane == 0) raise_error(err, DEV_ERANGE);
-        }
-    }
 }
 
 size_t route_plan_bytes(uint32_t n_expert) {
@@ -267,16 +285,8 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
                          float *out, int *err, int num_sms, cudaStream_t st) {
     const uint64_t n_pairs = n_tok * k;
     cudaError_t e;
-    // Padding rows map to nothing, pairs with a bad id to no row: -1 everywhere first.
-    if ((e = cudaMemsetAsync(row_to_out, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(src_row, 0xff, max_rows * sizeof(int32_t), st)) != cudaSuccess) return e;
-    if (dst_row && (e = cudaMemsetAsync(dst_row, 0xff, n_pairs * sizeof(int32_t), st)) != cudaSuccess) return e;
-    k_route_count<<<n_expert, ROUTE_THREADS, 0, st>>>(ids, n_pairs, n_expert, counts);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    int grid_bad = (int)((n_pairs + 7) / 8);
-    if (grid_bad > num_sms * 4) grid_bad = num_sms * 4;
-    if (grid_bad < 1) grid_bad = 1;
-    k_route_bad<<<grid_bad, 256, 0, st>>>(ids, n_pairs, n_expert, out_dim, out, err);
+    k_route_count<<<n_expert + 1, ROUTE_THREADS, 0, st>>>(ids, n_pairs, n_expert, counts, out_dim, out, err,
+                                                          row_to_out, src_row, max_rows, dst_row);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t plan_smem = 2 * (size_t)n_expert * sizeof(int32_t);
     if (plan_smem > 48 * 1024) {
