@@ -120,6 +120,8 @@ SHAPES = [
     (4096, 40, 130), (8192, 24, 5), (1280, 131, 200),
     # prefill with nb % 8 != 0: weights expanded to an fp16 plane instead of read raw
     (2112, 130, 150),
+    # one output tile with a long K: split over 32 CTAs, partial sums added in order
+    (16384, 96, 20),
     # in_dim % 256 != 0: rows not 16-byte aligned (slow path)
     (32, 5, 1), (96, 19, 7), (160, 50, 20), (4000, 8, 2),
 ]
