@@ -16,8 +16,9 @@
 //      a 16-row-aligned range of activation-plane rows and a range of work
 //      items of its class.
 //   3. k_route_fill  : one CTA per expert lists its pairs in increasing p
-//      (block-wide prefix sums), giving the plane-row -> output-row map and the
-//      plane-row -> input-row map used by the gathering quantiser.
+//      (block-wide prefix sums), giving the plane-row -> output-row map, the
+//      plane-row -> input-row map and the pair -> plane-row map used by the
+//      gathering quantiser.
 #include "q8_common.cuh"
 #include "q8_kernels.h"
 
