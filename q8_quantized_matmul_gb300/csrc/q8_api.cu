@@ -229,12 +229,27 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
     const uint64_t n_ld = (n_tok + 127) & ~(uint64_t)127;
     const uint64_t tiles = (m_ld / 128) * (n_ld / 128);
+    const uint64_t sms = (uint64_t)s->num_sms;
     uint64_t ksplit = 1;
-    if (tiles < (uint64_t)s->num_sms) {
-        ksplit = (uint64_t)s->num_sms / tiles;
+    if (tiles < sms) {
+        ksplit = sms / tiles;
         const uint64_t max_split = nb / 16 > 0 ? nb / 16 : 1;   // keep >= 16 blocks per split
         if (ksplit > max_split) ksplit = max_split;
         if (ksplit < 1) ksplit = 1;
+    } else {
+        // Tiles fill the SMs but may end in a thin last wave (256 tiles: 1.68 waves,
+        // 0.84 of the SMs busy on average): split K when that fills the waves better,
+        // keeping >= 64 blocks per split and charging 0.01 per extra split for the
+        // partial sums' traffic.
+        double best = 0.0;
+        for (uint64_t k = 1; k <= 8 && nb / k >= 64; ++k) {
+            const uint64_t units = tiles * k, waves = (units + sms - 1) / sms;
+            const double score = (double)units / (double)(waves * sms) - 0.01 * (double)(k - 1);
+            if (score > best + 1e-9) {
+                best = score;
+                ksplit = k;
+            }
+        }
     }
     uint64_t kb_per = (nb + ksplit - 1) / ksplit;
     kb_per = (kb_per + kb_align - 1) / kb_align * kb_align;
