@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(256) k_quantize_pairs(int8_t *__restrict__ qpl
     // The matmul that follows only prefetches weights before it waits for this
     // grid to finish, so it may be scheduled now.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched with programmatic serialisation: nothing is read before the previous grid is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t tc_rows = TC ? (uint64_t)tc_plan->row_end : 0;
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_pairs * nb;
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16,
                                                        uint64_t n_ld) {
     // The GEMM behind reads these planes only after its griddepcontrol.wait.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched with programmatic serialisation: nothing is read before the previous grid is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -204,6 +208,8 @@ __global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, f
                                                      uint64_t n_ld) {
     // The GEMM behind reads these planes only after its griddepcontrol.wait.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched with programmatic serialisation: nothing is read before the previous grid is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     for (uint64_t blk = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;
@@ -233,6 +239,25 @@ __global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, f
 }
 
 // ------------------------------------------------------------------ launchers
+// Launch behind the previous kernel with programmatic serialisation: the
+// launch overlaps that kernel's drain; the kernel waits for it in
+// griddepcontrol.wait before reading anything.
+template <class K, class... Args>
+static cudaError_t launch_pdl(K kernel, int grid, int block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 static int grid_for(uint64_t work_items, int per_cta, int num_sms) {
     uint64_t need = (work_items + per_cta - 1) / per_cta;
     uint64_t cap = (uint64_t)num_sms * 8;
@@ -250,6 +275,8 @@ cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x
                                    const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
+    // a plain launch: as a programmatic one behind the previous GEMV it made
+    // back-to-back 16-token calls about 1 us slower
     k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
     return cudaGetLastError();
 }
@@ -258,16 +285,14 @@ cudaError_t launch_quantize_f16t(__half *q16, float *dxT, const float *x, uint64
                                  uint64_t n_ld, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_ld * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
-    k_quantize_f16t<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(q16, dxT, x, in_dim, n_tok, n_ld);
-    return cudaGetLastError();
+    return launch_pdl(k_quantize_f16t, grid_for(nblk, 64, num_sms), 256, st, q16, dxT, x, in_dim, n_tok, n_ld);
 }
 
 cudaError_t launch_unpack_f16t(__half *q16, float *dxT, const uint8_t *xq, uint64_t in_dim, uint64_t n_tok,
                                uint64_t n_ld, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_ld * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
-    k_unpack_f16t<<<grid_for(nblk, 256, num_sms), 256, 0, st>>>(q16, dxT, xq, in_dim, n_tok, n_ld);
-    return cudaGetLastError();
+    return launch_pdl(k_unpack_f16t, grid_for(nblk, 256, num_sms), 256, st, q16, dxT, xq, in_dim, n_tok, n_ld);
 }
 
 cudaError_t launch_unpack_blocks(int8_t *qplane, float *dplane, const uint8_t *xq, uint64_t in_dim, uint64_t n_rows,
@@ -283,15 +308,12 @@ cudaError_t launch_quantize_pairs(int8_t *qplane, float *dplane, __half *q16, fl
                                   uint32_t k, int x_per_pair, const int32_t *dst_row, int num_sms, cudaStream_t st) {
     const uint64_t nblk = n_pairs * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
+    const int grid = grid_for(nblk, 64, num_sms);
     if (tc_plan)
-        k_quantize_pairs<true><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_pairs, k,
-                                                                           x_per_pair, dst_row, q16, dxT, n_ld,
-                                                                           tc_plan);
-    else
-        k_quantize_pairs<false><<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_pairs, k,
-                                                                            x_per_pair, dst_row, nullptr, nullptr,
-                                                                            0, nullptr);
-    return cudaGetLastError();
+        return launch_pdl(k_quantize_pairs<true>, grid, 256, st, qplane, dplane, x, in_dim, n_pairs, k, x_per_pair,
+                          dst_row, q16, dxT, n_ld, tc_plan);
+    return launch_pdl(k_quantize_pairs<false>, grid, 256, st, qplane, dplane, x, in_dim, n_pairs, k, x_per_pair,
+                      dst_row, (__half *)nullptr, (float *)nullptr, (uint64_t)0, (const PlanHeader *)nullptr);
 }
 
 }  // namespace q8
