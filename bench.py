@@ -8,8 +8,9 @@ multiply (q8_matmul).  Metric: weight GB/s (34 bytes per 32 weights read per
 call); prefill int8-equivalent TOPS and routed-expert GB/s are reported in
 the same JSON line under "secondary".
 
-Timing: W >= 3 warm-up steps, then exactly K steps replayed as CUDA graphs,
-bracketed by a barrier and a device synchronise, CUDA events on the launching
+Timing: W >= 3 warm-up steps, then exactly K steps replayed as CUDA graphs
+(each holding several consecutive steps, as an engine's graph holds a whole
+forward pass; the remainder of K as one-step graphs), bracketed by a barrier and a device synchronise, CUDA events on the launching
 stream, max over ranks.  Inputs larger than L2: every call of a step reads its
 own copy of the weights, rotating through copies totalling more than 4x L2.
 SM clocks are sampled with nvidia-smi during the timed region.
@@ -248,21 +249,26 @@ def run_ours(args, rank, world, local, dist):
                 call(n, copies[g * n_calls + c])
     stream.synchronize()
     assert q8.q8_last_error(stream) == 0
-    def capture():
-        gs = []
-        for g in range(n_graphs):
-            cg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(cg, stream=stream):
+    def capture(groups):
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            for g in groups:
                 for c, n in enumerate(N_TOKS):
                     call(n, copies[g * n_calls + c])
-            gs.append(cg)
-        return gs
-    graphs = capture()                       # the step as the bench times it
-    graph_replays(torch, stream, graphs, max(args.warmup, n_graphs))   # every graph runs at least once
+        return cg
+    # A decode engine captures a token's whole forward pass (many projections)
+    # in one graph, so consecutive steps run back to back: one graph holds
+    # n_graphs steps, each step on its own weight copies; the K % n_graphs
+    # steps left over replay one-step graphs, so exactly K steps are timed.
+    multi = capture(range(n_graphs))
+    singles = [capture([g]) for g in range(n_graphs)]
+    n_multi, n_rest = divmod(args.steps, n_graphs)
+    graph_replays(torch, stream, [multi], max(1, -(-args.warmup // n_graphs)))
+    graph_replays(torch, stream, singles, n_graphs)   # every graph runs at least once
     barrier(dist)
     torch.cuda.synchronize(dev)
     with ClockSampler(local if world > 1 else (torch.cuda.current_device())) as clk:
-        ms = graph_replays(torch, stream, graphs, args.steps)
+        ms = graph_replays(torch, stream, [multi] * n_multi + singles[:n_rest], n_multi + n_rest)
     torch.cuda.synchronize(dev)
     barrier(dist)
     ms = max_over_ranks(dist, ms)
@@ -351,15 +357,16 @@ def run_ours(args, rank, world, local, dist):
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {len(copies)} weight copies ({len(copies) * W_BYTES / 2 ** 20:.0f} MiB) "
                          f"rotated, each call reads its own copy (L2 {l2 / 2 ** 20:.0f} MiB)",
-                   "launch": "CUDA graph replay of the step (n_tok 1 and 4: one fused GEMV kernel each; "
-                             "n_tok 16: quantiser + GEMV)",
+                   "launch": f"CUDA graphs of {n_graphs} consecutive steps each (the last K mod {n_graphs} "
+                             "steps one-step graphs); per call n_tok 1 and 4: one fused GEMV kernel each; "
+                             "n_tok 16: quantiser + GEMV",
                    "tokens_per_s": round(tokens_per_s, 1)},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps * sum(1 if n <= 8 else 2 for n in N_TOKS),
         "clocks": clk.summary(),
     }
-    del copies, graphs
+    del copies, multi, singles
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_secondary:
         result["secondary"] = secondary(args, torch, q8, dev, stream, l2)
