@@ -99,6 +99,27 @@ int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
               const float *x, uint64_t n_tok, void *stream);
 
 /*
+ * q8_matmul with the activations and the result in HOST memory, the way an
+ * engine's decode step hands a token's activations to the GPU and reads the
+ * result back; the weights stay resident on the device (the pages keep the
+ * model mapped once and pass weight offsets into it).
+ *   out_host  out: fp32 [n_tok][out_dim], host memory.
+ *   W         in:  device pointer, as for q8_matmul (16-byte aligned).
+ *   x_host    in:  fp32 [n_tok][in_dim], host memory.
+ * On `stream`, in order: x_host is copied into a library-owned device staging
+ * buffer, the q8_matmul kernels run on it (same results, bit for bit), and the
+ * result is copied to out_host.  Host buffers need no alignment.  With
+ * page-locked host buffers the copies are asynchronous: x_host must stay
+ * unchanged and out_host is valid only once `stream` has synchronised.  With
+ * pageable host buffers the CUDA runtime stages the copies and the call may
+ * block until they are done.  The staging buffer is grow-only, per device,
+ * counted by q8_scratch_bytes and freed by q8_release; like the scratch, it
+ * must not be used from two streams at once.
+ */
+int q8_matmul_host(float *out_host, const void *W, uint64_t in_dim, uint64_t out_dim,
+                   const float *x_host, uint64_t n_tok, void *stream);
+
+/*
  * Same product from activations already quantised by q8_quantize_act
  * (xq: [n_tok][in_dim/32] Q8_0 blocks, 16-byte aligned).
  */
@@ -183,10 +204,11 @@ int q8_last_error(void *stream);
  * if none yet); for diagnostics. */
 const char *q8_last_cuda_error(void);
 
-/* Scratch bytes currently held on the current device (0 if none). */
+/* Scratch bytes currently held on the current device, the staging buffer of
+ * q8_matmul_host included (0 if none). */
 uint64_t q8_scratch_bytes(void);
 
-/* Frees the scratch of every device (synchronises each first). */
+/* Frees the scratch and staging buffers of every device (synchronises each first). */
 void q8_release(void);
 
 /*

@@ -26,7 +26,7 @@ Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
-           "q8_matmul_noalloc", "q8_last_cuda_error")
+           "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host")
 
 
 class Q8Error(RuntimeError):
@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "q8_quantize_act": ([vp, vp, u64, u64, vp], i32),
         "q8_matmul": ([vp, vp, u64, u64, vp, u64, vp], i32),
         "q8_matmul_q": ([vp, vp, u64, u64, vp, u64, vp], i32),
+        "q8_matmul_host": ([vp, vp, u64, u64, vp, u64, vp], i32),
         "q8_moe_matmul": ([vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64, vp], i32),
         "q8_repack_bytes": ([u64, u64], u64),
         "q8_repack": ([vp, vp, u64, u64, vp], i32),
@@ -116,6 +117,11 @@ def q8_matmul(out, W, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> 
 def q8_matmul_noalloc(out, W, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
     """q8_matmul with its scratch in the library's fixed device array (no allocation)."""
     return _get().q8_matmul_noalloc(_p(out), _p(W), in_dim, out_dim, _p(x), n_tok, _s(stream))
+
+
+def q8_matmul_host(out_host, W, in_dim: int, out_dim: int, x_host, n_tok: int, stream=None) -> int:
+    """q8_matmul with x and out in host memory (CPU tensors, ideally pinned); W on the device."""
+    return _get().q8_matmul_host(_p(out_host), _p(W), in_dim, out_dim, _p(x_host), n_tok, _s(stream))
 
 
 def q8_matmul_q(out, W, in_dim: int, out_dim: int, xq, n_tok: int, stream=None) -> int:

@@ -22,6 +22,8 @@ struct DeviceState {
     int *err = nullptr;          // device address of g_q8_device_error
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
+    void *stage = nullptr;       // device copies of host activations and results (q8_matmul_host)
+    size_t stage_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -110,31 +112,33 @@ int get_device(DeviceState **out) {
     return Q8_OK;
 }
 
-// Grow-only scratch of at least `bytes`.  Growing synchronises the device
+// Grow-only device buffer of at least `bytes`.  Growing synchronises the device
 // (cudaFree does), so a call that grows it must not overlap work of another
 // stream that still uses the old buffer -- scratch users are single-stream.
-int reserve_scratch(DeviceState *s, size_t bytes) {
-    if (bytes <= s->scratch_bytes) return Q8_OK;
+int reserve_buffer(void **buf, size_t *have, size_t bytes) {
+    if (bytes <= *have) return Q8_OK;
     if (g_fail_next_alloc > 0) {
         --g_fail_next_alloc;
         return Q8_ENOMEM;
     }
     size_t want = bytes + bytes / 4;
     want = (want + ((size_t)1 << 20) - 1) & ~(((size_t)1 << 20) - 1);
-    if (s->scratch) {
-        cudaFree(s->scratch);
-        s->scratch = nullptr;
-        s->scratch_bytes = 0;
+    if (*buf) {
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
     }
     void *p = nullptr;
     if (cudaMalloc(&p, want) != cudaSuccess) {
         cudaGetLastError();
         return Q8_ENOMEM;
     }
-    s->scratch = p;
-    s->scratch_bytes = want;
+    *buf = p;
+    *have = want;
     return Q8_OK;
 }
+
+int reserve_scratch(DeviceState *s, size_t bytes) { return reserve_buffer(&s->scratch, &s->scratch_bytes, bytes); }
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -336,17 +340,10 @@ int q8_quantize_act(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, v
                                                 static_cast<cudaStream_t>(stream)));
 }
 
-static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
-                         const void *xq, uint64_t n_tok, void *stream) {
-    int rc = check_dims(in_dim, out_dim, n_tok);
-    if (rc) return rc;
-    if (n_tok == 0 || out_dim == 0) return Q8_OK;
-    if (!out || !W || (!x && !xq)) return Q8_EINVAL;
-    if (!aligned16(out) || !aligned16(W) || (x && !aligned16(x)) || (xq && !aligned16(xq))) return Q8_EALIGN;
-    std::lock_guard<std::mutex> lk(g_mutex);
-    DeviceState *s;
-    if ((rc = get_device(&s))) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+// The dense product with arguments already validated, under g_mutex.
+static int dispatch_matmul(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
+                           const float *x, const void *xq, uint64_t n_tok, cudaStream_t st) {
+    int rc;
     const uint64_t nb = in_dim / q8::QK;
     if (n_tok > 16 && nb % 2 == 0) return run_tc(s, out, W, in_dim, out_dim, x, xq, n_tok, st);
     // small activations: one kernel, the GEMV quantises them itself
@@ -364,10 +361,45 @@ static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t ou
     return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st);
 }
 
+static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
+                         const void *xq, uint64_t n_tok, void *stream) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W || (!x && !xq)) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(W) || (x && !aligned16(x)) || (xq && !aligned16(xq))) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    return dispatch_matmul(s, out, W, in_dim, out_dim, x, xq, n_tok, static_cast<cudaStream_t>(stream));
+}
+
 int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x, uint64_t n_tok,
               void *stream) {
     if (!x && n_tok) return Q8_EINVAL;
     return matmul_common(out, W, in_dim, out_dim, x, nullptr, n_tok, stream);
+}
+
+int q8_matmul_host(float *out_host, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x_host,
+                   uint64_t n_tok, void *stream) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out_host || !W || !x_host) return Q8_EINVAL;
+    if (!aligned16(W)) return Q8_EALIGN;
+    if (out_dim > (((uint64_t)1 << 40) / n_tok)) return Q8_EINVAL;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    const size_t x_bytes = n_tok * in_dim * sizeof(float), out_bytes = n_tok * out_dim * sizeof(float);
+    if ((rc = reserve_buffer(&s->stage, &s->stage_bytes, align256(x_bytes) + align256(out_bytes)))) return rc;
+    Carver cv(s->stage);
+    float *xd = cv.take<float>(x_bytes);
+    float *od = cv.take<float>(out_bytes);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = status_of(cudaMemcpyAsync(xd, x_host, x_bytes, cudaMemcpyHostToDevice, st)))) return rc;
+    if ((rc = dispatch_matmul(s, od, W, in_dim, out_dim, xd, nullptr, n_tok, st))) return rc;
+    return status_of(cudaMemcpyAsync(out_host, od, out_bytes, cudaMemcpyDeviceToHost, st));
 }
 
 int q8_matmul_q(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const void *xq, uint64_t n_tok,
@@ -576,7 +608,7 @@ uint64_t q8_scratch_bytes(void) {
         cudaGetLastError();
         return 0;
     }
-    return g_dev[dev].scratch_bytes;
+    return g_dev[dev].scratch_bytes + g_dev[dev].stage_bytes;
 }
 
 void q8_release(void) {
@@ -587,12 +619,13 @@ void q8_release(void) {
         return;
     }
     for (int d = 0; d < MAX_DEVICES; ++d) {
-        if (!g_dev[d].scratch) continue;
+        if (!g_dev[d].scratch && !g_dev[d].stage) continue;
         cudaSetDevice(d);
         cudaDeviceSynchronize();
         cudaFree(g_dev[d].scratch);
-        g_dev[d].scratch = nullptr;
-        g_dev[d].scratch_bytes = 0;
+        cudaFree(g_dev[d].stage);
+        g_dev[d].scratch = g_dev[d].stage = nullptr;
+        g_dev[d].scratch_bytes = g_dev[d].stage_bytes = 0;
     }
     cudaSetDevice(cur);
 }

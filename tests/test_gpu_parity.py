@@ -471,6 +471,66 @@ def test_repack_layout_and_parity(q8, o):
     assert_close(got, ref, bound, "packed")
 
 
+# ------------------------------------------------------------------ host-buffer entry point
+def _host_call(q8, W, xh, out_dim, pinned):
+    n_tok, in_dim = xh.shape
+    x_host = torch.from_numpy(np.ascontiguousarray(xh))
+    out_host = torch.full((n_tok * out_dim + GUARD,), float("nan"), dtype=torch.float32)
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
+    rc = q8.q8_matmul_host(out_host, W, in_dim, out_dim, x_host, n_tok)
+    assert rc == 0, f"{q8.q8_strerror(rc)} {q8.q8_last_cuda_error()}"
+    assert q8.q8_last_error() == 0                      # synchronises the stream
+    h = out_host.numpy()
+    assert np.all(np.isnan(h[n_tok * out_dim:])), "guard band after the host output was written"
+    return h[:n_tok * out_dim].reshape(n_tok, out_dim)
+
+
+@pytest.mark.parametrize("n_tok,in_dim,out_dim", [(1, 1024, 300), (4, 1024, 300), (16, 1024, 3000),
+                                                   (40, 2048, 300), (700, 1024, 200)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_matmul_host_matches_matmul_bitwise(q8, n_tok, in_dim, out_dim, pinned):
+    """Host x and out around the same kernels: the bits of q8_matmul, for the fused
+    GEMV, the 9-16-token GEMV and both tensor-core variants."""
+    W = dev(inputs.weights(out_dim, in_dim, seed=91))
+    xh = inputs.normal((n_tok, in_dim), seed=92, p_out=0.01)
+    ref = q8.matmul(W, dev(xh), out_dim).cpu().numpy()
+    got = _host_call(q8, W, xh, out_dim, pinned)
+    assert np.array_equal(got.view(np.int32), ref.view(np.int32))
+
+
+def test_matmul_host_oracle_and_repeat(q8, o):
+    """Against the oracle, and back-to-back calls of different sizes on one stream
+    (each call's copy-in waits for the previous call's kernels)."""
+    Wh = inputs.weights(500, 2048, seed=93)
+    W = dev(Wh)
+    for n_tok in (5, 16, 1, 33):
+        xh = inputs.normal((n_tok, 2048), seed=94 + n_tok)
+        ref, bound = o.matmul(Wh, xh, 500)
+        assert_close(_host_call(q8, W, xh, 500, True), ref, bound, f"host {n_tok}")
+
+
+def test_matmul_host_errors(q8):
+    W = dev(inputs.weights(64, 256, seed=95))
+    x_host = torch.from_numpy(inputs.normal((3, 256), seed=96))
+    out_host = torch.empty((3, 64), dtype=torch.float32)
+    assert q8.q8_matmul_host(out_host, W, 256, 64, None, 3) == q8.Q8_EINVAL
+    assert q8.q8_matmul_host(None, W, 256, 64, x_host, 3) == q8.Q8_EINVAL
+    assert q8.q8_matmul_host(out_host, W, 250, 64, x_host, 3) == q8.Q8_EINVAL
+    assert q8.q8_matmul_host(out_host, W.data_ptr() + 1, 256, 64, x_host, 3) == q8.Q8_EALIGN
+    assert q8.q8_matmul_host(out_host, W, 256, 64, x_host, 0) == 0
+    # the staging buffer is library scratch: freed by q8_release, and an allocation
+    # failure enqueues nothing and leaves the next call working
+    q8.q8_release()
+    assert q8.q8_scratch_bytes() == 0
+    q8.q8_debug_fail_next_alloc(1)
+    assert q8.q8_matmul_host(out_host, W, 256, 64, x_host, 3) == q8.Q8_ENOMEM
+    assert q8.q8_matmul_host(out_host, W, 256, 64, x_host, 3) == 0
+    assert q8.q8_last_error() == 0
+    assert q8.q8_scratch_bytes() > 0
+    assert torch.equal(out_host, q8.matmul(W, x_host.to(DEV), 64).cpu())
+
+
 # ------------------------------------------------------------------ error paths and edges
 def test_empty_and_tiny(q8, o):
     W = dev(inputs.weights(3, 32, seed=71))
