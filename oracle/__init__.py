@@ -59,8 +59,14 @@ class Oracle:
         lib.q8o_moe.argtypes = [vp, vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64]
         lib.q8o_moe_sample.argtypes = [vp, vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64,
                                        vp, vp, u64]
+        lib.q8o_swiglu.argtypes = [vp, vp, vp, u64, ctypes.c_float]
+        lib.q8o_swiglu.restype = None
+        lib.q8o_combine.argtypes = [vp, vp, vp, vp, u64, u32, u64]
+        lib.q8o_combine.restype = None
+        lib.q8o_moe_ffn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, u32, u64, u64, vp, vp, u32,
+                                    u64, u64, u64, ctypes.c_float, vp, u64]
         for f in (lib.q8o_quantize, lib.q8o_matmul, lib.q8o_matmul_sample, lib.q8o_moe,
-                  lib.q8o_moe_sample):
+                  lib.q8o_moe_sample, lib.q8o_moe_ffn):
             f.restype = ctypes.c_int
         self.lib = lib
 
@@ -150,6 +156,54 @@ class Oracle:
         if rc < 0:
             raise ValueError("oracle moe_sample: bad arguments")
         return out, bound, rc
+
+    # -- the expert FFN around the routed product ----------------------------------
+    def swiglu(self, gate, up, limit: float):
+        """mid = silu(gate') * up' (gate' = min(gate, limit), up' = up clamped to
+        [-limit, limit]; limit = 0: no clamp), float32, same shape as gate."""
+        gate = np.ascontiguousarray(gate, dtype=np.float32)
+        up = np.ascontiguousarray(up, dtype=np.float32)
+        assert gate.shape == up.shape
+        mid = np.empty_like(gate)
+        self.lib.q8o_swiglu(mid.ctypes.data, gate.ctypes.data, up.ctypes.data, gate.size, float(limit))
+        return mid
+
+    def combine(self, y, w, n_tok: int, k: int):
+        """y float32 [n_tok*k, dim], w float32 [n_tok*k] -> (out float64 [n_tok, dim], bound)."""
+        y = np.ascontiguousarray(y, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+        dim = y.shape[1]
+        assert y.shape[0] == n_tok * k and w.size == n_tok * k
+        out = np.empty((n_tok, dim), dtype=np.float64)
+        bound = np.empty((n_tok, dim), dtype=np.float64)
+        self.lib.q8o_combine(out.ctypes.data, bound.ctypes.data, y.ctypes.data, w.ctypes.data, n_tok, k, dim)
+        return out, bound
+
+    def moe_ffn(self, W_gate, W_up, W_down, n_expert, gate_up_stride, down_stride, ids, w, in_dim, mid_dim,
+                out_dim, limit, x):
+        """The routed expert FFN.  x float32 [n_tok, in_dim]; ids int32 and w float32 [n_tok, k].
+        Returns a dict: out (float64 [n_tok, out_dim]), out_bound, y (float32 [n_tok*k, out_dim]),
+        y_bound, mid (float32 [n_tok*k, mid_dim]), midq (its blocks), flag."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        n_tok = x.shape[0]
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        k = ids.size // n_tok if n_tok else 1
+        n_pairs = n_tok * k
+        r = {"out": np.empty((n_tok, out_dim), np.float64), "out_bound": np.empty((n_tok, out_dim), np.float64),
+             "y": np.empty((n_pairs, out_dim), np.float32), "y_bound": np.empty((n_pairs, out_dim), np.float64),
+             "mid": np.empty((n_pairs, mid_dim), np.float32),
+             "midq": np.empty((n_pairs, mid_dim // QK * QBYTES), np.uint8)}
+        rc = self.lib.q8o_moe_ffn(r["out"].ctypes.data, r["out_bound"].ctypes.data, r["y"].ctypes.data,
+                                  r["y_bound"].ctypes.data, r["mid"].ctypes.data, r["midq"].ctypes.data,
+                                  np.ascontiguousarray(W_gate).ctypes.data, np.ascontiguousarray(W_up).ctypes.data,
+                                  np.ascontiguousarray(W_down).ctypes.data, n_expert, gate_up_stride, down_stride,
+                                  ids.ctypes.data, w.ctypes.data, k, in_dim, mid_dim, out_dim, float(limit),
+                                  x.ctypes.data, n_tok)
+        if rc < 0:
+            raise ValueError("oracle moe_ffn: bad dimensions")
+        r["flag"] = rc
+        return r
 
 
 _oracle = None

@@ -20,6 +20,11 @@
  *   - "routed MoE" (GPU code walkthrough, trace 5) and the expert pointer
  *     array (MoE C notes, section 1): each selected expert is a separate
  *     weight matrix; only the selected ones are read.
+ *   - the expert FFN around it (the same trace's four steps: gate and up
+ *     projections of the selected experts, SwiGLU, down projection, weighted
+ *     sum; the MoE study page's "SwiGLU activation" section for
+ *     mid = silu(gate) * up and the clamp of gate from above and of up to
+ *     [-limit, limit]).
  *
  * Readings where the pages are silent (each one also listed in the design notes):
  *   - block layout: 34 bytes, fp16 d little-endian then int8 q[32] (GGUF Q8_0);
@@ -31,12 +36,19 @@
  *   - accumulation is fp32 in block order b = 0..nb-1, each block adding
  *     (d_w * d_x) * (float) isum;
  *   - an expert id outside [0, n_expert) yields a zero output row and raises
- *     the error flag.
+ *     the error flag;
+ *   - SwiGLU: silu(g) = g / (1 + e^-g) (the pages print silu's use, not its
+ *     body), evaluated in double from the fp32 gate and up and rounded once
+ *     to fp32; the clamp applies when limit > 0 (limit = 0: none);
+ *   - the down projection's activations are the fp32 mid rows quantised with
+ *     the activation quantiser above, one row per pair;
+ *   - the weighted sum adds the k experts of a token in slot order, in double.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC.
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define QK 32
@@ -248,4 +260,79 @@ int q8o_moe_sample(float *out, double *bound, const uint8_t *W_experts, uint32_t
         if (bound) bound[s] = bd;
     }
     return flag;
+}
+
+/* ---- the expert FFN around the routed product --------------------------------- */
+
+/* SwiGLU with the optional clamp, element by element:
+ *   limit > 0: gate = min(gate, limit), up = min(max(up, -limit), limit)
+ *   mid = silu(gate) * up,  silu(g) = g / (1 + e^-g). */
+void q8o_swiglu(float *mid, const float *gate, const float *up, uint64_t n, float limit) {
+    for (uint64_t i = 0; i < n; ++i) {
+        double g = gate[i], u = up[i];
+        if (limit > 0.0f) {
+            if (g > limit) g = limit;
+            if (u > limit) u = limit;
+            if (u < -limit) u = -limit;
+        }
+        mid[i] = (float)(g / (1.0 + exp(-g)) * u);
+    }
+}
+
+/* Weighted sum of each token's k expert outputs: out[t][o] = sum_j w[t*k+j] *
+ * y[t*k+j][o] (j = 0..k-1, in double); bound[t][o] = sum_j |w y|. */
+void q8o_combine(double *out, double *bound, const float *y, const float *w, uint64_t n_tok, uint32_t k,
+                 uint64_t dim) {
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint64_t o = 0; o < dim; ++o) {
+            double s = 0.0, b = 0.0;
+            for (uint32_t j = 0; j < k; ++j) {
+                uint64_t p = t * k + j;
+                double v = (double)w[p] * (double)y[p * dim + o];
+                s += v;
+                b += fabs(v);
+            }
+            out[t * dim + o] = s;
+            if (bound) bound[t * dim + o] = b;
+        }
+}
+
+/* The routed expert FFN of n_tok tokens, k experts each (pair p = t*k + j,
+ * expert ids[p], weight w[p]):
+ *   gate[p] = W_gate[e] . xq[t],  up[p] = W_up[e] . xq[t]      (in_dim -> mid_dim)
+ *   mid[p]  = swiglu(gate[p], up[p])
+ *   y[p]    = W_down[e] . quantise(mid[p])                     (mid_dim -> out_dim)
+ *   out[t]  = sum_j w[t*k+j] y[t*k+j]
+ * x is fp32 [n_tok][in_dim] and is quantised here.  Expert e's gate and up
+ * matrices start at e * gate_up_stride bytes, its down matrix at e * down_stride.
+ * Returned besides out (double [n_tok][out_dim]) and its bound: y and y_bound
+ * ([n_pairs][out_dim]), mid ([n_pairs][mid_dim]) and its quantised blocks midq
+ * ([n_pairs][mid_dim/32] blocks).  Returns 1 when an id was out of range (that
+ * pair's gate, up, mid and y rows are zero), 0 otherwise, -1 on bad dimensions
+ * or allocation failure. */
+int q8o_moe_ffn(double *out, double *out_bound, float *y, double *y_bound, float *mid, uint8_t *midq,
+                const uint8_t *W_gate, const uint8_t *W_up, const uint8_t *W_down, uint32_t n_expert,
+                uint64_t gate_up_stride, uint64_t down_stride, const int32_t *ids, const float *w, uint32_t k,
+                uint64_t in_dim, uint64_t mid_dim, uint64_t out_dim, float limit, const float *x,
+                uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % QK || mid_dim == 0 || mid_dim % QK || k == 0) return -1;
+    uint64_t n_pairs = n_tok * k;
+    uint8_t *xq = malloc(n_tok * (in_dim / QK) * QBYTES + 1);
+    float *gate = malloc(n_pairs * mid_dim * sizeof(float) + 1);
+    float *up = malloc(n_pairs * mid_dim * sizeof(float) + 1);
+    int rc = -1;
+    if (xq && gate && up) {
+        q8o_quantize(xq, x, in_dim, n_tok);
+        int f1 = q8o_moe(gate, NULL, W_gate, n_expert, gate_up_stride, ids, k, in_dim, mid_dim, xq, 0, n_tok);
+        int f2 = q8o_moe(up, NULL, W_up, n_expert, gate_up_stride, ids, k, in_dim, mid_dim, xq, 0, n_tok);
+        q8o_swiglu(mid, gate, up, n_pairs * mid_dim, limit);
+        q8o_quantize(midq, mid, mid_dim, n_pairs);
+        int f3 = q8o_moe(y, y_bound, W_down, n_expert, down_stride, ids, k, mid_dim, out_dim, midq, 1, n_tok);
+        q8o_combine(out, out_bound, y, w, n_tok, k, out_dim);
+        rc = (f1 < 0 || f2 < 0 || f3 < 0) ? -1 : (f1 | f2 | f3);
+    }
+    free(xq);
+    free(gate);
+    free(up);
+    return rc;
 }

@@ -455,4 +455,152 @@ def pin_moe_bad_ids(o):
     assert np.array_equal(out[0], ref0[0]) and np.array_equal(out[3], ref3[0])
 
 
+# ---------------------------------------------------------------- the expert FFN around the routed product
+def _lambert_w(c: float) -> float:
+    """Principal branch of Lambert's W at c > 0 (w e^w = c), by Newton's method."""
+    w = 0.5
+    for _ in range(60):
+        ew = np.exp(w)
+        w -= (w * ew - c) / (ew * (w + 1.0))
+    return float(w)
+
+
+def pin_swiglu_closed_forms(o):
+    """silu at points with closed forms (no clamp): silu(0) = 0; at g = ln 3, e^-g = 1/3
+    so silu(g) = (3/4) ln 3; silu(g) - silu(-g) = g; silu(g) = g to fp32 precision for
+    large g and 0 for very negative g; the minimum of silu is -W(1/e), reached at
+    g = -(1 + W(1/e)) (W: Lambert's function).  mid is linear in up."""
+    u = np.array([1.0, -2.0, 0.5, 3.0], np.float32)
+    assert np.all(o.swiglu(np.zeros(4, np.float32), u, 0.0) == 0)
+    ln3 = np.float32(np.log(3.0))
+    m = o.swiglu(np.full(4, ln3, np.float32), u, 0.0).astype(np.float64)
+    ref = 0.75 * np.log(3.0) * u.astype(np.float64)
+    assert np.all(np.abs(m - ref) <= 1e-6 * np.abs(ref))
+    gs = np.linspace(-20.0, 20.0, 4001).astype(np.float32)
+    ones = np.ones_like(gs)
+    a = o.swiglu(gs, ones, 0.0).astype(np.float64)
+    b = o.swiglu(-gs, ones, 0.0).astype(np.float64)
+    assert np.all(np.abs(a - b - gs.astype(np.float64)) <= 2.0 ** -23 * (np.abs(a) + np.abs(b)) + 1e-30)
+    big = np.array([40.0, 60.0, 88.0, 1000.0], np.float32)
+    assert np.array_equal(o.swiglu(big, u, 0.0), big * u)
+    neg = np.array([-120.0, -200.0, -1000.0, -1e30], np.float32)
+    assert np.all(o.swiglu(neg, np.ones(4, np.float32), 0.0) == 0)
+    w1e = _lambert_w(np.exp(-1.0))
+    grid = np.linspace(-1.4, -1.15, 25001).astype(np.float32)
+    mg = o.swiglu(grid, np.ones_like(grid), 0.0).astype(np.float64)
+    assert abs(mg.min() + w1e) <= 1e-7
+    assert abs(float(grid[np.argmin(mg)]) + 1.0 + w1e) <= 2e-3
+    lin = o.swiglu(np.full(4, 1.5, np.float32), u, 0.0).astype(np.float64)
+    assert np.all(np.abs(lin - lin[0] * u) <= 2.0 ** -22 * np.abs(lin))
+
+
+def pin_swiglu_clamp(o):
+    """The clamp (MoE page, SwiGLU activation section): gate is limited from above only,
+    up to [-limit, limit]; values inside the band are unchanged; limit = 0 means none."""
+    L = 10.0
+    f = np.float32
+    s = lambda g, u, lim: o.swiglu(np.array([g], f), np.array([u], f), lim)[0]
+    for u in (1.0, -2.5, 7.0):
+        assert s(50.0, u, L) == s(10.0, u, L)
+        assert s(1e30, u, L) == s(10.0, u, L)
+    for g in (-3.0, 0.7, 4.0):
+        assert s(g, 50.0, L) == s(g, 10.0, L)
+        assert s(g, -50.0, L) == s(g, -10.0, L)
+        assert s(g, 9.5, L) == s(g, 9.5, 0.0)
+        assert s(g, 50.0, L) != s(g, 50.0, 0.0)
+    assert s(-50.0, 1.0, L) == s(-50.0, 1.0, 0.0)
+    assert -1e-18 < s(-50.0, 1.0, L) < 0.0
+    assert s(3.0, 2.0, L) == s(3.0, 2.0, 0.0)
+    assert s(50.0, 1.0, 0.0) == 50.0
+    assert abs(s(10.0, 1.0, L) - s(-10.0, 1.0, L) - 10.0) <= 2.0 ** -20
+
+
+def pin_combine_integer_exact(o):
+    """The weighted sum of a token's k expert rows, with integer rows and integer or
+    dyadic weights: exact, equal to integer arithmetic; the bound is sum |w y|; k = 1
+    with weight 1 returns the row."""
+    g = rng(21)
+    n_tok, k, dim = 3, 6, 40
+    y = g.integers(-1000, 1001, size=(n_tok * k, dim))
+    w = g.integers(-3, 4, size=n_tok * k)
+    out, bound = o.combine(y.astype(np.float32), w.astype(np.float32), n_tok, k)
+    yt, wt = y.reshape(n_tok, k, dim), w.reshape(n_tok, k)
+    assert np.array_equal(out, np.einsum("tj,tjo->to", wt, yt).astype(np.float64))
+    assert np.array_equal(bound, np.einsum("tj,tjo->to", np.abs(wt), np.abs(yt)).astype(np.float64))
+    wd = g.choice([0.25, -0.5, 1.0, 2.0, -0.125], size=n_tok * k)
+    out, _ = o.combine(y.astype(np.float32), wd.astype(np.float32), n_tok, k)
+    ref = np.einsum("tj,tjo->to", (wd * 8).astype(np.int64).reshape(n_tok, k), yt) / 8.0
+    assert np.array_equal(out, ref)
+    out1, _ = o.combine(y[:4].astype(np.float32), np.ones(4, np.float32), 4, 1)
+    assert np.array_equal(out1, y[:4].astype(np.float64))
+
+
+def pin_moe_ffn_exact_construction(o):
+    """A routed expert FFN whose every step is exact, against integer arithmetic.
+    Token t's x is 127 at column c_t < 32 and 0 elsewhere, so it quantises to d = 1 and
+    q = 127 e_{c_t}.  Every weight scale is 1 and block 0 of every gate row is all 1, so
+    gate = 127 exactly, and silu(127) rounds to 127 (e^-127 is far below fp32
+    resolution); up = 127 q_up[o][0][c_t] and mid = 16129 q_up[o][0][c_t].  The first
+    row of every 32-row block of up holds +/-127 in block 0, so each 32-block of mid has
+    scale 16129 exactly, quants q_up and stored binary16 scale 16128; then
+    y = 16128 Q_down q_up, and out = sum_j w_j y_j with dyadic weights.  Swapping gate
+    and up, feeding the down projection a token row, or mixing experts gives other
+    values (q_up has negative entries; experts and tokens differ)."""
+    g = rng(22)
+    n_exp, in_dim, mid_dim, out_dim, n_tok, k = 5, 64, 96, 48, 4, 2
+    nbi, nbm = in_dim // QK, mid_dim // QK
+    one = 0x3C00
+    qg = g.integers(-127, 128, size=(n_exp, mid_dim, nbi, QK))
+    qg[:, :, 0, :] = 1
+    qu = g.integers(-127, 128, size=(n_exp, mid_dim, nbi, QK))
+    qu[:, ::QK, 0, :] = 127 * g.choice([-1, 1], size=(n_exp, mid_dim // QK, QK))
+    qd = g.integers(-127, 128, size=(n_exp, out_dim, nbm, QK))
+    blocks = lambda q, rows, nb: make_blocks(np.full((rows, nb), one, np.uint16), q.reshape(rows, nb, QK)).reshape(-1)
+    Wg, Wu = blocks(qg, n_exp * mid_dim, nbi), blocks(qu, n_exp * mid_dim, nbi)
+    Wd = blocks(qd, n_exp * out_dim, nbm)
+    gu_stride, d_stride = mid_dim * nbi * QB, out_dim * nbm * QB
+    ids = np.stack([g.choice(n_exp, size=k, replace=False) for _ in range(n_tok)]).astype(np.int32)
+    w = g.choice([0.25, -0.5, 1.0, 2.0, 0.75], size=(n_tok, k)).astype(np.float32)
+    c = g.integers(0, QK, size=n_tok)
+    x = np.zeros((n_tok, in_dim), np.float32)
+    x[np.arange(n_tok), c] = 127.0
+    r = o.moe_ffn(Wg, Wu, Wd, n_exp, gu_stride, d_stride, ids, w, in_dim, mid_dim, out_dim, 0.0, x)
+    assert r["flag"] == 0
+    for t in range(n_tok):
+        exact = np.zeros(out_dim, np.int64)
+        tol = np.zeros(out_dim)
+        for j in range(k):
+            p, e = t * k + j, int(ids[t, j])
+            qmid = qu[e, :, 0, c[t]]
+            assert np.array_equal(r["mid"][p], (16129 * qmid).astype(np.float32)), (t, j)
+            dm, qm = split_blocks(r["midq"][p], nbm)
+            assert np.all(dm == 0x73E0) and np.array_equal(qm.reshape(-1), qmid)   # 16128 in binary16
+            terms = 16128 * np.einsum("obi,bi->ob", qd[e], qmid.reshape(nbm, QK))
+            yj = terms.sum(1)
+            tol_j = (nbm + 1) * 2.0 ** -24 * np.abs(terms).sum(1)
+            assert np.all(np.abs(r["y"][p].astype(np.float64) - yj) <= tol_j), (t, j)
+            exact += (int(w[t, j] * 4) * yj)
+            tol += abs(float(w[t, j])) * tol_j
+        assert np.all(np.abs(r["out"][t] - exact / 4.0) <= tol), t
+
+
+def pin_moe_ffn_bad_id(o):
+    """A pair with an out-of-range expert id contributes nothing and raises the flag; the
+    token's other pairs are unaffected."""
+    g = rng(23)
+    n_exp, in_dim, mid_dim, out_dim = 3, 64, 32, 8
+    Wg = _rand_weights(g, n_exp * mid_dim, in_dim).reshape(-1)
+    Wu = _rand_weights(g, n_exp * mid_dim, in_dim).reshape(-1)
+    Wd = _rand_weights(g, n_exp * out_dim, mid_dim).reshape(-1)
+    gu, ds = mid_dim * (in_dim // QK) * QB, out_dim * (mid_dim // QK) * QB
+    x = g.standard_normal((1, in_dim)).astype(np.float32)
+    w = np.array([[0.5, 0.25]], np.float32)
+    good = o.moe_ffn(Wg, Wu, Wd, n_exp, gu, ds, np.array([[2, 1]], np.int32), w, in_dim, mid_dim, out_dim, 10.0, x)
+    bad = o.moe_ffn(Wg, Wu, Wd, n_exp, gu, ds, np.array([[2, 9]], np.int32), w, in_dim, mid_dim, out_dim, 10.0, x)
+    assert good["flag"] == 0 and bad["flag"] == 1
+    assert np.all(bad["y"][1] == 0) and np.all(bad["mid"][1] == 0)
+    assert np.array_equal(bad["y"][0], good["y"][0])
+    assert np.array_equal(bad["out"][0], 0.5 * good["y"][0].astype(np.float64))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

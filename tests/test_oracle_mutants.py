@@ -38,6 +38,20 @@ MUTANTS = [
     ("moe_row_choice", "xq + (x_per_pair ? p : t) * nb * QBYTES", "xq + (x_per_pair ? t : p % n_tok) * nb * QBYTES"),
     ("moe_expert_stride", "W_experts + (uint64_t)e * expert_stride + o * nb * QBYTES", "W_experts + (uint64_t)e * out_dim * nb * QBYTES + o * nb * QBYTES"),
     ("moe_no_flag", "                    flag = 1;\n                } else {\n                    const uint8_t *w", "                    flag = 0;\n                } else {\n                    const uint8_t *w"),
+    # the expert FFN around the routed product
+    ("swiglu_sigmoid", "mid[i] = (float)(g / (1.0 + exp(-g)) * u);", "mid[i] = (float)(1.0 / (1.0 + exp(-g)) * u);"),
+    ("swiglu_exp_sign", "mid[i] = (float)(g / (1.0 + exp(-g)) * u);", "mid[i] = (float)(g / (1.0 + exp(g)) * u);"),
+    ("swiglu_swapped", "double g = gate[i], u = up[i];", "double g = up[i], u = gate[i];"),
+    ("swiglu_no_up_floor", "if (u < -limit) u = -limit;", ";"),
+    ("swiglu_gate_floor", "if (g > limit) g = limit;", "if (g > limit) g = limit;\n            if (g < -limit) g = -limit;"),
+    ("swiglu_always_clamped", "if (limit > 0.0f) {", "if (limit >= 0.0f) {"),
+    ("combine_drop_last", "for (uint32_t j = 0; j < k; ++j) {\n                uint64_t p = t * k + j;",
+     "for (uint32_t j = 0; j + 1 < k; ++j) {\n                uint64_t p = t * k + j;"),
+    ("combine_unweighted", "double v = (double)w[p] * (double)y[p * dim + o];", "double v = (double)y[p * dim + o];"),
+    ("ffn_up_as_gate", "q8o_moe(gate, NULL, W_gate,", "q8o_moe(gate, NULL, W_up,"),
+    ("ffn_down_token_rows", "midq, 1, n_tok);", "midq, 0, n_tok);"),
+    ("ffn_down_gate_stride", "q8o_moe(y, y_bound, W_down, n_expert, down_stride,", "q8o_moe(y, y_bound, W_down, n_expert, gate_up_stride,"),
+    ("ffn_no_bad_flag", "rc = (f1 < 0 || f2 < 0 || f3 < 0) ? -1 : (f1 | f2 | f3);", "rc = (f1 < 0 || f2 < 0 || f3 < 0) ? -1 : 0;"),
 ]
 
 
