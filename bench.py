@@ -467,6 +467,34 @@ def secondary(args, torch, q8, dev, stream, l2):
     assert q8.q8_last_error(stream) == 0
     torch.cuda.empty_cache()
 
+    # the routed expert FFN on the same routing: gate and up (one routing, one quantisation
+    # of x), SwiGLU with clamp 10, down on the re-quantised mid, weighted sum of the 6 experts
+    in_dim, mid_dim = 4096, 2048
+    Wg, Wu = (torch.from_numpy(inputs.weights(n_exp * mid_dim, in_dim, seed=s)).to(dev) for s in (2, 4))
+    Wd = torch.from_numpy(inputs.weights(n_exp * in_dim, mid_dim, seed=5)).to(dev)
+    gu_stride, d_stride = mid_dim * in_dim // QK * QB, in_dim * mid_dim // QK * QB
+    wts = torch.from_numpy(np.random.default_rng(0).random((n_tok, k)).astype(np.float32)).to(dev)
+    x = torch.from_numpy(inputs.normal((n_tok, in_dim), seed=2)).to(dev)
+    o = torch.empty((n_tok, in_dim), device=dev)
+    reps = 6
+    q8.q8_profile_arm(3 * reps)          # three timed launches per call: gate, up, down
+    ms = timed_eager(torch, stream, lambda i: q8.q8_moe_ffn(o, Wg, Wu, Wd, n_exp, gu_stride, d_stride, idsd, wts, k,
+                                                             in_dim, mid_dim, in_dim, 10.0, x, n_tok, stream), reps)
+    kms = sum(q8.q8_profile_read(i) for i in range(3 * reps)) / reps
+    q8.q8_profile_arm(0)
+    assert q8.q8_last_error(stream) == 0
+    wb = touched * (2 * gu_stride + d_stride)
+    out.append({"workload": "routed MoE FFN: 256 experts, gate/up [2048x4096], down [4096x2048], n_tok 64, "
+                            f"uniform top-6 ({touched} experts touched), SwiGLU clamp 10, weighted sum",
+                "ms_per_call": round(ms, 4), "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1),
+                "frac_of_hbm_peak": round(wb / (ms * 1e-3) / 1e9 / hbm, 4),
+                "matmul_kernels_ms": round(kms, 4),
+                "matmul_kernel_weight_gbs": round(wb / (kms * 1e-3) / 1e9, 1),
+                "launches_per_call": "3 routing + 1 quantiser + gate/up GEMVs + SwiGLU + 3 routing + 1 quantiser "
+                                     "+ down GEMVs + weighted sum"})
+    del Wg, Wu, Wd
+    torch.cuda.empty_cache()
+
     # long prefill layer slice: 4096 tokens through q_a, q_b, output_a, output_b, then routed
     # gate/up and down over 256 experts with Zipf(1.1) top-6 routing
     n = 4096

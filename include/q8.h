@@ -149,6 +149,53 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert,
                   uint64_t n_tok, void *stream);
 
 /*
+ * Routed expert FFN around the routed matmul (GPU code walkthrough, trace 5:
+ * ds4_gpu_routed_moe_one_tensor runs, for the selected experts, the gate and up
+ * projections, SwiGLU, the down projection and the weighted sum; the MoE study
+ * page, SwiGLU activation section, gives mid = silu(gate) * up and the clamp).
+ * Pairs p = t*k + j select expert e = expert_ids[p] with weight expert_weights[p]:
+ *   gate[p] = W_gate[e] . x[t],  up[p] = W_up[e] . x[t]        (in_dim -> mid_dim)
+ *   mid[p]  = silu(min(gate, limit)) * clamp(up, -limit, limit) (limit 0: no clamp)
+ *   y[p]    = W_down[e] . mid[p]                               (mid_dim -> out_dim)
+ *   out[t]  = sum_j expert_weights[t*k+j] * y[t*k+j]          (j in slot order)
+ * x and mid are quantised per 32-block exactly as q8_quantize_act does, and
+ * each projection is the q8_moe_matmul product (the gate and up projections
+ * share one routing and one quantisation of x).  silu(g) = g / (1 + e^-g) in
+ * fp32 (CUDA expf, IEEE division).
+ *   out               out: fp32 [n_tok][out_dim].
+ *   W_gate, W_up      in:  n_expert matrices each, expert e at e*gate_up_stride_bytes,
+ *                          each mid_dim rows of in_dim/32 Q8_0 blocks.
+ *   W_down            in:  n_expert matrices, expert e at e*down_stride_bytes, each
+ *                          out_dim rows of mid_dim/32 blocks.
+ *   expert_ids        in:  int32 [n_tok][k];  expert_weights in: fp32 [n_tok][k].
+ *   limit                  >= 0 (NaN or negative: Q8_EINVAL).
+ *   x                 in:  fp32 [n_tok][in_dim].
+ * in_dim and mid_dim are multiples of 32; strides are multiples of 16 and at
+ * least one matrix long.  Intermediates (gate, up, mid, y) live in the
+ * library scratch.  A pair with an id outside [0, n_expert) contributes zero
+ * and raises Q8_ERANGE for q8_last_error().
+ */
+int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_down,
+               uint32_t n_expert, uint64_t gate_up_stride_bytes, uint64_t down_stride_bytes,
+               const int32_t *expert_ids, const float *expert_weights, uint32_t k,
+               uint64_t in_dim, uint64_t mid_dim, uint64_t out_dim, float limit,
+               const float *x, uint64_t n_tok, void *stream);
+
+/*
+ * The FFN's elementwise steps on their own.
+ *   q8_swiglu:      mid[i] = silu(min(gate[i], limit)) * clamp(up[i], -limit, limit)
+ *                   for i < n (limit 0: no clamp; NaN or negative: Q8_EINVAL);
+ *                   mid, gate, up fp32, 16-byte aligned.
+ *   q8_moe_combine: out[t][o] = sum_{j<k} weights[t*k+j] * y[t*k+j][o], j in
+ *                   order, each product and sum rounded to fp32; out [n_tok][dim]
+ *                   and y [n_tok*k][dim] 16-byte aligned, weights [n_tok*k]
+ *                   4-byte aligned.
+ */
+int q8_swiglu(float *mid, const float *gate, const float *up, uint64_t n, float limit, void *stream);
+int q8_moe_combine(float *out, const float *y, const float *weights, uint64_t n_tok, uint32_t k,
+                   uint64_t dim, void *stream);
+
+/*
  * Optional load-time repack of Q8_0 rows into split planes (a quant plane
  * of int8 [rows][in_dim] followed by a scale plane of fp16 [rows][in_dim/32]),
  * the layout the ROCm MXFP4 work on the pages found fastest (16-byte

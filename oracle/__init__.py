@@ -221,3 +221,44 @@ def get() -> Oracle:
 def tolerance(bound: np.ndarray) -> np.ndarray:
     """Allowed |gpu - oracle| per output: 1e-4 * sum_b |d_w d_x isum_b| + 1e-6."""
     return 1e-4 * bound + 1e-6
+
+
+def _deq_abs(raw, nb):
+    """|d q| of raw Q8_0 rows [rows, nb*34] as float64 [rows, nb*32]."""
+    r = raw.reshape(raw.shape[0], nb, QBYTES)
+    d = (r[..., 0].astype(np.uint16) | (r[..., 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float64)
+    q = r[..., 2:].copy().view(np.int8).astype(np.float64)
+    return np.abs(d[..., None] * q).reshape(raw.shape[0], nb * QK)
+
+
+def ffn_tolerance(r, W_down, down_stride, ids, w, mid_dim, out_dim):
+    """Allowed |gpu - oracle| per output of the routed expert FFN, from the oracle's result r
+    (Oracle.moe_ffn).  Per pair: the matmul bound 1e-4 B + 1e-6 of the down projection
+    (B = y_bound); 2^-10 B for a block whose binary16 scale rounds the other way; one
+    quantisation step for every mid value whose quotient mid/d (d = amax/127 in fp32) lies
+    within 1e-3 of a rounding tie, where fp32 differences in gate and up can flip its code;
+    all weighted by |w|.  Then 2k 2^-24 sum_j |w_j y_j| for the fp32 weighted sum.  Pairs
+    whose id is out of range have zero mid and y on both sides; pass any valid id for them."""
+    ids = np.asarray(ids)
+    n_tok, k = ids.shape
+    nbm = mid_dim // QK
+    blk = r["mid"].reshape(-1, nbm, QK)
+    d = np.abs(blk).max(-1).astype(np.float32) / np.float32(127.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quo = np.abs(blk / d[..., None])
+    risk = (np.abs(quo - np.floor(quo) - 0.5) < 1e-3) & (d[..., None] > 0)
+    mq = r["midq"].reshape(-1, nbm, QBYTES)
+    dh = (mq[..., 0].astype(np.uint16) | (mq[..., 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float64)
+    step = (risk * dh[..., None]).reshape(-1, mid_dim)
+    tol = 2 * k * 2.0 ** -24 * r["out_bound"]
+    row_bytes = nbm * QBYTES
+    W_down = np.asarray(W_down).reshape(-1)
+    for t in range(n_tok):
+        for j in range(k):
+            p, e = t * k + j, int(ids[t, j])
+            flips = 0.0
+            if step[p].any():
+                We = W_down[e * down_stride:e * down_stride + out_dim * row_bytes].reshape(out_dim, row_bytes)
+                flips = _deq_abs(We, nbm) @ step[p]
+            tol[t] += abs(float(w[t, j])) * ((1e-4 + 2.0 ** -10) * r["y_bound"][p] + 1e-6 + flips)
+    return tol

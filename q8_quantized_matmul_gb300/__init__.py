@@ -26,7 +26,8 @@ Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
-           "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host")
+           "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host", "q8_moe_ffn", "q8_swiglu",
+           "q8_moe_combine")
 
 
 class Q8Error(RuntimeError):
@@ -50,6 +51,10 @@ def _load() -> ctypes.CDLL:
         "q8_matmul_q": ([vp, vp, u64, u64, vp, u64, vp], i32),
         "q8_matmul_host": ([vp, vp, u64, u64, vp, u64, vp], i32),
         "q8_moe_matmul": ([vp, vp, u32, u64, vp, u32, u64, u64, vp, i32, u64, vp], i32),
+        "q8_moe_ffn": ([vp, vp, vp, vp, u32, u64, u64, vp, vp, u32, u64, u64, u64, ctypes.c_float, vp, u64, vp],
+                       i32),
+        "q8_swiglu": ([vp, vp, vp, u64, ctypes.c_float, vp], i32),
+        "q8_moe_combine": ([vp, vp, vp, u64, u32, u64, vp], i32),
         "q8_repack_bytes": ([u64, u64], u64),
         "q8_repack": ([vp, vp, u64, u64, vp], i32),
         "q8_matmul_packed": ([vp, vp, u64, u64, vp, u64, vp], i32),
@@ -132,6 +137,22 @@ def q8_moe_matmul(out, W_experts, n_expert: int, expert_stride_bytes: int, exper
                   out_dim: int, x, x_per_pair: int, n_tok: int, stream=None) -> int:
     return _get().q8_moe_matmul(_p(out), _p(W_experts), n_expert, expert_stride_bytes, _p(expert_ids), k, in_dim,
                              out_dim, _p(x), int(x_per_pair), n_tok, _s(stream))
+
+
+def q8_moe_ffn(out, W_gate, W_up, W_down, n_expert: int, gate_up_stride_bytes: int, down_stride_bytes: int,
+               expert_ids, expert_weights, k: int, in_dim: int, mid_dim: int, out_dim: int, limit: float, x,
+               n_tok: int, stream=None) -> int:
+    return _get().q8_moe_ffn(_p(out), _p(W_gate), _p(W_up), _p(W_down), n_expert, gate_up_stride_bytes,
+                             down_stride_bytes, _p(expert_ids), _p(expert_weights), k, in_dim, mid_dim, out_dim,
+                             float(limit), _p(x), n_tok, _s(stream))
+
+
+def q8_swiglu(mid, gate, up, n: int, limit: float, stream=None) -> int:
+    return _get().q8_swiglu(_p(mid), _p(gate), _p(up), n, float(limit), _s(stream))
+
+
+def q8_moe_combine(out, y, weights, n_tok: int, k: int, dim: int, stream=None) -> int:
+    return _get().q8_moe_combine(_p(out), _p(y), _p(weights), n_tok, k, dim, _s(stream))
 
 
 def q8_repack_bytes(in_dim: int, rows: int) -> int:
@@ -229,6 +250,18 @@ def moe_matmul(W_experts, n_expert: int, expert_stride: int, ids, x, x_per_pair:
     out = torch.empty((n_tok * k, out_dim), dtype=torch.float32, device=x.device)
     _check(q8_moe_matmul(out, W_experts, n_expert, expert_stride, ids, k, in_dim, out_dim, x, int(x_per_pair),
                          n_tok), "q8_moe_matmul")
+    return out
+
+
+def moe_ffn(W_gate, W_up, W_down, n_expert: int, gate_up_stride: int, down_stride: int, ids, weights, x,
+            mid_dim: int, out_dim: int, limit: float):
+    """ids int32 and weights fp32 [n_tok, k]; x [n_tok, in] -> [n_tok, out_dim] (routed expert FFN)."""
+    import torch
+    n_tok, k = ids.shape
+    in_dim = x.shape[1]
+    out = torch.empty((n_tok, out_dim), dtype=torch.float32, device=x.device)
+    _check(q8_moe_ffn(out, W_gate, W_up, W_down, n_expert, gate_up_stride, down_stride, ids, weights, k, in_dim,
+                      mid_dim, out_dim, limit, x, n_tok), "q8_moe_ffn")
     return out
 
 

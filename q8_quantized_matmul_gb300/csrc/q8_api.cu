@@ -298,6 +298,170 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     return status_of(timed_launch(st, [&] { return q8::launch_tc_gemm(p, a16, b16, n_ld, grid, st); }));
 }
 
+// One routed-expert product, or two that share the routing and the quantised
+// activations (the gate and up projections of an expert FFN): W[w] -> out[w].
+struct MoeCall {
+    const void *W[2] = {nullptr, nullptr};
+    float *out[2] = {nullptr, nullptr};
+    int n_w = 1;
+    uint32_t n_expert = 0;
+    uint64_t stride = 0;          // bytes between experts' matrices
+    const int32_t *ids = nullptr;
+    uint32_t k = 0;
+    uint64_t in_dim = 0, out_dim = 0;
+    const float *x = nullptr;
+    int x_per_pair = 0;
+    uint64_t n_tok = 0;
+};
+
+// Scratch layout of a routed call.
+struct MoeLayout {
+    uint64_t nb = 0, n_pairs = 0, max_rows = 0, tc_cap = 0, tc_ld = 0;
+    size_t plan_bytes = 0, need = 0;
+    bool gemv_path = false;
+};
+
+MoeLayout moe_layout(const MoeCall &c) {
+    MoeLayout L;
+    L.nb = c.in_dim / q8::QK;
+    L.n_pairs = c.n_tok * c.k;
+    L.max_rows = q8::route_max_rows(L.n_pairs, c.n_expert);
+    L.plan_bytes = q8::route_plan_bytes(c.n_expert);
+    // Tensor-core class: experts of more than MOE_TC_MIN_ROWS rows, read as raw
+    // Q8_0 rows by the grouped GEMM; their activation rows go to the fp16 operand.
+    if (L.nb % 8 == 0 && L.n_pairs >= q8::MOE_TC_MIN_PAIRS) {
+        L.tc_cap = L.n_pairs / (q8::MOE_TC_MIN_ROWS + 1);
+        if (L.tc_cap > c.n_expert) L.tc_cap = c.n_expert;
+    }
+    const uint64_t tc_rows =
+        L.max_rows < L.n_pairs + 15 * L.tc_cap + 16 ? L.max_rows : L.n_pairs + 15 * L.tc_cap + 16;
+    L.tc_ld = ((tc_rows + 127) & ~(uint64_t)127) + 128;   // a tile may start at the last row
+    const size_t tc_bytes = L.tc_cap ? align256(L.tc_ld * c.in_dim * 2) + align256(L.nb * L.tc_ld * 4) : 0;
+    L.gemv_path = L.nb % 8 == 0;   // routed GEMV / tensor-core kernels (else the generic kernel)
+    L.need = align256(c.n_expert * 4) * 2 + q8::ROUTE_CLASSES * L.plan_bytes + align256(L.max_rows * 4) * 2 +
+             (L.gemv_path ? align256(L.n_pairs * 4) : 0) + planes_bytes(L.max_rows, c.in_dim) + tc_bytes;
+    return L;
+}
+
+// Routing, one quantisation of the activations, then the kernels of each weight
+// set; scratch at `base` holds L.need bytes.  Rows of pairs with an id out of
+// range are zeroed in out[0] only.
+int moe_run(DeviceState *s, const MoeCall &c, const MoeLayout &L, void *base, cudaStream_t st) {
+    Carver cv(base);
+    int32_t *counts = cv.take<int32_t>(c.n_expert * 4);
+    int32_t *row0_of = cv.take<int32_t>(c.n_expert * 4);
+    uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * L.plan_bytes);
+    int32_t *row_to_out = cv.take<int32_t>(L.max_rows * 4);
+    int32_t *src_row = cv.take<int32_t>(L.max_rows * 4);
+    int32_t *dst_row = L.gemv_path ? cv.take<int32_t>(L.n_pairs * 4) : nullptr;
+    int8_t *qx = cv.take<int8_t>(L.max_rows * c.in_dim);
+    float *dx = cv.take<float>(L.max_rows * L.nb * sizeof(float));
+    __half *b16 = L.tc_cap ? cv.take<__half>(L.tc_ld * c.in_dim * 2) : nullptr;
+    float *dxT = L.tc_cap ? cv.take<float>(L.nb * L.tc_ld * 4) : nullptr;
+    // GEMV items of up to 448 rows: 28 sixteen-row sub-items, two for each of the 14
+    // consumer warps.  (128-row items left 6 of the warps idle; at 64 tokens, top-6,
+    // the calls took 395 / 430 us with 128-row items, 352 / 374 with 224, 336 / 345
+    // with 448.)
+    uint32_t rows_gemv = (uint32_t)((c.out_dim + 15) & ~(uint64_t)15);
+    if (rows_gemv > 448) rows_gemv = 448;
+    cudaError_t e = q8::launch_route(c.ids, c.n_tok, c.k, c.n_expert, c.x_per_pair, (uint32_t)c.out_dim, rows_gemv,
+                                     (uint32_t)L.tc_cap, counts, row0_of, plans, row_to_out, src_row, dst_row,
+                                     L.max_rows, c.out[0], s->err, s->num_sms, st);
+    if (e != cudaSuccess) return status_of(e);
+    auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * L.plan_bytes); };
+    // The GEMV and tensor-core kernels read only the real rows: the quantiser walks
+    // the pairs and leaves the padding rows unwritten.  The generic kernel gets
+    // zero padding rows.
+    if (L.gemv_path)
+        e = q8::launch_quantize_pairs(qx, dx, b16, dxT, L.tc_ld, L.tc_cap ? plan_of(2) : nullptr, c.x, c.in_dim,
+                                      L.n_pairs, c.k, c.x_per_pair, dst_row, s->num_sms, st);
+    else
+        e = q8::launch_quantize_planes(qx, dx, c.x, c.in_dim, L.max_rows, src_row, 0, s->num_sms, st);
+    if (e != cudaSuccess) return status_of(e);
+    for (int w = 0; w < c.n_w; ++w) {
+        const uint8_t *W = static_cast<const uint8_t *>(c.W[w]);
+        float *out = c.out[w];
+        q8::MmaParams p{};
+        p.W = W;
+        p.expert_stride = c.stride;
+        p.in_dim = c.in_dim;
+        p.out_dim = (uint32_t)c.out_dim;
+        p.nb = (uint32_t)L.nb;
+        p.qx = qx;
+        p.dx = dx;
+        p.out = out;
+        p.err = s->err;
+        p.n_tok = 0;
+        p.row_to_out = row_to_out;
+        if (!L.gemv_path) {   // no tensor-core class here (tc_cap == 0)
+            const int hint = (int)(L.max_rows * c.out_dim > (1u << 30) ? (1u << 30) : L.max_rows * c.out_dim);
+            e = timed_launch(st, [&] {
+                for (int cls = 0; cls < q8::ROUTE_GEMV_CLASSES; ++cls) {
+                    p.plan = plan_of(cls);
+                    cudaError_t e2 = q8::launch_generic(p, hint, s->num_sms, st);
+                    if (e2 != cudaSuccess) return e2;
+                }
+                return cudaSuccess;
+            });
+            if (e != cudaSuccess) return status_of(e);
+            continue;
+        }
+        q8::GemvParams g{};
+        g.W = W;
+        g.expert_stride = c.stride;
+        g.in_dim = c.in_dim;
+        g.out_dim = (uint32_t)c.out_dim;
+        g.nb = (uint32_t)L.nb;
+        g.qx = qx;
+        g.dx = dx;
+        g.out = out;
+        g.err = s->err;
+        g.n_tok = 0;
+        g.rows_per_item = rows_gemv;
+        g.weights_early = 1;   // behind the quantiser, the grouped GEMM or another routed GEMV
+        g.row_to_out = row_to_out;
+        g.n_expert = c.n_expert;
+        q8::TcParams tp{};
+        tp.M = (int)c.out_dim;
+        tp.N = 0;
+        tp.nb = (int)L.nb;
+        tp.ksplit = 1;
+        tp.kb_per = (int)L.nb;
+        tp.dxT = dxT;
+        tp.dwT = nullptr;
+        tp.n_ld = L.tc_ld;
+        tp.m_ld = 0;
+        tp.out = out;
+        tp.partial = nullptr;
+        tp.err = s->err;
+        tp.plan = plan_of(2);
+        tp.row_to_out = row_to_out;
+        e = timed_launch(st, [&] {
+            if (L.tc_cap) {
+                cudaError_t e2 = q8::launch_tc_gemm_raw(tp, W, c.n_expert, c.stride, b16, L.tc_ld, s->num_sms, st);
+                if (e2 != cudaSuccess) return e2;
+            }
+            g.plan = plan_of(0);
+            cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
+            if (e2 != cudaSuccess) return e2;
+            g.plan = plan_of(1);
+            return q8::launch_gemv(g, 2, s->num_sms, st);
+        });
+        if (e != cudaSuccess) return status_of(e);
+    }
+    return Q8_OK;
+}
+
+// Host checks of a routed product's arguments (dimensions, expert count, stride).
+int check_moe(uint32_t n_expert, uint64_t stride, uint32_t k, uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
+    int rc = check_dims(in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_expert == 0 || n_expert > MAX_EXPERTS || k == 0 || k > n_expert) return Q8_EINVAL;
+    if (stride < out_dim * (in_dim / q8::QK) * q8::QB) return Q8_EINVAL;
+    if (n_tok * k > ((uint64_t)1 << 31) - 1) return Q8_EINVAL;
+    return Q8_OK;
+}
+
 }  // namespace
 
 namespace q8 {
@@ -411,12 +575,8 @@ int q8_matmul_q(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, co
 int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t expert_stride_bytes,
                   const int32_t *expert_ids, uint32_t k, uint64_t in_dim, uint64_t out_dim, const float *x,
                   int x_per_pair, uint64_t n_tok, void *stream) {
-    int rc = check_dims(in_dim, out_dim, n_tok);
+    int rc = check_moe(n_expert, expert_stride_bytes, k, in_dim, out_dim, n_tok);
     if (rc) return rc;
-    if (n_expert == 0 || n_expert > MAX_EXPERTS || k == 0 || k > n_expert) return Q8_EINVAL;
-    const uint64_t nb = in_dim / q8::QK;
-    if (expert_stride_bytes < out_dim * nb * q8::QB) return Q8_EINVAL;
-    if (n_tok * k > ((uint64_t)1 << 31) - 1) return Q8_EINVAL;
     if (n_tok == 0 || out_dim == 0) return Q8_OK;
     if (!out || !W_experts || !expert_ids || !x) return Q8_EINVAL;
     if (!aligned16(out) || !aligned16(W_experts) || !aligned16(x) || (expert_stride_bytes & 15u) ||
@@ -425,120 +585,120 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert, uint64_t
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
-    const uint64_t n_pairs = n_tok * k;
-    const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
-    const size_t plan_bytes = q8::route_plan_bytes(n_expert);
-    // Tensor-core class: experts of more than MOE_TC_MIN_ROWS rows, read as raw
-    // Q8_0 rows by the grouped GEMM; their activation rows go to the fp16 operand.
-    uint64_t tc_cap = 0;
-    if (nb % 8 == 0 && n_pairs >= q8::MOE_TC_MIN_PAIRS) {
-        tc_cap = n_pairs / (q8::MOE_TC_MIN_ROWS + 1);
-        if (tc_cap > n_expert) tc_cap = n_expert;
+    MoeCall c;
+    c.W[0] = W_experts;
+    c.out[0] = out;
+    c.n_expert = n_expert;
+    c.stride = expert_stride_bytes;
+    c.ids = expert_ids;
+    c.k = k;
+    c.in_dim = in_dim;
+    c.out_dim = out_dim;
+    c.x = x;
+    c.x_per_pair = x_per_pair;
+    c.n_tok = n_tok;
+    const MoeLayout L = moe_layout(c);
+    if ((rc = reserve_scratch(s, L.need))) return rc;
+    return moe_run(s, c, L, s->scratch, static_cast<cudaStream_t>(stream));
+}
+
+int q8_swiglu(float *mid, const float *gate, const float *up, uint64_t n, float limit, void *stream) {
+    if (!(limit >= 0.0f)) return Q8_EINVAL;   // negative or NaN
+    if (n == 0) return Q8_OK;
+    if (n > ((uint64_t)1 << 60)) return Q8_EINVAL;
+    if (!mid || !gate || !up) return Q8_EINVAL;
+    if (!aligned16(mid) || !aligned16(gate) || !aligned16(up)) return Q8_EALIGN;
+    int rc;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        DeviceState *s;
+        if ((rc = get_device(&s))) return rc;
+        sms = s->num_sms;
     }
-    const uint64_t tc_rows = max_rows < n_pairs + 15 * tc_cap + 16 ? max_rows : n_pairs + 15 * tc_cap + 16;
-    const uint64_t tc_ld = ((tc_rows + 127) & ~(uint64_t)127) + 128;   // a tile may start at the last row
-    const size_t tc_bytes = tc_cap ? align256(tc_ld * in_dim * 2) + align256(nb * tc_ld * 4) : 0;
-    const bool gemv_path = nb % 8 == 0;   // routed GEMV / tensor-core kernels (else the generic kernel)
-    const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * plan_bytes + align256(max_rows * 4) * 2 +
-                        (gemv_path ? align256(n_pairs * 4) : 0) + planes_bytes(max_rows, in_dim) + tc_bytes;
-    if ((rc = reserve_scratch(s, need))) return rc;
-    Carver cv(s->scratch);
-    int32_t *counts = cv.take<int32_t>(n_expert * 4);
-    int32_t *row0_of = cv.take<int32_t>(n_expert * 4);
-    uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * plan_bytes);
-    int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
-    int32_t *src_row = cv.take<int32_t>(max_rows * 4);
-    int32_t *dst_row = gemv_path ? cv.take<int32_t>(n_pairs * 4) : nullptr;
-    int8_t *qx = cv.take<int8_t>(max_rows * in_dim);
-    float *dx = cv.take<float>(max_rows * nb * sizeof(float));
-    __half *b16 = tc_cap ? cv.take<__half>(tc_ld * in_dim * 2) : nullptr;
-    float *dxT = tc_cap ? cv.take<float>(nb * tc_ld * 4) : nullptr;
+    return status_of(q8::launch_swiglu(mid, gate, up, n, limit, nullptr, 0, 0, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_moe_combine(float *out, const float *y, const float *weights, uint64_t n_tok, uint32_t k, uint64_t dim,
+                   void *stream) {
+    if (k == 0) return Q8_EINVAL;
+    if (n_tok == 0 || dim == 0) return Q8_OK;
+    if (n_tok > ((uint64_t)1 << 40) / k || dim > ((uint64_t)1 << 60) / (n_tok * k)) return Q8_EINVAL;
+    if (!out || !y || !weights) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(y) || (reinterpret_cast<uintptr_t>(weights) & 3u)) return Q8_EALIGN;
+    int rc;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        DeviceState *s;
+        if ((rc = get_device(&s))) return rc;
+        sms = s->num_sms;
+    }
+    return status_of(q8::launch_combine(out, y, weights, n_tok, k, dim, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_down, uint32_t n_expert,
+               uint64_t gate_up_stride_bytes, uint64_t down_stride_bytes, const int32_t *expert_ids,
+               const float *expert_weights, uint32_t k, uint64_t in_dim, uint64_t mid_dim, uint64_t out_dim,
+               float limit, const float *x, uint64_t n_tok, void *stream) {
+    int rc = check_moe(n_expert, gate_up_stride_bytes, k, in_dim, mid_dim, n_tok);
+    if (rc) return rc;
+    if ((rc = check_moe(n_expert, down_stride_bytes, k, mid_dim, out_dim, n_tok))) return rc;
+    if (mid_dim == 0 || !(limit >= 0.0f)) return Q8_EINVAL;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W_gate || !W_up || !W_down || !expert_ids || !expert_weights || !x) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(x) ||
+        (gate_up_stride_bytes & 15u) || (down_stride_bytes & 15u) ||
+        (reinterpret_cast<uintptr_t>(expert_ids) & 3u) || (reinterpret_cast<uintptr_t>(expert_weights) & 3u))
+        return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // GEMV items of up to 448 rows: 28 sixteen-row sub-items, two for each of the 14
-    // consumer warps.  (128-row items left 6 of the warps idle; at 64 tokens, top-6,
-    // the calls took 395 / 430 us with 128-row items, 352 / 374 with 224, 336 / 345
-    // with 448.)
-    uint32_t rows_gemv = (uint32_t)((out_dim + 15) & ~(uint64_t)15);
-    if (rows_gemv > 448) rows_gemv = 448;
-    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_gemv,
-                                     (uint32_t)tc_cap, counts, row0_of, plans, row_to_out, src_row, dst_row, max_rows,
-                                     out, s->err, s->num_sms, st);
-    if (e != cudaSuccess) return Q8_ECUDA;
-    auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes); };
-    // The GEMV and tensor-core kernels read only the real rows: the quantiser walks
-    // the pairs and leaves the padding rows unwritten.  The generic kernel gets
-    // zero padding rows.
-    if (gemv_path)
-        e = q8::launch_quantize_pairs(qx, dx, b16, dxT, tc_ld, tc_cap ? plan_of(2) : nullptr, x, in_dim, n_pairs, k,
-                                      x_per_pair, dst_row, s->num_sms, st);
-    else
-        e = q8::launch_quantize_planes(qx, dx, x, in_dim, max_rows, src_row, 0, s->num_sms, st);
-    if (e != cudaSuccess) return Q8_ECUDA;
-    q8::MmaParams p{};
-    p.W = static_cast<const uint8_t *>(W_experts);
-    p.expert_stride = expert_stride_bytes;
-    p.in_dim = in_dim;
-    p.out_dim = (uint32_t)out_dim;
-    p.nb = (uint32_t)nb;
-    p.qx = qx;
-    p.dx = dx;
-    p.out = out;
-    p.err = s->err;
-    p.n_tok = 0;
-    p.row_to_out = row_to_out;
-    if (nb % 8 != 0) {   // no tensor-core class here (tc_cap == 0)
-        const int hint = (int)(max_rows * out_dim > (1u << 30) ? (1u << 30) : max_rows * out_dim);
-        return status_of(timed_launch(st, [&] {
-            for (int cls = 0; cls < q8::ROUTE_GEMV_CLASSES; ++cls) {
-                p.plan = plan_of(cls);
-                cudaError_t e2 = q8::launch_generic(p, hint, s->num_sms, st);
-                if (e2 != cudaSuccess) return e2;
-            }
-            return cudaSuccess;
-        }));
-    }
-    q8::GemvParams g{};
-    g.W = p.W;
-    g.expert_stride = expert_stride_bytes;
-    g.in_dim = in_dim;
-    g.out_dim = (uint32_t)out_dim;
-    g.nb = (uint32_t)nb;
-    g.qx = qx;
-    g.dx = dx;
-    g.out = out;
-    g.err = s->err;
-    g.n_tok = 0;
-    g.rows_per_item = rows_gemv;
-    g.weights_early = 1;   // behind the quantiser or the grouped GEMM, then behind the previous class's GEMV
-    g.row_to_out = row_to_out;
-    g.n_expert = n_expert;
-    q8::TcParams tp{};
-    tp.M = (int)out_dim;
-    tp.N = 0;
-    tp.nb = (int)nb;
-    tp.ksplit = 1;
-    tp.kb_per = (int)nb;
-    tp.dxT = dxT;
-    tp.dwT = nullptr;
-    tp.n_ld = tc_ld;
-    tp.m_ld = 0;
-    tp.out = out;
-    tp.partial = nullptr;
-    tp.err = s->err;
-    tp.plan = plan_of(2);
-    tp.row_to_out = row_to_out;
-    return status_of(timed_launch(st, [&] {
-        if (tc_cap) {
-            cudaError_t e2 = q8::launch_tc_gemm_raw(tp, static_cast<const uint8_t *>(W_experts), n_expert,
-                                                    expert_stride_bytes, b16, tc_ld, s->num_sms, st);
-            if (e2 != cudaSuccess) return e2;
-        }
-        g.plan = plan_of(0);
-        cudaError_t e2 = q8::launch_gemv(g, 1, s->num_sms, st);
-        if (e2 != cudaSuccess) return e2;
-        g.plan = plan_of(1);
-        return q8::launch_gemv(g, 2, s->num_sms, st);
-    }));
+    const uint64_t n_pairs = n_tok * k;
+    MoeCall gu;   // gate and up: in_dim -> mid_dim on the token rows, one routing
+    gu.W[0] = W_gate;
+    gu.W[1] = W_up;
+    gu.n_w = 2;
+    gu.n_expert = n_expert;
+    gu.stride = gate_up_stride_bytes;
+    gu.ids = expert_ids;
+    gu.k = k;
+    gu.in_dim = in_dim;
+    gu.out_dim = mid_dim;
+    gu.x = x;
+    gu.x_per_pair = 0;
+    gu.n_tok = n_tok;
+    MoeCall dn = gu;   // down: mid_dim -> out_dim on the pair rows of mid
+    dn.W[0] = W_down;
+    dn.W[1] = nullptr;
+    dn.out[1] = nullptr;
+    dn.n_w = 1;
+    dn.stride = down_stride_bytes;
+    dn.in_dim = mid_dim;
+    dn.out_dim = out_dim;
+    dn.x_per_pair = 1;
+    const MoeLayout Lgu = moe_layout(gu), Ldn = moe_layout(dn);
+    // scratch: the routed calls' region (reused by both), then gate, up, mid and y
+    const size_t region = align256(Lgu.need > Ldn.need ? Lgu.need : Ldn.need);
+    const size_t mid_bytes = align256(n_pairs * mid_dim * 4);
+    if ((rc = reserve_scratch(s, region + 3 * mid_bytes + align256(n_pairs * out_dim * 4)))) return rc;
+    Carver cv(static_cast<uint8_t *>(s->scratch) + region);
+    float *gate = cv.take<float>(n_pairs * mid_dim * 4);
+    float *up = cv.take<float>(n_pairs * mid_dim * 4);
+    float *mid = cv.take<float>(n_pairs * mid_dim * 4);
+    float *y = cv.take<float>(n_pairs * out_dim * 4);
+    gu.out[0] = gate;
+    gu.out[1] = up;
+    if ((rc = moe_run(s, gu, Lgu, s->scratch, st))) return rc;
+    // a pair with a bad id: its gate row is zero, its up row unwritten; mid is zeroed
+    if ((rc = status_of(q8::launch_swiglu(mid, gate, up, n_pairs * mid_dim, limit, expert_ids, n_expert, mid_dim,
+                                          s->num_sms, st))))
+        return rc;
+    dn.x = mid;
+    dn.out[0] = y;
+    if ((rc = moe_run(s, dn, Ldn, s->scratch, st))) return rc;
+    return status_of(q8::launch_combine(out, y, expert_weights, n_tok, k, out_dim, s->num_sms, st));
 }
 
 uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows) {

@@ -137,6 +137,18 @@ inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
     return (uint32_t)items;
 }
 
+// Elementwise steps of the routed expert FFN (q8_ffn.cu).
+//   launch_swiglu:  mid[i] = silu(min(gate[i], L)) * clamp(up[i], -L, L) (L = limit; 0: no
+//                   clamp) for n values; gate, up, mid 16-byte aligned.  With ids, the values
+//                   are rows of row_len (a multiple of 4) and the row of a pair whose id is
+//                   outside [0, n_expert) is written as zeros.
+//   launch_combine: out[t][o] = sum_j w[t*k+j] * y[t*k+j][o], j in order; out and y
+//                   16-byte aligned.
+cudaError_t launch_swiglu(float *mid, const float *gate, const float *up, uint64_t n, float limit,
+                          const int32_t *ids, uint32_t n_expert, uint64_t row_len, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(float *out, const float *y, const float *w, uint64_t n_tok, uint32_t k, uint64_t dim,
+                           int num_sms, cudaStream_t st);
+
 // Prefill GEMM on tcgen05 (q8_tc.cu).  Weights as an fp16 plane [M][K] (from
 // launch_tc_expand) with block-major scales dwT[nb][m_ld]; activations as an
 // fp16 plane [n_ld rows][K] with block-major scales dxT[nb][n_ld]
