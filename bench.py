@@ -75,12 +75,13 @@ def dist_env():
     return rank, world, local
 
 
-def dist_init(world):
+def dist_init(world, backend: str = "nccl"):
+    """One process group over the ranks (NCCL for the bench; gloo runs the same plumbing on CPU)."""
     if world <= 1:
         return None
     import torch.distributed as dist
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group("nccl")
+    dist.init_process_group(backend)
     return dist
 
 
@@ -88,7 +89,7 @@ def max_over_ranks(dist, v: float) -> float:
     if dist is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
