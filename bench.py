@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "prefill_long", "moe",
-                                               "moe_zipf", "moe_zipf_small"),
+                                               "moe_zipf", "moe_zipf_small", "moe_ffn"),
                     help="run one workload's call a few times without timing (for ncu captures)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -626,6 +626,13 @@ def profile_case(case: str):
         W = torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=2)).to(dev)
         x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
         fn = lambda: q8.moe_matmul(W, 256, 2048 * 128 * QB, ids, x, False, 2048)
+    elif case == "moe_ffn":   # the routed expert FFN at the decode size (256 experts, 64 tokens, top-6)
+        ids = torch.from_numpy(inputs.route_uniform(64, 6, 256, seed=0)).to(dev)
+        Wg, Wu = (torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=s)).to(dev) for s in (2, 4))
+        Wd = torch.from_numpy(inputs.weights(256 * 4096, 2048, seed=5)).to(dev)
+        wts = torch.from_numpy(np.random.default_rng(0).random((64, 6)).astype(np.float32)).to(dev)
+        x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
+        fn = lambda: q8.moe_ffn(Wg, Wu, Wd, 256, 2048 * 128 * QB, 4096 * 64 * QB, ids, wts, x, 2048, 4096, 10.0)
     else:   # routed gate/up with Zipf(1.1) top-6: the layer slice's (moe_zipf) or 1024 tokens over 64 experts
         n, ne = (4096, 256) if case == "moe_zipf" else (1024, 64)
         ids = torch.from_numpy(inputs.route_zipf(n, 6, ne, s=1.1, seed=0)).to(dev)
