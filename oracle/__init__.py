@@ -65,8 +65,9 @@ class Oracle:
         lib.q8o_combine.restype = None
         lib.q8o_moe_ffn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, u32, u64, u64, vp, vp, u32,
                                     u64, u64, u64, ctypes.c_float, vp, u64]
+        lib.q8o_rmsnorm_quantize.argtypes = [vp, vp, vp, vp, u64, u64, ctypes.c_double]
         for f in (lib.q8o_quantize, lib.q8o_matmul, lib.q8o_matmul_sample, lib.q8o_moe,
-                  lib.q8o_moe_sample, lib.q8o_moe_ffn):
+                  lib.q8o_moe_sample, lib.q8o_moe_ffn, lib.q8o_rmsnorm_quantize):
             f.restype = ctypes.c_int
         self.lib = lib
 
@@ -204,6 +205,21 @@ class Oracle:
             raise ValueError("oracle moe_ffn: bad dimensions")
         r["flag"] = rc
         return r
+
+    # -- RMSNorm feeding the quantiser ----------------------------------------------
+    def rmsnorm_quantize(self, x, gamma, eps: float):
+        """x float32 [n_tok, dim], gamma float32 [dim] or None -> (xq uint8 [n_tok, dim/32*34],
+        y float32 [n_tok, dim])."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        n_tok, dim = x.shape
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
+        y = np.empty_like(x)
+        xq = np.empty((n_tok, dim // QK * QBYTES), dtype=np.uint8)
+        rc = self.lib.q8o_rmsnorm_quantize(xq.ctypes.data, y.ctypes.data, x.ctypes.data,
+                                           None if g is None else g.ctypes.data, dim, n_tok, float(eps))
+        if rc != 0:
+            raise ValueError("oracle rmsnorm_quantize: bad dims")
+        return xq, y
 
 
 _oracle = None

@@ -42,7 +42,11 @@
  *     to fp32; the clamp applies when limit > 0 (limit = 0: none);
  *   - the down projection's activations are the fp32 mid rows quantised with
  *     the activation quantiser above, one row per pair;
- *   - the weighted sum adds the k experts of a token in slot order, in double.
+ *   - the weighted sum adds the k experts of a token in slot order, in double;
+ *   - RMSNorm (the model's attn_norm / ffn_norm scales, model-architecture page,
+ *     weight table): y_i = x_i / sqrt(mean_j x_j^2 + eps) * gamma_i, the usual
+ *     definition (the pages name the norm but print no formula), evaluated in
+ *     double from the fp32 inputs and rounded once to fp32; eps > 0 is an argument.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC.
  */
@@ -335,4 +339,23 @@ int q8o_moe_ffn(double *out, double *out_bound, float *y, double *y_bound, float
     free(gate);
     free(up);
     return rc;
+}
+
+/* ---- RMSNorm feeding the quantiser ------------------------------------------- */
+
+/* Per token row t: r = 1 / sqrt(mean_i x_i^2 + eps), y_i = x_i * r * gamma_i
+ * (gamma == NULL: all ones), then xq = the activation quantiser of y.  y is
+ * fp32 [n_tok][dim], xq [n_tok][dim/32] blocks.  Returns -1 on bad dimensions. */
+int q8o_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
+                         uint64_t n_tok, double eps) {
+    if (dim == 0 || dim % QK) return -1;
+    for (uint64_t t = 0; t < n_tok; ++t) {
+        const float *xr = x + t * dim;
+        double s = 0.0;
+        for (uint64_t i = 0; i < dim; ++i) s += (double)xr[i] * (double)xr[i];
+        double r = 1.0 / sqrt(s / (double)dim + eps);
+        for (uint64_t i = 0; i < dim; ++i)
+            y[t * dim + i] = (float)((double)xr[i] * r * (gamma ? (double)gamma[i] : 1.0));
+    }
+    return q8o_quantize(xq, y, dim, n_tok);
 }

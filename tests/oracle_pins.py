@@ -603,4 +603,44 @@ def pin_moe_ffn_bad_id(o):
     assert np.array_equal(bad["out"][0], 0.5 * good["y"][0].astype(np.float64))
 
 
+# ---------------------------------------------------------------- RMSNorm feeding the quantiser
+def pin_rmsnorm_unit_rows(o):
+    """Rows of +/-1 have mean square 1, so with a negligible eps y = x * gamma exactly (the
+    scale 1/sqrt(1 + 2^-40) moves a value by far less than half an fp32 step); the
+    quantised output is the quantiser of y."""
+    g = rng(24)
+    n_tok, dim = 3, 96
+    x = g.choice([-1.0, 1.0], size=(n_tok, dim)).astype(np.float32)
+    gamma = (0.5 + g.random(dim)).astype(np.float32)
+    xq, y = o.rmsnorm_quantize(x, gamma, 2.0 ** -40)
+    assert np.array_equal(y, x * gamma)
+    assert np.array_equal(xq, o.quantize(y))
+    xq1, y1 = o.rmsnorm_quantize(x, None, 2.0 ** -40)
+    assert np.array_equal(y1, x)
+
+
+def pin_rmsnorm_invariants(o):
+    """Scale invariance under powers of two, the RMS of y / gamma equal to 1, the sign of
+    x * gamma kept, linearity in gamma (power of two), and the limit where eps dominates."""
+    g = rng(25)
+    n_tok, dim = 4, 256
+    x = g.standard_normal((n_tok, dim)).astype(np.float32)
+    gamma = (1.0 + 0.2 * g.standard_normal(dim)).astype(np.float32)
+    eps = 1e-30
+    _, y = o.rmsnorm_quantize(x, gamma, eps)
+    for k in (-3, 5):
+        _, yk = o.rmsnorm_quantize(x * np.float32(2.0 ** k), gamma, eps)
+        assert np.array_equal(yk, y)
+    rms = np.sqrt(np.mean((y.astype(np.float64) / gamma) ** 2, axis=1))
+    assert np.all(np.abs(rms - 1.0) <= 1e-6)
+    assert np.all(np.sign(y) == np.sign(x * gamma))
+    _, y2 = o.rmsnorm_quantize(x, 2 * gamma, eps)
+    assert np.array_equal(y2, 2 * y)
+    tiny = (1e-20 * x).astype(np.float32)            # mean square 1e-40, far below eps = 1
+    _, yt = o.rmsnorm_quantize(tiny, gamma, 1.0)
+    assert np.array_equal(yt, tiny * gamma)
+    xq0, y0 = o.rmsnorm_quantize(np.zeros((2, dim), np.float32), gamma, 1e-6)
+    assert np.all(y0 == 0) and np.all(xq0 == 0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

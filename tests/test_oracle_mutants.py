@@ -52,6 +52,13 @@ MUTANTS = [
     ("ffn_down_token_rows", "midq, 1, n_tok);", "midq, 0, n_tok);"),
     ("ffn_down_gate_stride", "q8o_moe(y, y_bound, W_down, n_expert, down_stride,", "q8o_moe(y, y_bound, W_down, n_expert, gate_up_stride,"),
     ("ffn_no_bad_flag", "rc = (f1 < 0 || f2 < 0 || f3 < 0) ? -1 : (f1 | f2 | f3);", "rc = (f1 < 0 || f2 < 0 || f3 < 0) ? -1 : 0;"),
+    # RMSNorm feeding the quantiser
+    ("rms_sum_not_mean", "double r = 1.0 / sqrt(s / (double)dim + eps);", "double r = 1.0 / sqrt(s + eps);"),
+    ("rms_no_sqrt", "double r = 1.0 / sqrt(s / (double)dim + eps);", "double r = 1.0 / (s / (double)dim + eps);"),
+    ("rms_eps_outside", "double r = 1.0 / sqrt(s / (double)dim + eps);", "double r = 1.0 / sqrt(s / (double)dim) + eps;"),
+    ("rms_no_gamma", "(gamma ? (double)gamma[i] : 1.0)", "1.0"),
+    ("rms_quantise_x", "return q8o_quantize(xq, y, dim, n_tok);", "return q8o_quantize(xq, x, dim, n_tok);"),
+    ("rms_abs_sum", "s += (double)xr[i] * (double)xr[i];", "s += fabs((double)xr[i]);"),
 ]
 
 
