@@ -422,6 +422,32 @@ def secondary(args, torch, q8, dev, stream, l2):
                 "timing": "graph of back-to-back calls, each on its own weight copy"})
     del copies, cg
 
+    # RMSNorm feeding the quantiser at the long-prefill input (4096 tokens x 4096): reads x,
+    # writes the Q8_0 rows; each call on its own copy of x (copies > 4x L2)
+    n, dim = 4096, 4096
+    xh = inputs.normal((n, dim), seed=6)
+    xcopies = weight_copies(torch, dev, xh, 4 * l2)
+    gamma = torch.from_numpy((1.0 + 0.1 * np.random.default_rng(6).standard_normal(dim)).astype(np.float32)).to(dev)
+    xq = torch.empty((n, dim // QK * QB), dtype=torch.uint8, device=dev)
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c in xcopies:
+            q8.q8_rmsnorm_quantize(xq, None, c, gamma, dim, n, 1e-6, stream)
+    stream.synchronize()
+    with torch.cuda.graph(cg, stream=stream):
+        for c in xcopies:
+            q8.q8_rmsnorm_quantize(xq, None, c, gamma, dim, n, 1e-6, stream)
+    graph_replays(torch, stream, [cg], 3)
+    ms = graph_replays(torch, stream, [cg], 10) / (10 * len(xcopies))
+    nbytes = n * dim * 4 + n * dim // QK * QB + dim * 4
+    out.append({"workload": f"RMSNorm + Q8_0 quantiser, {n} tokens x {dim} (long-prefill q_a input)",
+                "ms_per_call": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                "bytes_per_call": nbytes,
+                "timing": "graph of back-to-back calls, each on its own copy of x"})
+    assert q8.q8_last_error(stream) == 0
+    del xcopies, cg
+
     # prefill GEMMs (attn_output_a and shared-expert shapes) at n_tok = 512
     for in_dim, out_dim in ((32768, 1024), (4096, 2048), (2048, 4096)):
         n = 512

@@ -83,6 +83,26 @@ const char *q8_strerror(int status);
 int q8_quantize_act(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, void *stream);
 
 /*
+ * RMSNorm feeding the quantiser: the producer of a projection's input writes
+ * the quantised activations directly, so the separate quantiser pass goes away
+ * (the pages fold the HC RMS norm into the projection input: GPU concepts page,
+ * §4m, and the fused RMS-norm producers of §4n).  Per token row t:
+ *   r = 1 / sqrt(mean_i x[t][i]^2 + eps),  y[t][i] = (x[t][i] * r) * gamma[i]
+ *   xq[t] = the q8_quantize_act quantiser of y[t]     (bit for bit)
+ * The pages name the norm (attn_norm, ffn_norm) but print no formula; this is
+ * the usual RMSNorm.  fp32 arithmetic: the sum of squares in a fixed order
+ * (same bits on every run) with relative error at most (8 ceil(dim/2048) + 14)
+ * 2^-24; sqrt and division are IEEE.
+ *   xq     out: [n_tok][dim/32] Q8_0 blocks (input of q8_matmul_q).
+ *   y      out: fp32 [n_tok][dim], the normalised rows, or NULL.
+ *   x      in:  fp32 [n_tok][dim];  gamma in: fp32 [dim], or NULL for all ones.
+ *   eps    > 0 and finite (else Q8_EINVAL); dim % 32 == 0.
+ * xq, x, y and gamma 16-byte aligned (Q8_EALIGN).
+ */
+int q8_rmsnorm_quantize(void *xq, float *y, const float *x, const float *gamma, uint64_t dim,
+                        uint64_t n_tok, float eps, void *stream);
+
+/*
  * Q8_0 matmul from fp32 activations (GPU code walkthrough, trace 3:
  * ds4_gpu_matmul_q8_0_tensor(out, model_map, ..., weight_offset, in_dim,
  * out_dim, x, n_tok); here W is already a device pointer to the weight rows).

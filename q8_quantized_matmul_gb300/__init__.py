@@ -27,7 +27,7 @@ EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matm
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
            "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host", "q8_moe_ffn", "q8_swiglu",
-           "q8_moe_combine")
+           "q8_moe_combine", "q8_rmsnorm_quantize")
 
 
 class Q8Error(RuntimeError):
@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "q8_moe_ffn": ([vp, vp, vp, vp, u32, u64, u64, vp, vp, u32, u64, u64, u64, ctypes.c_float, vp, u64, vp],
                        i32),
         "q8_swiglu": ([vp, vp, vp, u64, ctypes.c_float, vp], i32),
+        "q8_rmsnorm_quantize": ([vp, vp, vp, vp, u64, u64, ctypes.c_float, vp], i32),
         "q8_moe_combine": ([vp, vp, vp, u64, u32, u64, vp], i32),
         "q8_repack_bytes": ([u64, u64], u64),
         "q8_repack": ([vp, vp, u64, u64, vp], i32),
@@ -145,6 +146,10 @@ def q8_moe_ffn(out, W_gate, W_up, W_down, n_expert: int, gate_up_stride_bytes: i
     return _get().q8_moe_ffn(_p(out), _p(W_gate), _p(W_up), _p(W_down), n_expert, gate_up_stride_bytes,
                              down_stride_bytes, _p(expert_ids), _p(expert_weights), k, in_dim, mid_dim, out_dim,
                              float(limit), _p(x), n_tok, _s(stream))
+
+
+def q8_rmsnorm_quantize(xq, y, x, gamma, dim: int, n_tok: int, eps: float, stream=None) -> int:
+    return _get().q8_rmsnorm_quantize(_p(xq), _p(y), _p(x), _p(gamma), dim, n_tok, float(eps), _s(stream))
 
 
 def q8_swiglu(mid, gate, up, n: int, limit: float, stream=None) -> int:
@@ -263,6 +268,17 @@ def moe_ffn(W_gate, W_up, W_down, n_expert: int, gate_up_stride: int, down_strid
     _check(q8_moe_ffn(out, W_gate, W_up, W_down, n_expert, gate_up_stride, down_stride, ids, weights, k, in_dim,
                       mid_dim, out_dim, limit, x, n_tok), "q8_moe_ffn")
     return out
+
+
+def rmsnorm_quantize(x, gamma, eps: float, want_y: bool = False):
+    """x float32 [n_tok, dim] (cuda), gamma [dim] or None -> Q8_0 blocks [n_tok, dim/32*34]
+    (and the normalised fp32 rows when want_y)."""
+    import torch
+    n_tok, dim = x.shape
+    xq = torch.empty((n_tok, dim // QK * QB), dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(x) if want_y else None
+    _check(q8_rmsnorm_quantize(xq, y, x, gamma, dim, n_tok, eps), "q8_rmsnorm_quantize")
+    return (xq, y) if want_y else xq
 
 
 def repack(W, in_dim: int, rows: int):

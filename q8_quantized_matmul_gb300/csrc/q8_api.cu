@@ -525,6 +525,21 @@ static int dispatch_matmul(DeviceState *s, float *out, const void *W, uint64_t i
     return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st);
 }
 
+int q8_rmsnorm_quantize(void *xq, float *y, const float *x, const float *gamma, uint64_t dim, uint64_t n_tok,
+                        float eps, void *stream) {
+    int rc = check_dims(dim, 1, n_tok);
+    if (rc) return rc;
+    if (!(eps > 0.0f) || eps == __builtin_inff()) return Q8_EINVAL;   // NaN, zero, negative or infinite
+    if (n_tok == 0) return Q8_OK;
+    if (!xq || !x) return Q8_EINVAL;
+    if (!aligned16(xq) || !aligned16(x) || (y && !aligned16(y)) || (gamma && !aligned16(gamma))) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    return status_of(q8::launch_rmsnorm_quantize(static_cast<uint8_t *>(xq), y, x, gamma, dim, n_tok, eps, s->num_sms,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
                          const void *xq, uint64_t n_tok, void *stream) {
     int rc = check_dims(in_dim, out_dim, n_tok);

@@ -137,6 +137,12 @@ inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
     return (uint32_t)items;
 }
 
+// RMSNorm feeding the quantiser (q8_quantize.cu): per token row, y = x / sqrt(mean x^2 + eps)
+// * gamma (gamma null: ones), xq = the activation quantiser of y ([n_tok][dim/32] blocks).
+// x, gamma, y 16-byte aligned; y may be null; dim % 32 == 0.
+cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
+                                    uint64_t n_tok, float eps, int num_sms, cudaStream_t st);
+
 // Elementwise steps of the routed expert FFN (q8_ffn.cu).
 //   launch_swiglu:  mid[i] = silu(min(gate[i], L)) * clamp(up[i], -L, L) (L = limit; 0: no
 //                   clamp) for n values; gate, up, mid 16-byte aligned.  With ids, the values

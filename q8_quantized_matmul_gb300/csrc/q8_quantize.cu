@@ -238,6 +238,86 @@ __global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, f
     }
 }
 
+// RMSNorm feeding the quantiser: one CTA per token row (grid-stride over rows).
+//   r = 1 / sqrt(mean_i x_i^2 + eps),  y_i = (x_i * r) * gamma_i,  xq = quantiser(y)
+// The usual RMSNorm (the model's attn_norm / ffn_norm scales); the pages name the
+// norm but print no formula.  The sum of squares runs in a fixed order -- each
+// thread adds its own values in sequence (8 consecutive values per 2048-value
+// stride), then a 5-level warp tree, then the 8 warps' sums in sequence -- so the
+// result is the same on every run, and its relative error is at most
+// (8 ceil(dim/2048) + 14) 2^-24.  Thread t's 8 values of a stride are lane
+// (t & 3)'s part of block t/4, the quantiser's lane layout, so quantize8 applies
+// unchanged: the quantised rows are the activation quantiser of the fp32 y.
+constexpr int RMS_THREADS = 256;
+
+__global__ void __launch_bounds__(RMS_THREADS) k_rmsnorm_quantize(uint8_t *__restrict__ xq, float *__restrict__ y,
+                                                                 const float *__restrict__ x,
+                                                                 const float *__restrict__ gamma, uint64_t dim,
+                                                                 uint64_t n_tok, float eps) {
+    __shared__ float part[RMS_THREADS / 32];
+    __shared__ float r_sh;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint64_t nb = dim / QK;
+    const uint64_t lane_q = (uint64_t)(t & 3);
+    for (uint64_t row = blockIdx.x; row < n_tok; row += gridDim.x) {
+        const float *xr = x + row * dim;
+        float s = 0.0f;
+        for (uint64_t e = (uint64_t)t * 8; e < dim; e += RMS_THREADS * 8) {
+            float x8[8];
+            load8(x8, xr + e);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s = __fadd_rn(s, __fmul_rn(x8[i], x8[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+        if (lane == 0) part[warp] = s;
+        __syncthreads();
+        if (t == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < RMS_THREADS / 32; ++w) tot = __fadd_rn(tot, part[w]);
+            r_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)dim), eps)));
+        }
+        __syncthreads();
+        const float r = r_sh;
+        // whole CTA iterates together: the quantiser's shuffles need every lane
+        for (uint64_t base = 0; base < dim; base += RMS_THREADS * 8) {
+            const uint64_t e = base + (uint64_t)t * 8;
+            const bool live = e < dim;
+            float y8[8];
+            if (live) {
+                float x8[8], g8[8];
+                load8(x8, xr + e);
+                if (gamma) {
+                    load8(g8, gamma + e);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) g8[i] = 1.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y8[i] = __fmul_rn(__fmul_rn(x8[i], r), g8[i]);
+                if (y) {
+                    float4 *yo = reinterpret_cast<float4 *>(y + row * dim + e);
+                    yo[0] = make_float4(y8[0], y8[1], y8[2], y8[3]);
+                    yo[1] = make_float4(y8[4], y8[5], y8[6], y8[7]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y8[i] = 0.0f;
+            }
+            const QuantBlock qb = quantize8(y8);
+            if (live) {
+                uint8_t *o = xq + (row * nb + e / QK) * QB;
+                if (lane_q == 0) *reinterpret_cast<uint16_t *>(o) = qb.dh;
+                uint16_t *qo = reinterpret_cast<uint16_t *>(o + 2 + lane_q * 8);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    qo[i] = (uint16_t)((uint8_t)qb.q[2 * i]) | (uint16_t)((uint16_t)(uint8_t)qb.q[2 * i + 1] << 8);
+            }
+        }
+        __syncthreads();   // part and r_sh are rewritten for the next row
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 // Launch behind the previous kernel with programmatic serialisation: the
 // launch overlaps that kernel's drain; the kernel waits for it in
@@ -314,6 +394,15 @@ cudaError_t launch_quantize_pairs(int8_t *qplane, float *dplane, __half *q16, fl
                           dst_row, q16, dxT, n_ld, tc_plan);
     return launch_pdl(k_quantize_pairs<false>, grid, 256, st, qplane, dplane, x, in_dim, n_pairs, k, x_per_pair,
                       dst_row, (__half *)nullptr, (float *)nullptr, (uint64_t)0, (const PlanHeader *)nullptr);
+}
+
+cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
+                                    uint64_t n_tok, float eps, int num_sms, cudaStream_t st) {
+    if (n_tok == 0) return cudaSuccess;
+    const uint64_t cap = (uint64_t)num_sms * 8;
+    const int grid = (int)(n_tok < cap ? n_tok : cap);
+    k_rmsnorm_quantize<<<grid, RMS_THREADS, 0, st>>>(xq, y, x, gamma, dim, n_tok, eps);
+    return cudaGetLastError();
 }
 
 }  // namespace q8
