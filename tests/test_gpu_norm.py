@@ -4,26 +4,16 @@ ABI, against the CPU oracle.
 * The quantised rows must be bit for bit the activation quantiser (q8_quantize_act,
   itself bit-exact to the oracle) applied to the kernel's own normalised rows y:
   the fused quantiser is the a1 quantiser.
-* y against the oracle's y (double, rounded once): the kernel's sum of squares has
-  relative error at most n_s 2^-24 with n_s = 8 ceil(dim/2048) + 14 (its fixed
-  reduction order); the mean, + eps, sqrt, reciprocal, two products and the
-  oracle's own rounding add at most 7 more roundings, and sqrt halves the sum's
-  error: ((n_s + 2) / 2 + 5) 2^-24 to first order; rho adds one more 2^-24 for the
-  second-order terms (plus 1e-37 near the subnormal range).  This holds while the
-  squares neither overflow nor underflow in fp32.
-* The oracle's quantised rows then differ only where that error can move a
-  decision: a quant by 1 where the oracle's |y/d| lies within a window of a
-  rounding tie, the binary16 scale by one step where the oracle's fp32 d lies
-  within 4 rho of a binary16 rounding midpoint.  The window is
-  max(1e-3, 3 (2 rho + 2^-22) 127), three times the largest movement of y/d.
+* y and the quantised rows against the oracle's: the rules of tests/allowances.py
+  (y within the relative bound of the kernel's fixed-order fp32 reduction; a quant
+  or a binary16 scale one step apart only where that error can move the decision).
 """
-import math
-
 import numpy as np
 import pytest
 
 import inputs
 import oracle
+from tests import allowances
 
 pytestmark = pytest.mark.gpu
 
@@ -52,55 +42,13 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def rho(dim):
-    n_s = 8 * math.ceil(dim / 2048) + 14
-    return ((n_s + 2) / 2 + 6) * 2.0 ** -24
-
-
-def split(xq, nb):
-    r = xq.reshape(xq.shape[0], nb, QB)
-    d = r[..., 0].astype(np.uint16) | (r[..., 1].astype(np.uint16) << 8)
-    q = r[..., 2:].copy().view(np.int8).astype(np.int32)
-    return d, q
-
-
-def f16_near_midpoint(d32, rel):
-    """True where the fp32 value lies within rel (relative) of a binary16 rounding midpoint."""
-    d = d32.astype(np.float64)
-    h = d32.astype(np.float16).astype(np.float64)
-    up = np.nextafter(d32.astype(np.float16), np.float16(np.inf)).astype(np.float64)
-    dn = np.nextafter(d32.astype(np.float16), np.float16(0)).astype(np.float64)
-    mids = np.stack([(h + up) / 2, (h + dn) / 2])
-    return np.any(np.abs(mids - d) <= rel * np.abs(d), axis=0)
-
-
 def check(q8, o, x, gamma, eps):
-    n_tok, dim = x.shape
-    nb = dim // QK
     xq, y = q8.rmsnorm_quantize(dev(x), None if gamma is None else dev(gamma), eps, want_y=True)
     assert q8.q8_last_error() == 0
     # the fused quantiser is the activation quantiser of the kernel's own y
     assert torch.equal(xq, q8.quantize_act(y))
     xq_o, y_o = o.rmsnorm_quantize(x, gamma, eps)
-    yg = y.cpu().numpy().astype(np.float64)
-    r = rho(dim)
-    err = np.abs(yg - y_o)
-    assert np.all(err <= r * np.abs(y_o) + 1e-37), f"y: worst relative {np.max(err / (np.abs(y_o) + 1e-30)):.3e}"
-    dg, qg = split(xq.cpu().numpy(), nb)
-    do, qo = split(xq_o, nb)
-    d32 = np.abs(y_o.reshape(n_tok, nb, QK)).max(-1).astype(np.float32) / np.float32(127.0)
-    near_mid = f16_near_midpoint(d32, 4 * r)
-    dgf = dg.view(np.float16).astype(np.float64)
-    dof = do.view(np.float16).astype(np.float64)
-    step = np.abs(np.nextafter(do.view(np.float16), np.float16(np.inf)).astype(np.float64) - dof)
-    assert np.all((dg == do) | (near_mid & (np.abs(dgf - dof) <= step))), "binary16 scale differs away from a midpoint"
-    window = max(1e-3, 3 * (2 * r + 2.0 ** -22) * 127)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        quo = np.abs(y_o.reshape(n_tok, nb, QK) / d32[..., None].astype(np.float64))
-    near_tie = np.abs(quo - np.floor(quo) - 0.5) < window
-    diff = qg != qo
-    assert np.all(np.abs(qg - qo) <= 1)
-    assert np.all(~diff | near_tie), f"{np.sum(diff & ~near_tie)} quants differ away from a tie"
+    allowances.check_rmsnorm(xq.cpu().numpy(), y.cpu().numpy(), xq_o, y_o)
     return xq, y
 
 
