@@ -475,7 +475,7 @@ int *device_error_word() {
 
 extern "C" {
 
-int q8_version(void) { return 10000; }
+int q8_version(void) { return 10100; }
 
 const char *q8_strerror(int status) {
     switch (status) {
