@@ -134,7 +134,7 @@ void q8o_quantize_block(uint8_t *out, const float *x) {
     uint16_t dh = 0;
     if (d != 0.0f) {
         for (int i = 0; i < QK; ++i)
-            out[2 + i] = (uint8_t)(int8_t)roundf(x[i] / d);
+            out[2 + i] = (uint8_t)(int8_t)(int)roundf(x[i] / d);   /* through int: defined at +-128 */
         dh = q8o_f32_to_f16(d);
     } else {
         for (int i = 0; i < QK; ++i) out[2 + i] = 0;

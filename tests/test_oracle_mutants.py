@@ -16,7 +16,7 @@ MUTANTS = [
     # quantiser
     ("reciprocal_multiply", "roundf(x[i] / d)", "roundf(x[i] * (1.0f / d))"),
     ("round_half_even", "roundf(x[i] / d)", "rintf(x[i] / d)"),
-    ("truncate", "(int8_t)roundf(x[i] / d)", "(int8_t)(x[i] / d)"),
+    ("truncate", "(int8_t)(int)roundf(x[i] / d)", "(int8_t)(int)(x[i] / d)"),
     ("scale_128", "amax / 127.0f", "amax / 128.0f"),
     ("signed_max", "float a = fabsf(x[i]);", "float a = x[i];"),
     ("store_f32_trunc", "dh = q8o_f32_to_f16(d);", "dh = (uint16_t)(q8o_f32_to_f16(d) & 0xfffeu);"),
