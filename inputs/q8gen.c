@@ -4,8 +4,10 @@
  * This module is shared by the test oracle and by the CUDA path's tests and
  * benchmark.  It holds none of the method's arithmetic: it only draws numbers.
  * Every value is a pure function of (seed, stream, element index), so any
- * slice can be produced independently and in parallel, with identical results
- * on x86_64 and aarch64.
+ * slice can be produced independently and in parallel.  The integer draws,
+ * weights and routing are identical on every platform; the N(0,1) values go
+ * through the C library's log1p, cos and sqrt and may differ in the last bit
+ * between C libraries (both sides of a comparison always use the same arrays).
  *
  * Random source: SplitMix64 (Steele, Lea and Flood, "Fast splittable
  * pseudorandom number generators", OOPSLA 2014), used in its counter form:
@@ -119,9 +121,15 @@ int q8g_route_uniform(int32_t *ids, uint64_t n_tok, uint32_t k,
                       uint32_t n_expert, uint64_t seed, uint64_t stream) {
     if (!ids || k == 0 || k > n_expert) return -1;
     const uint64_t key = stream_key(seed, stream);
+    int failed = 0;
     #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < (int64_t)n_tok; ++t) {
         int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * n_expert);
+        if (!perm) {
+            #pragma omp atomic write
+            failed = 1;
+            continue;
+        }
         for (uint32_t e = 0; e < n_expert; ++e) perm[e] = (int32_t)e;
         for (uint32_t j = 0; j < k; ++j) {
             uint64_t r = draw(key, (uint64_t)t * k + j);
@@ -132,7 +140,7 @@ int q8g_route_uniform(int32_t *ids, uint64_t n_tok, uint32_t k,
         }
         free(perm);
     }
-    return 0;
+    return failed ? -1 : 0;
 }
 
 /* k distinct experts per token, Zipf(s): P(rank r) proportional to r^-s,
@@ -142,10 +150,17 @@ int q8g_route_zipf(int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert,
     if (!ids || k == 0 || k > n_expert) return -1;
     const uint64_t key = stream_key(seed, stream);
     double *w0 = (double *)malloc(sizeof(double) * n_expert);
+    if (!w0) return -1;
     for (uint32_t r = 0; r < n_expert; ++r) w0[r] = pow((double)(r + 1), -s);
+    int failed = 0;
     #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < (int64_t)n_tok; ++t) {
         double *w = (double *)malloc(sizeof(double) * n_expert);
+        if (!w) {
+            #pragma omp atomic write
+            failed = 1;
+            continue;
+        }
         memcpy(w, w0, sizeof(double) * n_expert);
         for (uint32_t j = 0; j < k; ++j) {
             double total = 0.0;
@@ -165,5 +180,5 @@ int q8g_route_zipf(int32_t *ids, uint64_t n_tok, uint32_t k, uint32_t n_expert,
         free(w);
     }
     free(w0);
-    return 0;
+    return failed ? -1 : 0;
 }
