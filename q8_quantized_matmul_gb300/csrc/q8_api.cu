@@ -521,7 +521,7 @@ static int dispatch_matmul(DeviceState *s, float *out, const void *W, uint64_t i
     cudaError_t e = x ? q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st)
                       : q8::launch_unpack_blocks(qx, dx, static_cast<const uint8_t *>(xq), in_dim, n_pad, n_tok,
                                                  s->num_sms, st);
-    if (e != cudaSuccess) return Q8_ECUDA;
+    if (e != cudaSuccess) return status_of(e);
     return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st);
 }
 
@@ -750,8 +750,8 @@ int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_d
     int8_t *qx = cv.take<int8_t>(n_pad * in_dim);
     float *dx = cv.take<float>(n_pad * (in_dim / q8::QK) * sizeof(float));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st) != cudaSuccess)
-        return Q8_ECUDA;
+    if ((rc = status_of(q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st))))
+        return rc;
     return status_of(timed_launch(st, [&] {
         return q8::launch_matmul_packed(out, static_cast<const uint8_t *>(Wp), in_dim, out_dim, qx, dx, n_tok,
                                         s->num_sms, st);
@@ -763,15 +763,16 @@ int q8_last_error(void *stream) {
     DeviceState *s;
     int rc = get_device(&s);
     if (rc) return rc;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        return Q8_ECUDA;
+        return status_of(e);
     }
     int v = 0, zero = 0;
-    if (cudaMemcpy(&v, s->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(s->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    if ((e = cudaMemcpy(&v, s->err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(s->err, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
         cudaGetLastError();
-        return Q8_ECUDA;
+        return status_of(e);
     }
     return v;
 }
