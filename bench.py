@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "prefill_long", "moe",
-                                               "moe_zipf", "moe_zipf_small", "moe_ffn"),
+                                               "moe_zipf", "moe_zipf_small", "moe_ffn", "rmsnorm"),
                     help="run one workload's call a few times without timing (for ncu captures)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -652,6 +652,10 @@ def profile_case(case: str):
         W = torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=2)).to(dev)
         x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
         fn = lambda: q8.moe_matmul(W, 256, 2048 * 128 * QB, ids, x, False, 2048)
+    elif case == "rmsnorm":   # RMSNorm feeding the quantiser at the long-prefill input, 4096 x 4096
+        x = torch.from_numpy(inputs.normal((4096, 4096), seed=6)).to(dev)
+        gamma = torch.from_numpy((1.0 + 0.1 * np.random.default_rng(6).standard_normal(4096)).astype(np.float32)).to(dev)
+        fn = lambda: q8.rmsnorm_quantize(x, gamma, 1e-6)
     elif case == "moe_ffn":   # the routed expert FFN at the decode size (256 experts, 64 tokens, top-6)
         ids = torch.from_numpy(inputs.route_uniform(64, 6, 256, seed=0)).to(dev)
         Wg, Wu = (torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=s)).to(dev) for s in (2, 4))
