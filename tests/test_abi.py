@@ -98,3 +98,71 @@ def test_no_gpu_means_error_not_crash(q8):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert q8.lib.q8_matmul(A, B, 64, 8, A, 1, None) == q8.Q8_ECUDA
+
+
+def _no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+def test_matmul_host_argument_checks(q8):
+    L = q8.lib
+    assert L.q8_matmul_host(A, B, 64, 8, 0, 1, None) == q8.Q8_EINVAL        # no host x
+    assert L.q8_matmul_host(0, B, 64, 8, A, 1, None) == q8.Q8_EINVAL        # no host out
+    assert L.q8_matmul_host(A, B + 8, 64, 8, A, 1, None) == q8.Q8_EALIGN    # device W misaligned
+    assert L.q8_matmul_host(A, B, 48, 8, A, 1, None) == q8.Q8_EINVAL
+    assert L.q8_matmul_host(A, B, 64, 8, A, 0, None) == q8.Q8_OK
+    if _no_gpu():   # host buffers need no alignment: these pass validation and reach the device check
+        assert L.q8_matmul_host(A + 4, B, 64, 8, A + 3, 1, None) == q8.Q8_ECUDA
+
+
+def test_moe_ffn_argument_checks(q8):
+    L = q8.lib
+    gu, ds = 32 * 2 * 34, 16 * 1 * 34 + 8   # gate/up: mid 32 rows x 2 blocks; down: 16 rows x 1 block (+8)
+    ds16 = ds + 8
+
+    def call(**kw):
+        a = dict(out=A, Wg=B, Wu=B, Wd=B, n_exp=4, gu=gu, ds=ds16, ids=A, w=A, k=2, in_dim=64, mid=32, out_dim=16,
+                 limit=10.0, x=A, n_tok=3)
+        a.update(kw)
+        return L.q8_moe_ffn(a["out"], a["Wg"], a["Wu"], a["Wd"], a["n_exp"], a["gu"], a["ds"], a["ids"], a["w"],
+                            a["k"], a["in_dim"], a["mid"], a["out_dim"], a["limit"], a["x"], a["n_tok"], None)
+    assert call(limit=float("nan")) == q8.Q8_EINVAL
+    assert call(limit=-1.0) == q8.Q8_EINVAL
+    assert call(mid=48) == q8.Q8_EINVAL                 # mid_dim % 32
+    assert call(k=5) == q8.Q8_EINVAL                    # k > n_expert
+    assert call(gu=gu - 16) == q8.Q8_EINVAL             # gate/up stride shorter than a matrix
+    assert call(ds=16 * 34 - 16) == q8.Q8_EINVAL        # down stride shorter than a matrix
+    assert call(ds=ds) == q8.Q8_EALIGN                  # down stride not a multiple of 16
+    assert call(ids=A + 2) == q8.Q8_EALIGN
+    assert call(w=A + 2) == q8.Q8_EALIGN
+    assert call(x=A + 4) == q8.Q8_EALIGN
+    assert call(w=0) == q8.Q8_EINVAL
+    assert call(n_tok=0) == q8.Q8_OK
+    if _no_gpu():
+        assert call() == q8.Q8_ECUDA
+
+
+def test_elementwise_and_norm_argument_checks(q8):
+    L = q8.lib
+    assert L.q8_swiglu(A, A, A, 8, float("nan"), None) == q8.Q8_EINVAL
+    assert L.q8_swiglu(A, A, A, 8, -0.5, None) == q8.Q8_EINVAL
+    assert L.q8_swiglu(A, A, A, 0, 1.0, None) == q8.Q8_OK
+    assert L.q8_swiglu(0, A, A, 8, 1.0, None) == q8.Q8_EINVAL
+    assert L.q8_swiglu(A, A + 4, A, 8, 1.0, None) == q8.Q8_EALIGN
+    assert L.q8_moe_combine(A, A, A, 2, 0, 8, None) == q8.Q8_EINVAL        # k = 0
+    assert L.q8_moe_combine(A, A, A, 0, 2, 8, None) == q8.Q8_OK
+    assert L.q8_moe_combine(A, 0, A, 2, 2, 8, None) == q8.Q8_EINVAL
+    assert L.q8_moe_combine(A + 4, A, A, 2, 2, 8, None) == q8.Q8_EALIGN
+    assert L.q8_moe_combine(A, A, A + 2, 2, 2, 8, None) == q8.Q8_EALIGN
+    for eps in (0.0, -1.0, float("nan"), float("inf")):
+        assert L.q8_rmsnorm_quantize(A, 0, B, 0, 64, 2, eps, None) == q8.Q8_EINVAL
+    assert L.q8_rmsnorm_quantize(A, 0, B, 0, 48, 2, 1e-6, None) == q8.Q8_EINVAL
+    assert L.q8_rmsnorm_quantize(0, 0, B, 0, 64, 2, 1e-6, None) == q8.Q8_EINVAL
+    assert L.q8_rmsnorm_quantize(A, A + 4, B, 0, 64, 2, 1e-6, None) == q8.Q8_EALIGN   # y misaligned
+    assert L.q8_rmsnorm_quantize(A, 0, B, B + 8, 64, 2, 1e-6, None) == q8.Q8_EALIGN   # gamma misaligned
+    assert L.q8_rmsnorm_quantize(A, 0, B, 0, 64, 0, 1e-6, None) == q8.Q8_OK
+    if _no_gpu():
+        assert L.q8_swiglu(A, A, A, 8, 1.0, None) == q8.Q8_ECUDA
+        assert L.q8_moe_combine(A, A, A, 2, 2, 8, None) == q8.Q8_ECUDA
+        assert L.q8_rmsnorm_quantize(A, 0, B, 0, 64, 2, 1e-6, None) == q8.Q8_ECUDA
