@@ -124,6 +124,11 @@ SHAPES = [
     (16384, 96, 20),
     # in_dim % 256 != 0: rows not 16-byte aligned (slow path)
     (32, 5, 1), (96, 19, 7), (160, 50, 20), (4000, 8, 2),
+    # single and seven output rows (fewer rows than any tile or TMA box): the GEMV in
+    # each mode, the tcgen05 GEMM on raw and on expanded weights
+    (256, 1, 1), (1024, 7, 4), (4096, 1, 16), (512, 7, 100), (256, 1, 33), (2048, 1, 700), (1024, 7, 20),
+    # in_dim 64 (two blocks a row): the slow path, and the tcgen05 GEMM with one K stage
+    (64, 7, 1), (64, 1, 16), (64, 1, 20), (64, 130, 40), (64, 7, 300),
 ]
 
 
@@ -362,6 +367,37 @@ def test_config5_zipf_moe_sampled(q8, o):
     assert flag == 0
     assert_close(got[pair, row], ref, bound, "config 5 moe")
     assert not np.any(np.isnan(got)), "some routed output row was never written"
+
+
+def test_config5_zipf_moe_down_sampled(q8, o):
+    """The long-prefill slice's routed down projection at its real size: one input row per
+    pair (24576 pairs, Zipf(1.1) top-6 over 256 experts of 4096 x 2048), on the grouped
+    tcgen05 GEMM and the GEMV classes.  Random outputs plus whole rows of the hottest
+    expert's last pair and the coldest experts' first pairs are checked."""
+    n_exp, n_tok, k, in_dim, out_dim = 256, 4096, 6, 2048, 4096
+    ids = inputs.route_zipf(n_tok, k, n_exp, s=1.1, seed=0)
+    W = _moe_weights(n_exp, out_dim, in_dim, seed=4)
+    stride = out_dim * (in_dim // QK) * QB
+    x = inputs.normal((n_tok * k, in_dim), seed=5)
+    buf, n = gpu_moe(q8, dev(W), n_exp, stride, ids, x, 1, out_dim)
+    assert q8.q8_last_error() == 0
+    got = fetch(buf, n, (n_tok * k, out_dim))
+    assert not np.any(np.isnan(got)), "some routed output row was never written"
+    flat = ids.reshape(-1)
+    counts = np.bincount(flat, minlength=n_exp)
+    assert counts.max() > 1000 and counts[counts > 0].min() <= 16   # tensor-core and GEMV classes
+    hot_pair = int(np.flatnonzero(flat == int(np.argmax(counts)))[-1])
+    cold = np.flatnonzero(counts == counts[counts > 0].min())
+    cold_pairs = [int(np.flatnonzero(flat == e)[0]) for e in cold[:2]]
+    mid_e = int(np.flatnonzero((counts > 16) & (counts < 128))[0])           # a short tensor-core group
+    mid_pair = int(np.flatnonzero(flat == mid_e)[-1])
+    whole = [hot_pair, mid_pair] + cold_pairs
+    g = np.random.default_rng(6)
+    pair = np.concatenate([g.integers(0, n_tok * k, 4000), np.repeat(whole, out_dim)])
+    row = np.concatenate([g.integers(0, out_dim, 4000), np.tile(np.arange(out_dim), len(whole))])
+    ref, bound, flag = o.moe_sample(W, n_exp, stride, ids, in_dim, out_dim, o.quantize(x), 1, n_tok, pair, row)
+    assert flag == 0
+    assert_close(got[pair, row], ref, bound, "config 5 routed down")
 
 
 def _ids_with_counts(counts, k, seed):
