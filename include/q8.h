@@ -238,11 +238,21 @@ int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_d
  * that cannot afford the device-wide synchronisation and milliseconds that a
  * first-use cudaMalloc/cudaFree can cost.
  *
- * Same arguments, layouts, results and error codes as q8_matmul (the same
- * kernels run), but the quantised activations live in one fixed array of
+ * Same arguments, layouts and error codes as q8_matmul, and the same
+ * quantised activations (bit for bit), but those live in one fixed array of
  * Q8_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
- * library holds that array until the process exits.  The call needs
- * align256(n_pad*in_dim) + align256(n_pad*(in_dim/32)*4) bytes of it, with
+ * library holds that array until the process exits.  The kernels differ from
+ * q8_matmul's: the quantiser always writes activation planes into the array;
+ * up to 16 tokens on 16-byte-aligned rows (in_dim % 256 == 0) the
+ * weight-streaming GEMV reads them; above 16 tokens an mma.sync int8 kernel
+ * does (q8_matmul runs its tcgen05 GEMM there, whose fp16 operands would not
+ * fit the array), so such calls are several times slower than q8_matmul's;
+ * unaligned rows take the same plain kernel as q8_matmul.  The outputs
+ * therefore agree with q8_matmul's within the matmul tolerance
+ * (|diff| <= 1e-4 * sum_b |d_w d_x isum_b| + 1e-6 against the exact sum),
+ * not bit for bit: the kernels add the blocks in different fp32 orders.
+ * The call needs align256(n_pad*in_dim) + align256(n_pad*(in_dim/32)*4) bytes
+ * of the array, with
  * n_pad = n_tok rounded up to a multiple of 16 (for example n_tok <= 16 with
  * in_dim <= 200000, or n_tok = 512 with in_dim <= 7168); larger calls return
  * Q8_ESCRATCH and enqueue nothing.  It never calls cudaMalloc, cudaFree or any
@@ -300,6 +310,20 @@ int q8_profile_read(uint32_t i, float *ms);
  * without exhausting a shared GPU.
  */
 void q8_debug_fail_next_alloc(int count);
+
+/*
+ * Test hook for the bounded waits inside the kernels (the pages give their
+ * tensor-parallel poll gates a time budget and fail instead of hanging: GPU
+ * concepts page, §4, distributed inference).  The next `count` dense matmul
+ * kernels (the weight-streaming GEMV and the tcgen05 GEMM that q8_matmul,
+ * q8_matmul_q and q8_matmul_host launch) run with every wait limited to
+ * limit_ns nanoseconds (0: the normal 2 s) and with their producer issuing no
+ * copy at all, so the consumers wait on buffers that never fill.  Each such
+ * kernel then raises Q8_ETIMEOUT for q8_last_error(), stops waiting, lets any
+ * copy still in flight land and returns; its outputs are undefined.  Nothing
+ * traps and the context stays usable.  count 0 disarms the hook.
+ */
+void q8_debug_expire_waits(int count, uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

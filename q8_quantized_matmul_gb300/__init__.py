@@ -27,7 +27,7 @@ EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matm
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
            "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host", "q8_moe_ffn", "q8_swiglu",
-           "q8_moe_combine", "q8_rmsnorm_quantize")
+           "q8_moe_combine", "q8_rmsnorm_quantize", "q8_debug_expire_waits")
 
 
 class Q8Error(RuntimeError):
@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "q8_scratch_bytes": ([], u64),
         "q8_release": ([], None),
         "q8_debug_fail_next_alloc": ([i32], None),
+        "q8_debug_expire_waits": ([i32, u64], None),
         "q8_profile_arm": ([u32], i32),
         "q8_profile_used": ([], u64),
         "q8_profile_read": ([u32, ctypes.POINTER(ctypes.c_float)], i32),
@@ -186,6 +187,10 @@ def q8_release() -> None:
 
 def q8_debug_fail_next_alloc(count: int) -> None:
     _get().q8_debug_fail_next_alloc(count)
+
+
+def q8_debug_expire_waits(count: int, limit_ns: int) -> None:
+    _get().q8_debug_expire_waits(count, limit_ns)
 
 
 def q8_profile_arm(n_pairs: int) -> int:

@@ -29,6 +29,19 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_dev[MAX_DEVICES];
 int g_fail_next_alloc = 0;
+int g_expire_next = 0;            // q8_debug_expire_waits: dense kernels still to withhold their copies
+uint64_t g_expire_limit_ns = 0;   // ... and their wait limit
+
+// The failure-detection test hook, consumed by one dense GEMV or GEMM launch.
+void take_expiry(uint64_t &wait_ns, int &withhold) {
+    wait_ns = 0;
+    withhold = 0;
+    if (g_expire_next > 0) {
+        --g_expire_next;
+        wait_ns = g_expire_limit_ns;
+        withhold = 1;
+    }
+}
 
 // Kernel timing hook: event pairs recorded around the main matmul kernel.
 struct Profile {
@@ -193,6 +206,7 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)s->num_sms ? g.n_items : (uint32_t)s->num_sms);
         g.weights_early = x_fused ? 0 : 1;   // planes: the preceding kernel is the quantiser
+        take_expiry(g.wait_ns, g.withhold);
         return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st); }));
     }
     q8::MmaParams p{};
@@ -289,6 +303,7 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     p.out = out;
     p.partial = partial;
     p.err = s->err;
+    take_expiry(p.wait_ns, p.withhold);
     const uint64_t units = tiles * ksplit;
     const int grid = (int)(units < (uint64_t)s->num_sms ? units : (uint64_t)s->num_sms);
     if (raw)
@@ -470,6 +485,13 @@ int *device_error_word() {
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     return get_device(&s) ? nullptr : s->err;
+}
+
+// Status of a CUDA runtime result for entry points defined in other files: a
+// failure is recorded for q8_last_cuda_error() and becomes Q8_ECUDA.
+int record_cuda_status(cudaError_t e) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    return status_of(e);
 }
 }  // namespace q8
 
@@ -856,6 +878,12 @@ const char *q8_last_cuda_error(void) {
 void q8_debug_fail_next_alloc(int count) {
     std::lock_guard<std::mutex> lk(g_mutex);
     g_fail_next_alloc = count > 0 ? count : 0;
+}
+
+void q8_debug_expire_waits(int count, uint64_t limit_ns) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    g_expire_next = count > 0 ? count : 0;
+    g_expire_limit_ns = limit_ns;
 }
 
 }  // extern "C"

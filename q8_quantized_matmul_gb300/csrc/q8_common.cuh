@@ -22,8 +22,12 @@ constexpr int QB = 34;          // bytes per Q8_0 block
 constexpr int DEV_ERANGE = -3;
 constexpr int DEV_ETIMEOUT = -6;
 
-// ~2 s at 1 ns per %globaltimer tick: far beyond any legitimate wait.
+// ~2 s at 1 ns per %globaltimer tick: far beyond any legitimate wait.  Kernels
+// take their limit as a parameter (0 = this default); the drains of copies in
+// flight after an abort always use this default.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+__host__ __device__ __forceinline__ uint64_t wait_limit(uint64_t ns) { return ns ? ns : WAIT_LIMIT_NS; }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -71,16 +75,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and raises Q8_ETIMEOUT) when the limit expires; once `*abort` is set
-// (a CTA-wide flag in shared memory) it returns false at once.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort) {
+// false (and raises Q8_ETIMEOUT) when limit_ns expires; once `*abort` is set
+// (a CTA-wide flag in shared memory) it returns false within 256 retries.
+// A caller whose wait failed must not release the buffer it guards: the copy
+// may still be in flight, and only the producer's drain may wait for it.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u) {
             if (abort && *abort) return false;
-            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 raise_error(err, DEV_ETIMEOUT);
                 if (abort) *abort = 1;
                 return false;

@@ -223,14 +223,15 @@ __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it)
 }
 
 // Bounded wait until the producer has armed round r of a slot.
-__device__ __forceinline__ bool wait_armed(volatile uint32_t *armed, uint32_t r, int *err, volatile int *abort) {
+__device__ __forceinline__ bool wait_armed(volatile uint32_t *armed, uint32_t r, int *err, volatile int *abort,
+                                           uint64_t limit_ns) {
     if (*armed == r) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (*armed == r) return true;
         if ((it & 63u) == 0u) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 raise_error(err, DEV_ETIMEOUT);
                 *abort = 1;
                 return false;
@@ -258,11 +259,14 @@ __device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
 // slots and copies land out of order, so a warp may come to round r + 1 of a
 // slot while round r has not landed; its parity wait would then see the
 // previous phase as complete.  Waiting for armed[slot] == r first rules that
-// out.  Returns the number of slots planned.
+// out.  After an abort (a timed-out wait anywhere in the CTA) no further copy
+// is issued, and consumers release only slots whose copy they saw land, so a
+// slot never has two copies in flight: the drain at the end waits for each
+// slot's last armed round only.  Returns the number of slots planned.
 template <int TOKG>
 __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorMap *tmap, uint8_t *ring, uint64_t *full,
                                             uint64_t *empty, volatile uint32_t *armed, volatile int *abort_flag,
-                                            int lane) {
+                                            int lane, uint64_t lim) {
     using namespace gv;
     const uint32_t nk = (p.nb + KC - 1) / KC;
     uint32_t seqbase = 0;
@@ -275,7 +279,8 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
             if (idx < total) {
                 const uint32_t seq = seqbase + idx, slot = seq % NSLOT;
                 const uint32_t kk = idx / nsub, sub = idx - kk * nsub;
-                if (mbar_wait(&empty[slot], ((seq / NSLOT) & 1u) ^ 1u, p.err, abort_flag)) {
+                if (!p.withhold && mbar_wait(&empty[slot], ((seq / NSLOT) & 1u) ^ 1u, p.err, abort_flag, lim) &&
+                    !*abort_flag) {
                     mbar_arrive_expect_tx(&full[slot], SLOT);
                     tma_load_3d(ring + (size_t)slot * SLOT, tmap, (int)(kk * (KC * QB / 4)),
                                 (int)(it.r0 + sub * ROWS), it.expert, &full[slot]);
@@ -641,19 +646,23 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     }
     __syncthreads();
 
+    const uint64_t lim = wait_limit(p.wait_ns);
     if (warp == PRODUCER) {
         if (!p.weights_early) grid_dep_wait();
-        const uint32_t planned = produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane);
+        produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane, lim);
         // Every weight copy of this CTA is issued: a kernel launched behind this one
         // with programmatic serialisation may take the SMs freed from here on (its
         // reads of anything this grid writes wait in griddepcontrol.wait).
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // After a timed-out wait: let the copies still in flight land (with one
-        // overall time limit) before the CTA's shared memory goes away.
+        // overall time limit) before the CTA's shared memory goes away.  Each slot
+        // has at most one copy in flight, that of the last round armed on it.
         if (*abort_flag && lane == 0) {
             const uint64_t t_end = global_timer_ns() + WAIT_LIMIT_NS;
-            const uint32_t first = planned > (uint32_t)NSLOT ? planned - NSLOT : 0u;
-            for (uint32_t q = first; q < planned; ++q) mbar_drain(&full[q % NSLOT], (q / NSLOT) & 1u, t_end);
+            for (int s = 0; s < NSLOT; ++s) {
+                const uint32_t r = armed[s];
+                if (r != 0xffffffffu) mbar_drain(&full[s], r & 1u, t_end);
+            }
         }
         return;
     }
@@ -704,8 +713,8 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                     if (sub < nsub) {
                         const uint32_t seq = seqbase + kk * nsub + sub;
                         const uint32_t slot = seq % NSLOT;
-                        if (wait_armed(&armed[slot], seq / NSLOT, p.err, abort_flag))
-                            mbar_wait(&full[slot], (seq / NSLOT) & 1u, p.err, abort_flag);
+                        bool ok = wait_armed(&armed[slot], seq / NSLOT, p.err, abort_flag, lim);
+                        if (ok) ok = mbar_wait(&full[slot], (seq / NSLOT) & 1u, p.err, abort_flag, lim);
                         const uint8_t *sbase = ring + (size_t)slot * SLOT;
                         if (MODE == 0) {
                             float (&a8)[8] = *reinterpret_cast<float (*)[8]>(&accf[s2][0]);
@@ -714,7 +723,8 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                             slot_mma<NT>(sbase, act, dxs, bl0, lane, acc[s2]);
                         }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[slot]);
+                        // a slot whose copy did not land (timed out) is never handed back
+                        if (lane == 0 && ok) mbar_arrive(&empty[slot]);
                     }
                 }
             }

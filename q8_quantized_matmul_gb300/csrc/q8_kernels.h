@@ -109,6 +109,11 @@ struct GemvParams {
     const PlanHeader *plan;    // grouped: class plan; nullptr: dense
     const int32_t *row_to_out;
     uint32_t n_expert;         // grouped: number of expert matrices
+    // Failure-detection test hook (zero in normal calls): wait_ns limits every wait
+    // (0: the 2 s default); withhold != 0 makes the producer issue no copy, so the
+    // consumers' waits run out, the kernel raises Q8_ETIMEOUT and returns.
+    uint64_t wait_ns;
+    int withhold;
 };
 constexpr uint32_t GEMV_MAX_ROWS_PER_ITEM = 512;
 // Launched with programmatic stream serialisation; see GemvParams::weights_early.
@@ -178,6 +183,9 @@ struct TcParams {
     // ksplit and kb_per are unused (no K split).
     const PlanHeader *plan;
     const int32_t *row_to_out;
+    // Failure-detection test hook, as in GemvParams (zero in normal calls).
+    uint64_t wait_ns;
+    int withhold;
 };
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
                              int num_sms, cudaStream_t st);

@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(mma_cfg::NTHREADS, 1)
                 for (uint32_t kk = 0; kk < nchunks; ++kk) {
                     const uint32_t kcur = min(kc, nb - kk * kc);
                     const uint32_t cbytes = kcur * QB;
-                    const bool ok = mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag);
+                    // after an abort nothing more is issued (consumers release only
+                    // stages they saw land, so each stage has at most one fill in flight)
+                    const bool ok = mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag) && !*abort_flag;
                     if (ok) {
                         mbar_arrive_expect_tx(&full[stage], nr * cbytes);
                         uint8_t *dst = stages + (size_t)stage * stage_bytes;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(mma_cfg::NTHREADS, 1)
 
         for (uint32_t kk = 0; kk < nchunks; ++kk) {
             const uint32_t kcur = min(kc, nb - kk * kc);
-            mbar_wait(&full[stage], phase, p.err, abort_flag);
+            const bool staged = mbar_wait(&full[stage], phase, p.err, abort_flag);
             const uint8_t *st = stages + (size_t)stage * stage_bytes;
             const int nbw = (int)(kcur >> 3);   // this warp's blocks in the chunk
 
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(mma_cfg::NTHREADS, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (lane == 0 && staged) mbar_arrive(&empty[stage]);   // a timed-out stage is never handed back
             if (++stage == NSTAGE) {
                 stage = 0;
                 phase ^= 1u;

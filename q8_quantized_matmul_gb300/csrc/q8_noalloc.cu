@@ -2,8 +2,14 @@
 // device array, for callers that must not allocate device memory through this
 // library (an application whose own pool allocator owns the device's memory,
 // or a decode loop that cannot take the synchronisation and latency of a
-// first-use cudaMalloc).  The pages have no counterpart; the kernels are the
-// ones q8_matmul runs, only the place of the quantised activations differs.
+// first-use cudaMalloc).  The pages have no counterpart.  The quantiser
+// always writes activation planes into the fixed array; up to 16 tokens the
+// weight-streaming GEMV reads them (as q8_matmul does from 9 tokens on), above
+// that the mma.sync kernel of the odd block counts does (q8_matmul runs its
+// tcgen05 GEMM there, whose operands would not fit the array), and rows that
+// are not 16-byte aligned take the plain slow kernel, as in q8_matmul.  The
+// results agree with q8_matmul's within the matmul tolerance, not bit for bit:
+// the kernels add the blocks in different fp32 orders.
 #include <cstdint>
 #include <mutex>
 
@@ -12,7 +18,8 @@
 #include "q8_kernels.h"
 
 namespace q8 {
-int *device_error_word();   // q8_api.cu
+int *device_error_word();                 // q8_api.cu
+int record_cuda_status(cudaError_t e);    // q8_api.cu: Q8_OK, or Q8_ECUDA with the error recorded
 }
 
 namespace {
@@ -39,21 +46,22 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // Once per device, with the device current: the array's device address.
 int noalloc_device(NoallocDevice **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
         cudaGetLastError();
-        return Q8_ECUDA;
+        return q8::record_cuda_status(e != cudaSuccess ? e : cudaErrorInvalidDevice);
     }
     NoallocDevice &d = g_na[dev];
     if (!d.ready) {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess || !ptr) {
             cudaGetLastError();
-            return Q8_ECUDA;
+            return q8::record_cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
         }
         int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
             cudaGetLastError();
-            return Q8_ECUDA;
+            return q8::record_cuda_status(e);
         }
         d.scratch = static_cast<uint8_t *>(ptr);
         d.num_sms = sms;
@@ -93,10 +101,11 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int8_t *qx = reinterpret_cast<int8_t *>(d->scratch);
     float *dx = reinterpret_cast<float *>(d->scratch + q_bytes);
-    if (q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, d->num_sms, st) != cudaSuccess)
-        return Q8_ECUDA;
+    if ((rc = q8::record_cuda_status(
+             q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, d->num_sms, st))))
+        return rc;
 
-    // The same kernel choice as q8_matmul.
+    // Up to 16 tokens on 16-byte-aligned rows: the weight-streaming GEMV from planes.
     if (nb % 8 == 0 && n_tok <= 16) {
         q8::GemvParams g{};
         g.W = static_cast<const uint8_t *>(W);
@@ -108,13 +117,14 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
         g.out = out;
         g.err = err;
         g.n_tok = (uint32_t)n_tok;
-            g.n_items = q8::gemv_dense_items(out_dim, d->num_sms);
+        g.n_items = q8::gemv_dense_items(out_dim, d->num_sms);
         q8::gemv_dense_split(out_dim, g.n_items, g.sub_base, g.sub_rem);
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)d->num_sms ? g.n_items : (uint32_t)d->num_sms);
         g.weights_early = 1;   // the preceding kernel is the quantiser
-        return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+        return q8::record_cuda_status(q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st));
     }
+    // More tokens: the mma.sync kernel on aligned rows, else the plain kernel.
     q8::MmaParams p{};
     p.W = static_cast<const uint8_t *>(W);
     p.in_dim = in_dim;
@@ -128,8 +138,8 @@ extern "C" int q8_matmul_noalloc(float *out, const void *W, uint64_t in_dim, uin
     if (nb % 8 == 0) {
         const uint64_t items = ((out_dim + 15) / 16) * ((n_tok + 63) / 64);
         const int grid = (int)(items < (uint64_t)d->num_sms ? items : (uint64_t)d->num_sms);
-        return q8::launch_mma(p, grid, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+        return q8::record_cuda_status(q8::launch_mma(p, grid, st));
     }
     const uint64_t hint = n_tok * out_dim > (1u << 30) ? (1u << 30) : n_tok * out_dim;
-    return q8::launch_generic(p, (int)hint, d->num_sms, st) == cudaSuccess ? Q8_OK : Q8_ECUDA;
+    return q8::record_cuda_status(q8::launch_generic(p, (int)hint, d->num_sms, st));
 }

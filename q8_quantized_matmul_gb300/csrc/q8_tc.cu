@@ -285,6 +285,7 @@ struct TcEpi {
     uint8_t *smem;
     uint64_t *full, *empty, *tfull, *tempty;
     volatile int *abort_flag;
+    uint64_t lim;         // wait limit (ns)
     uint32_t lane_addr;   // TMEM address of this warp's lane quarter
     int m, h, lane;       // tile row, column half, lane
     uint32_t stage, phase, blk;
@@ -302,12 +303,12 @@ __device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit
     for (int kb = w.kb0; kb < w.kb1; kb += 2) {
         const uint8_t *st = e.smem + (size_t)e.stage * STAGE_BYTES;
         // the scales arrive with the stage (the MMA warp waited on the same barrier)
-        mbar_wait(&e.full[e.stage], e.phase, p.err, e.abort_flag);
+        const bool staged = mbar_wait(&e.full[e.stage], e.phase, p.err, e.abort_flag, e.lim);
         const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
         const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
         for (int j = 0; j < 2; ++j, ++e.blk) {
             const uint32_t slot = e.blk % NSLOT_T;
-            mbar_wait(&e.tfull[slot], (e.blk / NSLOT_T) & 1u, p.err, e.abort_flag);
+            mbar_wait(&e.tfull[slot], (e.blk / NSLOT_T) & 1u, p.err, e.abort_flag, e.lim);
             tc_fence_after();
             const uint64_t ww = tc_pair(dws[j * BM + e.m]);
             const float *dxj = dxs + j * BN + e.h * NCW;
@@ -331,7 +332,8 @@ __device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit
             if (e.lane == 0) mbar_arrive(&e.tempty[slot]);
         }
         __syncwarp();
-        if (e.lane == 0) mbar_arrive(&e.empty[e.stage]);
+        // a stage whose copies did not land (timed out) is never handed back
+        if (e.lane == 0 && staged) mbar_arrive(&e.empty[e.stage]);
         if (++e.stage == NSTAGE) {
             e.stage = 0;
             e.phase ^= 1u;
@@ -415,6 +417,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const uint64_t lim = wait_limit(p.wait_ns);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -432,7 +435,8 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
             for (int kb = w.kb0; kb < w.kb1; kb += 2) {
                 if constexpr (RAW) {
                     if ((kb - w.kb0) % RAW_KB == 0) {   // next raw copy: 8 blocks x 128 rows
-                        if (warp_all(mbar_wait(&raw_empty[rs], rph ^ 1u, p.err, abort_flag))) {
+                        if (warp_all(!p.withhold && mbar_wait(&raw_empty[rs], rph ^ 1u, p.err, abort_flag, lim) &&
+                                     !*abort_flag)) {
                             if (lane == 0) {
                                 mbar_arrive_expect_tx(&raw_full[rs], RAW_BYTES);
                                 tma_load_3d(raw_s + (size_t)rs * RAW_BYTES, &tmA, (kb / RAW_KB) * RAW_WORDS, m0,
@@ -447,7 +451,11 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                         }
                     }
                 }
-                if (warp_all(mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag))) {
+                // After an abort nothing more is issued; consumers release only
+                // stages and raw copies they saw land, so each has at most one copy
+                // in flight (its last fill), which the drain below waits for.
+                if (warp_all(!p.withhold && mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag, lim) &&
+                             !*abort_flag)) {
                     if (lane == 0) {
                         uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
                         float *dxs = reinterpret_cast<float *>(st + A_BYTES + B_BYTES);
@@ -481,7 +489,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
         }
         if (*abort_flag && lane == 0) {
             // let every copy this warp issued land before the CTA exits
-            const uint64_t t_end = global_timer_ns() + 1000000ull;
+            const uint64_t t_end = global_timer_ns() + WAIT_LIMIT_NS;
             for (int s = 0; s < NSTAGE; ++s)
                 if (fills[s]) mbar_drain(&full[s], (fills[s] - 1u) & 1u, t_end);
             for (int s = 0; s < NRAW; ++s)
@@ -507,26 +515,28 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                     }
                     continue;
                 }
-                mbar_wait(&full[stage], phase, p.err, abort_flag);
+                const bool staged = mbar_wait(&full[stage], phase, p.err, abort_flag, lim);
                 tc_fence_after();
                 const uint32_t a_s = smem_addr(smem + (size_t)stage * STAGE_BYTES);
                 const uint32_t b_s = a_s + A_BYTES;
                 for (int j = 0; j < 2; ++j, ++blk) {
                     const uint32_t slot = blk % NSLOT_T;
-                    mbar_wait(&tempty[slot], ((blk / NSLOT_T) & 1u) ^ 1u, p.err, abort_flag);
+                    const bool free_slot = mbar_wait(&tempty[slot], ((blk / NSLOT_T) & 1u) ^ 1u, p.err, abort_flag, lim);
                     tc_fence_after();
-                    if (lane == 0) {
+                    if (lane == 0 && staged && free_slot) {
                         const uint32_t d_tmem = tmem_base + slot * BN;
 #pragma unroll
                         for (int k16 = 0; k16 < 2; ++k16) {
                             const uint32_t koff = (uint32_t)(2 * j + k16) * 32u;   // 16 fp16 = 32 bytes
                             tc_mma_f16(d_tmem, sw128_desc(a_s + koff), sw128_desc(b_s + koff), idesc, k16);
                         }
-                        tc_commit(&tfull[slot]);
                     }
+                    if (lane == 0) tc_commit(&tfull[slot]);
                     __syncwarp();
                 }
-                if (lane == 0) tc_commit(&empty[stage]);
+                // the stage goes back to the producer once its MMAs are done, unless
+                // its copies never landed (timed out)
+                if (lane == 0 && staged) tc_commit(&empty[stage]);
                 __syncwarp();
                 if (++stage == NSTAGE) {
                     stage = 0;
@@ -536,14 +546,14 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
         }
         if (lane == 0) tc_commit(done);               // all MMAs issued by this thread
         __syncwarp();
-        mbar_wait(done, 0, p.err, nullptr);
+        mbar_wait(done, 0, p.err, nullptr);           // the fixed 2 s limit: TMEM is freed after this
     } else if (warp < 2 + NUM_EPI) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;                // column half
         const int m = q * 32 + lane;                  // row within the tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-        TcEpi e{smem, full, empty, tfull, tempty, abort_flag, lane_addr, m, h, lane, 0u, 0u, 0u};
+        TcEpi e{smem, full, empty, tfull, tempty, abort_flag, lim, lane_addr, m, h, lane, 0u, 0u, 0u};
         TcUnit w;
         int seg = 0;
         for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
@@ -559,11 +569,11 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
         int seg = 0;
         for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
             for (int kg = w.kb0; kg < w.kb1; kg += RAW_KB) {
-                const bool raw_ok = mbar_wait(&raw_full[rs], rph, p.err, abort_flag);
+                const bool raw_ok = mbar_wait(&raw_full[rs], rph, p.err, abort_flag, lim);
                 const uint8_t *raw = raw_s + (size_t)rs * RAW_BYTES;
 #pragma unroll
                 for (int J = 0; J < RAW_KB / 2; ++J) {
-                    const bool ok = mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag) && raw_ok;
+                    const bool ok = mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag, lim) && raw_ok;
                     if (ok) {
                         uint8_t *st = smem + (size_t)stage * STAGE_BYTES;
                         float *dws = reinterpret_cast<float *>(st + A_BYTES + B_BYTES + DX_BYTES);
