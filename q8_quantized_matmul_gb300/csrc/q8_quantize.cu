@@ -99,11 +99,11 @@ __global__ void __launch_bounds__(256) k_quantize_pairs(int8_t *__restrict__ qpl
                                                         const int32_t *__restrict__ dst_row,
                                                         __half *__restrict__ q16, float *__restrict__ dxT,
                                                         uint64_t n_ld, const PlanHeader *tc_plan) {
-    // The matmul that follows only prefetches weights before it waits for this
-    // grid to finish, so it may be scheduled now.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // launched with programmatic serialisation: nothing is read before the previous grid is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Only then may the matmul behind be scheduled: it reads the weights before its
+    // own griddepcontrol.wait, and a kernel before this one may have written them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t tc_rows = TC ? (uint64_t)tc_plan->row_end : 0;
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_pairs * nb;
@@ -175,10 +175,12 @@ __global__ void __launch_bounds__(256) k_unpack_blocks(int8_t *__restrict__ qpla
 __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
                                                        const float *__restrict__ x, uint64_t in_dim, uint64_t n_tok,
                                                        uint64_t n_ld) {
-    // The GEMM behind reads these planes only after its griddepcontrol.wait.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // launched with programmatic serialisation: nothing is read before the previous grid is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Only then may the GEMM behind be scheduled: it reads these planes after its
+    // griddepcontrol.wait, but the weights before it, and a kernel before this one
+    // may have written them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -206,10 +208,12 @@ __global__ void __launch_bounds__(256) k_quantize_f16t(__half *__restrict__ q16,
 __global__ void __launch_bounds__(256) k_unpack_f16t(__half *__restrict__ q16, float *__restrict__ dxT,
                                                      const uint8_t *__restrict__ xq, uint64_t in_dim, uint64_t n_tok,
                                                      uint64_t n_ld) {
-    // The GEMM behind reads these planes only after its griddepcontrol.wait.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // launched with programmatic serialisation: nothing is read before the previous grid is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Only then may the GEMM behind be scheduled: it reads these planes after its
+    // griddepcontrol.wait, but the weights before it, and a kernel before this one
+    // may have written them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_ld * nb;
     for (uint64_t blk = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;

@@ -153,7 +153,8 @@ def test_matmul_q_matches_matmul_bitwise(q8, o, in_dim, out_dim, n_tok):
 
 
 @pytest.mark.parametrize("n_tok,in_dim,out_dim", [(1, 256, 100), (2, 1024, 333), (3, 512, 64), (8, 1024, 1000),
-                                                   (8, 4096, 150), (5, 2048, 4100), (1, 16384, 40), (2, 8192, 77)])
+                                                   (8, 4096, 150), (5, 2048, 4100), (1, 16384, 40), (2, 8192, 77),
+                                                   (16, 1024, 300), (12, 2048, 77), (9, 512, 5000)])
 def test_fused_quantiser_matches_planes_bitwise(q8, n_tok, in_dim, out_dim):
     """Small dense calls quantise inside the GEMV; q8_matmul_q feeds the same GEMV
     from quantiser-kernel output.  Any difference in a quant or a scale (ties,
