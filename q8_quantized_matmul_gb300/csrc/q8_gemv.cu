@@ -451,7 +451,7 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
         for (int h = 0; h < RB; ++h) {
             const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
             const uint32_t t = pr / ka, b = pr - t * ka;
-            const QuantBlock qb = quantize8(xv[h]);   // all lanes: the block maximum is shuffled
+            const QuantBlock qb = quantize8_div(xv[h]);   // all lanes: the block maximum is shuffled
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

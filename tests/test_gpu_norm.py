@@ -52,7 +52,9 @@ def check(q8, o, x, gamma, eps):
     return xq, y
 
 
-@pytest.mark.parametrize("dim,n_tok", [(4096, 37), (1024, 5), (96, 3), (32, 7), (2080, 4), (6144, 9), (16384, 2)])
+@pytest.mark.parametrize("dim,n_tok", [(4096, 37), (1024, 5), (96, 3), (32, 7), (2080, 4), (6144, 9), (16384, 2),
+                                       # more rows than resident CTAs: each CTA loops, the next row in flight
+                                       (4096, 1000), (8192, 700), (2048, 2000)])
 @pytest.mark.parametrize("with_gamma", [True, False])
 def test_rmsnorm_quantize_parity(q8, o, dim, n_tok, with_gamma):
     x = inputs.normal((n_tok, dim), seed=dim + n_tok, p_out=0.01)
