@@ -126,15 +126,19 @@ int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
  *   out_host  out: fp32 [n_tok][out_dim], host memory.
  *   W         in:  device pointer, as for q8_matmul (16-byte aligned).
  *   x_host    in:  fp32 [n_tok][in_dim], host memory.
- * On `stream`, in order: x_host is copied into a library-owned device staging
- * buffer, the q8_matmul kernels run on it (same results, bit for bit), and the
- * result is copied to out_host.  Host buffers need no alignment.  With
- * page-locked host buffers the copies are asynchronous: x_host must stay
- * unchanged and out_host is valid only once `stream` has synchronised.  With
- * pageable host buffers the CUDA runtime stages the copies and the call may
- * block until they are done.  The staging buffer is grow-only, per device,
- * counted by q8_scratch_bytes and freed by q8_release; like the scratch, it
- * must not be used from two streams at once.
+ * When both buffers are page-locked (cudaHostAlloc, cudaMallocHost, or
+ * cudaHostRegister with mapping; pinned torch tensors) and 16-byte aligned,
+ * the q8_matmul kernels read x_host and write out_host directly through the
+ * GPU's host link (NVLink-C2C on Grace systems): one call is just the kernels.
+ * Otherwise, on `stream`, in order: x_host is copied into a library-owned
+ * device staging buffer, the kernels run on it, and the result is copied to
+ * out_host.  Either way the results are those of q8_matmul, bit for bit.
+ * Host buffers need no alignment.  The work is asynchronous: x_host must stay
+ * unchanged and out_host is valid only once `stream` has synchronised (with
+ * pageable buffers the CUDA runtime stages the copies and the call may block
+ * until they are done).  The staging buffer is grow-only, per device, counted
+ * by q8_scratch_bytes and freed by q8_release; like the scratch, it must not
+ * be used from two streams at once.
  */
 int q8_matmul_host(float *out_host, const void *W, uint64_t in_dim, uint64_t out_dim,
                    const float *x_host, uint64_t n_tok, void *stream);

@@ -526,6 +526,19 @@ int q8_quantize_act(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, v
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+// Device address of a page-locked host buffer (cudaHostAlloc, cudaMallocHost or
+// cudaHostRegister with mapping), 16-byte aligned, that the current device can
+// address; nullptr for pageable memory or anything else.
+static void *mapped_host_pointer(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned16(a.devicePointer)) return nullptr;
+    return a.devicePointer;
+}
+
 // The dense product with arguments already validated, under g_mutex.
 static int dispatch_matmul(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
                            const float *x, const void *xq, uint64_t n_tok, cudaStream_t st) {
@@ -592,12 +605,18 @@ int q8_matmul_host(float *out_host, const void *W, uint64_t in_dim, uint64_t out
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Page-locked host buffers are mapped into the device's address space and the
+    // GPU reaches them over its host link: the kernels then read x and write the
+    // result there directly, with no staging copies.
+    const float *xd_host = static_cast<const float *>(mapped_host_pointer(x_host));
+    float *od_host = static_cast<float *>(mapped_host_pointer(out_host));
+    if (xd_host && od_host) return dispatch_matmul(s, od_host, W, in_dim, out_dim, xd_host, nullptr, n_tok, st);
     const size_t x_bytes = n_tok * in_dim * sizeof(float), out_bytes = n_tok * out_dim * sizeof(float);
     if ((rc = reserve_buffer(&s->stage, &s->stage_bytes, align256(x_bytes) + align256(out_bytes)))) return rc;
     Carver cv(s->stage);
     float *xd = cv.take<float>(x_bytes);
     float *od = cv.take<float>(out_bytes);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = status_of(cudaMemcpyAsync(xd, x_host, x_bytes, cudaMemcpyHostToDevice, st)))) return rc;
     if ((rc = dispatch_matmul(s, od, W, in_dim, out_dim, xd, nullptr, n_tok, st))) return rc;
     return status_of(cudaMemcpyAsync(out_host, od, out_bytes, cudaMemcpyDeviceToHost, st));

@@ -84,6 +84,8 @@ constexpr int RING_BYTES = NSLOT * SLOT;
 constexpr int QT_BYTES = 20736;                  // fused quantiser: natural-order quants of a chunk
 constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + QT_BYTES + 2 * NSLOT * 8 + NSLOT * 4 + 16;
 constexpr int BAR_CONSUMERS = 1;                 // named barrier of the consumer warps
+constexpr int OUT_STRIDE = GEMV_MAX_ROWS_PER_ITEM;   // output staging: floats per token
+static_assert(16 * OUT_STRIDE * 4 <= ACT_BYTES, "output staging fits the activation buffer");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 static_assert(NSLOT >= 32, "one producer lane per slot of a batch");
 static_assert(SUBMAX * NCW * ROWS >= GEMV_MAX_ROWS_PER_ITEM, "rows per item");
@@ -760,7 +762,12 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                 }
             }
         }
-        // ---- outputs
+        // ---- outputs: gathered per token in shared memory (the activation buffer,
+        // free once every warp is past the compute and split-K steps), then
+        // written as contiguous runs with 16-byte stores -- few, full transactions,
+        // which matters most when the result lives in host memory
+        named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
+        float *obuf = reinterpret_cast<float *>(act);   // [token][row - r0], OUT_STRIDE floats a token
         if (MODE == 0) {
             // add the 8 block columns of each row (lanes differing in bits 0-2)
 #pragma unroll
@@ -779,16 +786,11 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                 for (int s2 = 0; s2 < SUBMAX; ++s2) {
                     const uint32_t sub = grp + (uint32_t)s2 * ngroups;
                     if (sub < nsub) {
-                        const uint32_t rs = it.r0 + sub * ROWS;
 #pragma unroll
                         for (int e = 0; e < NACC; ++e) {
                             const int tok = e >> 2;
-                            const uint32_t row = rs + (uint32_t)dp4a_row(rb, e & 3);
-                            if (tok < it.ntok && row < it.r0 + it.nrows) {
-                                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok]
-                                                            : (int64_t)(it.tok0 + tok);
-                                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + row] = accf[s2][e];
-                            }
+                            const uint32_t lr = sub * ROWS + (uint32_t)dp4a_row(rb, e & 3);
+                            if (tok < it.ntok && lr < it.nrows) obuf[tok * OUT_STRIDE + lr] = accf[s2][e];
                         }
                     }
                 }
@@ -799,21 +801,35 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             for (int s2 = 0; s2 < SUBMAX; ++s2) {
                 const uint32_t sub = grp + (uint32_t)s2 * ngroups;
                 if (sub < nsub) {
-                    const uint32_t rs = it.r0 + sub * ROWS;
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = t * 8 + 2 * c + (e & 1);
-                            const uint32_t row = rs + g + ((e & 2) ? 8 : 0);
-                            if (tok < it.ntok && row < it.r0 + it.nrows) {
-                                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok]
-                                                            : (int64_t)(it.tok0 + tok);
-                                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + row] = accf[s2][t * 4 + e];
-                            }
+                            const uint32_t lr = sub * ROWS + g + ((e & 2) ? 8 : 0);
+                            if (tok < it.ntok && lr < it.nrows) obuf[tok * OUT_STRIDE + lr] = accf[s2][t * 4 + e];
                         }
                     }
                 }
+            }
+        }
+        named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
+        if ((p.out_dim & 3u) == 0) {
+            // every run starts 16-byte aligned (out is, r0 is a multiple of 16, out_dim of 4)
+            // and is a whole number of float4 (nrows is a multiple of 4)
+            const uint32_t nv = it.nrows >> 2;
+            for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * nv; e += CONSUMER_THREADS) {
+                const uint32_t tok = e / nv, i = e - tok * nv;
+                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
+                if (orow >= 0)
+                    *reinterpret_cast<float4 *>(p.out + (uint64_t)orow * p.out_dim + it.r0 + 4 * i) =
+                        *reinterpret_cast<const float4 *>(obuf + tok * OUT_STRIDE + 4 * i);
+            }
+        } else {
+            for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * it.nrows; e += CONSUMER_THREADS) {
+                const uint32_t tok = e / it.nrows, i = e - tok * it.nrows;
+                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
+                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + it.r0 + i] = obuf[tok * OUT_STRIDE + i];
             }
         }
     }
