@@ -470,6 +470,29 @@ def secondary(args, torch, q8, dev, stream, l2):
                                  "(no int8 MMA instruction on sm_103a)"})
         del copies
 
+    # the same GEMM on weights repacked once into the tensor-core operand layout (no per-call
+    # expansion above 640 tokens); eager calls, each on its own copy of the packed weights
+    for in_dim, out_dim, n in ((32768, 1024, 512), (1024, 32768, 4096)):
+        W = inputs.weights(out_dim, in_dim, seed=1)
+        Wd = torch.from_numpy(W).to(dev)
+        pk = [q8.repack(Wd, in_dim, out_dim, q8.Q8_LAYOUT_TC)]
+        pk += [pk[0].clone() for _ in range(max(1, int(2 * l2 // pk[0].numel())))]
+        copies = [Wd] + [Wd.clone() for _ in range(max(1, int(2 * l2 // Wd.numel())))]
+        x = torch.from_numpy(inputs.normal((n, in_dim), seed=1)).to(dev)
+        o = torch.empty((n, out_dim), device=dev)
+        ms_raw = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim, x, n,
+                                                                    stream), 6)
+        ms_pk = timed_eager(torch, stream, lambda i: q8.q8_matmul_packed(o, pk[i % len(pk)], q8.Q8_LAYOUT_TC, in_dim,
+                                                                          out_dim, x, n, stream), 6)
+        ops = 2.0 * in_dim * out_dim * n
+        out.append({"workload": f"prefill in {in_dim} -> out {out_dim}, n_tok {n}: weights packed once in the "
+                                "tensor-core layout (q8_matmul_packed) against raw Q8_0 rows (q8_matmul)",
+                    "ms_per_call_packed": round(ms_pk, 4), "tops_packed": round(ops / (ms_pk * 1e-3) / 1e12, 2),
+                    "ms_per_call_raw": round(ms_raw, 4), "tops_raw": round(ops / (ms_raw * 1e-3) / 1e12, 2),
+                    "frac_of_bf16_peak_packed": round(ops / (ms_pk * 1e-3) / 1e12 / tflops, 4)})
+        del pk, copies, Wd
+    torch.cuda.empty_cache()
+
     # routed experts: gate/up (x per token) and down (x per pair), 256 experts, 64 tokens, uniform top-6
     n_exp, n_tok, k = 256, 64, 6
     ids = inputs.route_uniform(n_tok, k, n_exp, seed=0)

@@ -220,17 +220,31 @@ int q8_moe_combine(float *out, const float *y, const float *weights, uint64_t n_
                    uint64_t dim, void *stream);
 
 /*
- * Optional load-time repack of Q8_0 rows into split planes (a quant plane
- * of int8 [rows][in_dim] followed by a scale plane of fp16 [rows][in_dim/32]),
- * the layout the ROCm MXFP4 work on the pages found fastest (16-byte
- * aligned value slices with a separate scale array).  Bit-preserving.
- *   q8_repack_bytes: size of the packed buffer for rows x in_dim.
- *   q8_repack:       Wp (out, device, q8_repack_bytes bytes) <- W (in, raw rows).
- *   q8_matmul_packed: as q8_matmul, weights from a q8_repack buffer.
+ * Optional load-time repack of Q8_0 rows into a kernel-friendly layout (the
+ * ROCm MXFP4 work on the pages found 16-byte aligned value slices with a
+ * separate scale array fastest: GPU concepts page, §4c).  The repack copies or
+ * widens bits exactly; the products over a packed buffer are the q8_matmul
+ * products (same tolerance).
+ *   Q8_LAYOUT_PLANES: int8 quant plane [rows][in_dim], then the fp16 scale plane
+ *     [rows][in_dim/32]; the same 34 bytes per 32 weights.  Its matmul is a
+ *     plain mma.sync kernel (reference speed: the library's fast kernels read raw
+ *     Q8_0 rows in place, which TMA boxes make free of alignment costs).
+ *   Q8_LAYOUT_TC: the tcgen05 GEMM's weight operand: fp16 quants [m_ld][in_dim]
+ *     (exact integers), then fp32 scales block-major [in_dim/32][m_ld], m_ld =
+ *     rows rounded up to 128, padding rows zero; 2 bytes per weight plus 4 per
+ *     block.  Its matmul runs the tcgen05 GEMM on it directly for any n_tok,
+ *     skipping the weight expansion q8_matmul performs per call above 640
+ *     tokens.  in_dim must be a multiple of 64.
+ *   q8_repack_bytes: size of the packed buffer (0 for a bad layout or in_dim).
+ *   q8_repack:       Wp (out, device, q8_repack_bytes bytes, 16-byte aligned) <- W.
+ *   q8_matmul_packed: as q8_matmul, weights from a q8_repack buffer of `layout`.
+ * An unknown layout gives Q8_EINVAL.
  */
-uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows);
-int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, void *stream);
-int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_dim,
+#define Q8_LAYOUT_PLANES 0
+#define Q8_LAYOUT_TC 1
+uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows, int layout);
+int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, int layout, void *stream);
+int q8_matmul_packed(float *out, const void *Wp, int layout, uint64_t in_dim, uint64_t out_dim,
                      const float *x, uint64_t n_tok, void *stream);
 
 /*

@@ -21,6 +21,7 @@ QK = 32
 QB = 34
 Q8_OK, Q8_EINVAL, Q8_EALIGN, Q8_ERANGE, Q8_ENOMEM, Q8_ECUDA, Q8_ETIMEOUT, Q8_ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
+Q8_LAYOUT_PLANES, Q8_LAYOUT_TC = 0, 1
 
 # Every symbol include/q8.h declares.
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
@@ -56,9 +57,9 @@ def _load() -> ctypes.CDLL:
         "q8_swiglu": ([vp, vp, vp, u64, ctypes.c_float, vp], i32),
         "q8_rmsnorm_quantize": ([vp, vp, vp, vp, u64, u64, ctypes.c_float, vp], i32),
         "q8_moe_combine": ([vp, vp, vp, u64, u32, u64, vp], i32),
-        "q8_repack_bytes": ([u64, u64], u64),
-        "q8_repack": ([vp, vp, u64, u64, vp], i32),
-        "q8_matmul_packed": ([vp, vp, u64, u64, vp, u64, vp], i32),
+        "q8_repack_bytes": ([u64, u64, i32], u64),
+        "q8_repack": ([vp, vp, u64, u64, i32, vp], i32),
+        "q8_matmul_packed": ([vp, vp, i32, u64, u64, vp, u64, vp], i32),
         "q8_last_error": ([vp], i32),
         "q8_scratch_bytes": ([], u64),
         "q8_release": ([], None),
@@ -161,16 +162,16 @@ def q8_moe_combine(out, y, weights, n_tok: int, k: int, dim: int, stream=None) -
     return _get().q8_moe_combine(_p(out), _p(y), _p(weights), n_tok, k, dim, _s(stream))
 
 
-def q8_repack_bytes(in_dim: int, rows: int) -> int:
-    return _get().q8_repack_bytes(in_dim, rows)
+def q8_repack_bytes(in_dim: int, rows: int, layout: int = 0) -> int:
+    return _get().q8_repack_bytes(in_dim, rows, layout)
 
 
-def q8_repack(Wp, W, in_dim: int, rows: int, stream=None) -> int:
-    return _get().q8_repack(_p(Wp), _p(W), in_dim, rows, _s(stream))
+def q8_repack(Wp, W, in_dim: int, rows: int, layout: int = 0, stream=None) -> int:
+    return _get().q8_repack(_p(Wp), _p(W), in_dim, rows, layout, _s(stream))
 
 
-def q8_matmul_packed(out, Wp, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
-    return _get().q8_matmul_packed(_p(out), _p(Wp), in_dim, out_dim, _p(x), n_tok, _s(stream))
+def q8_matmul_packed(out, Wp, layout: int, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
+    return _get().q8_matmul_packed(_p(out), _p(Wp), layout, in_dim, out_dim, _p(x), n_tok, _s(stream))
 
 
 def q8_last_error(stream=None) -> int:
@@ -286,16 +287,19 @@ def rmsnorm_quantize(x, gamma, eps: float, want_y: bool = False):
     return (xq, y) if want_y else xq
 
 
-def repack(W, in_dim: int, rows: int):
+def repack(W, in_dim: int, rows: int, layout: int = 0):
     import torch
-    Wp = torch.empty(q8_repack_bytes(in_dim, rows), dtype=torch.uint8, device=W.device)
-    _check(q8_repack(Wp, W, in_dim, rows), "q8_repack")
+    nbytes = q8_repack_bytes(in_dim, rows, layout)
+    if nbytes == 0 and rows:
+        raise Q8Error(Q8_EINVAL, "q8_repack_bytes")
+    Wp = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check(q8_repack(Wp, W, in_dim, rows, layout), "q8_repack")
     return Wp
 
 
-def matmul_packed(Wp, x, out_dim: int):
+def matmul_packed(Wp, x, out_dim: int, layout: int = 0):
     import torch
     n_tok, in_dim = x.shape
     out = torch.empty((n_tok, out_dim), dtype=torch.float32, device=x.device)
-    _check(q8_matmul_packed(out, Wp, in_dim, out_dim, x, n_tok), "q8_matmul_packed")
+    _check(q8_matmul_packed(out, Wp, layout, in_dim, out_dim, x, n_tok), "q8_matmul_packed")
     return out

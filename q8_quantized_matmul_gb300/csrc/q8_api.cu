@@ -239,10 +239,14 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
 // to an fp16 plane with block-major scales (the in-kernel conversion costs
 // about 12 % of the GEMM, the expansion a fixed pass over the weights).
 constexpr uint64_t TC_RAW_MAX_TOKENS = 640;
+// a16_pre / dwT_pre: weights already in the GEMM's fp16 operand layout (a
+// Q8_LAYOUT_TC buffer; m_ld = out_dim rounded up to 128), used as they are.
 int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,
-           const void *xq, uint64_t n_tok, cudaStream_t st) {
+           const void *xq, uint64_t n_tok, cudaStream_t st, const __half *a16_pre = nullptr,
+           const float *dwT_pre = nullptr) {
     const uint64_t nb = in_dim / q8::QK;
-    const bool raw = nb % 8 == 0 && n_tok <= TC_RAW_MAX_TOKENS;   // raw Q8_0 rows, no fp16 plane
+    const bool packed = a16_pre != nullptr;
+    const bool raw = !packed && nb % 8 == 0 && n_tok <= TC_RAW_MAX_TOKENS;   // raw Q8_0 rows, no fp16 plane
     const uint64_t kb_align = raw ? 8 : 2;
     const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
     const uint64_t n_ld = (n_tok + 127) & ~(uint64_t)127;
@@ -272,20 +276,27 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
     uint64_t kb_per = (nb + ksplit - 1) / ksplit;
     kb_per = (kb_per + kb_align - 1) / kb_align * kb_align;
     ksplit = (nb + kb_per - 1) / kb_per;
-    const size_t need = (raw ? 0 : align256(out_dim * in_dim * 2) + align256(nb * m_ld * 4)) +
+    const bool expand = !raw && !packed;
+    const size_t need = (expand ? align256(out_dim * in_dim * 2) + align256(nb * m_ld * 4) : 0) +
                         align256(n_ld * in_dim * 2) + align256(nb * n_ld * 4) +
                         (ksplit > 1 ? align256(ksplit * n_tok * out_dim * 4) : 0);
     int rc = reserve_scratch(s, need);
     if (rc) return rc;
     Carver cv(s->scratch);
-    __half *a16 = raw ? nullptr : cv.take<__half>(out_dim * in_dim * 2);
-    float *dwT = raw ? nullptr : cv.take<float>(nb * m_ld * 4);
+    const __half *a16 = packed ? a16_pre : nullptr;
+    const float *dwT = packed ? dwT_pre : nullptr;
+    __half *a16_x = expand ? cv.take<__half>(out_dim * in_dim * 2) : nullptr;
+    float *dwT_x = expand ? cv.take<float>(nb * m_ld * 4) : nullptr;
     __half *b16 = cv.take<__half>(n_ld * in_dim * 2);
     float *dxT = cv.take<float>(nb * n_ld * 4);
     float *partial = ksplit > 1 ? cv.take<float>(ksplit * n_tok * out_dim * 4) : nullptr;
-    if (!raw && (rc = status_of(q8::launch_tc_expand(a16, dwT, static_cast<const uint8_t *>(W), (uint32_t)out_dim,
-                                                     (uint32_t)nb, (uint32_t)m_ld, s->num_sms, st))))
-        return rc;
+    if (expand) {
+        if ((rc = status_of(q8::launch_tc_expand(a16_x, dwT_x, static_cast<const uint8_t *>(W), (uint32_t)out_dim,
+                                                 (uint32_t)nb, (uint32_t)m_ld, s->num_sms, st))))
+            return rc;
+        a16 = a16_x;
+        dwT = dwT_x;
+    }
     cudaError_t e = x ? q8::launch_quantize_f16t(b16, dxT, x, in_dim, n_tok, n_ld, s->num_sms, st)
                       : q8::launch_unpack_f16t(b16, dxT, static_cast<const uint8_t *>(xq), in_dim, n_tok, n_ld,
                                                s->num_sms, st);
@@ -757,34 +768,60 @@ int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_d
     return status_of(q8::launch_combine(out, y, expert_weights, n_tok, k, out_dim, s->num_sms, st));
 }
 
-uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows) {
-    if (in_dim == 0 || in_dim % q8::QK) return 0;
-    return rows * in_dim + rows * (in_dim / q8::QK) * 2;
+uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows, int layout) {
+    if (in_dim == 0 || in_dim % q8::QK || check_dims(in_dim, rows, 1)) return 0;
+    const uint64_t nb = in_dim / q8::QK;
+    if (layout == Q8_LAYOUT_PLANES) return rows * in_dim + rows * nb * 2;
+    if (layout == Q8_LAYOUT_TC) {
+        if (in_dim % 64) return 0;   // the GEMM takes K in stages of two blocks
+        const uint64_t m_ld = (rows + 127) & ~(uint64_t)127;
+        return m_ld * in_dim * 2 + nb * m_ld * 4;
+    }
+    return 0;
 }
 
-int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, void *stream) {
+int q8_repack(void *Wp, const void *W, uint64_t in_dim, uint64_t rows, int layout, void *stream) {
     int rc = check_dims(in_dim, rows, 1);
     if (rc) return rc;
+    if (layout != Q8_LAYOUT_PLANES && layout != Q8_LAYOUT_TC) return Q8_EINVAL;
+    if (layout == Q8_LAYOUT_TC && in_dim % 64) return Q8_EINVAL;
     if (rows == 0) return Q8_OK;
     if (!Wp || !W) return Q8_EINVAL;
     if (!aligned16(Wp) || !aligned16(W)) return Q8_EALIGN;
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
-    return status_of(q8::launch_repack(static_cast<uint8_t *>(Wp), static_cast<const uint8_t *>(W), in_dim, rows,
-                                       s->num_sms, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (layout == Q8_LAYOUT_PLANES)
+        return status_of(q8::launch_repack(static_cast<uint8_t *>(Wp), static_cast<const uint8_t *>(W), in_dim, rows,
+                                           s->num_sms, st));
+    // the GEMM's operand: padding rows and their scales zero, then every real row widened
+    const uint64_t nb = in_dim / q8::QK, m_ld = (rows + 127) & ~(uint64_t)127;
+    if ((rc = status_of(cudaMemsetAsync(Wp, 0, q8_repack_bytes(in_dim, rows, layout), st)))) return rc;
+    uint8_t *base = static_cast<uint8_t *>(Wp);
+    return status_of(q8::launch_tc_expand(reinterpret_cast<__half *>(base), reinterpret_cast<float *>(base + m_ld * in_dim * 2),
+                                          static_cast<const uint8_t *>(W), (uint32_t)rows, (uint32_t)nb, (uint32_t)m_ld,
+                                          s->num_sms, st));
 }
 
-int q8_matmul_packed(float *out, const void *Wp, uint64_t in_dim, uint64_t out_dim, const float *x, uint64_t n_tok,
-                     void *stream) {
+int q8_matmul_packed(float *out, const void *Wp, int layout, uint64_t in_dim, uint64_t out_dim, const float *x,
+                     uint64_t n_tok, void *stream) {
     int rc = check_dims(in_dim, out_dim, n_tok);
     if (rc) return rc;
+    if (layout != Q8_LAYOUT_PLANES && layout != Q8_LAYOUT_TC) return Q8_EINVAL;
+    if (layout == Q8_LAYOUT_TC && in_dim % 64) return Q8_EINVAL;
     if (n_tok == 0 || out_dim == 0) return Q8_OK;
     if (!out || !Wp || !x) return Q8_EINVAL;
     if (!aligned16(out) || !aligned16(Wp) || !aligned16(x)) return Q8_EALIGN;
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
+    if (layout == Q8_LAYOUT_TC) {
+        const uint64_t m_ld = (out_dim + 127) & ~(uint64_t)127;
+        const uint8_t *base = static_cast<const uint8_t *>(Wp);
+        return run_tc(s, out, nullptr, in_dim, out_dim, x, nullptr, n_tok, static_cast<cudaStream_t>(stream),
+                      reinterpret_cast<const __half *>(base), reinterpret_cast<const float *>(base + m_ld * in_dim * 2));
+    }
     const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
     if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
     Carver cv(s->scratch);

@@ -43,9 +43,22 @@ def test_version_and_strerror(q8):
     assert q8.q8_strerror(12345) == "unknown status"
 
 
-def test_repack_bytes_is_the_same_footprint(q8):
-    assert q8.q8_repack_bytes(4096, 1024) == 1024 * 128 * 34
-    assert q8.q8_repack_bytes(33, 10) == 0
+def test_repack_bytes_per_layout(q8):
+    # split planes: the same 34 bytes per 32 weights
+    assert q8.q8_repack_bytes(4096, 1024, q8.Q8_LAYOUT_PLANES) == 1024 * 128 * 34
+    assert q8.q8_repack_bytes(33, 10, q8.Q8_LAYOUT_PLANES) == 0
+    # tensor-core operand: fp16 quants and fp32 block-major scales over rows rounded up to 128
+    assert q8.q8_repack_bytes(4096, 1000, q8.Q8_LAYOUT_TC) == 1024 * 4096 * 2 + 128 * 1024 * 4
+    assert q8.q8_repack_bytes(96, 10, q8.Q8_LAYOUT_TC) == 0          # in_dim not a multiple of 64
+    assert q8.q8_repack_bytes(4096, 1024, 2) == 0                     # unknown layout
+
+
+def test_repack_rejects_bad_layouts_before_any_launch(q8):
+    A = 0x10000
+    assert q8.lib.q8_repack(A, A, 4096, 16, 7, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_repack(A, A, 96, 16, q8.Q8_LAYOUT_TC, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_matmul_packed(A, A, 3, 4096, 16, A, 1, None) == q8.Q8_EINVAL
+    assert q8.lib.q8_matmul_packed(A, A, q8.Q8_LAYOUT_TC, 96, 16, A, 1, None) == q8.Q8_EINVAL
 
 
 # Host validation: fake (never dereferenced) addresses, returns before any CUDA call.

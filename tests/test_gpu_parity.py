@@ -508,6 +508,34 @@ def test_repack_layout_and_parity(q8, o):
     assert_close(got, ref, bound, "packed")
 
 
+@pytest.mark.parametrize("in_dim,out_dim", [(1024, 200), (2112, 130), (64, 7), (4096, 1024)])
+def test_repack_tensor_core_layout_and_parity(q8, o, in_dim, out_dim):
+    """The tcgen05 GEMM's weight operand built once: fp16 quants (exact integers) in [m_ld][in_dim] and
+    the binary16 scales as fp32 in [in_dim/32][m_ld], padding rows zero.  Its products match the oracle
+    for few and many tokens, and above 640 tokens are the bits of q8_matmul (which then expands the
+    weights into the same layout per call)."""
+    Wh = inputs.weights(out_dim, in_dim, seed=63)
+    W = dev(Wh)
+    Wp = q8.repack(W, in_dim, out_dim, q8.Q8_LAYOUT_TC)
+    nb, m_ld = in_dim // QK, (out_dim + 127) // 128 * 128
+    h = Wp.cpu().numpy()
+    q16 = h[:m_ld * in_dim * 2].view(np.float16).reshape(m_ld, nb, QK)
+    dT = h[m_ld * in_dim * 2:].view(np.float32).reshape(nb, m_ld)
+    blk = Wh.reshape(out_dim, nb, QB)
+    assert np.array_equal(q16[:out_dim].astype(np.int64), blk[..., 2:].view(np.int8).astype(np.int64))
+    assert np.array_equal(dT[:, :out_dim].T, blk[..., :2].copy().view(np.float16).reshape(out_dim, nb).astype(np.float32))
+    assert not np.any(q16[out_dim:]) and not np.any(dT[:, out_dim:])
+    for n_tok in (1, 16, 40, 700):
+        xh = inputs.normal((n_tok, in_dim), seed=64 + n_tok, p_out=0.01)
+        x = dev(xh)
+        got = q8.matmul_packed(Wp, x, out_dim, q8.Q8_LAYOUT_TC)
+        if n_tok <= 40:
+            ref, bound = o.matmul(Wh, xh, out_dim)
+            assert_close(got.cpu().numpy(), ref, bound, f"tc-packed {in_dim}x{out_dim}x{n_tok}")
+        else:
+            assert torch.equal(got, q8.matmul(W, x, out_dim))
+
+
 # ------------------------------------------------------------------ host-buffer entry point
 def _host_call(q8, W, xh, out_dim, pinned):
     n_tok, in_dim = xh.shape
