@@ -449,16 +449,17 @@ def secondary(args, torch, q8, dev, stream, l2):
     assert q8.q8_last_error(stream) == 0
     del xcopies, cg
 
-    # prefill GEMMs (attn_output_a and shared-expert shapes) at n_tok = 512
+    # prefill GEMMs (attn_output_a and shared-expert shapes) at n_tok = 512; every call reads its own
+    # copy of the weights and of the activations (each set of copies larger than L2)
     for in_dim, out_dim in ((32768, 1024), (4096, 2048), (2048, 4096)):
         n = 512
         W = inputs.weights(out_dim, in_dim, seed=1)
         copies = weight_copies(torch, dev, W, 2 * l2)
-        x = torch.from_numpy(inputs.normal((n, in_dim), seed=1)).to(dev)
+        xcopies = weight_copies(torch, dev, inputs.normal((n, in_dim), seed=1), 2 * l2)
         o = torch.empty((n, out_dim), device=dev)
         q8.q8_profile_arm(8)
-        ms = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim, x, n,
-                                                                stream), 8)
+        ms = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim,
+                                                                xcopies[i % len(xcopies)], n, stream), 8)
         kms = prof_mean(8)
         q8.q8_profile_arm(0)
         ops = 2.0 * in_dim * out_dim * n
@@ -467,8 +468,9 @@ def secondary(args, torch, q8, dev, stream, l2):
                     "kernel_ms": round(kms, 4), "kernel_tops": round(ops / (kms * 1e-3) / 1e12, 2),
                     "kernel_frac_of_bf16_peak": round(ops / (kms * 1e-3) / 1e12 / tflops, 4),
                     "peak_note": f"int8-equivalent ops vs {tkind} dense bf16 tensor peak {tflops} TFLOP/s "
-                                 "(no int8 MMA instruction on sm_103a)"})
-        del copies
+                                 "(no int8 MMA instruction on sm_103a)",
+                    "timing": "eager calls, each on its own copy of the weights and of x (both > L2)"})
+        del copies, xcopies
 
     # the same GEMM on weights repacked once into the tensor-core operand layout (no per-call
     # expansion above 640 tokens); eager calls, each on its own copy of the packed weights
@@ -478,19 +480,20 @@ def secondary(args, torch, q8, dev, stream, l2):
         pk = [q8.repack(Wd, in_dim, out_dim, q8.Q8_LAYOUT_TC)]
         pk += [pk[0].clone() for _ in range(max(1, int(2 * l2 // pk[0].numel())))]
         copies = [Wd] + [Wd.clone() for _ in range(max(1, int(2 * l2 // Wd.numel())))]
-        x = torch.from_numpy(inputs.normal((n, in_dim), seed=1)).to(dev)
+        xcopies = weight_copies(torch, dev, inputs.normal((n, in_dim), seed=1), 2 * l2)
         o = torch.empty((n, out_dim), device=dev)
-        ms_raw = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim, x, n,
-                                                                    stream), 6)
+        ms_raw = timed_eager(torch, stream, lambda i: q8.q8_matmul(o, copies[i % len(copies)], in_dim, out_dim,
+                                                                    xcopies[i % len(xcopies)], n, stream), 6)
         ms_pk = timed_eager(torch, stream, lambda i: q8.q8_matmul_packed(o, pk[i % len(pk)], q8.Q8_LAYOUT_TC, in_dim,
-                                                                          out_dim, x, n, stream), 6)
+                                                                          out_dim, xcopies[i % len(xcopies)], n,
+                                                                          stream), 6)
         ops = 2.0 * in_dim * out_dim * n
         out.append({"workload": f"prefill in {in_dim} -> out {out_dim}, n_tok {n}: weights packed once in the "
                                 "tensor-core layout (q8_matmul_packed) against raw Q8_0 rows (q8_matmul)",
                     "ms_per_call_packed": round(ms_pk, 4), "tops_packed": round(ops / (ms_pk * 1e-3) / 1e12, 2),
                     "ms_per_call_raw": round(ms_raw, 4), "tops_raw": round(ops / (ms_raw * 1e-3) / 1e12, 2),
                     "frac_of_bf16_peak_packed": round(ops / (ms_pk * 1e-3) / 1e12 / tflops, 4)})
-        del pk, copies, Wd
+        del pk, copies, Wd, xcopies
     torch.cuda.empty_cache()
 
     # routed experts: gate/up (x per token) and down (x per pair), 256 experts, 64 tokens, uniform top-6
