@@ -10,9 +10,10 @@
 // every product is an integer below 2^14 and a block's 32-product sum is below
 // 2^24, exact in the fp32 accumulator.  The scales differ per 32-value block,
 // so each block gets its own accumulator: two UMMAs (K = 16 each) write a fresh
-// 128 x 128 fp32 tile into one of four TMEM slots, and eight epilogue warps read
-// it back (tcgen05.ld, a warp's 64 columns in one batch and one wait) and fold
-// it into fp32 registers as
+// 128 x 128 fp32 tile into one of four TMEM slots, and the epilogue warps read
+// it back (tcgen05.ld 16x256b: a thread holds four rows and a quarter of its
+// warp's columns, so it loads a quarter of the activation scales a lane-per-row
+// read would need) and fold it into fp32 registers as
 // acc[o][t] += isum * d_x[t] * d_w[o] (packed f32x2 multiply and FMA).  That
 // epilogue costs two fp32 operations per output per block, 1/16 of the MMA's
 // multiply-adds, and the fp32 pipe, not the tensor pipe, sets the ceiling
@@ -26,10 +27,12 @@
 //           rows per four stages into a ring of two (four stages).
 //   warp 1  allocates TMEM (512 columns) and issues the UMMAs from one thread;
 //           tcgen05.commit signals "slot full" and, per stage, "stage consumed".
-//   2..9    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the 128
-//           columns; arrives "slot empty" after reading, "stage empty" after
-//           using the stage's scales.
-//   10, 11  raw weights only: converters.  Each stage's weight tile is written
+//   2..     epilogue, 8 warps (fp16 weights) or 16 (raw weights): warp w reads
+//           TMEM lanes 32*(w%4).. and one column group (half or quarter of the
+//           128); arrives "slot empty" after folding, "stage empty" after using
+//           the stage's scales.
+//   next    fp16 weights: the second MMA issuer.  Raw weights, two warps:
+//           converters.  Each stage's weight tile is written
 //           from the raw copy as exact fp16 in the layout the fp16 tensor map
 //           gives, with the weight scales beside it, then handed to the tensor
 //           core (proxy fence + the stage's "full" barrier).
@@ -54,7 +57,6 @@ constexpr int B_BYTES = BN * BK * 2;                   // 16384
 constexpr int DX_BYTES = 2 * BN * 4;                   // 1024
 constexpr int DW_BYTES = 2 * BM * 4;                   // 1024
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + DX_BYTES + DW_BYTES;   // 34 KiB, 1 KiB aligned
-constexpr int NUM_EPI = 8;                             // epilogue warps: 2 per TMEM lane quarter
 constexpr int NSLOT_T = 4;                             // TMEM accumulator slots of BN columns
 constexpr uint32_t TMEM_COLS = NSLOT_T * BN;           // 512
 // Raw-weight variant: the A operand arrives as raw Q8_0 rows, 8 blocks (272
@@ -69,11 +71,17 @@ static_assert(STAGE_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stage alignment
 
 template <bool RAW> struct Cfg {
     static constexpr int NSTAGE = RAW ? 4 : 6;
+    // Epilogue warps per TMEM lane quarter, each folding 128 / EPI_COLG columns.
+    // With raw weights the converters share the schedulers and four warps per
+    // quarter hide more latency; with fp16 weights two are faster (measured).
+    static constexpr int EPI_COLG = RAW ? 4 : 2;
+    static constexpr int NUM_EPI = 4 * EPI_COLG;
     // MMA issuers: the issuing thread shares its scheduler with two folding
     // epilogue warps and slows down while they fold; with fp16 weights a second
     // issuer on another scheduler takes every other stage.
     static constexpr int NMMA = RAW ? 1 : 2;
     static constexpr int NTHREADS = (2 + NUM_EPI + (RAW ? NCONV : 0) + (NMMA - 1)) * 32;
+    static constexpr int W_EXTRA = 2 + NUM_EPI;   // second MMA issuer, or the first converter warp
     static constexpr int NRAWS = RAW ? NRAW : 0;
     // full, empty, tfull, tempty, done, raw full, raw empty
     static constexpr int NBAR = 2 * NSTAGE + 2 * NSLOT_T + 1 + 2 * NRAWS;
@@ -121,16 +129,48 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
+// 16 lanes x 8 columns per repetition (NR repetitions, 8 columns apart): thread
+// t gets, per repetition g, (lane t/4, columns 8g + 2(t%4) and + 1) in v[4g],
+// v[4g+1] and the same columns of lane t/4 + 8 in v[4g+2], v[4g+3].
+template <int NR>
+__device__ __forceinline__ void tc_ld16x256(uint32_t taddr, uint32_t (&v)[4 * NR]) {
+    if constexpr (NR == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+            "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(taddr));
+    } else if constexpr (NR == 4) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+            : "r"(taddr));
+    } else if constexpr (NR == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                     : "r"(taddr));
+    } else {
+        static_assert(NR == 1, "repetitions");
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                     : "r"(taddr));
+    }
 }
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// No instruction: ties the registers of a finished tcgen05.ld to a point after
+// tcgen05.wait::ld, so that no use of them is scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void tc_regs_ready(uint32_t (&v)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) asm volatile("" : "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]));
+}
 
 // Shared-memory matrix descriptor: K-major tile with 128-byte swizzle, rows 128
 // bytes apart, 8-row groups 1024 bytes apart (the layout a 128-byte-swizzled
@@ -294,15 +334,26 @@ struct TcEpi {
 // One unit of an epilogue warp: NCW = columns of this warp (half the unit's N).
 // Per block, the warp's columns leave TMEM in one batch of x16 loads and are
 // folded into acc as isum * d_x[t] * d_w[o]; then the unit's outputs are stored.
+// One unit of an epilogue warp, NCW columns (its share of the unit's N), read
+// from TMEM 16 lanes at a time (16x256b): each thread holds four rows (lanes
+// t/4 + 0, 8, 16, 24 of its quarter) and 2 of every 8 columns, so per block it
+// needs NCW/4 activation scales (NCW/8 shared-memory loads, each one wavefront)
+// instead of all NCW.
 template <int NCW, bool G, int NSTAGE>
 __device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit &w, TcEpi &e) {
     using namespace tc;
-    uint64_t acc[NCW / 2];   // fp32 pairs
+    constexpr int NG = NCW / 8;              // 8-column groups
+    const int r4 = e.lane >> 2, c2 = 2 * (e.lane & 3);
+    const int q32 = e.m - e.lane;            // first row of the warp's lane quarter
+    uint64_t acc[2][2][NG];                  // [16-lane half][row + 0 / + 8][group]: fp32 pairs
 #pragma unroll
-    for (int i = 0; i < NCW / 2; ++i) acc[i] = 0ull;
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int g = 0; g < NG; ++g) acc[a][k][g] = 0ull;
     for (int kb = w.kb0; kb < w.kb1; kb += 2) {
         const uint8_t *st = e.smem + (size_t)e.stage * STAGE_BYTES;
-        // the scales arrive with the stage (the MMA warp waited on the same barrier)
         const bool staged = mbar_wait(&e.full[e.stage], e.phase, p.err, e.abort_flag, e.lim);
         const float *dxs = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES);
         const float *dws = reinterpret_cast<const float *>(st + A_BYTES + B_BYTES + DX_BYTES);
@@ -310,23 +361,30 @@ __device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit
             const uint32_t slot = e.blk % NSLOT_T;
             mbar_wait(&e.tfull[slot], (e.blk / NSLOT_T) & 1u, p.err, e.abort_flag, e.lim);
             tc_fence_after();
-            const uint64_t ww = tc_pair(dws[j * BM + e.m]);
-            const float *dxj = dxs + j * BN + e.h * NCW;
             const uint32_t col0 = e.lane_addr + slot * BN + e.h * NCW;
-            uint32_t v[NCW / 16][16];
+            uint32_t v[2][4 * NG];
+            tc_ld16x256<NG>(col0, v[0]);
+            tc_ld16x256<NG>(col0 + (16u << 16), v[1]);
+            uint64_t ww[2][2];
 #pragma unroll
-            for (int c = 0; c < NCW / 16; ++c) tc_ld16(col0 + c * 16, v[c]);
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) ww[a][k] = tc_pair(dws[j * BM + q32 + 16 * a + 8 * k + r4]);
+            const float *dxj = dxs + j * BN + e.h * NCW + c2;
             tc_wait_ld();
+            tc_regs_ready(v[0]);
+            tc_regs_ready(v[1]);
 #pragma unroll
-            for (int c = 0; c < NCW / 16; ++c) {
-                const float4 *x4 = reinterpret_cast<const float4 *>(dxj + c * 16);
+            for (int g = 0; g < NG; ++g) {
+                const float2 x = *reinterpret_cast<const float2 *>(dxj + 8 * g);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float4 x = x4[i];
-                    tc_fold(acc[c * 8 + 2 * i], v[c][4 * i], v[c][4 * i + 1], x.x, x.y, ww);
-                    tc_fold(acc[c * 8 + 2 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3], x.z, x.w, ww);
-                }
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        tc_fold(acc[a][k][g], v[a][4 * g + 2 * k], v[a][4 * g + 2 * k + 1], x.x, x.y, ww[a][k]);
             }
+            // (handing the slot back before the fold, with the accumulator already in
+            // registers, measured slower: the next block's MMAs then run against the fold)
             tc_fence_before();
             __syncwarp();
             if (e.lane == 0) mbar_arrive(&e.tempty[slot]);
@@ -340,28 +398,30 @@ __device__ __forceinline__ void tc_epilogue_unit(const TcParams &p, const TcUnit
         }
     }
     // ---- this unit's rows x this warp's tokens
-    const int row = w.mt * BM + e.m;
-    const int tok0 = e.h * NCW;                       // within the tile
-    if (row >= p.M) return;
-    if constexpr (G) {
+    const int tok0 = e.h * NCW + c2;                  // within the tile
 #pragma unroll
-        for (int i = 0; i < NCW / 2; ++i) {
-            const int t = tok0 + 2 * i;
-            if (t < w.n_valid)
-                p.out[(size_t)p.row_to_out[w.b_row + t] * p.M + row] = __uint_as_float((uint32_t)acc[i]);
-            if (t + 1 < w.n_valid)
-                p.out[(size_t)p.row_to_out[w.b_row + t + 1] * p.M + row] = __uint_as_float((uint32_t)(acc[i] >> 32));
-        }
-    } else {
-        const int ks = w.kb0 / p.kb_per;
-        float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int i = 0; i < NCW / 2; ++i) {
-            const int t = w.b_row + tok0 + 2 * i;
-            if (t < p.N) dst[(size_t)t * p.M + row] = __uint_as_float((uint32_t)acc[i]);
-            if (t + 1 < p.N) dst[(size_t)(t + 1) * p.M + row] = __uint_as_float((uint32_t)(acc[i] >> 32));
+        for (int k = 0; k < 2; ++k) {
+            const int row = w.mt * BM + q32 + 16 * a + 8 * k + r4;
+            if (row >= p.M) continue;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                const int t = tok0 + 8 * g;
+                const float lo = __uint_as_float((uint32_t)acc[a][k][g]);
+                const float hi = __uint_as_float((uint32_t)(acc[a][k][g] >> 32));
+                if constexpr (G) {
+                    if (t < w.n_valid) p.out[(size_t)p.row_to_out[w.b_row + t] * p.M + row] = lo;
+                    if (t + 1 < w.n_valid) p.out[(size_t)p.row_to_out[w.b_row + t + 1] * p.M + row] = hi;
+                } else {
+                    const int ks = w.kb0 / p.kb_per;
+                    float *dst = p.partial ? p.partial + (size_t)ks * p.N * p.M : p.out;
+                    const int tt = w.b_row + t;
+                    if (tt < p.N) dst[(size_t)tt * p.M + row] = lo;
+                    if (tt + 1 < p.N) dst[(size_t)(tt + 1) * p.M + row] = hi;
+                }
+            }
         }
-    }
 }
 
 template <bool G, bool RAW>
@@ -370,6 +430,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
     using namespace tc;
     constexpr int NSTAGE = Cfg<RAW>::NSTAGE;
     constexpr int NBAR = Cfg<RAW>::NBAR;
+    constexpr int NUM_EPI = Cfg<RAW>::NUM_EPI, EPI_COLG = Cfg<RAW>::EPI_COLG, W_EXTRA = Cfg<RAW>::W_EXTRA;
     if constexpr (G) {
         // The GEMV launched behind this grid waits for it before it reads or
         // writes anything this grid touches; let it take the SMs this grid frees.
@@ -496,7 +557,7 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
                 if (rfills[s]) mbar_drain(&raw_full[s], (rfills[s] - 1u) & 1u, t_end);
         }
         __syncwarp();
-    } else if (warp == 1 || (Cfg<RAW>::NMMA > 1 && warp == 2 + NUM_EPI)) {
+    } else if (warp == 1 || (Cfg<RAW>::NMMA > 1 && warp == W_EXTRA)) {
         // ------------------------------------------------ MMA issuers (stage s: issuer s % NMMA)
         // whole warp in the loop and the waits, lane 0 issues
         constexpr uint32_t NMMA = Cfg<RAW>::NMMA;
@@ -550,20 +611,20 @@ __global__ void __launch_bounds__(tc::Cfg<RAW>::NTHREADS, 1)
     } else if (warp < 2 + NUM_EPI) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const int h = (warp - 2) >> 2;                // column half
+        const int h = (warp - 2) >> 2;                // column group
         const int m = q * 32 + lane;                  // row within the tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         TcEpi e{smem, full, empty, tfull, tempty, abort_flag, lim, lane_addr, m, h, lane, 0u, 0u, 0u};
         TcUnit w;
         int seg = 0;
         for (int u = blockIdx.x; tc_unit<G>(p, u, w, seg); u += gridDim.x) {
-            if (w.ncols == 128) tc_epilogue_unit<64, G, NSTAGE>(p, w, e);
-            else if (w.ncols == 64) tc_epilogue_unit<32, G, NSTAGE>(p, w, e);
-            else tc_epilogue_unit<16, G, NSTAGE>(p, w, e);
+            if (w.ncols == 128) tc_epilogue_unit<128 / EPI_COLG, G, NSTAGE>(p, w, e);
+            else if (w.ncols == 64) tc_epilogue_unit<64 / EPI_COLG, G, NSTAGE>(p, w, e);
+            else tc_epilogue_unit<32 / EPI_COLG, G, NSTAGE>(p, w, e);
         }
     } else if constexpr (RAW) {
         // ------------------------------------------------ converters: raw copy -> fp16 A tile + scales
-        const int ct = threadIdx.x - (2 + NUM_EPI) * 32;   // 0 .. 63
+        const int ct = threadIdx.x - W_EXTRA * 32;   // 0 .. 63
         uint32_t stage = 0, phase = 0, rs = 0, rph = 0;
         TcUnit w;
         int seg = 0;
