@@ -473,7 +473,7 @@ def secondary(args, torch, q8, dev, stream, l2):
         del copies, xcopies
 
     # the same GEMM on weights repacked once into the tensor-core operand layout (no per-call
-    # expansion above 640 tokens); eager calls, each on its own copy of the packed weights
+    # expansion above 2048 tokens); eager calls, each on its own copy of the packed weights
     for in_dim, out_dim, n in ((32768, 1024, 512), (1024, 32768, 4096)):
         W = inputs.weights(out_dim, in_dim, seed=1)
         Wd = torch.from_numpy(W).to(dev)

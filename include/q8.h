@@ -233,8 +233,9 @@ int q8_moe_combine(float *out, const float *y, const float *weights, uint64_t n_
  *     (exact integers), then fp32 scales block-major [in_dim/32][m_ld], m_ld =
  *     rows rounded up to 128, padding rows zero; 2 bytes per weight plus 4 per
  *     block.  Its matmul runs the tcgen05 GEMM on it directly for any n_tok,
- *     skipping the weight expansion q8_matmul performs per call above 640
- *     tokens.  in_dim must be a multiple of 64.
+ *     skipping the weight expansion q8_matmul performs per call above 2048
+ *     tokens (or when in_dim/32 is not a multiple of 8).  in_dim must be a
+ *     multiple of 64.
  *   q8_repack_bytes: size of the packed buffer (0 for a bad layout or in_dim).
  *   q8_repack:       Wp (out, device, q8_repack_bytes bytes, 16-byte aligned) <- W.
  *   q8_matmul_packed: as q8_matmul, weights from a q8_repack buffer of `layout`.

@@ -236,9 +236,9 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
 // when the output tiles do not fill the GPU.  Up to TC_RAW_MAX_TOKENS tokens
 // (and in_dim / 32 a multiple of 8) the GEMM reads the raw Q8_0 rows and
 // converts them in shared memory; beyond that the weights are first expanded
-// to an fp16 plane with block-major scales (the in-kernel conversion costs
-// about 12 % of the GEMM, the expansion a fixed pass over the weights).
-constexpr uint64_t TC_RAW_MAX_TOKENS = 640;
+// to an fp16 plane with block-major scales (measured: the raw-weight GEMM is
+// faster than expansion plus GEMM up to 2048 tokens and about even at 4096).
+constexpr uint64_t TC_RAW_MAX_TOKENS = 2048;
 // a16_pre / dwT_pre: weights already in the GEMM's fp16 operand layout (a
 // Q8_LAYOUT_TC buffer; m_ld = out_dim rounded up to 128), used as they are.
 int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,

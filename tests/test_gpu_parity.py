@@ -126,7 +126,9 @@ SHAPES = [
     (32, 5, 1), (96, 19, 7), (160, 50, 20), (4000, 8, 2),
     # single and seven output rows (fewer rows than any tile or TMA box): the GEMV in
     # each mode, the tcgen05 GEMM on raw and on expanded weights
-    (256, 1, 1), (1024, 7, 4), (4096, 1, 16), (512, 7, 100), (256, 1, 33), (2048, 1, 700), (1024, 7, 20),
+    (256, 1, 1), (1024, 7, 4), (4096, 1, 16), (512, 7, 100), (256, 1, 33), (2048, 1, 2100), (1024, 7, 20),
+    # raw weights up to 2048 tokens (several token tiles, ragged last tile)
+    (1024, 130, 1000), (2048, 1, 700),
     # in_dim 64 (two blocks a row): the slow path, and the tcgen05 GEMM with one K stage
     (64, 7, 1), (64, 1, 16), (64, 1, 20), (64, 130, 40), (64, 7, 300),
 ]
@@ -512,7 +514,7 @@ def test_repack_layout_and_parity(q8, o):
 def test_repack_tensor_core_layout_and_parity(q8, o, in_dim, out_dim):
     """The tcgen05 GEMM's weight operand built once: fp16 quants (exact integers) in [m_ld][in_dim] and
     the binary16 scales as fp32 in [in_dim/32][m_ld], padding rows zero.  Its products match the oracle
-    for few and many tokens, and above 640 tokens are the bits of q8_matmul (which then expands the
+    for few and many tokens, and above 2048 tokens are the bits of q8_matmul (which then expands the
     weights into the same layout per call)."""
     Wh = inputs.weights(out_dim, in_dim, seed=63)
     W = dev(Wh)
@@ -525,7 +527,7 @@ def test_repack_tensor_core_layout_and_parity(q8, o, in_dim, out_dim):
     assert np.array_equal(q16[:out_dim].astype(np.int64), blk[..., 2:].view(np.int8).astype(np.int64))
     assert np.array_equal(dT[:, :out_dim].T, blk[..., :2].copy().view(np.float16).reshape(out_dim, nb).astype(np.float32))
     assert not np.any(q16[out_dim:]) and not np.any(dT[:, out_dim:])
-    for n_tok in (1, 16, 40, 700):
+    for n_tok in (1, 16, 40, 2100):
         xh = inputs.normal((n_tok, in_dim), seed=64 + n_tok, p_out=0.01)
         x = dev(xh)
         got = q8.matmul_packed(Wp, x, out_dim, q8.Q8_LAYOUT_TC)
