@@ -51,6 +51,8 @@ def _load():
             u64, i32, u32, dbl, vp = (ctypes.c_uint64, ctypes.c_int32, ctypes.c_uint32,
                                       ctypes.c_double, ctypes.c_void_p)
             lib.q8g_weights.argtypes = [vp, u64, u64, u64, u64, dbl, dbl]
+            lib.q8g_kq_weights.argtypes = [vp, u64, u64, i32, u64, u64, dbl, dbl, dbl, dbl]
+            lib.q8g_kq_weights.restype = ctypes.c_int
             lib.q8g_normal.argtypes = [vp, u64, u64, u64, dbl, dbl]
             lib.q8g_route_uniform.argtypes = [vp, u64, u32, u32, u64, u64]
             lib.q8g_route_zipf.argtypes = [vp, u64, u32, u32, dbl, u64, u64]
@@ -74,6 +76,25 @@ def weights(rows: int, in_dim: int, seed: int = 0, stream: int = STREAM_W,
     assert out.dtype == np.uint8 and out.flags.c_contiguous and out.nbytes == nbytes
     rc = _load().q8g_weights(_ptr(out), rows, in_dim, seed, stream, d_lo, d_hi)
     assert rc == 0
+    return out
+
+
+KQ_BLOCK = 256
+KQ_BYTES = {2: 84, 4: 144}      # Q2_K, Q4_K
+# d and dmin ranges (binary16 normal numbers) that give weights of a few hundredths
+KQ_SCALES = {2: (5e-4, 2e-3, 5e-4, 2e-3), 4: (6.2e-5, 1.5e-4, 6.2e-5, 1.5e-4)}
+
+
+def kq_weights(rows: int, in_dim: int, fmt: int, seed: int = 0, stream: int = STREAM_W,
+               scales=None, out: np.ndarray | None = None) -> np.ndarray:
+    """Raw K-quant rows (fmt 2: Q2_K, 4: Q4_K): uint8 [rows, in_dim/256*block bytes]."""
+    assert in_dim % KQ_BLOCK == 0 and fmt in KQ_BYTES
+    shape = (rows, in_dim // KQ_BLOCK * KQ_BYTES[fmt])
+    if out is None:
+        out = np.empty(shape, dtype=np.uint8)
+    assert out.dtype == np.uint8 and out.flags.c_contiguous and out.size == shape[0] * shape[1]
+    d_lo, d_hi, m_lo, m_hi = scales or KQ_SCALES[fmt]
+    assert _load().q8g_kq_weights(_ptr(out), rows, in_dim, fmt, seed, stream, d_lo, d_hi, m_lo, m_hi) == 0
     return out
 
 

@@ -97,6 +97,36 @@ int q8g_weights(uint8_t *W, uint64_t rows, uint64_t in_dim, uint64_t seed,
     return 0;
 }
 
+/* Raw K-quant weight rows: rows x (in_dim/256) blocks of 84 (fmt 2, Q2_K) or
+ * 144 (fmt 4, Q4_K) bytes.  d and dmin are drawn uniformly from [d_lo, d_hi]
+ * and [m_lo, m_hi] (both within the binary16 normal range) and placed on the
+ * binary16 grid at the block's d and dmin bytes; every other byte (scales,
+ * mins, quants) is uniform. */
+int q8g_kq_weights(uint8_t *W, uint64_t rows, uint64_t in_dim, int fmt, uint64_t seed, uint64_t stream,
+                   double d_lo, double d_hi, double m_lo, double m_hi) {
+    if (!W || in_dim % 256 || (fmt != 2 && fmt != 4) || d_lo < 0x1p-14 || m_lo < 0x1p-14) return -1;
+    const uint64_t bb = fmt == 2 ? 84 : 144;
+    const uint64_t d_off = fmt == 2 ? 80 : 0;
+    const uint64_t nblk = rows * (in_dim / 256);
+    const uint64_t kd = stream_key(seed, 100 + 2 * stream);   /* d, dmin */
+    const uint64_t kb = stream_key(seed, 101 + 2 * stream);   /* the other bytes */
+    #pragma omp parallel for schedule(static)
+    for (int64_t blk = 0; blk < (int64_t)nblk; ++blk) {
+        uint8_t *p = W + (uint64_t)blk * bb;
+        for (uint64_t i = 0; i < bb; i += 8) {
+            uint64_t r = draw(kb, (uint64_t)blk * 24 + i / 8);
+            for (uint64_t j = 0; j < 8 && i + j < bb; ++j) p[i + j] = (uint8_t)(r >> (8 * j));
+        }
+        uint16_t h = to_half_grid(d_lo + (d_hi - d_lo) * unit(draw(kd, 2 * (uint64_t)blk)));
+        uint16_t hm = to_half_grid(m_lo + (m_hi - m_lo) * unit(draw(kd, 2 * (uint64_t)blk + 1)));
+        p[d_off] = (uint8_t)(h & 0xff);
+        p[d_off + 1] = (uint8_t)(h >> 8);
+        p[d_off + 2] = (uint8_t)(hm & 0xff);
+        p[d_off + 3] = (uint8_t)(hm >> 8);
+    }
+    return 0;
+}
+
 /* N(0,1) activations; with probability p_out an element is multiplied by
  * out_scale (p_out = 0 disables). */
 int q8g_normal(float *x, uint64_t n, uint64_t seed, uint64_t stream,

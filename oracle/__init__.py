@@ -27,6 +27,8 @@ _lib = None
 
 QK = 32
 QBYTES = 34
+QKK = 256           # weights per K-quant block and values per Q8_K block
+KQ_Q2, KQ_Q4 = 2, 4  # K-quant formats: Q2_K (84-byte blocks), Q4_K (144-byte blocks)
 
 
 def compile_lib(src: str, dst: str) -> str:
@@ -66,8 +68,15 @@ class Oracle:
         lib.q8o_moe_ffn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, u32, u64, u64, vp, vp, u32,
                                     u64, u64, u64, ctypes.c_float, vp, u64]
         lib.q8o_rmsnorm_quantize.argtypes = [vp, vp, vp, vp, u64, u64, ctypes.c_double]
+        lib.q8o_kq_block_bytes.argtypes = [i32]
+        lib.q8o_kq_block_bytes.restype = u64
+        lib.q8o_kq_dequant.argtypes = [vp, vp, i32, u64, u64]
+        lib.q8o_quantize_q8k.argtypes = [vp, vp, vp, u64, u64]
+        lib.q8o_kq_matmul_q.argtypes = [vp, vp, vp, i32, u64, u64, vp, vp, u64]
+        lib.q8o_kq_moe.argtypes = [vp, vp, vp, i32, u32, u64, vp, u32, u64, u64, vp, vp, i32, u64]
         for f in (lib.q8o_quantize, lib.q8o_matmul, lib.q8o_matmul_sample, lib.q8o_moe,
-                  lib.q8o_moe_sample, lib.q8o_moe_ffn, lib.q8o_rmsnorm_quantize):
+                  lib.q8o_moe_sample, lib.q8o_moe_ffn, lib.q8o_rmsnorm_quantize, lib.q8o_kq_dequant,
+                  lib.q8o_quantize_q8k, lib.q8o_kq_matmul_q, lib.q8o_kq_moe):
             f.restype = ctypes.c_int
         self.lib = lib
 
@@ -220,6 +229,69 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rmsnorm_quantize: bad dims")
         return xq, y
+
+    # -- second weight format: Q2_K / Q4_K super-blocks against Q8_K activations -----
+    def kq_block_bytes(self, fmt: int) -> int:
+        return int(self.lib.q8o_kq_block_bytes(int(fmt)))
+
+    def kq_dequant(self, W: np.ndarray, fmt: int, in_dim: int, rows: int) -> np.ndarray:
+        """Raw K-quant rows -> float64 [rows, in_dim] weight values."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        assert W.nbytes == rows * in_dim // QKK * self.kq_block_bytes(fmt)
+        out = np.empty((rows, in_dim), dtype=np.float64)
+        if self.lib.q8o_kq_dequant(out.ctypes.data, W.ctypes.data, int(fmt), in_dim, rows) != 0:
+            raise ValueError("oracle kq_dequant: bad format or dims")
+        return out
+
+    def quantize_q8k(self, x: np.ndarray):
+        """x float32 [n_tok, in_dim] -> (d float32 [n_tok, in_dim/256], q int8 [n_tok, in_dim])."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        n_tok, in_dim = x.shape
+        d = np.empty((n_tok, in_dim // QKK), dtype=np.float32)
+        q = np.empty((n_tok, in_dim), dtype=np.int8)
+        if self.lib.q8o_quantize_q8k(d.ctypes.data, q.ctypes.data, x.ctypes.data, in_dim, n_tok) != 0:
+            raise ValueError("oracle quantize_q8k: bad dims")
+        return d, q
+
+    def kq_matmul_q(self, W, fmt: int, in_dim: int, out_dim: int, dx, qx):
+        """K-quant rows W [out_dim] against Q8_K rows (dx [n_tok, in_dim/256], qx [n_tok, in_dim]).
+        Returns (out float32 [n_tok, out_dim], bound float64 [n_tok, out_dim])."""
+        dx = np.ascontiguousarray(dx, dtype=np.float32)
+        qx = np.ascontiguousarray(qx, dtype=np.int8)
+        n_tok = qx.shape[0]
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        assert W.nbytes == out_dim * in_dim // QKK * self.kq_block_bytes(fmt) and qx.shape[1] == in_dim
+        out = np.empty((n_tok, out_dim), dtype=np.float32)
+        bound = np.empty((n_tok, out_dim), dtype=np.float64)
+        if self.lib.q8o_kq_matmul_q(out.ctypes.data, bound.ctypes.data, W.ctypes.data, int(fmt), in_dim, out_dim,
+                                    dx.ctypes.data, qx.ctypes.data, n_tok) != 0:
+            raise ValueError("oracle kq_matmul: bad format or dims")
+        return out, bound
+
+    def kq_matmul(self, W, fmt: int, x, out_dim: int):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        dx, qx = self.quantize_q8k(x)
+        return self.kq_matmul_q(W, fmt, x.shape[1], out_dim, dx, qx)
+
+    def kq_moe(self, W_experts, fmt: int, n_expert: int, expert_stride: int, ids, in_dim: int, out_dim: int, x,
+               x_per_pair: int):
+        """Routed K-quant experts; x float32 [n_tok or n_tok*k, in_dim] is quantised to Q8_K here.
+        Returns (out [n_tok*k, out_dim], bound, flag)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        n_tok, k = ids.shape
+        dx, qx = self.quantize_q8k(x)
+        out = np.empty((n_tok * k, out_dim), dtype=np.float32)
+        bound = np.empty((n_tok * k, out_dim), dtype=np.float64)
+        rc = self.lib.q8o_kq_moe(out.ctypes.data, bound.ctypes.data, np.ascontiguousarray(W_experts).ctypes.data,
+                                 int(fmt), n_expert, expert_stride, ids.ctypes.data, k, in_dim, out_dim,
+                                 dx.ctypes.data, qx.ctypes.data, int(x_per_pair), n_tok)
+        if rc < 0:
+            raise ValueError("oracle kq_moe: bad dims")
+        return out, bound, rc
 
 
 _oracle = None

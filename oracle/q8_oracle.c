@@ -43,6 +43,8 @@
  *   - the down projection's activations are the fp32 mid rows quantised with
  *     the activation quantiser above, one row per pair;
  *   - the weighted sum adds the k experts of a token in slot order, in double;
+ *   - the second weight format (Q2_K and Q4_K super-blocks against Q8_K
+ *     activations): see its own section at the end of this file;
  *   - RMSNorm (the model's attn_norm / ffn_norm scales, model-architecture page,
  *     weight table): y_i = x_i / sqrt(mean_j x_j^2 + eps) * gamma_i, the usual
  *     definition (the pages name the norm but print no formula), evaluated in
@@ -358,4 +360,189 @@ int q8o_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gam
             y[t * dim + i] = (float)((double)xr[i] * r * (gamma ? (double)gamma[i] : 1.0));
     }
     return q8o_quantize(xq, y, dim, n_tok);
+}
+
+/* ---- second weight format: K-quant super-blocks x Q8_K activations -----------
+ *
+ * Model-architecture page, quantisation section 3 ("Block layout"): 256 weights
+ * per block; Q2_K is 84 bytes (scales[16], qs[64] of 2-bit values, d, dmin) and
+ * Q4_K 144 bytes (d, dmin, scales[12] holding scales and mins, qs[128] of 4-bit
+ * values).  Section 1 prints the 2-bit field order inside a byte (field k is
+ * (byte >> 2k) & 3) and the Q8_K quantiser; section 4 the dot product of a
+ * K-quant row with a Q8_K row, whose value is the sum of dequantised weight
+ * times dequantised activation.  The routed experts of the code walkthrough
+ * (trace 5) and the MoE page's Q4_K expert path use these blocks.
+ *
+ * Readings where the pages are silent (each one also listed in the design notes):
+ *   - the pages name these blocks llama.cpp/GGML formats and print their field
+ *     order and sizes, not the packing inside them; the packing is GGML's k-quant
+ *     layout:
+ *       Q2_K: d, dmin binary16 little-endian at bytes 80 and 82; 16 sub-blocks of
+ *         16 weights; scales[i] holds sub-block i's scale (low nibble) and min
+ *         (high nibble); weight 128h + 32j + 16s + l (h < 2, j < 4, s < 2, l < 16)
+ *         is field j of byte qs[32h + 16s + l], in sub-block 8h + 2j + s.
+ *       Q4_K: d, dmin at bytes 0 and 2, scales[12] at 4, qs at 16; 8 sub-blocks of
+ *         32 weights with 6-bit scale sc and min m: for j < 4, sc = s[j] & 63 and
+ *         m = s[j+4] & 63; for j >= 4, sc = (s[j+4] & 15) | ((s[j-4] >> 6) << 4) and
+ *         m = (s[j+4] >> 4) | ((s[j] >> 6) << 4); weight 64c + l (c < 4, l < 32) is
+ *         the low nibble of qs[32c + l] (sub-block 2c), weight 64c + 32 + l its high
+ *         nibble (sub-block 2c + 1);
+ *   - a weight's value is d * sc * q - dmin * m (the printed comment's
+ *     "d * (scale * q + dmin * offset)" is garbled; a min offset is subtracted);
+ *   - Q8_K: fp32 d = amax / 127 and q = (int8) roundf(x / d) per 256-value block as
+ *     printed; an all-zero block stores d = 0 and q = 0;
+ *   - the product is the plain definition: out = sum_i w_i * (d_x * q_x,i) over the
+ *     dequantised values, evaluated in double and rounded once to fp32.
+ */
+#define QKK 256
+#define KQ_Q2 2
+#define KQ_Q4 4
+
+uint64_t q8o_kq_block_bytes(int fmt) {
+    return fmt == KQ_Q2 ? 84u : (fmt == KQ_Q4 ? 144u : 0u);
+}
+
+static uint16_t le16(const uint8_t *p) { return (uint16_t)(p[0] | ((uint16_t)p[1] << 8)); }
+
+/* Scale, min and 2- or 4-bit value of weight i (0..255) of one block. */
+static void kq_fields(const uint8_t *blk, int fmt, int i, int *sc, int *m, int *q, double *d, double *dmin) {
+    if (fmt == KQ_Q2) {
+        int h = i / 128, j = (i % 128) / 32, s = (i % 32) / 16, l = i % 16;
+        int sb = 8 * h + 2 * j + s;
+        *sc = blk[sb] & 15;
+        *m = blk[sb] >> 4;
+        *q = (blk[16 + 32 * h + 16 * s + l] >> (2 * j)) & 3;
+        *d = q8o_f16_to_f32(le16(blk + 80));
+        *dmin = q8o_f16_to_f32(le16(blk + 82));
+    } else {
+        const uint8_t *s = blk + 4;
+        int c = i / 64, hi = (i % 64) / 32, l = i % 32;
+        int j = 2 * c + hi;
+        if (j < 4) {
+            *sc = s[j] & 63;
+            *m = s[j + 4] & 63;
+        } else {
+            *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+            *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+        }
+        uint8_t byte = blk[16 + 32 * c + l];
+        *q = hi ? (byte >> 4) : (byte & 15);
+        *d = q8o_f16_to_f32(le16(blk));
+        *dmin = q8o_f16_to_f32(le16(blk + 2));
+    }
+}
+
+/* The 256 weights of one block as doubles: d * sc * q - dmin * m. */
+static void kq_dequant_block(double *w, const uint8_t *blk, int fmt) {
+    for (int i = 0; i < QKK; ++i) {
+        int sc, m, q;
+        double d, dmin;
+        kq_fields(blk, fmt, i, &sc, &m, &q, &d, &dmin);
+        w[i] = d * (double)sc * (double)q - dmin * (double)m;
+    }
+}
+
+/* W [rows][in_dim/256 blocks] -> out [rows][in_dim] doubles. */
+int q8o_kq_dequant(double *out, const uint8_t *W, int fmt, uint64_t in_dim, uint64_t rows) {
+    uint64_t bb = q8o_kq_block_bytes(fmt);
+    if (!bb || in_dim == 0 || in_dim % QKK) return -1;
+    uint64_t nsb = in_dim / QKK;
+    for (uint64_t r = 0; r < rows; ++r)
+        for (uint64_t b = 0; b < nsb; ++b)
+            kq_dequant_block(out + r * in_dim + b * QKK, W + (r * nsb + b) * bb, fmt);
+    return 0;
+}
+
+/* Q8_K: x [n_tok][in_dim] -> d [n_tok][in_dim/256] (fp32) and q [n_tok][in_dim]. */
+int q8o_quantize_q8k(float *d, int8_t *q, const float *x, uint64_t in_dim, uint64_t n_tok) {
+    if (in_dim == 0 || in_dim % QKK) return -1;
+    uint64_t nsb = in_dim / QKK;
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint64_t b = 0; b < nsb; ++b) {
+            const float *xb = x + t * in_dim + b * QKK;
+            int8_t *qb = q + t * in_dim + b * QKK;
+            float amax = 0.0f;
+            for (int i = 0; i < QKK; ++i) {
+                float a = fabsf(xb[i]);
+                if (a > amax) amax = a;
+            }
+            float scale = amax / 127.0f;
+            d[t * nsb + b] = scale;
+            for (int i = 0; i < QKK; ++i)
+                qb[i] = scale != 0.0f ? (int8_t)(int)roundf(xb[i] / scale) : 0;
+        }
+    return 0;
+}
+
+/* One output: K-quant row w (nsb blocks) against Q8_K row (dx [nsb], qx [nsb*256]).
+ * Returns the fp32 rounding of the double sum; *bound gets
+ * sum_b |d_x| (|d sum_j sc_j isum_j| + |dmin sum_j m_j xsum_j|) over the block's
+ * sub-blocks j (isum_j = sum q_w q_x, xsum_j = sum q_x): the terms a fixed-point
+ * evaluation adds in fp32. */
+float q8o_kq_dot_row(const uint8_t *w, int fmt, const float *dx, const int8_t *qx, uint64_t nsb, double *bound) {
+    uint64_t bb = q8o_kq_block_bytes(fmt);
+    double acc = 0.0, bsum = 0.0;
+    double wv[QKK];
+    for (uint64_t b = 0; b < nsb; ++b) {
+        const uint8_t *blk = w + b * bb;
+        kq_dequant_block(wv, blk, fmt);
+        double xd = (double)dx[b];
+        double dot = 0.0;
+        double t_sc = 0.0, t_m = 0.0, d = 0.0, dmin = 0.0;
+        for (int i = 0; i < QKK; ++i) {
+            int sc, m, q;
+            kq_fields(blk, fmt, i, &sc, &m, &q, &d, &dmin);
+            int qxi = qx[b * QKK + i];
+            dot += wv[i] * (xd * (double)qxi);
+            t_sc += (double)sc * (double)q * (double)qxi;
+            t_m += (double)m * (double)qxi;
+        }
+        acc += dot;
+        bsum += fabs(xd) * (fabs(d * t_sc) + fabs(dmin * t_m));
+    }
+    if (bound) *bound = bsum;
+    return (float)acc;
+}
+
+/* out[t][o] = row o of W against Q8_K row t. */
+int q8o_kq_matmul_q(float *out, double *bound, const uint8_t *W, int fmt, uint64_t in_dim, uint64_t out_dim,
+                    const float *dx, const int8_t *qx, uint64_t n_tok) {
+    uint64_t bb = q8o_kq_block_bytes(fmt);
+    if (!bb || in_dim == 0 || in_dim % QKK) return -1;
+    uint64_t nsb = in_dim / QKK;
+    for (uint64_t t = 0; t < n_tok; ++t)
+        for (uint64_t o = 0; o < out_dim; ++o) {
+            double bd = 0.0;
+            out[t * out_dim + o] = q8o_kq_dot_row(W + o * nsb * bb, fmt, dx + t * nsb, qx + t * in_dim, nsb, &bd);
+            if (bound) bound[t * out_dim + o] = bd;
+        }
+    return 0;
+}
+
+/* Routed K-quant experts: pair p = t*k + j multiplies expert ids[p]'s matrix
+ * (at W_experts + ids[p] * expert_stride bytes) by Q8_K row p (x_per_pair) or t.
+ * An id outside [0, n_expert) gives a zero row and return value 1. */
+int q8o_kq_moe(float *out, double *bound, const uint8_t *W_experts, int fmt, uint32_t n_expert,
+               uint64_t expert_stride, const int32_t *ids, uint32_t k, uint64_t in_dim, uint64_t out_dim,
+               const float *dx, const int8_t *qx, int x_per_pair, uint64_t n_tok) {
+    uint64_t bb = q8o_kq_block_bytes(fmt);
+    if (!bb || in_dim == 0 || in_dim % QKK || k == 0) return -1;
+    uint64_t nsb = in_dim / QKK;
+    int flag = 0;
+    for (uint64_t p = 0; p < n_tok * k; ++p) {
+        int32_t e = ids[p];
+        uint64_t xr = x_per_pair ? p : p / k;
+        for (uint64_t o = 0; o < out_dim; ++o) {
+            double bd = 0.0;
+            float v = 0.0f;
+            if (e < 0 || (uint32_t)e >= n_expert)
+                flag = 1;
+            else
+                v = q8o_kq_dot_row(W_experts + (uint64_t)e * expert_stride + o * nsb * bb, fmt, dx + xr * nsb,
+                                   qx + xr * in_dim, nsb, &bd);
+            out[p * out_dim + o] = v;
+            if (bound) bound[p * out_dim + o] = bd;
+        }
+    }
+    return flag;
 }

@@ -643,4 +643,139 @@ def pin_rmsnorm_invariants(o):
     assert np.all(y0 == 0) and np.all(xq0 == 0)
 
 
+# ---------------------------------------------------------------- second weight format (K-quants x Q8_K)
+QKK = 256
+KQ_BYTES = {2: 84, 4: 144}
+
+
+def _kq_golden():
+    with open(os.path.join(GOLDEN, "kquant_worked.json")) as f:
+        return json.load(f)
+
+
+def _rand_kq(g, fmt, rows, in_dim):
+    """Random K-quant rows: uniform bytes, then d and dmin set to binary16 normals of a few 2^-k."""
+    nbk = in_dim // QKK
+    raw = g.integers(0, 256, size=(rows, nbk, KQ_BYTES[fmt])).astype(np.uint8)
+    off = 80 if fmt == 2 else 0
+    for j in (0, 2):
+        bits = random_f16_normal_bits(g, rows * nbk, -12, -6).reshape(rows, nbk)
+        raw[..., off + j] = (bits & 0xFF).astype(np.uint8)
+        raw[..., off + j + 1] = (bits >> 8).astype(np.uint8)
+    return raw.reshape(rows, nbk * KQ_BYTES[fmt])
+
+
+def pin_kq_dequant_golden(o):
+    """Hand-derived weight values of hand-built Q2_K and Q4_K blocks (and one block sum)."""
+    for b in _kq_golden()["kquant"]:
+        w = o.kq_dequant(np.array(b["bytes"], np.uint8), b["fmt"], QKK, 1)[0]
+        for k, v in b["values"].items():
+            assert w[int(k)] == v, (b["name"], k, float(w[int(k)]), v)
+        if "sum" in b:
+            assert w.sum() == b["sum"], (b["name"], float(w.sum()))
+
+
+def pin_kq_scale_doubling(o):
+    """Doubling d and dmin (binary16 exponent + 1) doubles every weight; d = dmin = 0 zeroes them."""
+    g = rng(42)
+    for fmt in (2, 4):
+        W = _rand_kq(g, fmt, 3, 512)
+        W2 = W.copy().reshape(3, 2, KQ_BYTES[fmt])
+        W0 = W2.copy()
+        off = 80 if fmt == 2 else 0
+        for j in (off, off + 2):
+            bits = W2[..., j].astype(np.uint16) | (W2[..., j + 1].astype(np.uint16) << 8)
+            bits = bits + (1 << 10)
+            W2[..., j] = (bits & 0xFF).astype(np.uint8)
+            W2[..., j + 1] = (bits >> 8).astype(np.uint8)
+            W0[..., j] = 0
+            W0[..., j + 1] = 0
+        w = o.kq_dequant(W, fmt, 512, 3)
+        assert np.array_equal(o.kq_dequant(W2.reshape(3, -1), fmt, 512, 3), 2 * w)
+        assert not o.kq_dequant(W0.reshape(3, -1), fmt, 512, 3).any()
+
+
+def pin_q8k_golden(o):
+    """The Q8_K quantiser on hand-worked 256-value blocks."""
+    for c in _kq_golden()["q8k"]:
+        x = np.zeros((1, QKK), np.float32)
+        x[0, :len(c["x_head"])] = c["x_head"]
+        d, q = o.quantize_q8k(x)
+        assert d[0, 0] == np.float32(c["d"]), (c["name"], float(d[0, 0]))
+        n = len(c["q_head"])
+        assert list(q[0, :n]) == c["q_head"] and not q[0, n:].any(), c["name"]
+
+
+def pin_q8k_invariants(o):
+    """|x/d - q| <= 1/2 in fp32, |q| <= 127 with 127 at the block maximum, sign symmetry,
+    power-of-two scaling, zero blocks."""
+    g = rng(43)
+    x = (g.standard_normal((4, 1024)) * np.exp(g.uniform(-6, 6, size=(4, 1)))).astype(np.float32)
+    x[1, 256:512] = 0.0
+    d, q = o.quantize_q8k(x)
+    for t in range(4):
+        for b in range(4):
+            blk = x[t, b * QKK:(b + 1) * QKK]
+            qb = q[t, b * QKK:(b + 1) * QKK].astype(np.int64)
+            if not blk.any():
+                assert d[t, b] == 0 and not qb.any()
+                continue
+            assert np.abs(qb).max() == 127 and abs(qb[np.argmax(np.abs(blk))]) == 127
+            quo = blk / np.float32(d[t, b])
+            assert np.all(np.abs(quo.astype(np.float64) - qb) <= 0.5)
+    dn, qn = o.quantize_q8k(-x)
+    assert np.array_equal(dn, d) and np.array_equal(qn, -q)
+    d4, q4 = o.quantize_q8k(x * np.float32(4))
+    assert np.array_equal(d4, 4 * d) and np.array_equal(q4, q)
+
+
+def pin_kq_matmul_exact(o):
+    """Tiny shapes: the product is the fp32 rounding of the exact rational sum of dequantised
+    weight times dequantised activation (weights from the golden-pinned dequantiser); the
+    bound is at least the sum's magnitude."""
+    g = rng(44)
+    for fmt in (2, 4):
+        for in_dim, out_dim, n_tok in [(256, 1, 1), (512, 3, 2), (768, 2, 3)]:
+            W = _rand_kq(g, fmt, out_dim, in_dim)
+            x = g.standard_normal((n_tok, in_dim)).astype(np.float32)
+            dx, qx = o.quantize_q8k(x)
+            out, bound = o.kq_matmul_q(W, fmt, in_dim, out_dim, dx, qx)
+            w = o.kq_dequant(W, fmt, in_dim, out_dim)
+            for t in range(n_tok):
+                xs = [Fraction(float(dx[t, i // QKK])) * int(qx[t, i]) for i in range(in_dim)]
+                for r in range(out_dim):
+                    ex = sum(Fraction(float(w[r, i])) * xs[i] for i in range(in_dim))
+                    slack = abs(ex) * Fraction(1, 1 << 23) + Fraction(float(bound[t, r])) * Fraction(1, 10 ** 12)
+                    assert abs(Fraction(float(out[t, r])) - ex) <= slack, (fmt, in_dim, t, r)
+                    assert bound[t, r] >= abs(float(ex)) * (1 - 1e-12)
+
+
+def pin_kq_block_sum(o):
+    """The hand-built Q2_K block against all-ones Q8_K activations (d_x = 1, q = 1): 3040."""
+    b = [c for c in _kq_golden()["kquant"] if c["name"] == "q2k_fields"][0]
+    W = np.array(b["bytes"] * 2, np.uint8).reshape(1, -1)
+    out, _ = o.kq_matmul_q(W, 2, 512, 1, np.ones((1, 2), np.float32), np.ones((1, 512), np.int8))
+    assert out[0, 0] == 2 * b["sum"]
+
+
+def pin_kq_moe_brute(o):
+    """Routed K-quant experts: each pair equals the dense product of its expert and its row;
+    bad ids give zero rows and raise the flag."""
+    g = rng(45)
+    for fmt in (2, 4):
+        n_exp, in_dim, out_dim, n_tok, k = 4, 512, 3, 3, 2
+        stride = out_dim * in_dim // QKK * KQ_BYTES[fmt]
+        Wall = _rand_kq(g, fmt, n_exp * out_dim, in_dim).reshape(-1)
+        ids = np.array([[0, 3], [2, 1], [3, 9]], dtype=np.int32)
+        for per_pair in (0, 1):
+            x = g.standard_normal((n_tok * k if per_pair else n_tok, in_dim)).astype(np.float32)
+            out, bound, flag = o.kq_moe(Wall, fmt, n_exp, stride, ids, in_dim, out_dim, x, per_pair)
+            assert flag == 1 and not out[5].any()
+            for p in range(5):
+                e = int(ids.reshape(-1)[p])
+                xr = x[p if per_pair else p // k][None]
+                ref, _ = o.kq_matmul(Wall[e * stride:(e + 1) * stride], fmt, xr, out_dim)
+                assert np.array_equal(out[p], ref[0]), (fmt, per_pair, p)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -48,3 +48,22 @@ def test_routing_zipf_skew():
     assert counts[0] == 4096 or counts[0] > 3000  # the top-ranked expert is nearly always chosen
     assert counts[0] >= counts[10] >= counts[100] and counts.sum() == 4096 * 6
     assert (counts > 0).sum() == 256
+
+
+def test_kquant_weights_deterministic_and_in_range():
+    """K-quant rows: d and dmin on the binary16 grid inside the stated ranges, other bytes uniform,
+    counter-based (a prefix does not depend on the total)."""
+    for fmt, bb, off in ((2, 84, 80), (4, 144, 0)):
+        a = inputs.kq_weights(32, 512, fmt, seed=0)
+        assert a.shape == (32, 2 * bb)
+        assert np.array_equal(a, inputs.kq_weights(32, 512, fmt, seed=0))
+        assert not np.array_equal(a, inputs.kq_weights(32, 512, fmt, seed=1))
+        assert np.array_equal(inputs.kq_weights(4, 512, fmt, seed=0), a[:4])
+        blk = a.reshape(-1, bb)
+        d_lo, d_hi, m_lo, m_hi = inputs.KQ_SCALES[fmt]
+        for j, (lo, hi) in ((off, (d_lo, d_hi)), (off + 2, (m_lo, m_hi))):
+            v = (blk[:, j].astype(np.uint16) | (blk[:, j + 1].astype(np.uint16) << 8)).view(np.float16)
+            v = v.astype(np.float64)
+            assert v.min() >= lo * (1 - 1e-3) and v.max() <= hi * (1 + 1e-3)
+        rest = np.delete(blk, [off, off + 1, off + 2, off + 3], axis=1).astype(np.float64)
+        assert abs(rest.mean() - 127.5) < 3.0 and rest.min() == 0 and rest.max() == 255

@@ -59,6 +59,24 @@ MUTANTS = [
     ("rms_no_gamma", "(gamma ? (double)gamma[i] : 1.0)", "1.0"),
     ("rms_quantise_x", "return q8o_quantize(xq, y, dim, n_tok);", "return q8o_quantize(xq, x, dim, n_tok);"),
     ("rms_abs_sum", "s += (double)xr[i] * (double)xr[i];", "s += fabs((double)xr[i]);"),
+    # second weight format (K-quant blocks x Q8_K)
+    ("q2k_scale_min_swapped", "*sc = blk[sb] & 15;\n        *m = blk[sb] >> 4;", "*sc = blk[sb] >> 4;\n        *m = blk[sb] & 15;"),
+    ("q2k_field_order", "*q = (blk[16 + 32 * h + 16 * s + l] >> (2 * j)) & 3;", "*q = (blk[16 + 32 * h + 16 * s + l] >> (6 - 2 * j)) & 3;"),
+    ("q2k_byte_order", "*q = (blk[16 + 32 * h + 16 * s + l] >> (2 * j)) & 3;", "*q = (blk[16 + 16 * h + 32 * s + l] >> (2 * j)) & 3;"),
+    ("q2k_subblock", "int sb = 8 * h + 2 * j + s;", "int sb = 8 * h + j + 4 * s;"),
+    ("q2k_d_offset", "*d = q8o_f16_to_f32(le16(blk + 80));", "*d = q8o_f16_to_f32(le16(blk + 82));"),
+    ("q4k_nibbles_swapped", "*q = hi ? (byte >> 4) : (byte & 15);", "*q = hi ? (byte & 15) : (byte >> 4);"),
+    ("q4k_high_scale_bits", "*sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);", "*sc = (s[j + 4] & 15) | ((s[j - 4] >> 4) << 4);"),
+    ("q4k_min_low", "*m = s[j + 4] & 63;", "*m = s[j] & 63;"),
+    ("q4k_min_high", "*m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);", "*m = (s[j + 4] >> 4) | ((s[j - 4] >> 6) << 4);"),
+    ("q4k_dmin_offset", "*dmin = q8o_f16_to_f32(le16(blk + 2));", "*dmin = q8o_f16_to_f32(le16(blk));"),
+    ("kq_min_added", "w[i] = d * (double)sc * (double)q - dmin * (double)m;", "w[i] = d * (double)sc * (double)q + dmin * (double)m;"),
+    ("q8k_scale_128", "float scale = amax / 127.0f;", "float scale = amax / 128.0f;"),
+    ("q8k_round_even", "qb[i] = scale != 0.0f ? (int8_t)(int)roundf(xb[i] / scale) : 0;", "qb[i] = scale != 0.0f ? (int8_t)(int)rintf(xb[i] / scale) : 0;"),
+    ("kq_dot_drop_block", "    for (uint64_t b = 0; b < nsb; ++b) {\n        const uint8_t *blk = w + b * bb;", "    for (uint64_t b = 0; b + 1 < nsb; ++b) {\n        const uint8_t *blk = w + b * bb;"),
+    ("kq_dot_block_scale", "        double xd = (double)dx[b];", "        double xd = (double)dx[0];"),
+    ("kq_moe_row", "uint64_t xr = x_per_pair ? p : p / k;", "uint64_t xr = x_per_pair ? p / k : p;"),
+    ("kq_moe_stride", "W_experts + (uint64_t)e * expert_stride + o * nsb * bb", "W_experts + (uint64_t)e * out_dim * bb + o * nsb * bb"),
 ]
 
 
