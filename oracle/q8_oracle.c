@@ -474,11 +474,17 @@ int q8o_quantize_q8k(float *d, int8_t *q, const float *x, uint64_t in_dim, uint6
     return 0;
 }
 
+/* Sub-block of weight i: Q2_K 16 sub-blocks of 16, Q4_K 8 of 32 (layout above). */
+static int kq_subblock(int fmt, int i) {
+    if (fmt == KQ_Q2) return 8 * (i / 128) + 2 * ((i % 128) / 32) + (i % 32) / 16;
+    return 2 * (i / 64) + (i % 64) / 32;
+}
+
 /* One output: K-quant row w (nsb blocks) against Q8_K row (dx [nsb], qx [nsb*256]).
  * Returns the fp32 rounding of the double sum; *bound gets
- * sum_b |d_x| (|d sum_j sc_j isum_j| + |dmin sum_j m_j xsum_j|) over the block's
- * sub-blocks j (isum_j = sum q_w q_x, xsum_j = sum q_x): the terms a fixed-point
- * evaluation adds in fp32. */
+ * sum_b sum_j |d_x| (|d sc_j isum_j| + |dmin m_j xsum_j|) over the blocks' sub-blocks j
+ * (isum_j = sum q_w q_x, xsum_j = sum q_x): the terms a fixed-point evaluation
+ * adds in fp32, one per sub-block as the Q8_0 bound has one per 32-value block. */
 float q8o_kq_dot_row(const uint8_t *w, int fmt, const float *dx, const int8_t *qx, uint64_t nsb, double *bound) {
     uint64_t bb = q8o_kq_block_bytes(fmt);
     double acc = 0.0, bsum = 0.0;
@@ -487,18 +493,19 @@ float q8o_kq_dot_row(const uint8_t *w, int fmt, const float *dx, const int8_t *q
         const uint8_t *blk = w + b * bb;
         kq_dequant_block(wv, blk, fmt);
         double xd = (double)dx[b];
-        double dot = 0.0;
-        double t_sc = 0.0, t_m = 0.0, d = 0.0, dmin = 0.0;
+        double dot = 0.0, d = 0.0, dmin = 0.0;
+        double t_sc[16] = {0}, t_m[16] = {0};
         for (int i = 0; i < QKK; ++i) {
             int sc, m, q;
             kq_fields(blk, fmt, i, &sc, &m, &q, &d, &dmin);
             int qxi = qx[b * QKK + i];
+            int j = kq_subblock(fmt, i);
             dot += wv[i] * (xd * (double)qxi);
-            t_sc += (double)sc * (double)q * (double)qxi;
-            t_m += (double)m * (double)qxi;
+            t_sc[j] += (double)sc * (double)q * (double)qxi;
+            t_m[j] += (double)m * (double)qxi;
         }
         acc += dot;
-        bsum += fabs(xd) * (fabs(d * t_sc) + fabs(dmin * t_m));
+        for (int j = 0; j < 16; ++j) bsum += fabs(xd) * (fabs(d * t_sc[j]) + fabs(dmin * t_m[j]));
     }
     if (bound) *bound = bsum;
     return (float)acc;
