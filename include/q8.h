@@ -173,6 +173,57 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert,
                   uint64_t n_tok, void *stream);
 
 /*
+ * Second weight format: K-quant blocks against Q8_K activations (model-
+ * architecture page, quantisation section 3, "Block layout": Q2_K and Q4_K
+ * blocks of 256 weights; section 1: the 2-bit field order and the Q8_K
+ * quantiser; section 4: the K-quant x Q8_K dot; the routed experts of the GPU
+ * code walkthrough, trace 5, and the MoE page's Q4_K expert path use them).
+ * The pages give the blocks' fields and sizes; the packing inside a block is
+ * GGML's k-quant layout, the format the pages attribute these blocks to:
+ *   Q2_K (fmt Q8_KQ_Q2_K, 84 bytes): scales[16], qs[64], d, dmin (binary16,
+ *     little-endian).  Sub-block i (16 weights) has scale scales[i] & 15 and min
+ *     scales[i] >> 4; weight 128h + 32j + 16s + l is 2-bit field j
+ *     ((byte >> 2j) & 3) of qs[32h + 16s + l], in sub-block 8h + 2j + s.
+ *   Q4_K (fmt Q8_KQ_Q4_K, 144 bytes): d, dmin, scales[12], qs[128].  Sub-block
+ *     j (32 weights) has 6-bit scale and min: j < 4: s[j] & 63, s[j+4] & 63;
+ *     j >= 4: (s[j+4] & 15) | (s[j-4] >> 6) << 4, (s[j+4] >> 4) | (s[j] >> 6) << 4.
+ *     Weight 64c + l is the low nibble of qs[32c + l] (sub-block 2c), weight
+ *     64c + 32 + l its high nibble (sub-block 2c + 1).
+ *   Weight value: d * sc * q - dmin * m.
+ * Rows are in_dim/256 consecutive blocks; in_dim % 256 == 0.
+ *   Q8_K block (292 bytes): fp32 d = max|x| / 127, int8 qs[256] = roundf(x / d)
+ *     (an all-zero block: d = 0, q = 0), then int16 sums of each 16 quants.
+ *
+ * q8_kq_row_bytes:  bytes of one row (0 for a bad fmt or in_dim).
+ * q8_quantize_q8k:  xq (out, [n_tok][in_dim/256] Q8_K blocks, 4-byte aligned)
+ *                   <- x (fp32 [n_tok][in_dim], 16-byte aligned); bit-exact to
+ *                   the formula (IEEE fp32 division, roundf).
+ * q8_kq_matmul:     out[t][o] = sum over blocks and sub-blocks of
+ *                   d_x * (d * sc * sum q_w q_x - dmin * m * sum q_x), the
+ *                   integer sums exact, the rest fp32; x is quantised to Q8_K in
+ *                   the library scratch.  out fp32 [n_tok][out_dim]; W out_dim
+ *                   rows (16-byte aligned for Q4_K, 4-byte for Q2_K).
+ * q8_kq_moe_matmul: the routed product over K-quant experts, arguments as
+ *                   q8_moe_matmul's (expert_stride_bytes >= one matrix, a
+ *                   multiple of 16 for Q4_K and of 4 for Q2_K); an id outside
+ *                   [0, n_expert) gives a zero row and raises Q8_ERANGE.
+ * The matmuls run a weight-streaming kernel (dp4a on the integer quants, one
+ * lane per sub-block) over token groups of up to 16; more tokens re-read the
+ * weights once per group.
+ */
+#define Q8_KQ_Q2_K 2
+#define Q8_KQ_Q4_K 4
+#define Q8_Q8K_BLOCK_BYTES 292
+uint64_t q8_kq_row_bytes(uint64_t in_dim, int fmt);
+int q8_quantize_q8k(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, void *stream);
+int q8_kq_matmul(float *out, const void *W, int fmt, uint64_t in_dim, uint64_t out_dim,
+                 const float *x, uint64_t n_tok, void *stream);
+int q8_kq_moe_matmul(float *out, const void *W_experts, int fmt, uint32_t n_expert,
+                     uint64_t expert_stride_bytes, const int32_t *expert_ids, uint32_t k,
+                     uint64_t in_dim, uint64_t out_dim, const float *x, int x_per_pair,
+                     uint64_t n_tok, void *stream);
+
+/*
  * Routed expert FFN around the routed matmul (GPU code walkthrough, trace 5:
  * ds4_gpu_routed_moe_one_tensor runs, for the selected experts, the gate and up
  * projections, SwiGLU, the down projection and the weighted sum; the MoE study

@@ -22,13 +22,16 @@ QB = 34
 Q8_OK, Q8_EINVAL, Q8_EALIGN, Q8_ERANGE, Q8_ENOMEM, Q8_ECUDA, Q8_ETIMEOUT, Q8_ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 Q8_LAYOUT_PLANES, Q8_LAYOUT_TC = 0, 1
+Q8_KQ_Q2_K, Q8_KQ_Q4_K = 2, 4
+Q8_Q8K_BLOCK_BYTES = 292
 
 # Every symbol include/q8.h declares.
 EXPORTS = ("q8_version", "q8_strerror", "q8_quantize_act", "q8_matmul", "q8_matmul_q", "q8_moe_matmul",
            "q8_repack_bytes", "q8_repack", "q8_matmul_packed", "q8_last_error", "q8_scratch_bytes",
            "q8_release", "q8_debug_fail_next_alloc", "q8_profile_arm", "q8_profile_used", "q8_profile_read",
            "q8_matmul_noalloc", "q8_last_cuda_error", "q8_matmul_host", "q8_moe_ffn", "q8_swiglu",
-           "q8_moe_combine", "q8_rmsnorm_quantize", "q8_debug_expire_waits")
+           "q8_moe_combine", "q8_rmsnorm_quantize", "q8_debug_expire_waits", "q8_kq_row_bytes",
+           "q8_quantize_q8k", "q8_kq_matmul", "q8_kq_moe_matmul")
 
 
 class Q8Error(RuntimeError):
@@ -70,6 +73,10 @@ def _load() -> ctypes.CDLL:
         "q8_profile_read": ([u32, ctypes.POINTER(ctypes.c_float)], i32),
         "q8_matmul_noalloc": ([vp, vp, u64, u64, vp, u64, vp], i32),
         "q8_last_cuda_error": ([], ctypes.c_char_p),
+        "q8_kq_row_bytes": ([u64, i32], u64),
+        "q8_quantize_q8k": ([vp, vp, u64, u64, vp], i32),
+        "q8_kq_matmul": ([vp, vp, i32, u64, u64, vp, u64, vp], i32),
+        "q8_kq_moe_matmul": ([vp, vp, i32, u32, u64, vp, u32, u64, u64, vp, i32, u64, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -172,6 +179,24 @@ def q8_repack(Wp, W, in_dim: int, rows: int, layout: int = 0, stream=None) -> in
 
 def q8_matmul_packed(out, Wp, layout: int, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
     return _get().q8_matmul_packed(_p(out), _p(Wp), layout, in_dim, out_dim, _p(x), n_tok, _s(stream))
+
+
+def q8_kq_row_bytes(in_dim: int, fmt: int) -> int:
+    return _get().q8_kq_row_bytes(in_dim, fmt)
+
+
+def q8_quantize_q8k(xq, x, in_dim: int, n_tok: int, stream=None) -> int:
+    return _get().q8_quantize_q8k(_p(xq), _p(x), in_dim, n_tok, _s(stream))
+
+
+def q8_kq_matmul(out, W, fmt: int, in_dim: int, out_dim: int, x, n_tok: int, stream=None) -> int:
+    return _get().q8_kq_matmul(_p(out), _p(W), fmt, in_dim, out_dim, _p(x), n_tok, _s(stream))
+
+
+def q8_kq_moe_matmul(out, W_experts, fmt: int, n_expert: int, expert_stride_bytes: int, expert_ids, k: int,
+                     in_dim: int, out_dim: int, x, x_per_pair: int, n_tok: int, stream=None) -> int:
+    return _get().q8_kq_moe_matmul(_p(out), _p(W_experts), fmt, n_expert, expert_stride_bytes, _p(expert_ids), k,
+                                   in_dim, out_dim, _p(x), x_per_pair, n_tok, _s(stream))
 
 
 def q8_last_error(stream=None) -> int:
@@ -302,4 +327,33 @@ def matmul_packed(Wp, x, out_dim: int, layout: int = 0):
     n_tok, in_dim = x.shape
     out = torch.empty((n_tok, out_dim), dtype=torch.float32, device=x.device)
     _check(q8_matmul_packed(out, Wp, layout, in_dim, out_dim, x, n_tok), "q8_matmul_packed")
+    return out
+
+
+def quantize_q8k(x):
+    """x float32 [n_tok, in_dim] (cuda) -> uint8 [n_tok, in_dim/256*292] Q8_K blocks."""
+    import torch
+    n_tok, in_dim = x.shape
+    xq = torch.empty((n_tok, in_dim // 256 * Q8_Q8K_BLOCK_BYTES), dtype=torch.uint8, device=x.device)
+    _check(q8_quantize_q8k(xq, x, in_dim, n_tok), "q8_quantize_q8k")
+    return xq
+
+
+def kq_matmul(W, fmt: int, x, out_dim: int):
+    """W uint8 K-quant rows [out_dim, q8_kq_row_bytes]; x float32 [n_tok, in_dim] -> [n_tok, out_dim]."""
+    import torch
+    n_tok, in_dim = x.shape
+    out = torch.empty((n_tok, out_dim), dtype=torch.float32, device=x.device)
+    _check(q8_kq_matmul(out, W, fmt, in_dim, out_dim, x, n_tok), "q8_kq_matmul")
+    return out
+
+
+def kq_moe_matmul(W_experts, fmt: int, n_expert: int, expert_stride: int, ids, x, x_per_pair: bool, out_dim: int):
+    """ids int32 [n_tok, k]; x [n_tok, in] or [n_tok*k, in] -> [n_tok*k, out_dim] (K-quant experts)."""
+    import torch
+    n_tok, k = ids.shape
+    in_dim = x.shape[1]
+    out = torch.empty((n_tok * k, out_dim), dtype=torch.float32, device=x.device)
+    _check(q8_kq_moe_matmul(out, W_experts, fmt, n_expert, expert_stride, ids, k, in_dim, out_dim, x,
+                            int(x_per_pair), n_tok), "q8_kq_moe_matmul")
     return out

@@ -768,6 +768,167 @@ int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_d
     return status_of(q8::launch_combine(out, y, expert_weights, n_tok, k, out_dim, s->num_sms, st));
 }
 
+// ---- second weight format: K-quant blocks against Q8_K activations
+
+static uint64_t kq_block_bytes(int fmt) {
+    return fmt == Q8_KQ_Q2_K ? 84u : (fmt == Q8_KQ_Q4_K ? 144u : 0u);
+}
+
+uint64_t q8_kq_row_bytes(uint64_t in_dim, int fmt) {
+    const uint64_t bb = kq_block_bytes(fmt);
+    if (!bb || in_dim == 0 || in_dim % 256 || in_dim > ((uint64_t)1 << 40)) return 0;
+    return in_dim / 256 * bb;
+}
+
+// Dimensions of a K-quant product with n_rows activation rows.
+static int check_kq(int fmt, uint64_t in_dim, uint64_t out_dim, uint64_t n_rows) {
+    if (!kq_block_bytes(fmt) || in_dim == 0 || in_dim % 256 || in_dim > ((uint64_t)1 << 40)) return Q8_EINVAL;
+    if (out_dim > ((uint64_t)1 << 31) || (out_dim && in_dim / 256 > (((uint64_t)1 << 62) / 144) / out_dim))
+        return Q8_EINVAL;
+    if (n_rows && in_dim > ((uint64_t)1 << 40) / n_rows) return Q8_EINVAL;
+    return Q8_OK;
+}
+
+static size_t q8k_planes_bytes(uint64_t rows, uint64_t in_dim) {
+    return align256(rows * in_dim) + align256(rows * (in_dim / 256) * 4) + align256(rows * (in_dim / 16) * 2);
+}
+
+struct Q8kPlanes {
+    int8_t *qx;
+    float *dx;
+    int16_t *xs;
+};
+
+static Q8kPlanes take_q8k_planes(Carver &cv, uint64_t rows, uint64_t in_dim) {
+    Q8kPlanes q;
+    q.qx = cv.take<int8_t>(rows * in_dim);
+    q.dx = cv.take<float>(rows * (in_dim / 256) * 4);
+    q.xs = cv.take<int16_t>(rows * (in_dim / 16) * 2);
+    return q;
+}
+
+// Rows per GEMV work item: a multiple of the CTA's 8 warps, 8..64, about four
+// items per CTA slot (4 CTAs per SM) when the rows allow.
+static uint32_t kq_rows_per_item(uint64_t out_dim, uint64_t groups, int num_sms) {
+    uint64_t want = (out_dim * groups + (uint64_t)num_sms * 16 - 1) / ((uint64_t)num_sms * 16);
+    want = (want + 7) & ~(uint64_t)7;
+    if (want < 8) want = 8;
+    if (want > 64) want = 64;
+    return (uint32_t)want;
+}
+
+int q8_quantize_q8k(void *xq, const float *x, uint64_t in_dim, uint64_t n_tok, void *stream) {
+    int rc = check_kq(Q8_KQ_Q4_K, in_dim, 1, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0) return Q8_OK;
+    if (!xq || !x) return Q8_EINVAL;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(xq) & 3u)) return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    return status_of(q8::launch_quantize_q8k(nullptr, nullptr, nullptr, static_cast<uint8_t *>(xq), x, in_dim, n_tok,
+                                             s->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_kq_matmul(float *out, const void *W, int fmt, uint64_t in_dim, uint64_t out_dim, const float *x,
+                 uint64_t n_tok, void *stream) {
+    int rc = check_kq(fmt, in_dim, out_dim, n_tok);
+    if (rc) return rc;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W || !x) return Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(x) ||
+        (reinterpret_cast<uintptr_t>(W) & (fmt == Q8_KQ_Q4_K ? 15u : 3u)))
+        return Q8_EALIGN;
+    if (n_tok > ((uint64_t)1 << 31) - 1) return Q8_EINVAL;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = reserve_scratch(s, q8k_planes_bytes(n_tok, in_dim)))) return rc;
+    Carver cv(s->scratch);
+    const Q8kPlanes q = take_q8k_planes(cv, n_tok, in_dim);
+    cudaError_t e = q8::launch_quantize_q8k(q.qx, q.dx, q.xs, nullptr, x, in_dim, n_tok, s->num_sms, st);
+    if (e != cudaSuccess) return status_of(e);
+    const int tokg = n_tok <= 8 ? 8 : 16;
+    q8::KqParams p{};
+    p.W = static_cast<const uint8_t *>(W);
+    p.in_dim = in_dim;
+    p.out_dim = (uint32_t)out_dim;
+    p.nsb = (uint32_t)(in_dim / 256);
+    p.fmt = fmt;
+    p.qx = q.qx;
+    p.dx = q.dx;
+    p.xs = q.xs;
+    p.out = out;
+    p.err = s->err;
+    p.n_tok = (uint32_t)n_tok;
+    p.rows_per_item = kq_rows_per_item(out_dim, (n_tok + tokg - 1) / tokg, s->num_sms);
+    return status_of(timed_launch(st, [&] { return q8::launch_kq_gemv(p, tokg, s->num_sms, st); }));
+}
+
+int q8_kq_moe_matmul(float *out, const void *W_experts, int fmt, uint32_t n_expert, uint64_t expert_stride_bytes,
+                     const int32_t *expert_ids, uint32_t k, uint64_t in_dim, uint64_t out_dim, const float *x,
+                     int x_per_pair, uint64_t n_tok, void *stream) {
+    if (n_expert == 0 || n_expert > MAX_EXPERTS || k == 0 || k > n_expert) return Q8_EINVAL;
+    if (n_tok > (((uint64_t)1 << 31) - 1) / k) return Q8_EINVAL;
+    const uint64_t n_pairs = n_tok * k, x_rows = x_per_pair ? n_pairs : n_tok;
+    int rc = check_kq(fmt, in_dim, out_dim, x_rows);
+    if (rc) return rc;
+    if (expert_stride_bytes < out_dim * q8_kq_row_bytes(in_dim, fmt)) return Q8_EINVAL;
+    if (n_tok == 0 || out_dim == 0) return Q8_OK;
+    if (!out || !W_experts || !expert_ids || !x) return Q8_EINVAL;
+    const uintptr_t wmask = fmt == Q8_KQ_Q4_K ? 15u : 3u;
+    if (!aligned16(out) || !aligned16(x) || (reinterpret_cast<uintptr_t>(W_experts) & wmask) ||
+        (expert_stride_bytes & wmask) || (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
+        return Q8_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState *s;
+    if ((rc = get_device(&s))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t max_rows = q8::route_max_rows(n_pairs, n_expert);
+    const size_t plan_bytes = q8::route_plan_bytes(n_expert);
+    const size_t need = align256(n_expert * 4) * 2 + q8::ROUTE_CLASSES * align256(plan_bytes) +
+                        align256(max_rows * 4) * 2 + q8k_planes_bytes(x_rows, in_dim);
+    if ((rc = reserve_scratch(s, need))) return rc;
+    Carver cv(s->scratch);
+    int32_t *counts = cv.take<int32_t>(n_expert * 4);
+    int32_t *row0_of = cv.take<int32_t>(n_expert * 4);
+    uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * plan_bytes);
+    int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
+    int32_t *src_row = cv.take<int32_t>(max_rows * 4);
+    const Q8kPlanes q = take_q8k_planes(cv, x_rows, in_dim);
+    const uint32_t rows_item = 32;   // an expert of 2048 rows: 64 items per token group
+    cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_item, 0,
+                                     counts, row0_of, plans, row_to_out, src_row, nullptr, max_rows, out, s->err,
+                                     s->num_sms, st);
+    if (e != cudaSuccess) return status_of(e);
+    if ((e = q8::launch_quantize_q8k(q.qx, q.dx, q.xs, nullptr, x, in_dim, x_rows, s->num_sms, st)) != cudaSuccess)
+        return status_of(e);
+    q8::KqParams p{};
+    p.W = static_cast<const uint8_t *>(W_experts);
+    p.expert_stride = expert_stride_bytes;
+    p.in_dim = in_dim;
+    p.out_dim = (uint32_t)out_dim;
+    p.nsb = (uint32_t)(in_dim / 256);
+    p.fmt = fmt;
+    p.qx = q.qx;
+    p.dx = q.dx;
+    p.xs = q.xs;
+    p.out = out;
+    p.err = s->err;
+    p.rows_per_item = rows_item;
+    p.src_row = src_row;
+    p.row_to_out = row_to_out;
+    return status_of(timed_launch(st, [&] {
+        for (int cls = 0; cls < q8::ROUTE_GEMV_CLASSES; ++cls) {
+            p.plan = reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes);
+            cudaError_t e2 = q8::launch_kq_gemv(p, cls == 0 ? 8 : 16, s->num_sms, st);
+            if (e2 != cudaSuccess) return e2;
+        }
+        return cudaSuccess;
+    }));
+}
+
 uint64_t q8_repack_bytes(uint64_t in_dim, uint64_t rows, int layout) {
     if (in_dim == 0 || in_dim % q8::QK || check_dims(in_dim, rows, 1)) return 0;
     const uint64_t nb = in_dim / q8::QK;

@@ -187,6 +187,38 @@ struct TcParams {
     uint64_t wait_ns;
     int withhold;
 };
+// Second weight format (q8_kq.cu): Q2_K / Q4_K rows against Q8_K activation
+// planes (quants [rows][in_dim], fp32 scales [rows][in_dim/256], int16 sums of
+// each 16 quants [rows][in_dim/16]).  Dense: tokens 0..n_tok-1, work items of
+// rows_per_item rows x one token group.  Routed: the items of one GEMV-class
+// routing plan (token groups of 8 for class 0, 16 for class 1); plane row i
+// reads activation row src_row[i] and writes output row row_to_out[i].
+constexpr int KQ_Q2 = 2, KQ_Q4 = 4;
+struct KqParams {
+    const uint8_t *W;
+    uint64_t expert_stride;
+    uint64_t in_dim;
+    uint32_t out_dim;
+    uint32_t nsb;              // blocks per row (in_dim / 256)
+    int fmt;                   // KQ_Q2 or KQ_Q4
+    const int8_t *qx;
+    const float *dx;
+    const int16_t *xs;
+    float *out;                // [rows][out_dim]
+    int *err;
+    uint32_t n_tok;            // dense
+    uint32_t rows_per_item;
+    const PlanHeader *plan;    // routed: class plan; nullptr: dense
+    const int32_t *src_row;
+    const int32_t *row_to_out;
+};
+// x [n_rows][in_dim] -> the planes (qx, dx, xs; all or none) and/or canonical
+// 292-byte Q8_K blocks (fp32 d, int8 qs[256], int16 sums of each 16 quants).
+cudaError_t launch_quantize_q8k(int8_t *qx, float *dx, int16_t *xs, uint8_t *blocks, const float *x, uint64_t in_dim,
+                                uint64_t n_rows, int num_sms, cudaStream_t st);
+// tokg: 8 or 16 (the token group of the plan's class; dense: either).
+cudaError_t launch_kq_gemv(const KqParams &p, int tokg, int num_sms, cudaStream_t st);
+
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
                              int num_sms, cudaStream_t st);
 // n_rows_b: rows of the b16 plane (the tensor map's extent).  Dense only.

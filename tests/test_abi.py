@@ -21,7 +21,7 @@ def declared_functions():
     with open(os.path.join(ROOT, "include", "q8.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(q8_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(q8_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -179,3 +179,35 @@ def test_elementwise_and_norm_argument_checks(q8):
         assert L.q8_swiglu(A, A, A, 8, 1.0, None) == q8.Q8_ECUDA
         assert L.q8_moe_combine(A, A, A, 2, 2, 8, None) == q8.Q8_ECUDA
         assert L.q8_rmsnorm_quantize(A, 0, B, 0, 64, 2, 1e-6, None) == q8.Q8_ECUDA
+
+
+def test_kquant_argument_checks(q8):
+    """The second weight format's entry points: bad formats, dimensions, strides and alignments are
+    rejected on the host; empty work is a no-op."""
+    L = q8.lib
+    assert q8.q8_kq_row_bytes(512, q8.Q8_KQ_Q2_K) == 2 * 84 and q8.q8_kq_row_bytes(512, q8.Q8_KQ_Q4_K) == 2 * 144
+    assert q8.q8_kq_row_bytes(512, 3) == 0 and q8.q8_kq_row_bytes(320, q8.Q8_KQ_Q4_K) == 0
+    for fmt in (0, 3, 8):
+        assert L.q8_kq_matmul(A, B, fmt, 512, 8, A, 1, None) == q8.Q8_EINVAL
+    for in_dim in (0, 32, 128, 320):
+        assert L.q8_kq_matmul(A, B, q8.Q8_KQ_Q4_K, in_dim, 8, A, 1, None) == q8.Q8_EINVAL
+        assert L.q8_quantize_q8k(A, B, in_dim, 1, None) == q8.Q8_EINVAL
+    assert L.q8_kq_matmul(A, B + 4, q8.Q8_KQ_Q4_K, 512, 8, A, 1, None) == q8.Q8_EALIGN   # Q4_K rows: 16 bytes
+    assert L.q8_kq_matmul(A, B + 2, q8.Q8_KQ_Q2_K, 512, 8, A, 1, None) == q8.Q8_EALIGN   # Q2_K rows: 4 bytes
+    assert L.q8_kq_matmul(A, B, q8.Q8_KQ_Q4_K, 512, 8, A + 8, 1, None) == q8.Q8_EALIGN   # x
+    assert L.q8_quantize_q8k(A + 2, B, 512, 1, None) == q8.Q8_EALIGN
+    assert L.q8_kq_matmul(A, B, q8.Q8_KQ_Q4_K, 512, 8, A, 0, None) == q8.Q8_OK
+    assert L.q8_kq_matmul(A, B, q8.Q8_KQ_Q4_K, 512, 0, A, 3, None) == q8.Q8_OK
+    assert L.q8_quantize_q8k(A, B, 512, 0, None) == q8.Q8_OK
+    stride = 8 * 2 * 144
+    m = L.q8_kq_moe_matmul
+    assert m(A, B, q8.Q8_KQ_Q4_K, 0, stride, A, 1, 512, 8, A, 0, 1, None) == q8.Q8_EINVAL       # no experts
+    assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride, A, 5, 512, 8, A, 0, 1, None) == q8.Q8_EINVAL       # k > n_expert
+    assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride - 16, A, 2, 512, 8, A, 0, 1, None) == q8.Q8_EINVAL  # stride too small
+    assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride + 4, A, 2, 512, 8, A, 0, 1, None) == q8.Q8_EALIGN   # stride % 16
+    assert m(A, B, q8.Q8_KQ_Q2_K, 4, 8 * 2 * 84 + 2, A, 2, 512, 8, A, 0, 1, None) == q8.Q8_EALIGN   # stride % 4
+    assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride, A + 2, 2, 512, 8, A, 0, 1, None) == q8.Q8_EALIGN   # ids
+    assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride, A, 2, 512, 8, A, 0, 0, None) == q8.Q8_OK
+    if _no_gpu():
+        assert L.q8_kq_matmul(A, B, q8.Q8_KQ_Q2_K, 512, 8, A, 1, None) == q8.Q8_ECUDA
+        assert m(A, B, q8.Q8_KQ_Q4_K, 4, stride, A, 2, 512, 8, A, 0, 1, None) == q8.Q8_ECUDA
