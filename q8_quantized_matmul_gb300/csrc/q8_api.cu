@@ -850,6 +850,7 @@ int q8_kq_matmul(float *out, const void *W, int fmt, uint64_t in_dim, uint64_t o
     cudaError_t e = q8::launch_quantize_q8k(q.qx, q.dx, q.xs, nullptr, x, in_dim, n_tok, s->num_sms, st);
     if (e != cudaSuccess) return status_of(e);
     const int tokg = n_tok <= 8 ? 8 : 16;
+    const uint32_t stream_rows = aligned16(W) ? q8::kq_stream_rows(q8_kq_row_bytes(in_dim, fmt), in_dim, tokg) : 0;
     q8::KqParams p{};
     p.W = static_cast<const uint8_t *>(W);
     p.in_dim = in_dim;
@@ -862,6 +863,10 @@ int q8_kq_matmul(float *out, const void *W, int fmt, uint64_t in_dim, uint64_t o
     p.out = out;
     p.err = s->err;
     p.n_tok = (uint32_t)n_tok;
+    if (stream_rows) {   // weights staged through shared memory by bulk copies
+        p.rows_per_item = stream_rows;
+        return status_of(timed_launch(st, [&] { return q8::launch_kq_stream(p, tokg, s->num_sms, st); }));
+    }
     p.rows_per_item = kq_rows_per_item(out_dim, (n_tok + tokg - 1) / tokg, s->num_sms);
     return status_of(timed_launch(st, [&] { return q8::launch_kq_gemv(p, tokg, s->num_sms, st); }));
 }
@@ -897,7 +902,12 @@ int q8_kq_moe_matmul(float *out, const void *W_experts, int fmt, uint32_t n_expe
     int32_t *row_to_out = cv.take<int32_t>(max_rows * 4);
     int32_t *src_row = cv.take<int32_t>(max_rows * 4);
     const Q8kPlanes q = take_q8k_planes(cv, x_rows, in_dim);
-    const uint32_t rows_item = 32;   // an expert of 2048 rows: 64 items per token group
+    // staged kernel when rows, matrix and stride are 16-byte multiples: items of its
+    // rows per slot; else the direct kernel, items of 32 rows
+    const uint32_t stream_rows = aligned16(W_experts) && (expert_stride_bytes & 15u) == 0
+                                     ? q8::kq_stream_rows(q8_kq_row_bytes(in_dim, fmt), in_dim, 16)
+                                     : 0;
+    const uint32_t rows_item = stream_rows ? stream_rows : 32;
     cudaError_t e = q8::launch_route(expert_ids, n_tok, k, n_expert, x_per_pair, (uint32_t)out_dim, rows_item, 0,
                                      counts, row0_of, plans, row_to_out, src_row, nullptr, max_rows, out, s->err,
                                      s->num_sms, st);
@@ -922,7 +932,8 @@ int q8_kq_moe_matmul(float *out, const void *W_experts, int fmt, uint32_t n_expe
     return status_of(timed_launch(st, [&] {
         for (int cls = 0; cls < q8::ROUTE_GEMV_CLASSES; ++cls) {
             p.plan = reinterpret_cast<const q8::PlanHeader *>(plans + cls * plan_bytes);
-            cudaError_t e2 = q8::launch_kq_gemv(p, cls == 0 ? 8 : 16, s->num_sms, st);
+            cudaError_t e2 = stream_rows ? q8::launch_kq_stream(p, cls == 0 ? 8 : 16, s->num_sms, st)
+                                         : q8::launch_kq_gemv(p, cls == 0 ? 8 : 16, s->num_sms, st);
             if (e2 != cudaSuccess) return e2;
         }
         return cudaSuccess;

@@ -218,6 +218,13 @@ cudaError_t launch_quantize_q8k(int8_t *qx, float *dx, int16_t *xs, uint8_t *blo
                                 uint64_t n_rows, int num_sms, cudaStream_t st);
 // tokg: 8 or 16 (the token group of the plan's class; dense: either).
 cudaError_t launch_kq_gemv(const KqParams &p, int tokg, int num_sms, cudaStream_t st);
+// The staged variant (weights through a shared-memory ring by bulk copies).
+// kq_stream_rows: rows per work item it takes for rows of row_bytes and token
+// groups of tokg (0: rows not 16-byte multiples, or the rows or the group's
+// activations too long: use launch_kq_gemv).  W and the expert stride must be
+// 16-byte aligned; rows_per_item <= kq_stream_rows(row bytes, in_dim, tokg).
+uint32_t kq_stream_rows(uint64_t row_bytes, uint64_t in_dim, int tokg);
+cudaError_t launch_kq_stream(const KqParams &p, int tokg, int num_sms, cudaStream_t st);
 
 cudaError_t launch_tc_expand(__half *a16, float *dwT, const uint8_t *W, uint32_t rows, uint32_t nb, uint32_t m_ld,
                              int num_sms, cudaStream_t st);

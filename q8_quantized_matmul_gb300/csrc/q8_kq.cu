@@ -19,7 +19,8 @@
 //
 // The product (same page, section 4, fixed-point dot): per sub-block the exact
 // integers isum = sum q_w q_x (dp4a) and xsum = sum q_x, then in fp32
-// d_x * (d * (sc * isum) - dmin * (m * xsum)), summed over sub-blocks and blocks.
+// d_x * ((d * sc) * isum - (dmin * m) * xsum) (d * sc and dmin * m are exact in
+// fp32), summed over sub-blocks and blocks.
 // One lane takes one sub-block: Q4_K 8 lanes per block (4 blocks a warp pass),
 // Q2_K 16 lanes (2 blocks).  A warp owns a weight row, reads each block once for
 // all tokens of its group, and reduces its lanes' sums at the row's end.
@@ -100,12 +101,22 @@ struct KqItem {
     uint32_t r0, nrows;
 };
 
+// Work items are dealt to the CTAs in turn (item i to CTA i mod grid): routed
+// items are ordered by the experts' pair counts, so contiguous ranges would give
+// the first CTAs all the widest token groups.  The routing plan's segment table
+// is searched per item; CTAs copy it to shared memory when it fits.
+constexpr int KQ_SEG_CACHE = 1024;
+
+struct KqSegs {
+    const Segment *segs;   // shared-memory copy, or the plan's own table
+    int nseg, n_items;
+};
+
 template <int TOKG>
-__device__ __forceinline__ bool kq_item(const KqParams &p, int i, KqItem &it) {
+__device__ __forceinline__ bool kq_item_at(const KqParams &p, const KqSegs &sg, int i, KqItem &it) {
     const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
     if (!p.plan) {
-        const int n_tg = (int)((p.n_tok + TOKG - 1) / TOKG);
-        if (i >= n_rb * n_tg) return false;
+        if (i >= n_rb * (int)((p.n_tok + TOKG - 1) / TOKG)) return false;
         const int tg = i / n_rb, rb = i - tg * n_rb;
         it.expert = 0;
         it.xrow0 = tg * TOKG;
@@ -114,15 +125,14 @@ __device__ __forceinline__ bool kq_item(const KqParams &p, int i, KqItem &it) {
         it.nrows = min(p.rows_per_item, p.out_dim - it.r0);
         return true;
     }
-    if (i >= p.plan->n_items) return false;
-    const Segment *segs = reinterpret_cast<const Segment *>(p.plan + 1);
-    int lo = 0, hi = p.plan->n_segments - 1;
+    if (i >= sg.n_items) return false;
+    int lo = 0, hi = sg.nseg - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (segs[mid].item_start <= i) lo = mid;
+        if (sg.segs[mid].item_start <= i) lo = mid;
         else hi = mid - 1;
     }
-    const Segment s = segs[lo];
+    const Segment s = sg.segs[lo];
     const int local = i - s.item_start;
     const int tg = local / n_rb, rb = local - tg * n_rb;
     it.expert = s.expert;
@@ -133,12 +143,25 @@ __device__ __forceinline__ bool kq_item(const KqParams &p, int i, KqItem &it) {
     return true;
 }
 
-__device__ __forceinline__ float f16_bits(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu))); }
-
-__device__ __forceinline__ uint32_t byte_of(uint32_t w0, uint32_t w1, uint32_t w2, int k) {
-    const uint32_t w = k < 4 ? w0 : (k < 8 ? w1 : w2);
-    return (w >> (8 * (k & 3))) & 0xffu;
+// The segment table for kq_item_at: copied into cache (KQ_SEG_CACHE entries of
+// shared memory) by threads [0, nthreads) when it fits; the caller synchronises
+// those threads before the first lookup.
+__device__ __forceinline__ KqSegs kq_segs(const KqParams &p, Segment *cache, int tid, int nthreads) {
+    KqSegs sg{nullptr, 0, 0};
+    if (!p.plan) return sg;
+    const Segment *g = reinterpret_cast<const Segment *>(p.plan + 1);
+    sg.nseg = p.plan->n_segments;
+    sg.n_items = p.plan->n_items;
+    if (sg.nseg <= KQ_SEG_CACHE) {
+        for (int e = tid; e < sg.nseg; e += nthreads) cache[e] = g[e];
+        sg.segs = cache;
+    } else {
+        sg.segs = g;
+    }
+    return sg;
 }
+
+__device__ __forceinline__ float f16_bits(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu))); }
 
 // This lane's sub-block of one block: 8 (Q4_K) or 4 (Q2_K) words of quants,
 // each byte one weight of the 4 activations in the matching word of x, with
@@ -148,80 +171,118 @@ template <int FMT> struct SubBlock {
     uint32_t q[WORDS];
     int sc, m;
     float d, dmin;
+    float fd, fm;    // d * sc and dmin * m (exact: products of an 11-bit and a 6-bit significand)
     uint32_t xoff;   // offset of the sub-block's first value within the block
     uint32_t grp;    // first 16-value group of the sub-block within the block
 };
 
+// The words of a block this lane's sub-block needs, as loaded (all loads of a
+// row's passes are issued before any is decoded).
+template <int FMT> struct RawSub {
+    static constexpr int N = FMT == KQ_Q4 ? 12 : 6;
+    uint32_t w[N];
+};
+
 template <int FMT>
-__device__ __forceinline__ void load_sub(SubBlock<FMT> &u, const uint8_t *blk, int sub) {
+__device__ __forceinline__ void load_raw(RawSub<FMT> &r, const uint8_t *blk, int sub) {
     if constexpr (FMT == KQ_Q4) {
-        const uint4 h = __ldg(reinterpret_cast<const uint4 *>(blk));
-        u.d = f16_bits(h.x);
-        u.dmin = f16_bits(h.x >> 16);
-        const int j = sub;
-        if (j < 4) {
-            u.sc = (int)(byte_of(h.y, h.z, h.w, j) & 63u);
-            u.m = (int)(byte_of(h.y, h.z, h.w, j + 4) & 63u);
-        } else {
-            u.sc = (int)((byte_of(h.y, h.z, h.w, j + 4) & 15u) | ((byte_of(h.y, h.z, h.w, j - 4) >> 6) << 4));
-            u.m = (int)((byte_of(h.y, h.z, h.w, j + 4) >> 4) | ((byte_of(h.y, h.z, h.w, j) >> 6) << 4));
-        }
-        const int c = j >> 1, hi = j & 1;
-        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+        const uint4 h = __ldg(reinterpret_cast<const uint4 *>(blk));       // d, dmin, scales[12]
+        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (sub >> 1));
         const uint4 a = __ldg(qs), b = __ldg(qs + 1);
-        const uint32_t raw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) u.q[k] = (raw[k] >> (4 * hi)) & 0x0f0f0f0fu;
-        u.xoff = 64u * c + 32u * hi;
-        u.grp = 4u * c + 2u * hi;
+        r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
+        r.w[4] = a.x; r.w[5] = a.y; r.w[6] = a.z; r.w[7] = a.w;
+        r.w[8] = b.x; r.w[9] = b.y; r.w[10] = b.z; r.w[11] = b.w;
     } else {
-        const int sb = sub, h = sb >> 3, j = (sb >> 1) & 3, s = sb & 1;
-        const uint32_t sw = __ldg(reinterpret_cast<const uint32_t *>(blk) + (sb >> 2));
-        const uint32_t sbyte = (sw >> (8 * (sb & 3))) & 0xffu;
-        u.sc = (int)(sbyte & 15u);
-        u.m = (int)(sbyte >> 4);
-        const uint32_t dd = __ldg(reinterpret_cast<const uint32_t *>(blk + 80));
-        u.d = f16_bits(dd);
-        u.dmin = f16_bits(dd >> 16);
+        const int sb = sub, h = sb >> 3, s = sb & 1;
         const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + 16 * s);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) u.q[k] = (__ldg(qs + k) >> (2 * j)) & 0x03030303u;
+        for (int k = 0; k < 4; ++k) r.w[k] = __ldg(qs + k);
+        r.w[4] = __ldg(reinterpret_cast<const uint32_t *>(blk) + (sb >> 2));   // its scale byte
+        r.w[5] = __ldg(reinterpret_cast<const uint32_t *>(blk + 80));          // d, dmin
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ void decode_sub(SubBlock<FMT> &u, const RawSub<FMT> &r, int sub) {
+    if constexpr (FMT == KQ_Q4) {
+        u.d = f16_bits(r.w[0]);
+        u.dmin = f16_bits(r.w[0] >> 16);
+        // scales[0..3] in w[1], [4..7] in w[2], [8..11] in w[3]; byte (j & 3) of each
+        const int j = sub;
+        const uint32_t sh = 8u * (uint32_t)(j & 3);
+        const uint32_t lo_sc = (r.w[1] >> sh) & 63u, lo_m = (r.w[2] >> sh) & 63u;
+        const uint32_t hi_sc = ((r.w[3] >> sh) & 15u) | (((r.w[1] >> (sh + 6)) & 3u) << 4);
+        const uint32_t hi_m = ((r.w[3] >> (sh + 4)) & 15u) | (((r.w[2] >> (sh + 6)) & 3u) << 4);
+        u.sc = (int)(j < 4 ? lo_sc : hi_sc);
+        u.m = (int)(j < 4 ? lo_m : hi_m);
+        const int c = j >> 1, hi = j & 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) u.q[k] = (r.w[4 + k] >> (4 * hi)) & 0x0f0f0f0fu;
+        u.xoff = 64u * c + 32u * hi;
+        u.grp = 4u * c + 2u * hi;
+        u.fd = u.d * (float)u.sc;
+        u.fm = u.dmin * (float)u.m;
+    } else {
+        const int sb = sub, h = sb >> 3, j = (sb >> 1) & 3, s = sb & 1;
+        const uint32_t sbyte = (r.w[4] >> (8 * (sb & 3))) & 0xffu;
+        u.sc = (int)(sbyte & 15u);
+        u.m = (int)(sbyte >> 4);
+        u.d = f16_bits(r.w[5]);
+        u.dmin = f16_bits(r.w[5] >> 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) u.q[k] = (r.w[k] >> (2 * j)) & 0x03030303u;
         u.xoff = 128u * h + 32u * j + 16u * s;
         u.grp = (uint32_t)sb;
+        u.fd = u.d * (float)u.sc;
+        u.fm = u.dmin * (float)u.m;
     }
 }
 
 template <int FMT, int TOKG>
-__global__ void __launch_bounds__(kq::THREADS) k_kq_gemv(const KqParams p) {
+__global__ void __launch_bounds__(kq::THREADS, 2) k_kq_gemv(const KqParams p) {
     constexpr int LPB = FMT == KQ_Q4 ? 8 : 16;   // lanes per block, one sub-block each
     constexpr int BPP = 32 / LPB;                 // blocks per warp pass
     constexpr int BB = FMT == KQ_Q4 ? 144 : 84;   // bytes per block
+    constexpr int U = FMT == KQ_Q4 ? 4 : 8;       // warp passes whose loads are issued together
     using SB = SubBlock<FMT>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane % LPB, bsel = lane / LPB;
     const uint32_t nsb = p.nsb;
     const uint64_t row_bytes = (uint64_t)nsb * BB;
     const uint64_t in_dim = p.in_dim;
+    __shared__ int arow[TOKG], orow[TOKG];   // the item's activation and output rows
+    __shared__ Segment seg_cache[KQ_SEG_CACHE];
+    const KqSegs sg = kq_segs(p, seg_cache, threadIdx.x, kq::THREADS);
+    __syncthreads();
     KqItem it;
-    for (int i = blockIdx.x; kq_item<TOKG>(p, i, it); i += gridDim.x) {
-        int arow[TOKG], orow[TOKG];
-#pragma unroll
-        for (int t = 0; t < TOKG; ++t) {
+    for (int i = blockIdx.x; kq_item_at<TOKG>(p, sg, i, it); i += gridDim.x) {
+        __syncthreads();   // every warp is done with the previous item's rows
+        if (threadIdx.x < TOKG) {
+            const int t = threadIdx.x;
             const bool on = t < it.ntok;
             arow[t] = !on ? 0 : (p.plan ? p.src_row[it.xrow0 + t] : it.xrow0 + t);
             orow[t] = !on ? -1 : (p.plan ? p.row_to_out[it.xrow0 + t] : it.xrow0 + t);
         }
+        __syncthreads();
         const uint8_t *wmat = p.W + (uint64_t)it.expert * p.expert_stride;
         for (uint32_t r = it.r0 + warp; r < it.r0 + it.nrows; r += kq::WARPS) {
             const uint8_t *wrow = wmat + (uint64_t)r * row_bytes;
             float acc[TOKG];
 #pragma unroll
             for (int t = 0; t < TOKG; ++t) acc[t] = 0.0f;
-            for (uint32_t b0 = 0; b0 < nsb; b0 += BPP) {
-                const uint32_t b = b0 + bsel;
+            for (uint32_t b0 = 0; b0 < nsb; b0 += BPP * U) {
+                RawSub<FMT> raw[U];
+#pragma unroll
+                for (int v = 0; v < U; ++v) {
+                    const uint32_t b = b0 + (uint32_t)(v * BPP + bsel);
+                    if (b < nsb) load_raw<FMT>(raw[v], wrow + (uint64_t)b * BB, sub);
+                }
+#pragma unroll
+                for (int v = 0; v < U; ++v) {
+                const uint32_t b = b0 + (uint32_t)(v * BPP + bsel);
                 if (b >= nsb) continue;
                 SB u;
-                load_sub<FMT>(u, wrow + (uint64_t)b * BB, sub);
+                decode_sub<FMT>(u, raw[v], sub);
 #pragma unroll
                 for (int t = 0; t < TOKG; ++t) {
                     if (t >= it.ntok) break;
@@ -251,7 +312,8 @@ __global__ void __launch_bounds__(kq::THREADS) k_kq_gemv(const KqParams p) {
                         xsum = (int)__ldg(p.xs + xr * (in_dim / 16) + (uint64_t)b * 16 + u.grp);
                     }
                     const float dxv = __ldg(p.dx + xr * nsb + b);
-                    acc[t] += dxv * (u.d * (float)(u.sc * isum) - u.dmin * (float)(u.m * xsum));
+                    acc[t] = fmaf(dxv, fmaf(-u.fm, (float)xsum, u.fd * (float)isum), acc[t]);
+                }
                 }
             }
             float mine = 0.0f;
@@ -264,14 +326,297 @@ __global__ void __launch_bounds__(kq::THREADS) k_kq_gemv(const KqParams p) {
                 if (lane == t) mine = v;
             }
             if (lane < it.ntok) {
-                int o = -1;
-#pragma unroll
-                for (int t = 0; t < TOKG; ++t)
-                    if (t == lane) o = orow[t];
+                const int o = orow[lane];
                 if (o >= 0) p.out[(uint64_t)o * p.out_dim + r] = mine;
             }
         }
     }
+}
+
+// ---------------------------------------------------------------- staged GEMV
+// The same product with the weights streamed through shared memory: a
+// producer warp copies each work item's rows (contiguous in the matrix) into
+// a ring of slots with one bulk asynchronous copy, and each of 16 consumer
+// warps takes one row of the slot.  Needs 16-byte aligned rows (row bytes, the
+// matrix and the expert stride multiples of 16) of at most SLOT_BYTES / 1.
+namespace kqs {
+constexpr int NCONS = 16;                        // consumer warps: one weight row each per item
+constexpr int THREADS = (NCONS + 1) * 32;
+constexpr uint32_t SLOT_BYTES = 40 * 1024;       // a work item's rows (at most 16)
+constexpr int CHUNK = 16;                        // consecutive items a CTA takes in turn
+// Shared-memory layout per token group size: ring slots, then the token
+// group's Q8_K planes (4864 bytes a token: in_dim up to 4096), then barriers.
+template <int TOKG> struct Layout {
+    static constexpr int NSLOT = TOKG == 8 ? 4 : 3;
+    static constexpr uint32_t ACT_BYTES = TOKG * 4864;
+    static constexpr size_t META_OFF = (size_t)NSLOT * SLOT_BYTES + ACT_BYTES;
+    static constexpr size_t SEG_OFF = META_OFF + 2 * NSLOT * 8 + 16 + NSLOT * 36 * 4 + 8;   // ... + act_bar
+    static constexpr size_t SMEM = SEG_OFF + KQ_SEG_CACHE * sizeof(Segment);
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+// Bytes of one token's staged activations: quants, fp32 scales, int16 sums of 16.
+__host__ __device__ constexpr uint64_t act_row_bytes(uint64_t in_dim) { return in_dim + in_dim / 64 + in_dim / 8; }
+}  // namespace kqs
+
+// This lane's words of a block in shared memory (plain loads: the read-only
+// global path must not be used on shared addresses).
+template <int FMT>
+__device__ __forceinline__ void load_raw_smem(RawSub<FMT> &r, const uint8_t *blk, int sub) {
+    if constexpr (FMT == KQ_Q4) {
+        const uint4 h = *reinterpret_cast<const uint4 *>(blk);
+        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (sub >> 1));
+        const uint4 a = qs[0], b = qs[1];
+        r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
+        r.w[4] = a.x; r.w[5] = a.y; r.w[6] = a.z; r.w[7] = a.w;
+        r.w[8] = b.x; r.w[9] = b.y; r.w[10] = b.z; r.w[11] = b.w;
+    } else {
+        const int sb = sub, h = sb >> 3, s = sb & 1;
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + 16 * s);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r.w[k] = qs[k];
+        r.w[4] = reinterpret_cast<const uint32_t *>(blk)[sb >> 2];
+        r.w[5] = *reinterpret_cast<const uint32_t *>(blk + 80);
+    }
+}
+
+// Per-slot description of its work item, written by the producer before the
+// slot's copy is armed (ntok < 0: no more items).  group identifies the token
+// group (its first plane row): consecutive items of one group share staged
+// activations.
+struct KqSlotMeta {
+    int ntok, group;
+    uint32_t r0, nrows;
+    int arow[16], orow[16];
+};
+
+template <int FMT, int TOKG>
+__global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p) {
+    using namespace kqs;
+    constexpr int NSLOT = Layout<TOKG>::NSLOT;
+    constexpr size_t META_OFF = Layout<TOKG>::META_OFF;
+    constexpr int LPB = FMT == KQ_Q4 ? 8 : 16;
+    constexpr int BPP = 32 / LPB;
+    constexpr int BB = FMT == KQ_Q4 ? 144 : 84;
+    using SB = SubBlock<FMT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *slots = smem;
+    uint8_t *act = smem + (size_t)NSLOT * SLOT_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + META_OFF);
+    uint64_t *empty = full + NSLOT;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NSLOT);
+    KqSlotMeta *meta = reinterpret_cast<KqSlotMeta *>(smem + META_OFF + 2 * NSLOT * 8 + 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCONS);
+        }
+        mbar_init(reinterpret_cast<uint64_t *>(meta + NSLOT), NCONS);   // act_bar
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t nsb = p.nsb;
+    const uint64_t row_bytes = (uint64_t)nsb * BB;
+    if (warp == NCONS) {
+        // ---------------- producer warp: item order, slot metadata, one bulk copy per item
+        uint32_t slot = 0, phase = 0;
+        uint32_t fills[NSLOT];
+        for (int s = 0; s < NSLOT; ++s) fills[s] = 0;
+        KqItem it;
+        Segment *seg_cache = reinterpret_cast<Segment *>(smem + Layout<TOKG>::SEG_OFF);
+        const KqSegs sg = kq_segs(p, seg_cache, lane, 32);
+        __syncwarp();
+        int group = -1, my_arow = 0, my_orow = -1;
+        bool more = true;
+        // chunks of consecutive items (one token group, mostly) dealt in turn: the
+        // staged activations change once per chunk; up to CHUNK items a chunk while
+        // every CTA still gets about four chunks
+        const int n_items = p.plan ? sg.n_items
+                                   : (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item) *
+                                         (int)((p.n_tok + TOKG - 1) / TOKG);
+        const int chunk = max(1, min(CHUNK, n_items / (4 * (int)gridDim.x)));
+        for (int k = 0; more; ++k) {
+            const int i = ((k / chunk) * (int)gridDim.x + (int)blockIdx.x) * chunk + k % chunk;
+            more = kq_item_at<TOKG>(p, sg, i, it);
+            // after an abort nothing more is issued; consumers release only the
+            // slots they saw land, so each slot has at most its last fill in flight
+            bool ok = false;
+            if (lane == 0) ok = mbar_wait(&empty[slot], phase ^ 1u, p.err, abort_flag) && !*abort_flag;
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+            if (!ok) break;
+            KqSlotMeta &m = meta[slot];
+            if (more && it.xrow0 != group) {   // a new token group: its rows (lane t: token t)
+                group = it.xrow0;
+                const bool on = lane < it.ntok;
+                my_arow = !on ? 0 : (p.plan ? p.src_row[it.xrow0 + lane] : it.xrow0 + lane);
+                my_orow = !on ? -1 : (p.plan ? p.row_to_out[it.xrow0 + lane] : it.xrow0 + lane);
+            }
+            if (lane < TOKG) {
+                m.arow[lane] = my_arow;
+                m.orow[lane] = more ? my_orow : -1;
+            }
+            if (lane == 0) {
+                m.ntok = more ? it.ntok : -1;
+                m.group = more ? it.xrow0 : -1;
+                m.r0 = more ? it.r0 : 0u;
+                m.nrows = more ? it.nrows : 0u;
+            }
+            __syncwarp();
+            // the item's bytes are armed first; then each row is one bulk copy, issued by
+            // one lane each so that the rows stream in parallel
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], more ? it.nrows * (uint32_t)row_bytes : 0u);
+            __syncwarp();
+            if (more && (uint32_t)lane < it.nrows)
+                bulk_g2s(slots + (size_t)slot * SLOT_BYTES + (size_t)lane * row_bytes,
+                         p.W + (uint64_t)it.expert * p.expert_stride + (uint64_t)(it.r0 + (uint32_t)lane) * row_bytes,
+                         (uint32_t)row_bytes, &full[slot]);
+            ++fills[slot];
+            if (++slot == NSLOT) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+        if (lane == 0)
+            for (int s = 0; s < NSLOT; ++s)   // every copy lands before the CTA exits
+                if (fills[s]) mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.err, nullptr);
+        return;
+    }
+    // ---------------- consumers: warp w takes row w of each item
+    // The token group's activations are staged in shared memory once per group:
+    // a bounded barrier (act_bar, two phases) first lets every warp finish the
+    // previous group, then every warp copies its share and arrives again.
+    const int sub = lane % LPB, bsel = lane / LPB;
+    const uint64_t in_dim = p.in_dim;
+    const uint32_t nxs = (uint32_t)(in_dim / 16);
+    int8_t *qx_s = reinterpret_cast<int8_t *>(act);
+    float *dx_s = reinterpret_cast<float *>(act + (size_t)TOKG * in_dim);
+    int16_t *xs_s = reinterpret_cast<int16_t *>(act + (size_t)TOKG * in_dim + (size_t)TOKG * nsb * 4);
+    uint64_t *act_bar = reinterpret_cast<uint64_t *>(meta + NSLOT);
+    const int ctid = warp * 32 + lane;
+    constexpr int CT = NCONS * 32;
+    int group = -1;
+    uint32_t slot = 0, phase = 0;
+    for (;;) {
+        // a consumer whose wait failed leaves (an abort); it hands no slot back
+        if (!mbar_wait(&full[slot], phase, p.err, abort_flag)) break;
+        const KqSlotMeta &m = meta[slot];
+        const int ntok = m.ntok;
+        if (ntok < 0) break;   // the end marker: its slot needs no release
+        if (m.group != group) {
+            group = m.group;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(act_bar);   // done with the previous group
+            if (!mbar_wait(act_bar, 0u, p.err, abort_flag)) break;
+            for (uint32_t e = (uint32_t)ctid; e < (uint32_t)ntok * nxs; e += CT) {
+                const uint32_t t = e / nxs, c = e - t * nxs;
+                reinterpret_cast<uint4 *>(qx_s + (size_t)t * in_dim)[c] =
+                    __ldg(reinterpret_cast<const uint4 *>(p.qx + (uint64_t)m.arow[t] * in_dim) + c);
+            }
+            for (uint32_t e = (uint32_t)ctid; e < (uint32_t)ntok * nsb; e += CT) {
+                const uint32_t t = e / nsb, c = e - t * nsb;
+                dx_s[t * nsb + c] = __ldg(p.dx + (uint64_t)m.arow[t] * nsb + c);
+            }
+            for (uint32_t e = (uint32_t)ctid; e < (uint32_t)ntok * (nxs / 2); e += CT) {
+                const uint32_t t = e / (nxs / 2), c = e - t * (nxs / 2);
+                reinterpret_cast<uint32_t *>(xs_s + (size_t)t * nxs)[c] =
+                    __ldg(reinterpret_cast<const uint32_t *>(p.xs + (uint64_t)m.arow[t] * nxs) + c);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(act_bar);   // this warp's share is staged
+            if (!mbar_wait(act_bar, 1u, p.err, abort_flag)) break;
+        }
+        if ((uint32_t)warp < m.nrows) {
+            const uint32_t r = m.r0 + (uint32_t)warp;
+            const uint8_t *wrow = slots + (size_t)slot * SLOT_BYTES + (size_t)warp * row_bytes;
+            float acc[TOKG];
+#pragma unroll
+            for (int t = 0; t < TOKG; ++t) acc[t] = 0.0f;
+            for (uint32_t b0 = 0; b0 < nsb; b0 += BPP) {
+                const uint32_t b = b0 + (uint32_t)bsel;
+                if (b >= nsb) continue;
+                RawSub<FMT> raw;
+                load_raw_smem<FMT>(raw, wrow + (size_t)b * BB, sub);
+                SB u;
+                decode_sub<FMT>(u, raw, sub);
+#pragma unroll
+                for (int t = 0; t < TOKG; ++t) {
+                    if (t >= ntok) break;
+                    const int8_t *xq = qx_s + (size_t)t * in_dim + (size_t)b * kq::QKK + u.xoff;
+                    int isum = 0, xsum;
+                    if constexpr (FMT == KQ_Q4) {
+                        const uint4 xa = reinterpret_cast<const uint4 *>(xq)[0];
+                        const uint4 xb = reinterpret_cast<const uint4 *>(xq)[1];
+                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
+                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
+                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
+                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
+                        isum = __dp4a((int)u.q[4], (int)xb.x, isum);
+                        isum = __dp4a((int)u.q[5], (int)xb.y, isum);
+                        isum = __dp4a((int)u.q[6], (int)xb.z, isum);
+                        isum = __dp4a((int)u.q[7], (int)xb.w, isum);
+                        const uint32_t s2 = *reinterpret_cast<const uint32_t *>(xs_s + (size_t)t * nxs + b * 16 + u.grp);
+                        xsum = (int)(int16_t)(s2 & 0xffffu) + (int)(int16_t)(s2 >> 16);
+                    } else {
+                        const uint4 xa = reinterpret_cast<const uint4 *>(xq)[0];
+                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
+                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
+                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
+                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
+                        xsum = (int)xs_s[(size_t)t * nxs + b * 16 + u.grp];
+                    }
+                    acc[t] = fmaf(dx_s[t * nsb + b], fmaf(-u.fm, (float)xsum, u.fd * (float)isum), acc[t]);
+                }
+            }
+            float mine = 0.0f;
+#pragma unroll
+            for (int t = 0; t < TOKG; ++t) {
+                if (t >= ntok) break;
+                float v = acc[t];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == t) mine = v;
+            }
+            if (lane < ntok) {
+                const int o = m.orow[lane];
+                if (o >= 0) p.out[(uint64_t)o * p.out_dim + r] = mine;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == NSLOT) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+uint32_t kq_stream_rows(uint64_t row_bytes, uint64_t in_dim, int tokg) {
+    if (row_bytes == 0 || row_bytes % 16 || row_bytes > kqs::SLOT_BYTES) return 0;
+    if (in_dim % 256 || kqs::act_row_bytes(in_dim) > 4864) return 0;
+    const uint64_t r = kqs::SLOT_BYTES / row_bytes;
+    return (uint32_t)(r < (uint64_t)kqs::NCONS ? r : (uint64_t)kqs::NCONS);
+}
+
+template <int FMT, int TOKG> static cudaError_t launch_stream(const KqParams &p, int num_sms, cudaStream_t st) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_kq_stream<FMT, TOKG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kqs::Layout<TOKG>::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    k_kq_stream<FMT, TOKG><<<num_sms, kqs::THREADS, kqs::Layout<TOKG>::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kq_stream(const KqParams &p, int tokg, int num_sms, cudaStream_t st) {
+    const uint64_t row_bytes = (uint64_t)p.nsb * (p.fmt == KQ_Q4 ? 144 : 84);
+    if (p.rows_per_item == 0 || p.rows_per_item > kq_stream_rows(row_bytes, p.in_dim, tokg))
+        return cudaErrorInvalidValue;
+    if (p.fmt == KQ_Q4) return tokg == 8 ? launch_stream<KQ_Q4, 8>(p, num_sms, st) : launch_stream<KQ_Q4, 16>(p, num_sms, st);
+    if (p.fmt == KQ_Q2) return tokg == 8 ? launch_stream<KQ_Q2, 8>(p, num_sms, st) : launch_stream<KQ_Q2, 16>(p, num_sms, st);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_kq_gemv(const KqParams &p, int tokg, int num_sms, cudaStream_t st) {

@@ -114,6 +114,23 @@ def test_kq_matmul_parity(q8, o, fmt, in_dim, out_dim, n_tok):
     assert_close(fetch(buf, n_tok * out_dim, (n_tok, out_dim)), ref, bound, f"kq{fmt} {in_dim}x{out_dim}x{n_tok}")
 
 
+def test_kq_matmul_direct_kernel_cases(q8, o):
+    """Rows the staged kernel does not take: Q2_K rows that are not 16-byte multiples (in_dim 1280), a
+    Q2_K matrix only 4-byte aligned, and Q4_K rows longer than a shared-memory slot (in_dim 73728)."""
+    cases = [(2, 1280, 50, 5, 0), (2, 1024, 40, 3, 4), (4, 73728, 6, 3, 0)]
+    for fmt, in_dim, out_dim, n_tok, offset in cases:
+        W = inputs.kq_weights(out_dim, in_dim, fmt, seed=in_dim + offset)
+        x = _acts(np.random.default_rng(in_dim), n_tok, in_dim)
+        ref, bound = o.kq_matmul(W, fmt, x, out_dim)
+        Wd = torch.zeros(W.nbytes + 16, dtype=torch.uint8, device=DEV)
+        Wd[offset:offset + W.nbytes] = dev(W.reshape(-1))
+        buf = poisoned(n_tok * out_dim)
+        rc = q8.q8_kq_matmul(buf, Wd.data_ptr() + offset, fmt, in_dim, out_dim, dev(x), n_tok)
+        assert rc == 0, q8.q8_strerror(rc)
+        assert q8.q8_last_error() == 0
+        assert_close(fetch(buf, n_tok * out_dim, (n_tok, out_dim)), ref, bound, f"kq{fmt} direct {in_dim}+{offset}")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_kq_matmul_decode_projection_full(q8, o, fmt):
     """A routed expert's gate projection, 4096 -> 2048, one token: every output."""
