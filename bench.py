@@ -521,6 +521,28 @@ def secondary(args, torch, q8, dev, stream, l2):
     assert q8.q8_last_error(stream) == 0
     torch.cuda.empty_cache()
 
+    # the second weight format on the same routing: Q4_K and Q2_K experts against Q8_K activations
+    for fmt, fname in ((q8.Q8_KQ_Q4_K, "Q4_K"), (q8.Q8_KQ_Q2_K, "Q2_K")):
+        for name, in_dim, out_dim, per_pair in (("gate/up", 4096, 2048, 0), ("down", 2048, 4096, 1)):
+            stride = out_dim * q8.q8_kq_row_bytes(in_dim, fmt)
+            W = torch.from_numpy(inputs.kq_weights(n_exp * out_dim, in_dim, fmt, seed=2).reshape(-1)).to(dev)
+            x = torch.from_numpy(inputs.normal((n_tok * k if per_pair else n_tok, in_dim), seed=2)).to(dev)
+            o = torch.empty((n_tok * k, out_dim), device=dev)
+            q8.q8_profile_arm(6)
+            ms = timed_eager(torch, stream, lambda i: q8.q8_kq_moe_matmul(o, W, fmt, n_exp, stride, idsd, k, in_dim,
+                                                                           out_dim, x, per_pair, n_tok, stream), 6)
+            kms = prof_mean(6)
+            q8.q8_profile_arm(0)
+            wb = touched * stride
+            out.append({"workload": f"routed {fname} experts {name}: 256 experts [{out_dim}x{in_dim}], Q8_K "
+                                    f"activations, n_tok 64, uniform top-6 ({touched} experts touched)",
+                        "ms_per_call": round(ms, 4), "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1),
+                        "kernel_ms": round(kms, 4), "kernel_weight_gbs": round(wb / (kms * 1e-3) / 1e9, 1),
+                        "kernel_frac_of_hbm_peak": round(wb / (kms * 1e-3) / 1e9 / hbm, 4)})
+            del W
+    assert q8.q8_last_error(stream) == 0
+    torch.cuda.empty_cache()
+
     # the routed expert FFN on the same routing: gate and up (one routing, one quantisation
     # of x), SwiGLU with clamp 10, down on the re-quantised mid, weighted sum of the 6 experts
     in_dim, mid_dim = 4096, 2048
