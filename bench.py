@@ -60,7 +60,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-case", choices=("decode1", "decode4", "decode16", "prefill", "prefill_long", "moe",
-                                               "moe_zipf", "moe_zipf_small", "moe_ffn", "rmsnorm"),
+                                               "moe_zipf", "moe_zipf_small", "moe_ffn", "rmsnorm", "kq_moe_q4k",
+                                               "kq_moe_q2k"),
                     help="run one workload's call a few times without timing (for ncu captures)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -899,6 +900,13 @@ def profile_case(case: str):
         W = torch.from_numpy(inputs.weights(256 * 2048, 4096, seed=2)).to(dev)
         x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
         fn = lambda: q8.moe_matmul(W, 256, 2048 * 128 * QB, ids, x, False, 2048)
+    elif case in ("kq_moe_q4k", "kq_moe_q2k"):   # routed K-quant experts, gate/up shape, 64 tokens, top-6
+        fmt = q8.Q8_KQ_Q4_K if case.endswith("q4k") else q8.Q8_KQ_Q2_K
+        ids = torch.from_numpy(inputs.route_uniform(64, 6, 256, seed=0)).to(dev)
+        W = torch.from_numpy(inputs.kq_weights(256 * 2048, 4096, fmt, seed=2).reshape(-1)).to(dev)
+        x = torch.from_numpy(inputs.normal((64, 4096), seed=2)).to(dev)
+        stride = 2048 * q8.q8_kq_row_bytes(4096, fmt)
+        fn = lambda: q8.kq_moe_matmul(W, fmt, 256, stride, ids, x, False, 2048)
     elif case == "rmsnorm":   # RMSNorm feeding the quantiser at the long-prefill input, 4096 x 4096
         x = torch.from_numpy(inputs.normal((4096, 4096), seed=6)).to(dev)
         gamma = torch.from_numpy((1.0 + 0.1 * np.random.default_rng(6).standard_normal(4096)).astype(np.float32)).to(dev)
