@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -609,6 +610,12 @@ def secondary(args, torch, q8, dev, stream, l2):
                 "per_call": rows,
                 "timing": "eager calls (quantise + expand + GEMM each), CUDA events, mean of 3"})
     torch.cuda.empty_cache()
+    # every line also as tokens per second: the tokens a call (or the slice) processes over its time
+    for d in out:
+        m = re.search(r"n_tok (\d+)|(\d+) tokens", d["workload"])
+        ms = d.get("ms_per_call", d.get("ms_per_slice", d.get("ms_per_call_packed")))
+        if m and ms:
+            d["tokens_per_s"] = round(int(m.group(1) or m.group(2)) / (ms * 1e-3), 1)
     return out
 
 
