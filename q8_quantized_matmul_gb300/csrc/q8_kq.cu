@@ -21,8 +21,9 @@
 // integers isum = sum q_w q_x (dp4a) and xsum = sum q_x, then in fp32
 // d_x * ((d * sc) * isum - (dmin * m) * xsum) (d * sc and dmin * m are exact in
 // fp32), summed over sub-blocks and blocks.
-// One lane takes one sub-block: Q4_K 8 lanes per block (4 blocks a warp pass),
-// Q2_K 16 lanes (2 blocks).  A warp owns a weight row, reads each block once for
+// One lane takes two sub-blocks of a block, whose scaled integer sums it adds
+// exactly before the fp32 step: Q4_K 4 lanes per block (8 blocks a warp pass),
+// Q2_K 8 lanes (4 blocks).  A warp owns a weight row, reads each block once for
 // all tokens of its group, and reduces its lanes' sums at the row's end.
 #include "q8_common.cuh"
 #include "q8_kernels.h"
@@ -163,90 +164,164 @@ __device__ __forceinline__ KqSegs kq_segs(const KqParams &p, Segment *cache, int
 
 __device__ __forceinline__ float f16_bits(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu))); }
 
-// This lane's sub-block of one block: 8 (Q4_K) or 4 (Q2_K) words of quants,
-// each byte one weight of the 4 activations in the matching word of x, with
-// the sub-block's scale, min and the block's d and dmin.
-template <int FMT> struct SubBlock {
-    static constexpr int WORDS = FMT == KQ_Q4 ? 8 : 4;
-    uint32_t q[WORDS];
-    int sc, m;
+// This lane's unit of one block: two sub-blocks.  Q4_K: chunk c (4 units a
+// block), the low and high nibbles of qs[32c .. 32c + 31], sub-blocks 2c and
+// 2c + 1, weights 64c .. 64c + 63.  Q2_K: unit 4h + j (8 units a block), field j
+// of qs[32h .. 32h + 31], sub-blocks 8h + 2j and 8h + 2j + 1, weights
+// 128h + 32j .. + 31.  q holds the weights one per byte (each word meets the
+// matching word of the activations), the first sub-block's words first.  The
+// two sub-blocks' scaled integer sums are combined exactly before the fp32 step.
+template <int FMT> struct Unit {
+    static constexpr int NW = FMT == KQ_Q4 ? 16 : 8;
+    uint32_t q[NW];
+    int sc0, sc1, m0, m1;
     float d, dmin;
-    float fd, fm;    // d * sc and dmin * m (exact: products of an 11-bit and a 6-bit significand)
-    uint32_t xoff;   // offset of the sub-block's first value within the block
-    uint32_t grp;    // first 16-value group of the sub-block within the block
 };
 
-// The words of a block this lane's sub-block needs, as loaded (all loads of a
-// row's passes are issued before any is decoded).
-template <int FMT> struct RawSub {
-    static constexpr int N = FMT == KQ_Q4 ? 12 : 6;
+// The words of a block this lane's unit needs, as loaded (all loads of a row's
+// passes are issued before any is decoded).
+template <int FMT> struct RawUnit {
+    static constexpr int N = FMT == KQ_Q4 ? 12 : 10;
     uint32_t w[N];
 };
 
-template <int FMT>
-__device__ __forceinline__ void load_raw(RawSub<FMT> &r, const uint8_t *blk, int sub) {
+template <int FMT> __host__ __device__ constexpr int units_per_block() { return FMT == KQ_Q4 ? 4 : 8; }
+
+// Offsets of a unit within its block: its first activation value and first
+// 16-value group of activation sums.
+template <int FMT> __device__ __forceinline__ uint32_t unit_xoff(int u) {
+    return FMT == KQ_Q4 ? 64u * (uint32_t)u : 128u * (uint32_t)(u >> 2) + 32u * (uint32_t)(u & 3);
+}
+template <int FMT> __device__ __forceinline__ uint32_t unit_grp(int u) {
+    return FMT == KQ_Q4 ? 4u * (uint32_t)u : 8u * (uint32_t)(u >> 2) + 2u * (uint32_t)(u & 3);
+}
+
+// SMEM: the block lies in shared memory (plain loads; the read-only global
+// path must not be used on shared addresses).
+template <int FMT, bool SMEM>
+__device__ __forceinline__ void load_raw(RawUnit<FMT> &r, const uint8_t *blk, int u) {
+    auto ld4 = [](const uint32_t *p) { return SMEM ? *p : __ldg(p); };
+    auto ld16 = [](const uint4 *p) { return SMEM ? *p : __ldg(p); };
     if constexpr (FMT == KQ_Q4) {
-        const uint4 h = __ldg(reinterpret_cast<const uint4 *>(blk));       // d, dmin, scales[12]
-        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (sub >> 1));
-        const uint4 a = __ldg(qs), b = __ldg(qs + 1);
+        const uint4 h = ld16(reinterpret_cast<const uint4 *>(blk));        // d, dmin, scales[12]
+        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * u);
+        const uint4 a = ld16(qs), b = ld16(qs + 1);
         r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
         r.w[4] = a.x; r.w[5] = a.y; r.w[6] = a.z; r.w[7] = a.w;
         r.w[8] = b.x; r.w[9] = b.y; r.w[10] = b.z; r.w[11] = b.w;
-    } else {
-        const int sb = sub, h = sb >> 3, s = sb & 1;
-        const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + 16 * s);
+    } else {   // Q2_K blocks are 4-byte aligned only
+        const int h = u >> 2, j = u & 3;
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) r.w[k] = __ldg(qs + k);
-        r.w[4] = __ldg(reinterpret_cast<const uint32_t *>(blk) + (sb >> 2));   // its scale byte
-        r.w[5] = __ldg(reinterpret_cast<const uint32_t *>(blk + 80));          // d, dmin
+        for (int k = 0; k < 8; ++k) r.w[k] = ld4(qs + k);
+        r.w[8] = ld4(reinterpret_cast<const uint32_t *>(blk) + 2 * h + (j >> 1));   // scales of 8h+2j, +1
+        r.w[9] = ld4(reinterpret_cast<const uint32_t *>(blk + 80));                  // d, dmin
     }
 }
 
 template <int FMT>
-__device__ __forceinline__ void decode_sub(SubBlock<FMT> &u, const RawSub<FMT> &r, int sub) {
+__device__ __forceinline__ void decode_unit(Unit<FMT> &v, const RawUnit<FMT> &r, int u) {
     if constexpr (FMT == KQ_Q4) {
-        u.d = f16_bits(r.w[0]);
-        u.dmin = f16_bits(r.w[0] >> 16);
-        // scales[0..3] in w[1], [4..7] in w[2], [8..11] in w[3]; byte (j & 3) of each
-        const int j = sub;
-        const uint32_t sh = 8u * (uint32_t)(j & 3);
-        const uint32_t lo_sc = (r.w[1] >> sh) & 63u, lo_m = (r.w[2] >> sh) & 63u;
-        const uint32_t hi_sc = ((r.w[3] >> sh) & 15u) | (((r.w[1] >> (sh + 6)) & 3u) << 4);
-        const uint32_t hi_m = ((r.w[3] >> (sh + 4)) & 15u) | (((r.w[2] >> (sh + 6)) & 3u) << 4);
-        u.sc = (int)(j < 4 ? lo_sc : hi_sc);
-        u.m = (int)(j < 4 ? lo_m : hi_m);
-        const int c = j >> 1, hi = j & 1;
+        v.d = f16_bits(r.w[0]);
+        v.dmin = f16_bits(r.w[0] >> 16);
+        // scales[0..3] in w[1], [4..7] in w[2], [8..11] in w[3]; sub-blocks 2u, 2u + 1
+        const uint32_t sh0 = 8u * (uint32_t)((2 * u) & 3), sh1 = sh0 + 8u;
+        if (u < 2) {
+            v.sc0 = (int)((r.w[1] >> sh0) & 63u);
+            v.sc1 = (int)((r.w[1] >> sh1) & 63u);
+            v.m0 = (int)((r.w[2] >> sh0) & 63u);
+            v.m1 = (int)((r.w[2] >> sh1) & 63u);
+        } else {
+            v.sc0 = (int)(((r.w[3] >> sh0) & 15u) | (((r.w[1] >> (sh0 + 6)) & 3u) << 4));
+            v.sc1 = (int)(((r.w[3] >> sh1) & 15u) | (((r.w[1] >> (sh1 + 6)) & 3u) << 4));
+            v.m0 = (int)(((r.w[3] >> (sh0 + 4)) & 15u) | (((r.w[2] >> (sh0 + 6)) & 3u) << 4));
+            v.m1 = (int)(((r.w[3] >> (sh1 + 4)) & 15u) | (((r.w[2] >> (sh1 + 6)) & 3u) << 4));
+        }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) u.q[k] = (r.w[4 + k] >> (4 * hi)) & 0x0f0f0f0fu;
-        u.xoff = 64u * c + 32u * hi;
-        u.grp = 4u * c + 2u * hi;
-        u.fd = u.d * (float)u.sc;
-        u.fm = u.dmin * (float)u.m;
+        for (int k = 0; k < 8; ++k) {
+            v.q[k] = r.w[4 + k] & 0x0f0f0f0fu;
+            v.q[8 + k] = (r.w[4 + k] >> 4) & 0x0f0f0f0fu;
+        }
     } else {
-        const int sb = sub, h = sb >> 3, j = (sb >> 1) & 3, s = sb & 1;
-        const uint32_t sbyte = (r.w[4] >> (8 * (sb & 3))) & 0xffu;
-        u.sc = (int)(sbyte & 15u);
-        u.m = (int)(sbyte >> 4);
-        u.d = f16_bits(r.w[5]);
-        u.dmin = f16_bits(r.w[5] >> 16);
+        const int j = u & 3;
+        const uint32_t s0 = 16u * (uint32_t)(j & 1), s1 = s0 + 8u;   // bytes of sub-blocks 8h+2j, +1 in w[8]
+        v.sc0 = (int)((r.w[8] >> s0) & 15u);
+        v.m0 = (int)((r.w[8] >> (s0 + 4)) & 15u);
+        v.sc1 = (int)((r.w[8] >> s1) & 15u);
+        v.m1 = (int)((r.w[8] >> (s1 + 4)) & 15u);
+        v.d = f16_bits(r.w[9]);
+        v.dmin = f16_bits(r.w[9] >> 16);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) u.q[k] = (r.w[k] >> (2 * j)) & 0x03030303u;
-        u.xoff = 128u * h + 32u * j + 16u * s;
-        u.grp = (uint32_t)sb;
-        u.fd = u.d * (float)u.sc;
-        u.fm = u.dmin * (float)u.m;
+        for (int k = 0; k < 8; ++k) v.q[k] = (r.w[k] >> (2 * j)) & 0x03030303u;
     }
+}
+
+// Staged activation quants in shared memory: 16-byte unit u of a token row is
+// stored at u ^ (block & 7) (16 units a 256-value block), so that the lanes of a
+// warp pass, which read the same offsets of different blocks, spread over all
+// eight 16-byte bank groups.
+__device__ __forceinline__ uint32_t act_swz(uint32_t u) { return u ^ ((u >> 4) & 7u); }
+
+// The unit's term for one token, before the activation scale:
+// d * (sc0 isum0 + sc1 isum1) - dmin * (m0 xsum0 + m1 xsum1), the integer sums
+// exact.  xrow: the token's quants (SMEM: the swizzled staged row), u0 the
+// 16-byte unit of the unit's first value; xs: its 16-value sums from the unit's
+// first group.
+template <int FMT, bool SMEM>
+__device__ __forceinline__ float unit_term(const Unit<FMT> &v, const int8_t *xrow, uint32_t u0, const int16_t *xs) {
+    auto ld4 = [](const uint32_t *p) { return SMEM ? *p : __ldg(p); };
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(xrow);
+    auto ldx = [&](uint32_t k) { return SMEM ? x4[act_swz(u0 + k)] : __ldg(x4 + u0 + k); };
+    int i0 = 0, i1 = 0, xs0, xs1;
+    if constexpr (FMT == KQ_Q4) {
+        const uint4 a = ldx(0), b = ldx(1), c = ldx(2), e = ldx(3);
+        i0 = __dp4a((int)v.q[0], (int)a.x, i0);
+        i0 = __dp4a((int)v.q[1], (int)a.y, i0);
+        i0 = __dp4a((int)v.q[2], (int)a.z, i0);
+        i0 = __dp4a((int)v.q[3], (int)a.w, i0);
+        i0 = __dp4a((int)v.q[4], (int)b.x, i0);
+        i0 = __dp4a((int)v.q[5], (int)b.y, i0);
+        i0 = __dp4a((int)v.q[6], (int)b.z, i0);
+        i0 = __dp4a((int)v.q[7], (int)b.w, i0);
+        i1 = __dp4a((int)v.q[8], (int)c.x, i1);
+        i1 = __dp4a((int)v.q[9], (int)c.y, i1);
+        i1 = __dp4a((int)v.q[10], (int)c.z, i1);
+        i1 = __dp4a((int)v.q[11], (int)c.w, i1);
+        i1 = __dp4a((int)v.q[12], (int)e.x, i1);
+        i1 = __dp4a((int)v.q[13], (int)e.y, i1);
+        i1 = __dp4a((int)v.q[14], (int)e.z, i1);
+        i1 = __dp4a((int)v.q[15], (int)e.w, i1);
+        const uint32_t g01 = ld4(reinterpret_cast<const uint32_t *>(xs));
+        const uint32_t g23 = ld4(reinterpret_cast<const uint32_t *>(xs) + 1);
+        xs0 = (int)(int16_t)(g01 & 0xffffu) + (int)(int16_t)(g01 >> 16);
+        xs1 = (int)(int16_t)(g23 & 0xffffu) + (int)(int16_t)(g23 >> 16);
+    } else {
+        const uint4 a = ldx(0), b = ldx(1);
+        i0 = __dp4a((int)v.q[0], (int)a.x, i0);
+        i0 = __dp4a((int)v.q[1], (int)a.y, i0);
+        i0 = __dp4a((int)v.q[2], (int)a.z, i0);
+        i0 = __dp4a((int)v.q[3], (int)a.w, i0);
+        i1 = __dp4a((int)v.q[4], (int)b.x, i1);
+        i1 = __dp4a((int)v.q[5], (int)b.y, i1);
+        i1 = __dp4a((int)v.q[6], (int)b.z, i1);
+        i1 = __dp4a((int)v.q[7], (int)b.w, i1);
+        const uint32_t g01 = ld4(reinterpret_cast<const uint32_t *>(xs));
+        xs0 = (int)(int16_t)(g01 & 0xffffu);
+        xs1 = (int)(int16_t)(g01 >> 16);
+    }
+    const int S = v.sc0 * i0 + v.sc1 * i1, M = v.m0 * xs0 + v.m1 * xs1;
+    return fmaf(-v.dmin, (float)M, v.d * (float)S);
 }
 
 template <int FMT, int TOKG>
 __global__ void __launch_bounds__(kq::THREADS, 2) k_kq_gemv(const KqParams p) {
-    constexpr int LPB = FMT == KQ_Q4 ? 8 : 16;   // lanes per block, one sub-block each
+    constexpr int LPB = units_per_block<FMT>();   // lanes per block, one unit (two sub-blocks) each
     constexpr int BPP = 32 / LPB;                 // blocks per warp pass
     constexpr int BB = FMT == KQ_Q4 ? 144 : 84;   // bytes per block
-    constexpr int U = FMT == KQ_Q4 ? 4 : 8;       // warp passes whose loads are issued together
-    using SB = SubBlock<FMT>;
+    constexpr int U = FMT == KQ_Q4 ? 2 : 4;       // warp passes whose loads are issued together
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane % LPB, bsel = lane / LPB;
+    const int unit = lane % LPB, bsel = lane / LPB;
+    const uint32_t xoff = unit_xoff<FMT>(unit), grp = unit_grp<FMT>(unit);
     const uint32_t nsb = p.nsb;
     const uint64_t row_bytes = (uint64_t)nsb * BB;
     const uint64_t in_dim = p.in_dim;
@@ -271,49 +346,27 @@ __global__ void __launch_bounds__(kq::THREADS, 2) k_kq_gemv(const KqParams p) {
 #pragma unroll
             for (int t = 0; t < TOKG; ++t) acc[t] = 0.0f;
             for (uint32_t b0 = 0; b0 < nsb; b0 += BPP * U) {
-                RawSub<FMT> raw[U];
+                RawUnit<FMT> raw[U];
 #pragma unroll
                 for (int v = 0; v < U; ++v) {
                     const uint32_t b = b0 + (uint32_t)(v * BPP + bsel);
-                    if (b < nsb) load_raw<FMT>(raw[v], wrow + (uint64_t)b * BB, sub);
+                    if (b < nsb) load_raw<FMT, false>(raw[v], wrow + (uint64_t)b * BB, unit);
                 }
 #pragma unroll
                 for (int v = 0; v < U; ++v) {
-                const uint32_t b = b0 + (uint32_t)(v * BPP + bsel);
-                if (b >= nsb) continue;
-                SB u;
-                decode_sub<FMT>(u, raw[v], sub);
+                    const uint32_t b = b0 + (uint32_t)(v * BPP + bsel);
+                    if (b >= nsb) continue;
+                    Unit<FMT> un;
+                    decode_unit<FMT>(un, raw[v], unit);
 #pragma unroll
-                for (int t = 0; t < TOKG; ++t) {
-                    if (t >= it.ntok) break;
-                    const uint64_t xr = (uint64_t)arow[t];
-                    const int8_t *xq = p.qx + xr * in_dim + (uint64_t)b * kq::QKK + u.xoff;
-                    int isum = 0, xsum;
-                    if constexpr (FMT == KQ_Q4) {
-                        const uint4 xa = __ldg(reinterpret_cast<const uint4 *>(xq));
-                        const uint4 xb = __ldg(reinterpret_cast<const uint4 *>(xq) + 1);
-                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
-                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
-                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
-                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
-                        isum = __dp4a((int)u.q[4], (int)xb.x, isum);
-                        isum = __dp4a((int)u.q[5], (int)xb.y, isum);
-                        isum = __dp4a((int)u.q[6], (int)xb.z, isum);
-                        isum = __dp4a((int)u.q[7], (int)xb.w, isum);
-                        const uint32_t s2 = __ldg(reinterpret_cast<const uint32_t *>(
-                            p.xs + xr * (in_dim / 16) + (uint64_t)b * 16 + u.grp));
-                        xsum = (int)(int16_t)(s2 & 0xffffu) + (int)(int16_t)(s2 >> 16);
-                    } else {
-                        const uint4 xa = __ldg(reinterpret_cast<const uint4 *>(xq));
-                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
-                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
-                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
-                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
-                        xsum = (int)__ldg(p.xs + xr * (in_dim / 16) + (uint64_t)b * 16 + u.grp);
+                    for (int t = 0; t < TOKG; ++t) {
+                        if (t >= it.ntok) break;
+                        const uint64_t xr = (uint64_t)arow[t];
+                        const float term = unit_term<FMT, false>(
+                            un, p.qx + xr * in_dim, (uint32_t)((b * kq::QKK + xoff) / 16u),
+                            p.xs + xr * (in_dim / 16) + (uint64_t)b * 16 + grp);
+                        acc[t] = fmaf(__ldg(p.dx + xr * nsb + b), term, acc[t]);
                     }
-                    const float dxv = __ldg(p.dx + xr * nsb + b);
-                    acc[t] = fmaf(dxv, fmaf(-u.fm, (float)xsum, u.fd * (float)isum), acc[t]);
-                }
                 }
             }
             float mine = 0.0f;
@@ -358,27 +411,6 @@ template <int TOKG> struct Layout {
 __host__ __device__ constexpr uint64_t act_row_bytes(uint64_t in_dim) { return in_dim + in_dim / 64 + in_dim / 8; }
 }  // namespace kqs
 
-// This lane's words of a block in shared memory (plain loads: the read-only
-// global path must not be used on shared addresses).
-template <int FMT>
-__device__ __forceinline__ void load_raw_smem(RawSub<FMT> &r, const uint8_t *blk, int sub) {
-    if constexpr (FMT == KQ_Q4) {
-        const uint4 h = *reinterpret_cast<const uint4 *>(blk);
-        const uint4 *qs = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (sub >> 1));
-        const uint4 a = qs[0], b = qs[1];
-        r.w[0] = h.x; r.w[1] = h.y; r.w[2] = h.z; r.w[3] = h.w;
-        r.w[4] = a.x; r.w[5] = a.y; r.w[6] = a.z; r.w[7] = a.w;
-        r.w[8] = b.x; r.w[9] = b.y; r.w[10] = b.z; r.w[11] = b.w;
-    } else {
-        const int sb = sub, h = sb >> 3, s = sb & 1;
-        const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + 16 * s);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) r.w[k] = qs[k];
-        r.w[4] = reinterpret_cast<const uint32_t *>(blk)[sb >> 2];
-        r.w[5] = *reinterpret_cast<const uint32_t *>(blk + 80);
-    }
-}
-
 // Per-slot description of its work item, written by the producer before the
 // slot's copy is armed (ntok < 0: no more items).  group identifies the token
 // group (its first plane row): consecutive items of one group share staged
@@ -394,10 +426,9 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
     using namespace kqs;
     constexpr int NSLOT = Layout<TOKG>::NSLOT;
     constexpr size_t META_OFF = Layout<TOKG>::META_OFF;
-    constexpr int LPB = FMT == KQ_Q4 ? 8 : 16;
+    constexpr int LPB = units_per_block<FMT>();   // lanes per block, one unit (two sub-blocks) each
     constexpr int BPP = 32 / LPB;
     constexpr int BB = FMT == KQ_Q4 ? 144 : 84;
-    using SB = SubBlock<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *slots = smem;
     uint8_t *act = smem + (size_t)NSLOT * SLOT_BYTES;
@@ -486,7 +517,8 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
     // The token group's activations are staged in shared memory once per group:
     // a bounded barrier (act_bar, two phases) first lets every warp finish the
     // previous group, then every warp copies its share and arrives again.
-    const int sub = lane % LPB, bsel = lane / LPB;
+    const int unit = lane % LPB, bsel = lane / LPB;
+    const uint32_t xoff = unit_xoff<FMT>(unit), grp = unit_grp<FMT>(unit);
     const uint64_t in_dim = p.in_dim;
     const uint32_t nxs = (uint32_t)(in_dim / 16);
     int8_t *qx_s = reinterpret_cast<int8_t *>(act);
@@ -510,7 +542,7 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             if (!mbar_wait(act_bar, 0u, p.err, abort_flag)) break;
             for (uint32_t e = (uint32_t)ctid; e < (uint32_t)ntok * nxs; e += CT) {
                 const uint32_t t = e / nxs, c = e - t * nxs;
-                reinterpret_cast<uint4 *>(qx_s + (size_t)t * in_dim)[c] =
+                reinterpret_cast<uint4 *>(qx_s + (size_t)t * in_dim)[act_swz(c)] =
                     __ldg(reinterpret_cast<const uint4 *>(p.qx + (uint64_t)m.arow[t] * in_dim) + c);
             }
             for (uint32_t e = (uint32_t)ctid; e < (uint32_t)ntok * nsb; e += CT) {
@@ -535,37 +567,16 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             for (uint32_t b0 = 0; b0 < nsb; b0 += BPP) {
                 const uint32_t b = b0 + (uint32_t)bsel;
                 if (b >= nsb) continue;
-                RawSub<FMT> raw;
-                load_raw_smem<FMT>(raw, wrow + (size_t)b * BB, sub);
-                SB u;
-                decode_sub<FMT>(u, raw, sub);
+                RawUnit<FMT> raw;
+                load_raw<FMT, true>(raw, wrow + (size_t)b * BB, unit);
+                Unit<FMT> un;
+                decode_unit<FMT>(un, raw, unit);
 #pragma unroll
                 for (int t = 0; t < TOKG; ++t) {
                     if (t >= ntok) break;
-                    const int8_t *xq = qx_s + (size_t)t * in_dim + (size_t)b * kq::QKK + u.xoff;
-                    int isum = 0, xsum;
-                    if constexpr (FMT == KQ_Q4) {
-                        const uint4 xa = reinterpret_cast<const uint4 *>(xq)[0];
-                        const uint4 xb = reinterpret_cast<const uint4 *>(xq)[1];
-                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
-                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
-                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
-                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
-                        isum = __dp4a((int)u.q[4], (int)xb.x, isum);
-                        isum = __dp4a((int)u.q[5], (int)xb.y, isum);
-                        isum = __dp4a((int)u.q[6], (int)xb.z, isum);
-                        isum = __dp4a((int)u.q[7], (int)xb.w, isum);
-                        const uint32_t s2 = *reinterpret_cast<const uint32_t *>(xs_s + (size_t)t * nxs + b * 16 + u.grp);
-                        xsum = (int)(int16_t)(s2 & 0xffffu) + (int)(int16_t)(s2 >> 16);
-                    } else {
-                        const uint4 xa = reinterpret_cast<const uint4 *>(xq)[0];
-                        isum = __dp4a((int)u.q[0], (int)xa.x, isum);
-                        isum = __dp4a((int)u.q[1], (int)xa.y, isum);
-                        isum = __dp4a((int)u.q[2], (int)xa.z, isum);
-                        isum = __dp4a((int)u.q[3], (int)xa.w, isum);
-                        xsum = (int)xs_s[(size_t)t * nxs + b * 16 + u.grp];
-                    }
-                    acc[t] = fmaf(dx_s[t * nsb + b], fmaf(-u.fm, (float)xsum, u.fd * (float)isum), acc[t]);
+                    const float term = unit_term<FMT, true>(un, qx_s + (size_t)t * in_dim, (b * kq::QKK + xoff) / 16u,
+                                                            xs_s + (size_t)t * nxs + b * 16 + grp);
+                    acc[t] = fmaf(dx_s[t * nsb + b], term, acc[t]);
                 }
             }
             float mine = 0.0f;
