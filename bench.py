@@ -345,8 +345,13 @@ def run_ours(args, rank, world, local, dist):
         e1.record(stream)
     e1.synchronize()
     assert q8.q8_last_error(stream) == 0
-    for n in N_TOKS:        # every weight copy holds the same bytes: the graph-replayed results
-        assert torch.equal(oh[n], outs[n].cpu()), "host-buffer result differs from the device-buffer one"
+    for n in N_TOKS:
+        # every weight copy holds the same bytes.  With 3 or more tokens the host-result
+        # call splits each CTA's rows in two items (partial sums added in another
+        # order), so it agrees with the device-result call to rounding, not bitwise
+        ref = outs[n].cpu()
+        err = (oh[n] - ref).abs().max().item()
+        assert err <= 1e-4 * ref.abs().max().item(), f"host-buffer result differs from the device one ({err})"
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.steps
     e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "ms_per_step": round(e2e_ms, 4),

@@ -130,9 +130,15 @@ int q8_matmul(float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
  * cudaHostRegister with mapping; pinned torch tensors) and 16-byte aligned,
  * the q8_matmul kernels read x_host and write out_host directly through the
  * GPU's host link (NVLink-C2C on Grace systems): one call is just the kernels.
+ * From 3 to 16 tokens x_host is then read once, by the quantiser kernel (not
+ * by every CTA of the GEMV), and from 3 tokens and 12 x 152 16-row sub-items of
+ * output up each CTA of the GEMV takes two items, so that the first one's
+ * results cross the link while the second one's weights stream; those results
+ * agree with q8_matmul's within the matmul's error bound (partial sums of two
+ * warps are added in another order), all others bit for bit.
  * Otherwise, on `stream`, in order: x_host is copied into a library-owned
  * device staging buffer, the kernels run on it, and the result is copied to
- * out_host.  Either way the results are those of q8_matmul, bit for bit.
+ * out_host: the results of q8_matmul, bit for bit.
  * Host buffers need no alignment.  The work is asynchronous: x_host must stay
  * unchanged and out_host is valid only once `stream` has synchronised (with
  * pageable buffers the CUDA runtime stages the copies and the call may block

@@ -183,8 +183,9 @@ int check_dims(uint64_t in_dim, uint64_t out_dim, uint64_t n_tok) {
 
 // out = W x from activation planes already in scratch (n_pad rows), or, with
 // x_fused given, from the fp32 rows quantised inside the GEMV.
+// out_remote: the result lives in host memory (see q8_matmul_host).
 int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const int8_t *qx,
-              const float *dx, const float *x_fused, uint64_t n_tok, cudaStream_t st) {
+              const float *dx, const float *x_fused, uint64_t n_tok, cudaStream_t st, bool out_remote = false) {
     const uint32_t nb = (uint32_t)(in_dim / q8::QK);
     if (nb % 8 == 0 && n_tok <= 16) {
         q8::GemvParams g{};
@@ -200,6 +201,14 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.err = s->err;
         g.n_tok = (uint32_t)n_tok;
         g.n_items = q8::gemv_dense_items(out_dim, s->num_sms);
+        // A result in host memory crosses the host link at a fraction of the HBM
+        // rate, and an item writes its results only once its last weights are in.
+        // With 3 or more tokens (at least 384 KB of results for out 32768) each CTA
+        // takes two items when each still keeps 12 of the 14 consumer warps busy (six
+        // or more 16-row sub-items, two warps a sub-item): the first item's results
+        // then cross the link while the second item's weights stream.
+        const uint64_t nsub = (out_dim + 15) / 16;
+        if (out_remote && n_tok >= 3 && nsub >= 12 * (uint64_t)g.n_items) g.n_items *= 2;
         q8::gemv_dense_split(out_dim, g.n_items, g.sub_base, g.sub_rem);
         g.plan = nullptr;
         g.row_to_out = nullptr;
@@ -551,24 +560,29 @@ static void *mapped_host_pointer(const void *p) {
 }
 
 // The dense product with arguments already validated, under g_mutex.
+// host_io: x and out are host memory mapped into the device's address space.
 static int dispatch_matmul(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t out_dim,
-                           const float *x, const void *xq, uint64_t n_tok, cudaStream_t st) {
+                           const float *x, const void *xq, uint64_t n_tok, cudaStream_t st, bool host_io = false) {
     int rc;
     const uint64_t nb = in_dim / q8::QK;
     if (n_tok > 16 && nb % 2 == 0) return run_tc(s, out, W, in_dim, out_dim, x, xq, n_tok, st);
-    // small activations: one kernel, the GEMV quantises them itself
-    if (x && nb % 8 == 0 && q8::gemv_fuses_quantiser(n_tok, nb))
+    // small activations: one kernel, the GEMV quantises them itself.  For host
+    // activations only up to 2 tokens: every CTA reads all of x over the host link
+    // (measured per call at out 32768: 1 token 11.5 us fused against 14.4 us
+    // through the quantiser; 4 tokens, 152 x 16 KB, 21 against 16 us), where the
+    // quantiser reads each value once.
+    if (x && (!host_io || n_tok <= 2) && nb % 8 == 0 && q8::gemv_fuses_quantiser(n_tok, nb))
         return run_dense(s, out, W, in_dim, out_dim, nullptr, nullptr, x, n_tok, st);
     const uint64_t n_pad = (n_tok + 15) & ~(uint64_t)15;
     if ((rc = reserve_scratch(s, planes_bytes(n_pad, in_dim)))) return rc;
     Carver cv(s->scratch);
     int8_t *qx = cv.take<int8_t>(n_pad * in_dim);
     float *dx = cv.take<float>(n_pad * nb * sizeof(float));
-    cudaError_t e = x ? q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st)
+    cudaError_t e = x ? q8::launch_quantize_planes(qx, dx, x, in_dim, n_pad, nullptr, n_tok, s->num_sms, st, host_io)
                       : q8::launch_unpack_blocks(qx, dx, static_cast<const uint8_t *>(xq), in_dim, n_pad, n_tok,
                                                  s->num_sms, st);
     if (e != cudaSuccess) return status_of(e);
-    return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st);
+    return run_dense(s, out, W, in_dim, out_dim, qx, dx, nullptr, n_tok, st, host_io);
 }
 
 int q8_rmsnorm_quantize(void *xq, float *y, const float *x, const float *gamma, uint64_t dim, uint64_t n_tok,
@@ -622,7 +636,7 @@ int q8_matmul_host(float *out_host, const void *W, uint64_t in_dim, uint64_t out
     // result there directly, with no staging copies.
     const float *xd_host = static_cast<const float *>(mapped_host_pointer(x_host));
     float *od_host = static_cast<float *>(mapped_host_pointer(out_host));
-    if (xd_host && od_host) return dispatch_matmul(s, od_host, W, in_dim, out_dim, xd_host, nullptr, n_tok, st);
+    if (xd_host && od_host) return dispatch_matmul(s, od_host, W, in_dim, out_dim, xd_host, nullptr, n_tok, st, true);
     const size_t x_bytes = n_tok * in_dim * sizeof(float), out_bytes = n_tok * out_dim * sizeof(float);
     if ((rc = reserve_buffer(&s->stage, &s->stage_bytes, align256(x_bytes) + align256(out_bytes)))) return rc;
     Carver cv(s->stage);

@@ -44,8 +44,11 @@ struct MmaParams {
 
 // Quantiser (q8_quantize.cu)
 cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, int num_sms, cudaStream_t st);
+// programmatic: launch with programmatic stream serialisation (the kernel waits
+// for the previous grid before it reads or writes anything).
 cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
-                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st);
+                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st,
+                                   bool programmatic = false);
 // Routed pairs straight to their plane rows: pair p (activation row p, or p / k
 // when x holds one row per token) goes to plane row dst_row[p]; padding rows are
 // not written.  With tc_plan, rows [0, tc_plan->row_end) go to the tensor-core

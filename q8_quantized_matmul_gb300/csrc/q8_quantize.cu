@@ -53,13 +53,17 @@ __device__ __forceinline__ void store_f16_quants(__half *dst, const QuantBlock &
     *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-__global__ void __launch_bounds__(256) k_quantize_planes(int8_t *__restrict__ qplane, float *__restrict__ dplane,
+__global__ void __launch_bounds__(256, 8) k_quantize_planes(int8_t *__restrict__ qplane, float *__restrict__ dplane,
                                                          const float *__restrict__ x, uint64_t in_dim,
                                                          uint64_t n_rows, const int32_t *__restrict__ src_row,
                                                          uint64_t n_src) {
     // The matmul that follows only prefetches weights before it waits for this
     // grid to finish, so it may be scheduled now.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // when launched with programmatic serialisation: nothing is read or written
+    // before the previous grid is done (it may still read the planes this kernel
+    // rewrites); after a plain launch this returns at once
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t nb = in_dim / QK;
     const uint64_t nblk = n_rows * nb;
     const uint64_t lane_q = threadIdx.x & 3u;
@@ -450,12 +454,24 @@ cudaError_t launch_quantize_blocks(uint8_t *xq, const float *x, uint64_t nblk, i
 }
 
 cudaError_t launch_quantize_planes(int8_t *qplane, float *dplane, const float *x, uint64_t in_dim, uint64_t n_rows,
-                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st) {
+                                   const int32_t *src_row, uint64_t n_src, int num_sms, cudaStream_t st,
+                                   bool programmatic) {
     const uint64_t nblk = n_rows * (in_dim / QK);
     if (nblk == 0) return cudaSuccess;
-    // a plain launch: as a programmatic one behind the previous GEMV it made
-    // back-to-back 16-token calls about 1 us slower
-    k_quantize_planes<<<grid_for(nblk, 64, num_sms), 256, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
+    // Small inputs (the GEMV's 9-16 tokens) in CTAs of 128 threads at <= 32
+    // registers (4096 registers): one fits on an SM beside a GEMV CTA (61,440
+    // registers, 218 KB of shared memory).
+    const int threads = nblk <= (uint64_t)num_sms * 32 ? 128 : 256;
+    const int grid = grid_for(nblk, threads / 4, num_sms);
+    // Behind a GEMV whose results cross the host link, a programmatic launch lets
+    // this kernel sit beside that GEMV's CTAs while its writes drain, and the next
+    // GEMV start its weight stream meanwhile (host-buffer calls at out 32768: 4
+    // tokens 16.4 -> 13.9 us, 16 tokens 24.5 -> 21.7 us).  Between device-buffer
+    // calls the plain launch measured faster (16-token calls back to back in a
+    // graph 13.4 against 14.7 us).
+    if (programmatic)
+        return launch_pdl(k_quantize_planes, grid, threads, st, qplane, dplane, x, in_dim, n_rows, src_row, n_src);
+    k_quantize_planes<<<grid, threads, 0, st>>>(qplane, dplane, x, in_dim, n_rows, src_row, n_src);
     return cudaGetLastError();
 }
 

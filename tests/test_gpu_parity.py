@@ -557,8 +557,9 @@ def _host_call(q8, W, xh, out_dim, pinned):
                                                    (40, 2048, 300), (700, 1024, 200)])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_matmul_host_matches_matmul_bitwise(q8, n_tok, in_dim, out_dim, pinned):
-    """Host x and out around the same kernels: the bits of q8_matmul, for the fused
-    GEMV, the 9-16-token GEMV and both tensor-core variants."""
+    """Host x and out around the same kernels: the bits of q8_matmul, for the
+    GEMV (from the quantiser's planes when x is mapped host memory, fused otherwise:
+    the same quantised values either way), and both tensor-core variants."""
     W = dev(inputs.weights(out_dim, in_dim, seed=91))
     xh = inputs.normal((n_tok, in_dim), seed=92, p_out=0.01)
     ref = q8.matmul(W, dev(xh), out_dim).cpu().numpy()
@@ -575,6 +576,20 @@ def test_matmul_host_oracle_and_repeat(q8, o):
         xh = inputs.normal((n_tok, 2048), seed=94 + n_tok)
         ref, bound = o.matmul(Wh, xh, 500)
         assert_close(_host_call(q8, W, xh, 500, True), ref, bound, f"host {n_tok}")
+
+
+@pytest.mark.parametrize("n_tok", [4, 16])
+def test_matmul_host_two_items_per_cta(q8, o, n_tok):
+    """out 32768 with the result in host memory: every CTA takes two items of six or
+    seven 16-row sub-items (two warps a sub-item, partial sums added in slice order),
+    so the first item's results cross the host link while the second item's weights
+    stream.  Every output against the oracle."""
+    in_dim, out_dim = 1024, 32768
+    Wh = inputs.weights(out_dim, in_dim, seed=97)
+    W = dev(Wh)
+    xh = inputs.normal((n_tok, in_dim), seed=98 + n_tok, p_out=0.01)
+    ref, bound = o.matmul(Wh, xh, out_dim)
+    assert_close(_host_call(q8, W, xh, out_dim, True), ref, bound, f"host out {out_dim} x {n_tok}")
 
 
 def test_matmul_host_errors(q8):
