@@ -214,8 +214,8 @@ int q8_moe_matmul(float *out, const void *W_experts, uint32_t n_expert,
  *                   multiple of 16 for Q4_K and of 4 for Q2_K); an id outside
  *                   [0, n_expert) gives a zero row and raises Q8_ERANGE.
  * The matmuls run a weight-streaming kernel (dp4a on the integer quants, one
- * lane per sub-block) over token groups of up to 16; more tokens re-read the
- * weights once per group.
+ * lane per two sub-blocks) over token groups of up to 16; more tokens re-read
+ * the weights once per group.
  */
 #define Q8_KQ_Q2_K 2
 #define Q8_KQ_Q4_K 4
@@ -241,7 +241,9 @@ int q8_kq_moe_matmul(float *out, const void *W_experts, int fmt, uint32_t n_expe
  *   out[t]  = sum_j expert_weights[t*k+j] * y[t*k+j]          (j in slot order)
  * x and mid are quantised per 32-block exactly as q8_quantize_act does, and
  * each projection is the q8_moe_matmul product (the gate and up projections
- * share one routing and one quantisation of x).  silu(g) = g / (1 + e^-g) in
+ * share one routing and one quantisation of x; below 1024 pairs one kernel
+ * streams both against one staging of x and applies SwiGLU in its epilogue,
+ * with the same bits as the separate steps).  silu(g) = g / (1 + e^-g) in
  * fp32 (CUDA expf, IEEE division).
  *   out               out: fp32 [n_tok][out_dim].
  *   W_gate, W_up      in:  n_expert matrices each, expert e at e*gate_up_stride_bytes,

@@ -347,6 +347,10 @@ struct MoeCall {
     const float *x = nullptr;
     int x_per_pair = 0;
     uint64_t n_tok = 0;
+    // Gate/up pair: W[0] gate, W[1] up, and out[0] receives swiglu1(gate, up, limit)
+    // from one GEMV pass per class (GEMV path without a tensor-core class only).
+    bool pair = false;
+    float limit = 0.0f;
 };
 
 // Scratch layout of a routed call.
@@ -396,9 +400,11 @@ int moe_run(DeviceState *s, const MoeCall &c, const MoeLayout &L, void *base, cu
     // GEMV items of up to 448 rows: 28 sixteen-row sub-items, two for each of the 14
     // consumer warps.  (128-row items left 6 of the warps idle; at 64 tokens, top-6,
     // the calls took 395 / 430 us with 128-row items, 352 / 374 with 224, 336 / 345
-    // with 448.)
+    // with 448.)  A gate/up pair streams two matrices per item: 224 rows of each.
+    if (c.pair && (!L.gemv_path || L.tc_cap)) return Q8_EINVAL;
+    const uint32_t rows_cap = c.pair ? 224 : 448;
     uint32_t rows_gemv = (uint32_t)((c.out_dim + 15) & ~(uint64_t)15);
-    if (rows_gemv > 448) rows_gemv = 448;
+    if (rows_gemv > rows_cap) rows_gemv = rows_cap;
     cudaError_t e = q8::launch_route(c.ids, c.n_tok, c.k, c.n_expert, c.x_per_pair, (uint32_t)c.out_dim, rows_gemv,
                                      (uint32_t)L.tc_cap, counts, row0_of, plans, row_to_out, src_row, dst_row,
                                      L.max_rows, c.out[0], s->err, s->num_sms, st);
@@ -413,7 +419,7 @@ int moe_run(DeviceState *s, const MoeCall &c, const MoeLayout &L, void *base, cu
     else
         e = q8::launch_quantize_planes(qx, dx, c.x, c.in_dim, L.max_rows, src_row, 0, s->num_sms, st);
     if (e != cudaSuccess) return status_of(e);
-    for (int w = 0; w < c.n_w; ++w) {
+    for (int w = 0; w < (c.pair ? 1 : c.n_w); ++w) {
         const uint8_t *W = static_cast<const uint8_t *>(c.W[w]);
         float *out = c.out[w];
         q8::MmaParams p{};
@@ -456,6 +462,10 @@ int moe_run(DeviceState *s, const MoeCall &c, const MoeLayout &L, void *base, cu
         g.weights_early = 1;   // behind the quantiser, the grouped GEMM or another routed GEMV
         g.row_to_out = row_to_out;
         g.n_expert = c.n_expert;
+        if (c.pair) {
+            g.W2 = static_cast<const uint8_t *>(c.W[1]);
+            g.limit = c.limit;
+        }
         q8::TcParams tp{};
         tp.M = (int)c.out_dim;
         tp.N = 0;
@@ -769,13 +779,24 @@ int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_d
     float *up = cv.take<float>(n_pairs * mid_dim * 4);
     float *mid = cv.take<float>(n_pairs * mid_dim * 4);
     float *y = cv.take<float>(n_pairs * out_dim * 4);
-    gu.out[0] = gate;
-    gu.out[1] = up;
-    if ((rc = moe_run(s, gu, Lgu, s->scratch, st))) return rc;
-    // a pair with a bad id: its gate row is zero, its up row unwritten; mid is zeroed
-    if ((rc = status_of(q8::launch_swiglu(mid, gate, up, n_pairs * mid_dim, limit, expert_ids, n_expert, mid_dim,
-                                          s->num_sms, st))))
-        return rc;
+    if (Lgu.gemv_path && !Lgu.tc_cap) {
+        // Every expert group on the GEMV (decode sizes): gate and up rows stream
+        // through one kernel per class against one staging of the activations, and
+        // its epilogue writes mid = swiglu1(gate, up).  The routing zeroes the mid
+        // row of a pair with a bad id.
+        gu.pair = true;
+        gu.limit = limit;
+        gu.out[0] = mid;
+        if ((rc = moe_run(s, gu, Lgu, s->scratch, st))) return rc;
+    } else {
+        gu.out[0] = gate;
+        gu.out[1] = up;
+        if ((rc = moe_run(s, gu, Lgu, s->scratch, st))) return rc;
+        // a pair with a bad id: its gate row is zero, its up row unwritten; mid is zeroed
+        if ((rc = status_of(q8::launch_swiglu(mid, gate, up, n_pairs * mid_dim, limit, expert_ids, n_expert, mid_dim,
+                                              s->num_sms, st))))
+            return rc;
+    }
     dn.x = mid;
     dn.out[0] = y;
     if ((rc = moe_run(s, dn, Ldn, s->scratch, st))) return rc;

@@ -139,4 +139,16 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4]
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// SwiGLU of one gate/up pair (MoE study page, SwiGLU activation section):
+// silu(min(g, L)) * clamp(u, -L, L), L = limit (0: no clamp), silu(g) = g / (1 + e^-g)
+// in fp32 with CUDA's expf and IEEE division.  The routed FFN's separate pass and
+// the gate/up pair GEMV's epilogue both use it, so they give the same bits.
+__device__ __forceinline__ float swiglu1(float g, float u, float limit) {
+    if (limit > 0.0f) {
+        g = fminf(g, limit);
+        u = fminf(fmaxf(u, -limit), limit);
+    }
+    return g / (1.0f + expf(-g)) * u;
+}
+
 }  // namespace q8

@@ -19,14 +19,6 @@ namespace {
 
 constexpr int FFN_THREADS = 256;
 
-__device__ __forceinline__ float swiglu1(float g, float u, float limit) {
-    if (limit > 0.0f) {
-        g = fminf(g, limit);
-        u = fminf(fmaxf(u, -limit), limit);
-    }
-    return g / (1.0f + expf(-g)) * u;
-}
-
 // n values; with ids, the values form rows of row_len (a multiple of 4) and a row
 // whose pair has an expert id outside [0, n_expert) is written as zeros.
 __global__ void __launch_bounds__(FFN_THREADS) k_swiglu(float *__restrict__ mid, const float *__restrict__ gate,

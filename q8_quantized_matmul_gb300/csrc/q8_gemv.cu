@@ -46,6 +46,10 @@
 //     2^14, block sums below 2^24); it is then scaled by d_w*d_x and added in
 //     fp32 with packed f32x2 instructions.  fp16 rather than int8 MMA: on GB300
 //     mma.sync runs int8 at 251 and fp16 at 942 MAC per SM per clock (measured).
+//   * Gate/up pair (the routed FFN's first step, ds4 GPU code walkthrough, trace 5):
+//     an item streams the gate's sub-items and then the up's, same rows, against
+//     one staging of its activations; their results are staged side by side and
+//     the epilogue writes swiglu1(gate, up) instead of either product.
 //   * Small activations (at most 8 tokens, 1024 token-block pairs per CTA) are
 //     quantised by the consumer warps themselves from the fp32 rows, with the
 //     quantiser kernels' arithmetic: one kernel per call.  Otherwise the
@@ -265,27 +269,29 @@ __device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
 // is issued, and consumers release only slots whose copy they saw land, so a
 // slot never has two copies in flight: the drain at the end waits for each
 // slot's last armed round only.  Returns the number of slots planned.
-template <int TOKG>
-__device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorMap *tmap, uint8_t *ring, uint64_t *full,
-                                            uint64_t *empty, volatile uint32_t *armed, volatile int *abort_flag,
-                                            int lane, uint64_t lim) {
+template <int TOKG, bool PAIR>
+__device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorMap *tmap, const CUtensorMap *tmap2,
+                                            uint8_t *ring, uint64_t *full, uint64_t *empty, volatile uint32_t *armed,
+                                            volatile int *abort_flag, int lane, uint64_t lim) {
     using namespace gv;
     const uint32_t nk = (p.nb + KC - 1) / KC;
     uint32_t seqbase = 0;
     GItem it;
     for (int item_i = blockIdx.x; gemv_item<TOKG>(p, item_i, it); item_i += gridDim.x) {
-        const uint32_t nsub = (it.nrows + ROWS - 1) / ROWS;
+        const uint32_t nh = (it.nrows + ROWS - 1) / ROWS;   // sub-items of one matrix
+        const uint32_t nsub = PAIR ? 2 * nh : nh;           // a pair: the gate's, then the up's
         const uint32_t total = nk * nsub;
         for (uint32_t base = 0; base < total; base += 32) {
             const uint32_t idx = base + (uint32_t)lane;
             if (idx < total) {
                 const uint32_t seq = seqbase + idx, slot = seq % NSLOT;
                 const uint32_t kk = idx / nsub, sub = idx - kk * nsub;
+                const bool second = sub >= nh;
                 if (!p.withhold && mbar_wait(&empty[slot], ((seq / NSLOT) & 1u) ^ 1u, p.err, abort_flag, lim) &&
                     !*abort_flag) {
                     mbar_arrive_expect_tx(&full[slot], SLOT);
-                    tma_load_3d(ring + (size_t)slot * SLOT, tmap, (int)(kk * (KC * QB / 4)),
-                                (int)(it.r0 + sub * ROWS), it.expert, &full[slot]);
+                    tma_load_3d(ring + (size_t)slot * SLOT, second ? tmap2 : tmap, (int)(kk * (KC * QB / 4)),
+                                (int)(it.r0 + (second ? sub - nh : sub) * ROWS), it.expert, &full[slot]);
                     __threadfence_block();
                     armed[slot] = seq / NSLOT;
                 }
@@ -614,8 +620,10 @@ __device__ __forceinline__ void slot_mma(const uint8_t *sbase, const uint8_t *ac
     }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, const __grid_constant__ CUtensorMap tmap) {
+// PAIR: the gate/up pair of GemvParams::W2 (grouped calls only).
+template <int MODE, bool PAIR>
+__global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, const __grid_constant__ CUtensorMap tmap,
+                                                           const __grid_constant__ CUtensorMap tmap2) {
     using namespace gv;
     using M = Mode<MODE>;
     constexpr int NT = M::NT;
@@ -640,6 +648,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
         if (s == 0) {
             *abort_flag = 0;
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+            if (PAIR) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap2)) : "memory");
         }
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
@@ -651,7 +660,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     const uint64_t lim = wait_limit(p.wait_ns);
     if (warp == PRODUCER) {
         if (!p.weights_early) grid_dep_wait();
-        produce<M::TOKG>(p, &tmap, ring, full, empty, armed, abort_flag, lane, lim);
+        produce<M::TOKG, PAIR>(p, &tmap, &tmap2, ring, full, empty, armed, abort_flag, lane, lim);
         // Every weight copy of this CTA is issued: a kernel launched behind this one
         // with programmatic serialisation may take the SMs freed from here on (its
         // reads of anything this grid writes wait in griddepcontrol.wait).
@@ -678,7 +687,11 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     for (int item_i = blockIdx.x;; item_i += gridDim.x) {
         GItem it;
         if (!gemv_item<M::TOKG>(p, item_i, it)) break;
-        const uint32_t nsub = (it.nrows + ROWS - 1) / ROWS;
+        // sub-items: with a gate/up pair, nh of the gate and then nh of the up;
+        // sub-item v's results are staged at local row 16v + r, so the up rows
+        // follow the gate rows at 16 nh
+        const uint32_t nh = (it.nrows + ROWS - 1) / ROWS;
+        const uint32_t nsub = PAIR ? 2 * nh : nh;
         const uint32_t wpi = item_wpi(nsub, nk);
         const uint32_t ngroups = (uint32_t)NCW / wpi;
         const uint32_t slice = (uint32_t)warp % wpi, grp = (uint32_t)warp / wpi;
@@ -732,6 +745,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             }
         }
         seqbase += nk * nsub;
+        const uint32_t nh_e = (it.nrows + ROWS - 1) / ROWS;   // recomputed: not kept live through the stream
 
         if (MODE != 0) {
 #pragma unroll
@@ -789,8 +803,9 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 #pragma unroll
                         for (int e = 0; e < NACC; ++e) {
                             const int tok = e >> 2;
-                            const uint32_t lr = sub * ROWS + (uint32_t)dp4a_row(rb, e & 3);
-                            if (tok < it.ntok && lr < it.nrows) obuf[tok * OUT_STRIDE + lr] = accf[s2][e];
+                            const uint32_t rr = (uint32_t)dp4a_row(rb, e & 3);
+                            const uint32_t hr = (sub < nh_e ? sub : sub - nh_e) * ROWS + rr;   // row in its matrix
+                            if (tok < it.ntok && hr < it.nrows) obuf[tok * OUT_STRIDE + sub * ROWS + rr] = accf[s2][e];
                         }
                     }
                 }
@@ -806,8 +821,10 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tok = t * 8 + 2 * c + (e & 1);
-                            const uint32_t lr = sub * ROWS + g + ((e & 2) ? 8 : 0);
-                            if (tok < it.ntok && lr < it.nrows) obuf[tok * OUT_STRIDE + lr] = accf[s2][t * 4 + e];
+                            const uint32_t rr = (uint32_t)g + ((e & 2) ? 8u : 0u);
+                            const uint32_t hr = (sub < nh_e ? sub : sub - nh_e) * ROWS + rr;   // row in its matrix
+                            if (tok < it.ntok && hr < it.nrows)
+                                obuf[tok * OUT_STRIDE + sub * ROWS + rr] = accf[s2][t * 4 + e];
                         }
                     }
                 }
@@ -821,15 +838,25 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * nv; e += CONSUMER_THREADS) {
                 const uint32_t tok = e / nv, i = e - tok * nv;
                 const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
-                if (orow >= 0)
-                    *reinterpret_cast<float4 *>(p.out + (uint64_t)orow * p.out_dim + it.r0 + 4 * i) =
-                        *reinterpret_cast<const float4 *>(obuf + tok * OUT_STRIDE + 4 * i);
+                if (orow >= 0) {
+                    float4 v = *reinterpret_cast<const float4 *>(obuf + tok * OUT_STRIDE + 4 * i);
+                    if (PAIR) {
+                        const float4 u = *reinterpret_cast<const float4 *>(obuf + tok * OUT_STRIDE + nh_e * ROWS + 4 * i);
+                        v = make_float4(swiglu1(v.x, u.x, p.limit), swiglu1(v.y, u.y, p.limit),
+                                        swiglu1(v.z, u.z, p.limit), swiglu1(v.w, u.w, p.limit));
+                    }
+                    *reinterpret_cast<float4 *>(p.out + (uint64_t)orow * p.out_dim + it.r0 + 4 * i) = v;
+                }
             }
         } else {
             for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * it.nrows; e += CONSUMER_THREADS) {
                 const uint32_t tok = e / it.nrows, i = e - tok * it.nrows;
                 const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
-                if (orow >= 0) p.out[(uint64_t)orow * p.out_dim + it.r0 + i] = obuf[tok * OUT_STRIDE + i];
+                if (orow >= 0) {
+                    float v = obuf[tok * OUT_STRIDE + i];
+                    if (PAIR) v = swiglu1(v, obuf[tok * OUT_STRIDE + nh_e * ROWS + i], p.limit);
+                    p.out[(uint64_t)orow * p.out_dim + it.r0 + i] = v;
+                }
             }
         }
     }
@@ -840,20 +867,33 @@ bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint6
                       uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
 cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st) {
-    static bool attr_done[3] = {false, false, false};
-    if (mode < 0 || mode > 2) return cudaErrorInvalidValue;
-    const void *fn = mode == 0 ? (const void *)k_gemv<0> : (mode == 1 ? (const void *)k_gemv<1> : (const void *)k_gemv<2>);
-    if (!attr_done[mode]) {
+    static bool attr_done[5] = {false, false, false, false, false};
+    if (mode < 0 || mode > 2 || (p.W2 && mode == 0)) return cudaErrorInvalidValue;
+    // variants: modes 0-2, then the gate/up pair for modes 1 and 2 (grouped calls)
+    const int v = p.W2 ? 2 + mode : mode;
+    const void *fns[5] = {(const void *)k_gemv<0, false>, (const void *)k_gemv<1, false>,
+                          (const void *)k_gemv<2, false>, (const void *)k_gemv<1, true>,
+                          (const void *)k_gemv<2, true>};
+    const void *fn = fns[v];
+    if (!attr_done[v]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gv::SMEM);
         if (e != cudaSuccess) return e;
-        attr_done[mode] = true;
+        attr_done[v] = true;
     }
-    alignas(64) CUtensorMap tmap;
+    alignas(64) CUtensorMap tmap, tmap2;
     const uint64_t row_bytes = (uint64_t)p.nb * QB;
     const uint64_t mats = p.plan ? p.n_expert : 1;
-    if (!encode_rows_tmap(&tmap, p.W, row_bytes, p.out_dim, mats, p.plan ? p.expert_stride : (uint64_t)p.out_dim * row_bytes,
-                          gv::BOX_WORDS, gv::ROWS))
+    const uint64_t mstride = p.plan ? p.expert_stride : (uint64_t)p.out_dim * row_bytes;
+    if (!encode_rows_tmap(&tmap, p.W, row_bytes, p.out_dim, mats, mstride, gv::BOX_WORDS, gv::ROWS))
         return cudaErrorInvalidValue;
+    if (p.W2) {
+        // the pair's staged results take 2 x rows_per_item floats a token
+        if (!p.plan || p.rows_per_item > gv::OUT_STRIDE / 2) return cudaErrorInvalidValue;
+        if (!encode_rows_tmap(&tmap2, p.W2, row_bytes, p.out_dim, mats, mstride, gv::BOX_WORDS, gv::ROWS))
+            return cudaErrorInvalidValue;
+    } else {
+        tmap2 = tmap;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(gv::NTHREADS);
@@ -865,7 +905,7 @@ cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     GemvParams pp = p;
-    void *args[] = {&pp, &tmap};
+    void *args[] = {&pp, &tmap, &tmap2};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -112,6 +112,12 @@ struct GemvParams {
     const PlanHeader *plan;    // grouped: class plan; nullptr: dense
     const int32_t *row_to_out;
     uint32_t n_expert;         // grouped: number of expert matrices
+    // Gate/up pair (grouped only; nullptr otherwise): W holds the gate and W2 the up
+    // projections (same shape and expert stride).  An item streams both row ranges
+    // against one staging of its activations, and out receives
+    // swiglu1(gate, up, limit) instead of either product; rows_per_item <= 256.
+    const uint8_t *W2;
+    float limit;
     // Failure-detection test hook (zero in normal calls): wait_ns limits every wait
     // (0: the 2 s default); withhold != 0 makes the producer issue no copy, so the
     // consumers' waits run out, the kernel raises Q8_ETIMEOUT and returns.

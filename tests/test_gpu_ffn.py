@@ -184,6 +184,7 @@ def test_moe_ffn_exact_instance(q8, o, n_exp, in_dim, mid_dim, out_dim, n_tok, k
 @pytest.mark.parametrize("n_exp,in_dim,mid_dim,out_dim,n_tok,k,limit", [
     (16, 512, 256, 384, 24, 4, 10.0),    # routed GEMV, clamp on
     (16, 512, 256, 384, 24, 4, 0.0),     # clamp off
+    (64, 1024, 480, 256, 40, 6, 10.0),   # gate/up pair items of 224, 224 and 32 rows, both GEMV classes
     (8, 256, 256, 256, 512, 2, 10.0),    # tensor-core class for gate, up and down
     (6, 96, 64, 40, 5, 2, 10.0),         # generic kernel
 ])
