@@ -728,6 +728,97 @@ int q8_moe_combine(float *out, const float *y, const float *weights, uint64_t n_
     return status_of(q8::launch_combine(out, y, weights, n_tok, k, dim, sms, static_cast<cudaStream_t>(stream)));
 }
 
+// The routed FFN when every expert group of both projections is on the GEMV (in_dim
+// and mid_dim multiples of 256, fewer than 1024 pairs): one routing serves both.
+// Plane rows depend only on the pairs, and a GEMV counts its items from its own
+// width (GemvParams::plan_rb), so: routing -> gathering quantiser of x -> gate/up
+// pair GEMVs writing mid as Q8_0 planes at the pairs' plane rows -> down GEMVs on
+// those planes -> weighted sum.  The routing zeroes y's row of a pair with a bad id.
+static int ffn_gemv_run(DeviceState *s, const MoeCall &gu, const MoeLayout &L, const void *W_down,
+                        uint64_t down_stride, uint64_t out_dim, float limit, const float *expert_weights, float *out,
+                        cudaStream_t st) {
+    const uint64_t mid_dim = gu.out_dim;
+    const uint64_t nbm = mid_dim / q8::QK;
+    if ((L.nb % 8) || (nbm % 8) || L.tc_cap) return Q8_EINVAL;
+    int rc;
+    const size_t region = align256(L.need);
+    if ((rc = reserve_scratch(s, region + planes_bytes(L.max_rows, mid_dim) + align256(L.n_pairs * out_dim * 4))))
+        return rc;
+    Carver cv(s->scratch);
+    int32_t *counts = cv.take<int32_t>(gu.n_expert * 4);
+    int32_t *row0_of = cv.take<int32_t>(gu.n_expert * 4);
+    uint8_t *plans = cv.take<uint8_t>(q8::ROUTE_CLASSES * L.plan_bytes);
+    int32_t *row_to_out = cv.take<int32_t>(L.max_rows * 4);
+    int32_t *src_row = cv.take<int32_t>(L.max_rows * 4);
+    int32_t *dst_row = cv.take<int32_t>(L.n_pairs * 4);
+    int8_t *qx = cv.take<int8_t>(L.max_rows * gu.in_dim);
+    float *dx = cv.take<float>(L.max_rows * L.nb * sizeof(float));
+    Carver cv2(static_cast<uint8_t *>(s->scratch) + region);
+    int8_t *qmid = cv2.take<int8_t>(L.max_rows * mid_dim);
+    float *dmid = cv2.take<float>(L.max_rows * nbm * sizeof(float));
+    float *y = cv2.take<float>(L.n_pairs * out_dim * 4);
+    // pair items of 224 rows of each matrix (14 + 14 sub-items); the routing counts
+    // its items for the down projection's width
+    const uint32_t rows_pair = mid_dim < 224 ? (uint32_t)mid_dim : 224u;
+    uint32_t rows_down = (uint32_t)((out_dim + 15) & ~(uint64_t)15);
+    if (rows_down > 448) rows_down = 448;
+    const uint32_t rows_route = 224;
+    const uint32_t plan_rb = (uint32_t)((out_dim + rows_route - 1) / rows_route);
+    cudaError_t e = q8::launch_route(gu.ids, gu.n_tok, gu.k, gu.n_expert, 0, (uint32_t)out_dim, rows_route, 0, counts,
+                                     row0_of, plans, row_to_out, src_row, dst_row, L.max_rows, y, s->err, s->num_sms,
+                                     st);
+    if (e != cudaSuccess) return status_of(e);
+    e = q8::launch_quantize_pairs(qx, dx, nullptr, nullptr, 0, nullptr, gu.x, gu.in_dim, L.n_pairs, gu.k, 0, dst_row,
+                                  s->num_sms, st);
+    if (e != cudaSuccess) return status_of(e);
+    auto plan_of = [&](int cls) { return reinterpret_cast<const q8::PlanHeader *>(plans + cls * L.plan_bytes); };
+    q8::GemvParams g{};
+    g.W = static_cast<const uint8_t *>(gu.W[0]);
+    g.W2 = static_cast<const uint8_t *>(gu.W[1]);
+    g.expert_stride = gu.stride;
+    g.in_dim = gu.in_dim;
+    g.out_dim = (uint32_t)mid_dim;
+    g.nb = (uint32_t)L.nb;
+    g.qx = qx;
+    g.dx = dx;
+    g.err = s->err;
+    g.rows_per_item = rows_pair;
+    g.plan_rb = plan_rb;
+    g.weights_early = 1;   // behind this library's quantiser
+    g.row_to_out = row_to_out;
+    g.n_expert = gu.n_expert;
+    g.limit = limit;
+    g.q_out = qmid;
+    g.d_out = dmid;
+    auto classes = [&](q8::GemvParams &gp) {
+        return timed_launch(st, [&] {
+            gp.plan = plan_of(0);
+            cudaError_t e2 = q8::launch_gemv(gp, 1, s->num_sms, st);
+            if (e2 != cudaSuccess) return e2;
+            gp.plan = plan_of(1);
+            return q8::launch_gemv(gp, 2, s->num_sms, st);
+        });
+    };
+    if ((rc = status_of(classes(g)))) return rc;
+    q8::GemvParams d{};
+    d.W = static_cast<const uint8_t *>(W_down);
+    d.expert_stride = down_stride;
+    d.in_dim = mid_dim;
+    d.out_dim = (uint32_t)out_dim;
+    d.nb = (uint32_t)nbm;
+    d.qx = qmid;
+    d.dx = dmid;
+    d.out = y;
+    d.err = s->err;
+    d.rows_per_item = rows_down;
+    d.plan_rb = plan_rb;
+    d.weights_early = 1;   // behind the pair GEMV, which writes no weights
+    d.row_to_out = row_to_out;
+    d.n_expert = gu.n_expert;
+    if ((rc = status_of(classes(d)))) return rc;
+    return status_of(q8::launch_combine(out, y, expert_weights, gu.n_tok, gu.k, out_dim, s->num_sms, st));
+}
+
 int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_down, uint32_t n_expert,
                uint64_t gate_up_stride_bytes, uint64_t down_stride_bytes, const int32_t *expert_ids,
                const float *expert_weights, uint32_t k, uint64_t in_dim, uint64_t mid_dim, uint64_t out_dim,
@@ -770,6 +861,8 @@ int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_d
     dn.out_dim = out_dim;
     dn.x_per_pair = 1;
     const MoeLayout Lgu = moe_layout(gu), Ldn = moe_layout(dn);
+    if (Lgu.gemv_path && Ldn.gemv_path && !Lgu.tc_cap && !Ldn.tc_cap)
+        return ffn_gemv_run(s, gu, Lgu, W_down, down_stride_bytes, out_dim, limit, expert_weights, out, st);
     // scratch: the routed calls' region (reused by both), then gate, up, mid and y
     const size_t region = align256(Lgu.need > Ldn.need ? Lgu.need : Ldn.need);
     const size_t mid_bytes = align256(n_pairs * mid_dim * 4);
@@ -780,10 +873,11 @@ int q8_moe_ffn(float *out, const void *W_gate, const void *W_up, const void *W_d
     float *mid = cv.take<float>(n_pairs * mid_dim * 4);
     float *y = cv.take<float>(n_pairs * out_dim * 4);
     if (Lgu.gemv_path && !Lgu.tc_cap) {
-        // Every expert group on the GEMV (decode sizes): gate and up rows stream
-        // through one kernel per class against one staging of the activations, and
-        // its epilogue writes mid = swiglu1(gate, up).  The routing zeroes the mid
-        // row of a pair with a bad id.
+        // Every gate/up group on the GEMV, the down projection not (mid_dim not a
+        // multiple of 256): gate and up rows stream through one kernel per class
+        // against one staging of the activations, and its epilogue writes
+        // mid = swiglu1(gate, up) as fp32 rows.  The routing zeroes the mid row of
+        // a pair with a bad id.
         gu.pair = true;
         gu.limit = limit;
         gu.out[0] = mid;

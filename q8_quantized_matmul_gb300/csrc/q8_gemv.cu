@@ -189,9 +189,14 @@ struct GItem {
     uint32_t nrows;
 };
 
-template <int TOKG>
+// Kernel kinds: the dense product, a grouped (routed) one, a grouped gate/up pair.
+constexpr int KIND_DENSE = 0, KIND_GROUPED = 1, KIND_PAIR = 2;
+
+// GROUPED: p.plan is set (the variants are separate so that the dense kernel
+// carries none of the plan decoding).
+template <int TOKG, bool GROUPED>
 __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it) {
-    if (!p.plan) {
+    if constexpr (!GROUPED) {
         // dense: n_items contiguous ranges of whole sub-items, sizes differing by at
         // most one (the split is computed on the host: a 64-bit division here
         // would delay the first weight copy)
@@ -206,18 +211,22 @@ __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it)
         it.r0 = s0 * gv::ROWS;
         it.nrows = min((s1 - s0) * gv::ROWS, p.out_dim - it.r0);
         return true;
-    }
-    if (i >= p.plan->n_items) return false;
+    } else {
+    // A GEMV class's segments start at multiples of the plan's row blocks per
+    // token group, so item_start / prb counts the token groups before a segment.
+    const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
+    const int prb = p.plan_rb ? (int)p.plan_rb : n_rb;
+    if (i >= p.plan->n_items / prb * n_rb) return false;
+    const int gstart = i / n_rb * prb;   // the item's token group, in the plan's item units
     const Segment *segs = reinterpret_cast<const Segment *>(p.plan + 1);
     int lo = 0, hi = p.plan->n_segments - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (segs[mid].item_start <= i) lo = mid;
+        if (segs[mid].item_start <= gstart) lo = mid;
         else hi = mid - 1;
     }
     const Segment s = segs[lo];
-    const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
-    const int local = i - s.item_start;
+    const int local = i - s.item_start / prb * n_rb;
     const int tg = local / n_rb, rb = local - tg * n_rb;
     it.expert = s.expert;
     it.tok0 = tg * TOKG;
@@ -226,6 +235,7 @@ __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it)
     it.r0 = (uint32_t)rb * p.rows_per_item;
     it.nrows = min(p.rows_per_item, p.out_dim - it.r0);
     return true;
+    }
 }
 
 // Bounded wait until the producer has armed round r of a slot.
@@ -269,7 +279,7 @@ __device__ __forceinline__ uint32_t item_wpi(uint32_t nsub, uint32_t nk) {
 // is issued, and consumers release only slots whose copy they saw land, so a
 // slot never has two copies in flight: the drain at the end waits for each
 // slot's last armed round only.  Returns the number of slots planned.
-template <int TOKG, bool PAIR>
+template <int TOKG, int KIND>
 __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorMap *tmap, const CUtensorMap *tmap2,
                                             uint8_t *ring, uint64_t *full, uint64_t *empty, volatile uint32_t *armed,
                                             volatile int *abort_flag, int lane, uint64_t lim) {
@@ -277,7 +287,8 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
     const uint32_t nk = (p.nb + KC - 1) / KC;
     uint32_t seqbase = 0;
     GItem it;
-    for (int item_i = blockIdx.x; gemv_item<TOKG>(p, item_i, it); item_i += gridDim.x) {
+    constexpr bool PAIR = KIND == KIND_PAIR;
+    for (int item_i = blockIdx.x; gemv_item<TOKG, KIND != KIND_DENSE>(p, item_i, it); item_i += gridDim.x) {
         const uint32_t nh = (it.nrows + ROWS - 1) / ROWS;   // sub-items of one matrix
         const uint32_t nsub = PAIR ? 2 * nh : nh;           // a pair: the gate's, then the up's
         const uint32_t total = nk * nsub;
@@ -286,7 +297,7 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
             if (idx < total) {
                 const uint32_t seq = seqbase + idx, slot = seq % NSLOT;
                 const uint32_t kk = idx / nsub, sub = idx - kk * nsub;
-                const bool second = sub >= nh;
+                const bool second = PAIR && sub >= nh;
                 if (!p.withhold && mbar_wait(&empty[slot], ((seq / NSLOT) & 1u) ^ 1u, p.err, abort_flag, lim) &&
                     !*abort_flag) {
                     mbar_arrive_expect_tx(&full[slot], SLOT);
@@ -620,12 +631,16 @@ __device__ __forceinline__ void slot_mma(const uint8_t *sbase, const uint8_t *ac
     }
 }
 
-// PAIR: the gate/up pair of GemvParams::W2 (grouped calls only).
-template <int MODE, bool PAIR>
+// KIND: dense, grouped, or the grouped gate/up pair of GemvParams::W2.
+// SUBM: sub-items a consumer warp holds in one item (items of at most 14 SUBM
+// sub-items); the accumulators take SUBM x NT x 2 registers pairs, so the host
+// picks the smallest that covers the call's items.
+template <int MODE, int KIND, int SUBM>
 __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, const __grid_constant__ CUtensorMap tmap,
                                                            const __grid_constant__ CUtensorMap tmap2) {
     using namespace gv;
     using M = Mode<MODE>;
+    constexpr bool PAIR = KIND == KIND_PAIR;
     constexpr int NT = M::NT;
     constexpr int KA = M::KA;
     constexpr int NACC = M::NACC;
@@ -660,7 +675,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     const uint64_t lim = wait_limit(p.wait_ns);
     if (warp == PRODUCER) {
         if (!p.weights_early) grid_dep_wait();
-        produce<M::TOKG, PAIR>(p, &tmap, &tmap2, ring, full, empty, armed, abort_flag, lane, lim);
+        produce<M::TOKG, KIND>(p, &tmap, &tmap2, ring, full, empty, armed, abort_flag, lane, lim);
         // Every weight copy of this CTA is issued: a kernel launched behind this one
         // with programmatic serialisation may take the SMs freed from here on (its
         // reads of anything this grid writes wait in griddepcontrol.wait).
@@ -686,7 +701,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 
     for (int item_i = blockIdx.x;; item_i += gridDim.x) {
         GItem it;
-        if (!gemv_item<M::TOKG>(p, item_i, it)) break;
+        if (!gemv_item<M::TOKG, KIND != KIND_DENSE>(p, item_i, it)) break;
         // sub-items: with a gate/up pair, nh of the gate and then nh of the up;
         // sub-item v's results are staged at local row 16v + r, so the up rows
         // follow the gate rows at 16 nh
@@ -700,10 +715,10 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             waited_dep = true;
         }
 
-        float accf[SUBMAX][NACC];
-        uint64_t acc[SUBMAX][NT][2];
+        float accf[SUBM][NACC];
+        uint64_t acc[SUBM][NT][2];
 #pragma unroll
-        for (int s2 = 0; s2 < SUBMAX; ++s2) {
+        for (int s2 = 0; s2 < SUBM; ++s2) {
 #pragma unroll
             for (int e = 0; e < NACC; ++e) accf[s2][e] = 0.0f;
 #pragma unroll
@@ -723,7 +738,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                 if (kb >= kb0 + ka) break;                     // belongs to the next chunk
                 const uint32_t bl0 = kb - kb0;
 #pragma unroll
-                for (int s2 = 0; s2 < SUBMAX; ++s2) {
+                for (int s2 = 0; s2 < SUBM; ++s2) {
                     const uint32_t sub = grp + (uint32_t)s2 * ngroups;
                     if (sub < nsub) {
                         const uint32_t seq = seqbase + kk * nsub + sub;
@@ -749,7 +764,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 
         if (MODE != 0) {
 #pragma unroll
-            for (int s2 = 0; s2 < SUBMAX; ++s2)
+            for (int s2 = 0; s2 < SUBM; ++s2)
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     accf[s2][t * 4 + 0] = lo_of(acc[s2][t][0]);
@@ -785,7 +800,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
         if (MODE == 0) {
             // add the 8 block columns of each row (lanes differing in bits 0-2)
 #pragma unroll
-            for (int s2 = 0; s2 < SUBMAX; ++s2)
+            for (int s2 = 0; s2 < SUBM; ++s2)
 #pragma unroll
                 for (int e = 0; e < NACC; ++e) {
                     float v = accf[s2][e];
@@ -797,14 +812,14 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             if (slice == 0 && (lane & 7) == 0) {
                 const int rb = lane >> 3;
 #pragma unroll
-                for (int s2 = 0; s2 < SUBMAX; ++s2) {
+                for (int s2 = 0; s2 < SUBM; ++s2) {
                     const uint32_t sub = grp + (uint32_t)s2 * ngroups;
                     if (sub < nsub) {
 #pragma unroll
                         for (int e = 0; e < NACC; ++e) {
                             const int tok = e >> 2;
                             const uint32_t rr = (uint32_t)dp4a_row(rb, e & 3);
-                            const uint32_t hr = (sub < nh_e ? sub : sub - nh_e) * ROWS + rr;   // row in its matrix
+                            const uint32_t hr = (PAIR && sub >= nh_e ? sub - nh_e : sub) * ROWS + rr;   // row in its matrix
                             if (tok < it.ntok && hr < it.nrows) obuf[tok * OUT_STRIDE + sub * ROWS + rr] = accf[s2][e];
                         }
                     }
@@ -813,7 +828,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
         } else if (slice == 0) {
             const int g = lane >> 2, c = lane & 3;
 #pragma unroll
-            for (int s2 = 0; s2 < SUBMAX; ++s2) {
+            for (int s2 = 0; s2 < SUBM; ++s2) {
                 const uint32_t sub = grp + (uint32_t)s2 * ngroups;
                 if (sub < nsub) {
 #pragma unroll
@@ -822,7 +837,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                         for (int e = 0; e < 4; ++e) {
                             const int tok = t * 8 + 2 * c + (e & 1);
                             const uint32_t rr = (uint32_t)g + ((e & 2) ? 8u : 0u);
-                            const uint32_t hr = (sub < nh_e ? sub : sub - nh_e) * ROWS + rr;   // row in its matrix
+                            const uint32_t hr = (PAIR && sub >= nh_e ? sub - nh_e : sub) * ROWS + rr;   // row in its matrix
                             if (tok < it.ntok && hr < it.nrows)
                                 obuf[tok * OUT_STRIDE + sub * ROWS + rr] = accf[s2][t * 4 + e];
                         }
@@ -831,13 +846,43 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             }
         }
         named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
-        if ((p.out_dim & 3u) == 0) {
+        if (PAIR && p.q_out) {
+            // mid = swiglu1(gate, up) as Q8_0 planes at the pair's activation-plane row:
+            // four lanes a 32-value block (item rows and r0 are multiples of 32).  All
+            // consumer threads run the same trips: the quantiser shuffles within a warp.
+            const uint32_t nblk = it.nrows / QK, nbm = p.out_dim / QK;
+            const uint32_t total = (uint32_t)it.ntok * nblk * 4;
+            for (uint32_t base = 0; base < total; base += CONSUMER_THREADS) {
+                const uint32_t e = base + threadIdx.x;
+                const bool live = e < total;
+                const uint32_t tok = live ? (e >> 2) / nblk : 0u, b = live ? (e >> 2) - tok * nblk : 0u;
+                const uint32_t c0 = b * QK + (e & 3u) * 8;   // first of this lane's 8 values
+                float v8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    v8[j] = live ? swiglu1(obuf[tok * OUT_STRIDE + c0 + j], obuf[tok * OUT_STRIDE + nh_e * ROWS + c0 + j],
+                                           p.limit)
+                                 : 0.0f;
+                const QuantBlock qb = quantize8(v8);
+                if (live) {
+                    const uint64_t row = (uint64_t)(it.xrow0 + (int)tok);
+                    uint32_t lo = 0, hi = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        lo |= (uint32_t)(uint8_t)qb.q[j] << (8 * j);
+                        hi |= (uint32_t)(uint8_t)qb.q[4 + j] << (8 * j);
+                    }
+                    *reinterpret_cast<uint2 *>(p.q_out + row * p.out_dim + it.r0 + c0) = make_uint2(lo, hi);
+                    if ((e & 3u) == 0) p.d_out[row * nbm + it.r0 / QK + b] = qb.d_stored;
+                }
+            }
+        } else if ((p.out_dim & 3u) == 0) {
             // every run starts 16-byte aligned (out is, r0 is a multiple of 16, out_dim of 4)
             // and is a whole number of float4 (nrows is a multiple of 4)
             const uint32_t nv = it.nrows >> 2;
             for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * nv; e += CONSUMER_THREADS) {
                 const uint32_t tok = e / nv, i = e - tok * nv;
-                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
+                const int64_t orow = KIND != KIND_DENSE ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
                 if (orow >= 0) {
                     float4 v = *reinterpret_cast<const float4 *>(obuf + tok * OUT_STRIDE + 4 * i);
                     if (PAIR) {
@@ -851,7 +896,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
         } else {
             for (uint32_t e = threadIdx.x; e < (uint32_t)it.ntok * it.nrows; e += CONSUMER_THREADS) {
                 const uint32_t tok = e / it.nrows, i = e - tok * it.nrows;
-                const int64_t orow = p.plan ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
+                const int64_t orow = KIND != KIND_DENSE ? (int64_t)p.row_to_out[it.xrow0 + tok] : (int64_t)(it.tok0 + tok);
                 if (orow >= 0) {
                     float v = obuf[tok * OUT_STRIDE + i];
                     if (PAIR) v = swiglu1(v, obuf[tok * OUT_STRIDE + nh_e * ROWS + i], p.limit);
@@ -866,19 +911,42 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
 bool encode_rows_tmap(CUtensorMap *map, const void *W, uint64_t row_bytes, uint64_t rows, uint64_t n_mat,
                       uint64_t mat_stride, uint32_t box_words, uint32_t box_rows);
 
+// The kernel variant of a call: kind, mode and sub-items per warp.
+template <int KIND, int SUBM> static const void *gemv_fn(int mode) {
+    if constexpr (KIND == KIND_DENSE) {
+        return mode == 0 ? (const void *)k_gemv<0, KIND, SUBM>
+                         : (mode == 1 ? (const void *)k_gemv<1, KIND, SUBM> : (const void *)k_gemv<2, KIND, SUBM>);
+    } else {
+        return mode == 1 ? (const void *)k_gemv<1, KIND, SUBM> : (const void *)k_gemv<2, KIND, SUBM>;
+    }
+}
+
 cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st) {
-    static bool attr_done[5] = {false, false, false, false, false};
-    if (mode < 0 || mode > 2 || (p.W2 && mode == 0)) return cudaErrorInvalidValue;
-    // variants: modes 0-2, then the gate/up pair for modes 1 and 2 (grouped calls)
-    const int v = p.W2 ? 2 + mode : mode;
-    const void *fns[5] = {(const void *)k_gemv<0, false>, (const void *)k_gemv<1, false>,
-                          (const void *)k_gemv<2, false>, (const void *)k_gemv<1, true>,
-                          (const void *)k_gemv<2, true>};
-    const void *fn = fns[v];
-    if (!attr_done[v]) {
+    if (mode < 0 || mode > 2 || (p.plan && mode == 0) || (p.W2 && !p.plan) || (p.q_out && !p.W2))
+        return cudaErrorInvalidValue;
+    const int kind = !p.plan ? KIND_DENSE : (p.W2 ? KIND_PAIR : KIND_GROUPED);
+    // the most sub-items of one item (a pair's gate and up sub-items both count)
+    uint32_t max_sub = !p.plan ? p.sub_base + (p.sub_rem ? 1u : 0u) : (p.rows_per_item + gv::ROWS - 1) / gv::ROWS;
+    if (kind == KIND_PAIR) max_sub *= 2;
+    const int subm = (int)((max_sub + gv::NCW - 1) / gv::NCW);
+    if (subm < 1 || subm > (kind == KIND_DENSE ? 3 : 2)) return cudaErrorInvalidValue;
+    static const void *const fns[3][3][3] = {
+        {{gemv_fn<KIND_DENSE, 1>(0), gemv_fn<KIND_DENSE, 1>(1), gemv_fn<KIND_DENSE, 1>(2)},
+         {gemv_fn<KIND_DENSE, 2>(0), gemv_fn<KIND_DENSE, 2>(1), gemv_fn<KIND_DENSE, 2>(2)},
+         {gemv_fn<KIND_DENSE, 3>(0), gemv_fn<KIND_DENSE, 3>(1), gemv_fn<KIND_DENSE, 3>(2)}},
+        {{nullptr, gemv_fn<KIND_GROUPED, 1>(1), gemv_fn<KIND_GROUPED, 1>(2)},
+         {nullptr, gemv_fn<KIND_GROUPED, 2>(1), gemv_fn<KIND_GROUPED, 2>(2)},
+         {nullptr, nullptr, nullptr}},
+        {{nullptr, gemv_fn<KIND_PAIR, 1>(1), gemv_fn<KIND_PAIR, 1>(2)},
+         {nullptr, gemv_fn<KIND_PAIR, 2>(1), gemv_fn<KIND_PAIR, 2>(2)},
+         {nullptr, nullptr, nullptr}}};
+    static bool attr_done[3][3][3] = {};
+    const void *fn = fns[kind][subm - 1][mode];
+    if (!fn) return cudaErrorInvalidValue;
+    if (!attr_done[kind][subm - 1][mode]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gv::SMEM);
         if (e != cudaSuccess) return e;
-        attr_done[v] = true;
+        attr_done[kind][subm - 1][mode] = true;
     }
     alignas(64) CUtensorMap tmap, tmap2;
     const uint64_t row_bytes = (uint64_t)p.nb * QB;
@@ -887,8 +955,10 @@ cudaError_t launch_gemv(const GemvParams &p, int mode, int grid, cudaStream_t st
     if (!encode_rows_tmap(&tmap, p.W, row_bytes, p.out_dim, mats, mstride, gv::BOX_WORDS, gv::ROWS))
         return cudaErrorInvalidValue;
     if (p.W2) {
-        // the pair's staged results take 2 x rows_per_item floats a token
+        // the pair's staged results take 2 x rows_per_item floats a token; Q8_0
+        // output wants whole 32-value blocks in every item
         if (!p.plan || p.rows_per_item > gv::OUT_STRIDE / 2) return cudaErrorInvalidValue;
+        if (p.q_out && (!p.d_out || p.rows_per_item % QK || p.out_dim % QK)) return cudaErrorInvalidValue;
         if (!encode_rows_tmap(&tmap2, p.W2, row_bytes, p.out_dim, mats, mstride, gv::BOX_WORDS, gv::ROWS))
             return cudaErrorInvalidValue;
     } else {

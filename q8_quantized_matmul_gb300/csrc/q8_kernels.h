@@ -118,6 +118,15 @@ struct GemvParams {
     // swiglu1(gate, up, limit) instead of either product; rows_per_item <= 256.
     const uint8_t *W2;
     float limit;
+    // With a pair: q_out / d_out non-null take mid as Q8_0 planes instead of fp32
+    // rows in out (row = the activation-plane row of the pair, out_dim values a row;
+    // the quantiser's arithmetic, so the bits of quantising the fp32 rows).
+    int8_t *q_out;
+    float *d_out;
+    // Grouped: the plan's GEMV items were counted with plan_rb row blocks per token
+    // group (0: this call's own ceil(out_dim / rows_per_item)), so one routing
+    // serves products of different widths.
+    uint32_t plan_rb;
     // Failure-detection test hook (zero in normal calls): wait_ns limits every wait
     // (0: the 2 s default); withhold != 0 makes the producer issue no copy, so the
     // consumers' waits run out, the kernel raises Q8_ETIMEOUT and returns.

@@ -184,7 +184,8 @@ def test_moe_ffn_exact_instance(q8, o, n_exp, in_dim, mid_dim, out_dim, n_tok, k
 @pytest.mark.parametrize("n_exp,in_dim,mid_dim,out_dim,n_tok,k,limit", [
     (16, 512, 256, 384, 24, 4, 10.0),    # routed GEMV, clamp on
     (16, 512, 256, 384, 24, 4, 0.0),     # clamp off
-    (64, 1024, 480, 256, 40, 6, 10.0),   # gate/up pair items of 224, 224 and 32 rows, both GEMV classes
+    (64, 1024, 512, 256, 40, 6, 10.0),   # one routing: pair items of 224, 224, 64 rows write mid as Q8_0
+    (64, 1024, 480, 256, 40, 6, 10.0),   # mid_dim % 256 != 0: pair items (224, 224, 32 rows) write fp32 mid
     (8, 256, 256, 256, 512, 2, 10.0),    # tensor-core class for gate, up and down
     (6, 96, 64, 40, 5, 2, 10.0),         # generic kernel
 ])
@@ -228,8 +229,9 @@ def test_moe_ffn_decode_config_sampled(q8, o):
         assert_ffn_close(got[sl], r, oracle.ffn_tolerance(r, Wd, ds, ids[sl], w[sl], mid_dim, out_dim), f"token {t}")
 
 
-def test_moe_ffn_bad_id_and_determinism(q8, o):
-    n_exp, in_dim, mid_dim, out_dim, n_tok, k = 6, 256, 128, 96, 5, 3
+@pytest.mark.parametrize("mid_dim", [128, 256])   # down on the generic kernel / the one-routing path
+def test_moe_ffn_bad_id_and_determinism(q8, o, mid_dim):
+    n_exp, in_dim, out_dim, n_tok, k = 6, 256, 96, 5, 3
     Wg = inputs.weights(n_exp * mid_dim, in_dim, seed=31).reshape(-1)
     Wu = inputs.weights(n_exp * mid_dim, in_dim, seed=32).reshape(-1)
     Wd = inputs.weights(n_exp * out_dim, mid_dim, seed=33).reshape(-1)
