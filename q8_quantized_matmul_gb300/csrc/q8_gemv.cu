@@ -471,12 +471,7 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
             const uint32_t pr = threadIdx.x / 4 + (r0 + h) * GROUPS;
             const uint32_t t = pr / ka, b = pr - t * ka;
             const QuantBlock qb = quantize8_div(xv[h]);   // all lanes: the block maximum is shuffled
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
-                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
-            }
+            const uint32_t lo = qb.lo, hi = qb.hi;
             if (MODE == 0) {
                 // lane q holds words X[2q] = lo, X[2q+1] = hi; arrange as in stage_chunk
                 const uint32_t nbw = __shfl_sync(0xffffffffu, lo, (threadIdx.x & ~3u) | ((lane_q + 1) & 3u));
@@ -866,13 +861,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
                 const QuantBlock qb = quantize8(v8);
                 if (live) {
                     const uint64_t row = (uint64_t)(it.xrow0 + (int)tok);
-                    uint32_t lo = 0, hi = 0;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        lo |= (uint32_t)(uint8_t)qb.q[j] << (8 * j);
-                        hi |= (uint32_t)(uint8_t)qb.q[4 + j] << (8 * j);
-                    }
-                    *reinterpret_cast<uint2 *>(p.q_out + row * p.out_dim + it.r0 + c0) = make_uint2(lo, hi);
+                    *reinterpret_cast<uint2 *>(p.q_out + row * p.out_dim + it.r0 + c0) = make_uint2(qb.lo, qb.hi);
                     if ((e & 3u) == 0) p.d_out[row * nbm + it.r0 / QK + b] = qb.d_stored;
                 }
             }

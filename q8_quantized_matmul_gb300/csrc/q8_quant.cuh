@@ -19,29 +19,31 @@ namespace q8 {
 
 struct QuantBlock {
     int8_t q[8];      // this lane's eight quants
+    uint32_t lo, hi;  // the same packed: q[0..3], q[4..7] (byte i = q[i])
     uint16_t dh;      // stored binary16 scale (same on the four lanes)
     float d_stored;   // dh as fp32 (exact)
 };
 
-// roundf(x / d), with x / d the IEEE fp32 quotient, without dividing in the
-// common case.  With u = 2^-24 and rd = fl(1/d) = (1/d)(1 + e1), the product
+// 1.5 * 2^23: adding it to |v| < 2^22 rounds v to the nearest integer (ties to
+// even) and leaves that integer, as two's complement, in the low bits of the sum.
+constexpr float ROUND_MAGIC = 12582912.0f;
+
+// x8: this lane's eight values of the block; lanes 4i..4i+3 hold one block.
+//
+// q_i = roundf(x_i / d), with x_i / d the IEEE fp32 quotient, without dividing in
+// the common case.  With u = 2^-24 and rd = fl(1/d) = (1/d)(1 + e1), the product
 // qa = fl(x rd) = (x/d)(1 + e1)(1 + e2) and the quotient fl(x/d) = (x/d)(1 + e3),
 // |e_i| <= u, differ by at most (3u + u^2)|x/d| < 2.3e-5 while |x/d| <= 128.
 // roundf changes value only at half-integers, so when qa is more than 1e-4 from
-// every half-integer (and |qa| < 127.75) both lie on the same side of all of them
-// and roundf(qa) = roundf(fl(x/d)).  Otherwise (about 2e-4 of evenly spread
-// values, and every exact tie) the quotient is taken with the IEEE division; a
-// subnormal d whose reciprocal overflows always takes the division.
-// Away from half-integers roundf and round-half-even agree, so the fast path is
-// one rint and the distance |qa - k| < 0.4999 (exact: k and qa are within 1/2).
-__device__ __forceinline__ float round_quotient(float x, float d, float rd) {
-    const float qa = __fmul_rn(x, rd);
-    const float k = rintf(qa);
-    if (fabsf(__fsub_rn(qa, k)) < 0.4999f && fabsf(qa) < 127.75f) return k;
-    return roundf(__fdiv_rn(x, d));
-}
-
-// x8: this lane's eight values of the block; lanes 4i..4i+3 hold one block.
+// every half-integer both lie on the same side of all of them and roundf(qa) =
+// roundf(fl(x/d)); away from half-integers roundf and round-half-even agree, so
+// the fast path rounds qa with one add of ROUND_MAGIC (the quant is the sum's
+// low byte) and checks the distance |qa - k| < 0.4999 (exact: k and qa are
+// within 1/2).  |qa| <= 127 (1 + 3u), so k never leaves [-127, 127].  A value
+// that fails the check (about 2e-4 of evenly spread values, and every exact tie)
+// takes the IEEE division; so does every value of a block whose d is subnormal
+// enough for its reciprocal to overflow (qa is then infinite or NaN and fails).
+// The warp takes the slow path only when one of its lanes needs it.
 __device__ __forceinline__ QuantBlock quantize8(const float (&x8)[8]) {
     float amax = 0.0f;
 #pragma unroll
@@ -50,15 +52,43 @@ __device__ __forceinline__ QuantBlock quantize8(const float (&x8)[8]) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const float d = __fdiv_rn(amax, 127.0f);
     QuantBlock r;
+    uint32_t w[2] = {0u, 0u};   // packed quants, byte i of w[h] = q[4h + i]
+    uint32_t bad = 0;
     if (d != 0.0f) {
-        const float rd = __frcp_rn(d);   // inf for a subnormal d: every value then takes the division
+        const float rd = __frcp_rn(d);   // inf for a subnormal d: every value then fails the check
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r.q[i] = static_cast<int8_t>(static_cast<int>(round_quotient(x8[i], d, rd)));
+        for (int h = 0; h < 2; ++h) {
+            uint32_t t[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = 4 * h + j;
+                const float qa = __fmul_rn(x8[i], rd);
+                const float sm = __fadd_rn(qa, ROUND_MAGIC);
+                const float k = __fsub_rn(sm, ROUND_MAGIC);
+                t[j] = __float_as_uint(sm);
+                bad |= (fabsf(__fsub_rn(qa, k)) < 0.4999f ? 0u : 1u) << i;
+            }
+            w[h] = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+        }
         r.dh = __half_as_ushort(__float2half_rn(d));
     } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) r.q[i] = 0;
         r.dh = 0;
+    }
+    if (__any_sync(0xffffffffu, bad != 0u)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (bad & (1u << i)) {
+                const uint32_t q = (uint32_t)(uint8_t)(int8_t)(int)roundf(__fdiv_rn(x8[i], d));
+                const int sh = 8 * (i & 3);
+                w[i >> 2] = (w[i >> 2] & ~(0xffu << sh)) | (q << sh);
+            }
+    }
+    r.lo = w[0];
+    r.hi = w[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.q[i] = (int8_t)(r.lo >> (8 * i));
+        r.q[4 + i] = (int8_t)(r.hi >> (8 * i));
     }
     r.d_stored = half_bits_to_float(r.dh);
     return r;
@@ -84,6 +114,12 @@ __device__ __forceinline__ QuantBlock quantize8_div(const float (&x8)[8]) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) r.q[i] = 0;
         r.dh = 0;
+    }
+    r.lo = r.hi = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.lo |= (uint32_t)(uint8_t)r.q[i] << (8 * i);
+        r.hi |= (uint32_t)(uint8_t)r.q[4 + i] << (8 * i);
     }
     r.d_stored = half_bits_to_float(r.dh);
     return r;

@@ -33,9 +33,10 @@ __global__ void __launch_bounds__(256) k_quantize_blocks(uint8_t *__restrict__ x
             uint8_t *o = xq + blk * QB;
             if (lane_q == 0) *reinterpret_cast<uint16_t *>(o) = r.dh;
             uint16_t *qo = reinterpret_cast<uint16_t *>(o + 2 + lane_q * 8);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                qo[i] = (uint16_t)((uint8_t)r.q[2 * i]) | (uint16_t)((uint16_t)(uint8_t)r.q[2 * i + 1] << 8);
+            qo[0] = (uint16_t)r.lo;
+            qo[1] = (uint16_t)(r.lo >> 16);
+            qo[2] = (uint16_t)r.hi;
+            qo[3] = (uint16_t)(r.hi >> 16);
         }
     }
 }
@@ -44,12 +45,23 @@ __global__ void __launch_bounds__(256) k_quantize_blocks(uint8_t *__restrict__ x
 // dplane [n_rows][nb] fp32 (the stored binary16 scale as fp32).  Output row r
 // is quantised from x row src_row[r] when src_row is given (a negative entry
 // gives a zero row), else from x row r when r < n_src, else it is zero.
+// Four packed int8 -> two fp16x2 holding the same integers exactly (bytes 0, 1
+// -> lo; 2, 3 -> hi): each byte biased to unsigned sits under the fp16 exponent
+// of 1024 (1024 + q + 128), then 1152 is subtracted (exact; q = 0 gives +0, as
+// the integer conversion does).
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const uint32_t bias = 0x64806480u;   // fp16 (1152, 1152)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
 __device__ __forceinline__ void store_f16_quants(__half *dst, const QuantBlock &qb) {
     uint32_t h[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        h[i] = (uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i])) |
-               ((uint32_t)__half_as_ushort(__int2half_rn(qb.q[2 * i + 1])) << 16);
+    s8x4_to_f16x4(qb.lo, h[0], h[1]);
+    s8x4_to_f16x4(qb.hi, h[2], h[3]);
     *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
 }
 
@@ -83,12 +95,7 @@ __global__ void __launch_bounds__(256, 8) k_quantize_planes(int8_t *__restrict__
         }
         const QuantBlock qb = quantize8(x8);
         if (live) {
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
-                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
-            }
+            const uint32_t lo = qb.lo, hi = qb.hi;
             *reinterpret_cast<uint2 *>(qplane + r * in_dim + b * QK + lane_q * 8) = make_uint2(lo, hi);
             if (lane_q == 0) dplane[r * nb + b] = qb.d_stored;
         }
@@ -133,12 +140,7 @@ __global__ void __launch_bounds__(256) k_quantize_pairs(int8_t *__restrict__ qpl
             store_f16_quants(q16 + ru * in_dim + b * QK + lane_q * 8, qb);
             if (lane_q == 0) dxT[b * n_ld + ru] = qb.d_stored;
         } else {
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                lo |= (uint32_t)(uint8_t)qb.q[i] << (8 * i);
-                hi |= (uint32_t)(uint8_t)qb.q[4 + i] << (8 * i);
-            }
+            const uint32_t lo = qb.lo, hi = qb.hi;
             *reinterpret_cast<uint2 *>(qplane + ru * in_dim + b * QK + lane_q * 8) = make_uint2(lo, hi);
             if (lane_q == 0) dplane[ru * nb + b] = qb.d_stored;
         }
@@ -318,9 +320,10 @@ __global__ void __launch_bounds__(RMS_THREADS) k_rmsnorm_quantize(uint8_t *__res
                 uint8_t *o = xq + (row * nb + e / QK) * QB;
                 if (lane_q == 0) *reinterpret_cast<uint16_t *>(o) = qb.dh;
                 uint16_t *qo = reinterpret_cast<uint16_t *>(o + 2 + lane_q * 8);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    qo[i] = (uint16_t)((uint8_t)qb.q[2 * i]) | (uint16_t)((uint16_t)(uint8_t)qb.q[2 * i + 1] << 8);
+                qo[0] = (uint16_t)qb.lo;
+                qo[1] = (uint16_t)(qb.lo >> 16);
+                qo[2] = (uint16_t)qb.hi;
+                qo[3] = (uint16_t)(qb.hi >> 16);
             }
         }
         __syncthreads();   // part and r_sh are rewritten for the next row
@@ -407,9 +410,10 @@ __global__ void __launch_bounds__(RMS_THREADS, MINB) k_rmsnorm_quantize_reg(uint
                 uint8_t *o = xq + (row * nb + e / QK) * QB;
                 if (lane_q == 0) *reinterpret_cast<uint16_t *>(o) = qb.dh;
                 uint16_t *qo = reinterpret_cast<uint16_t *>(o + 2 + lane_q * 8);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    qo[i] = (uint16_t)((uint8_t)qb.q[2 * i]) | (uint16_t)((uint16_t)(uint8_t)qb.q[2 * i + 1] << 8);
+                qo[0] = (uint16_t)qb.lo;
+                qo[1] = (uint16_t)(qb.lo >> 16);
+                qo[2] = (uint16_t)qb.hi;
+                qo[3] = (uint16_t)(qb.hi >> 16);
             }
         }
 #pragma unroll
