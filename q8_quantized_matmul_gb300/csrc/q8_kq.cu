@@ -23,8 +23,10 @@
 // fp32), summed over sub-blocks and blocks.
 // One lane takes two sub-blocks of a block, whose scaled integer sums it adds
 // exactly before the fp32 step: Q4_K 4 lanes per block (8 blocks a warp pass),
-// Q2_K 8 lanes (4 blocks).  A warp owns a weight row, reads each block once for
-// all tokens of its group, and reduces its lanes' sums at the row's end.
+// Q2_K 8 lanes (4 blocks).  A warp reads each block once for all tokens of its
+// group and reduces its lanes' sums at the row's end.  In the streaming kernel a
+// warp owns two weight rows of an item, so each activation load from shared
+// memory (the limit there) serves two rows; in the direct kernel, one row.
 #include "q8_common.cuh"
 #include "q8_kernels.h"
 
@@ -262,55 +264,61 @@ __device__ __forceinline__ void decode_unit(Unit<FMT> &v, const RawUnit<FMT> &r,
 // eight 16-byte bank groups.
 __device__ __forceinline__ uint32_t act_swz(uint32_t u) { return u ^ ((u >> 4) & 7u); }
 
+// One token's activations for a unit: its quants (Q4_K 64, Q2_K 32) and its two
+// sub-blocks' 16-value sums (packed int16 pairs).
+template <int FMT> struct XUnit {
+    static constexpr int NX = FMT == KQ_Q4 ? 4 : 2;
+    uint4 x[NX];
+    uint32_t g[FMT == KQ_Q4 ? 2 : 1];
+};
+
+// xrow: the token's quants (SMEM: the swizzled staged row), u0 the 16-byte unit
+// of the unit's first value; xs: its 16-value sums from the unit's first group.
+template <int FMT, bool SMEM>
+__device__ __forceinline__ void load_x(XUnit<FMT> &a, const int8_t *xrow, uint32_t u0, const int16_t *xs) {
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(xrow);
+#pragma unroll
+    for (int k = 0; k < XUnit<FMT>::NX; ++k) a.x[k] = SMEM ? x4[act_swz(u0 + (uint32_t)k)] : __ldg(x4 + u0 + k);
+    const uint32_t *g = reinterpret_cast<const uint32_t *>(xs);
+#pragma unroll
+    for (int k = 0; k < (FMT == KQ_Q4 ? 2 : 1); ++k) a.g[k] = SMEM ? g[k] : __ldg(g + k);
+}
+
 // The unit's term for one token, before the activation scale:
 // d * (sc0 isum0 + sc1 isum1) - dmin * (m0 xsum0 + m1 xsum1), the integer sums
-// exact.  xrow: the token's quants (SMEM: the swizzled staged row), u0 the
-// 16-byte unit of the unit's first value; xs: its 16-value sums from the unit's
-// first group.
-template <int FMT, bool SMEM>
-__device__ __forceinline__ float unit_term(const Unit<FMT> &v, const int8_t *xrow, uint32_t u0, const int16_t *xs) {
-    auto ld4 = [](const uint32_t *p) { return SMEM ? *p : __ldg(p); };
-    const uint4 *x4 = reinterpret_cast<const uint4 *>(xrow);
-    auto ldx = [&](uint32_t k) { return SMEM ? x4[act_swz(u0 + k)] : __ldg(x4 + u0 + k); };
+// exact.
+template <int FMT>
+__device__ __forceinline__ float term_x(const Unit<FMT> &v, const XUnit<FMT> &a) {
     int i0 = 0, i1 = 0, xs0, xs1;
+    constexpr int H = Unit<FMT>::NW / 2;   // words of the first sub-block
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+        const uint4 &xa = a.x[k >> 2];
+        const uint32_t xw = (k & 3) == 0 ? xa.x : ((k & 3) == 1 ? xa.y : ((k & 3) == 2 ? xa.z : xa.w));
+        i0 = __dp4a((int)v.q[k], (int)xw, i0);
+    }
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+        const uint4 &xa = a.x[(H + k) >> 2];
+        const uint32_t xw = (k & 3) == 0 ? xa.x : ((k & 3) == 1 ? xa.y : ((k & 3) == 2 ? xa.z : xa.w));
+        i1 = __dp4a((int)v.q[H + k], (int)xw, i1);
+    }
     if constexpr (FMT == KQ_Q4) {
-        const uint4 a = ldx(0), b = ldx(1), c = ldx(2), e = ldx(3);
-        i0 = __dp4a((int)v.q[0], (int)a.x, i0);
-        i0 = __dp4a((int)v.q[1], (int)a.y, i0);
-        i0 = __dp4a((int)v.q[2], (int)a.z, i0);
-        i0 = __dp4a((int)v.q[3], (int)a.w, i0);
-        i0 = __dp4a((int)v.q[4], (int)b.x, i0);
-        i0 = __dp4a((int)v.q[5], (int)b.y, i0);
-        i0 = __dp4a((int)v.q[6], (int)b.z, i0);
-        i0 = __dp4a((int)v.q[7], (int)b.w, i0);
-        i1 = __dp4a((int)v.q[8], (int)c.x, i1);
-        i1 = __dp4a((int)v.q[9], (int)c.y, i1);
-        i1 = __dp4a((int)v.q[10], (int)c.z, i1);
-        i1 = __dp4a((int)v.q[11], (int)c.w, i1);
-        i1 = __dp4a((int)v.q[12], (int)e.x, i1);
-        i1 = __dp4a((int)v.q[13], (int)e.y, i1);
-        i1 = __dp4a((int)v.q[14], (int)e.z, i1);
-        i1 = __dp4a((int)v.q[15], (int)e.w, i1);
-        const uint32_t g01 = ld4(reinterpret_cast<const uint32_t *>(xs));
-        const uint32_t g23 = ld4(reinterpret_cast<const uint32_t *>(xs) + 1);
-        xs0 = (int)(int16_t)(g01 & 0xffffu) + (int)(int16_t)(g01 >> 16);
-        xs1 = (int)(int16_t)(g23 & 0xffffu) + (int)(int16_t)(g23 >> 16);
+        xs0 = (int)(int16_t)(a.g[0] & 0xffffu) + (int)(int16_t)(a.g[0] >> 16);
+        xs1 = (int)(int16_t)(a.g[1] & 0xffffu) + (int)(int16_t)(a.g[1] >> 16);
     } else {
-        const uint4 a = ldx(0), b = ldx(1);
-        i0 = __dp4a((int)v.q[0], (int)a.x, i0);
-        i0 = __dp4a((int)v.q[1], (int)a.y, i0);
-        i0 = __dp4a((int)v.q[2], (int)a.z, i0);
-        i0 = __dp4a((int)v.q[3], (int)a.w, i0);
-        i1 = __dp4a((int)v.q[4], (int)b.x, i1);
-        i1 = __dp4a((int)v.q[5], (int)b.y, i1);
-        i1 = __dp4a((int)v.q[6], (int)b.z, i1);
-        i1 = __dp4a((int)v.q[7], (int)b.w, i1);
-        const uint32_t g01 = ld4(reinterpret_cast<const uint32_t *>(xs));
-        xs0 = (int)(int16_t)(g01 & 0xffffu);
-        xs1 = (int)(int16_t)(g01 >> 16);
+        xs0 = (int)(int16_t)(a.g[0] & 0xffffu);
+        xs1 = (int)(int16_t)(a.g[0] >> 16);
     }
     const int S = v.sc0 * i0 + v.sc1 * i1, M = v.m0 * xs0 + v.m1 * xs1;
     return fmaf(-v.dmin, (float)M, v.d * (float)S);
+}
+
+template <int FMT, bool SMEM>
+__device__ __forceinline__ float unit_term(const Unit<FMT> &v, const int8_t *xrow, uint32_t u0, const int16_t *xs) {
+    XUnit<FMT> a;
+    load_x<FMT, SMEM>(a, xrow, u0, xs);
+    return term_x<FMT>(v, a);
 }
 
 template <int FMT, int TOKG>
@@ -393,7 +401,9 @@ __global__ void __launch_bounds__(kq::THREADS, 2) k_kq_gemv(const KqParams p) {
 // warps takes one row of the slot.  Needs 16-byte aligned rows (row bytes, the
 // matrix and the expert stride multiples of 16) of at most SLOT_BYTES / 1.
 namespace kqs {
-constexpr int NCONS = 16;                        // consumer warps: one weight row each per item
+constexpr int NCONS = 14;                        // consumer warps (15 warps: 128 registers a thread)
+constexpr int NGRP = 2;                          // groups of consumer warps, alternate fills
+constexpr int WPG = NCONS / NGRP;                // warps of a group: two weight rows each per item
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr uint32_t SLOT_BYTES = 40 * 1024;       // a work item's rows (at most 16)
 constexpr int CHUNK = 16;                        // consecutive items a CTA takes in turn
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NCONS);
+            mbar_init(&empty[s], WPG);   // one group's warps consume a fill
         }
         mbar_init(reinterpret_cast<uint64_t *>(meta + NSLOT), NCONS);   // act_bar
         *abort_flag = 0;
@@ -451,15 +461,16 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
     const uint64_t row_bytes = (uint64_t)nsb * BB;
     if (warp == NCONS) {
         // ---------------- producer warp: item order, slot metadata, one bulk copy per item
-        uint32_t slot = 0, phase = 0;
-        uint32_t fills[NSLOT];
-        for (int s = 0; s < NSLOT; ++s) fills[s] = 0;
+        // Fills alternate between the two consumer groups (even fills: group 0).  A
+        // token group may begin only at an even fill, so that both groups meet every
+        // change of staged activations at the same pair of fills: an odd fill that
+        // would start a new group carries a no-op item (no rows, same group) instead.
+        // Two end markers, at an even fill and the next, close both groups.
         KqItem it;
         Segment *seg_cache = reinterpret_cast<Segment *>(smem + Layout<TOKG>::SEG_OFF);
         const KqSegs sg = kq_segs(p, seg_cache, lane, 32);
         __syncwarp();
-        int group = -1, my_arow = 0, my_orow = -1;
-        bool more = true;
+        int group = -1, group_ntok = 0, my_arow = 0, my_orow = -1;
         // chunks of consecutive items (one token group, mostly) dealt in turn: the
         // staged activations change once per chunk; up to CHUNK items a chunk while
         // every CTA still gets about four chunks
@@ -467,9 +478,24 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
                                    : (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item) *
                                          (int)((p.n_tok + TOKG - 1) / TOKG);
         const int chunk = max(1, min(CHUNK, n_items / (4 * (int)gridDim.x)));
-        for (int k = 0; more; ++k) {
-            const int i = ((k / chunk) * (int)gridDim.x + (int)blockIdx.x) * chunk + k % chunk;
-            more = kq_item_at<TOKG>(p, sg, i, it);
+        uint32_t fills[NSLOT];
+        for (int s2 = 0; s2 < NSLOT; ++s2) fills[s2] = 0;
+        bool have = false, done = false;
+        int ends = 0;
+        for (uint32_t kf = 0, q = 0; ends < NGRP; ++kf) {
+            if (!have && !done) {
+                const int i = (((int)q / chunk) * (int)gridDim.x + (int)blockIdx.x) * chunk + (int)q % chunk;
+                if (kq_item_at<TOKG>(p, sg, i, it)) {
+                    have = true;
+                    ++q;
+                } else {
+                    done = true;
+                }
+            }
+            const bool odd = (kf & 1u) != 0u;
+            // 0: end marker, 1: no-op, 2: the item
+            const int kind = have ? ((odd && it.xrow0 != group) ? 1 : 2) : ((odd && ends == 0) ? 1 : 0);
+            const uint32_t slot = kf % NSLOT, phase = (kf / NSLOT) & 1u;
             // after an abort nothing more is issued; consumers release only the
             // slots they saw land, so each slot has at most its last fill in flight
             bool ok = false;
@@ -477,43 +503,45 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
             if (!ok) break;
             KqSlotMeta &m = meta[slot];
-            if (more && it.xrow0 != group) {   // a new token group: its rows (lane t: token t)
+            if (kind == 2 && it.xrow0 != group) {   // a new token group: its rows (lane t: token t)
                 group = it.xrow0;
+                group_ntok = it.ntok;
                 const bool on = lane < it.ntok;
                 my_arow = !on ? 0 : (p.plan ? p.src_row[it.xrow0 + lane] : it.xrow0 + lane);
                 my_orow = !on ? -1 : (p.plan ? p.row_to_out[it.xrow0 + lane] : it.xrow0 + lane);
             }
             if (lane < TOKG) {
                 m.arow[lane] = my_arow;
-                m.orow[lane] = more ? my_orow : -1;
+                m.orow[lane] = kind == 2 ? my_orow : -1;
             }
             if (lane == 0) {
-                m.ntok = more ? it.ntok : -1;
-                m.group = more ? it.xrow0 : -1;
-                m.r0 = more ? it.r0 : 0u;
-                m.nrows = more ? it.nrows : 0u;
+                // a no-op keeps its group's tokens: a warp may stage the group from it
+                m.ntok = kind == 2 ? it.ntok : (kind == 1 ? group_ntok : -1);
+                m.group = kind == 0 ? -1 : group;
+                m.r0 = kind == 2 ? it.r0 : 0u;
+                m.nrows = kind == 2 ? it.nrows : 0u;
             }
             __syncwarp();
             // the item's bytes are armed first; then each row is one bulk copy, issued by
             // one lane each so that the rows stream in parallel
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], more ? it.nrows * (uint32_t)row_bytes : 0u);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], kind == 2 ? it.nrows * (uint32_t)row_bytes : 0u);
             __syncwarp();
-            if (more && (uint32_t)lane < it.nrows)
+            if (kind == 2 && (uint32_t)lane < it.nrows)
                 bulk_g2s(slots + (size_t)slot * SLOT_BYTES + (size_t)lane * row_bytes,
                          p.W + (uint64_t)it.expert * p.expert_stride + (uint64_t)(it.r0 + (uint32_t)lane) * row_bytes,
                          (uint32_t)row_bytes, &full[slot]);
             ++fills[slot];
-            if (++slot == NSLOT) {
-                slot = 0;
-                phase ^= 1u;
-            }
+            if (kind == 2) have = false;
+            if (kind == 0) ++ends;
         }
         if (lane == 0)
-            for (int s = 0; s < NSLOT; ++s)   // every copy lands before the CTA exits
-                if (fills[s]) mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.err, nullptr);
+            for (int s2 = 0; s2 < NSLOT; ++s2)   // every copy lands before the CTA exits
+                if (fills[s2]) mbar_wait(&full[s2], (fills[s2] - 1u) & 1u, p.err, nullptr);
         return;
     }
-    // ---------------- consumers: warp w takes row w of each item
+    // ---------------- consumers: two groups of WPG warps take alternate fills; warp
+    // w of a group takes rows 2w and 2w + 1 of its items, so each staged activation
+    // load serves two weight rows.
     // The token group's activations are staged in shared memory once per group:
     // a bounded barrier (act_bar, two phases) first lets every warp finish the
     // previous group, then every warp copies its share and arrives again.
@@ -527,9 +555,10 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
     uint64_t *act_bar = reinterpret_cast<uint64_t *>(meta + NSLOT);
     const int ctid = warp * 32 + lane;
     constexpr int CT = NCONS * 32;
+    const int wg = warp / WPG, wr = warp % WPG;
     int group = -1;
-    uint32_t slot = 0, phase = 0;
-    for (;;) {
+    for (uint32_t kf = (uint32_t)wg;; kf += NGRP) {
+        const uint32_t slot = kf % NSLOT, phase = (kf / NSLOT) & 1u;
         // a consumer whose wait failed leaves (an abort); it hands no slot back
         if (!mbar_wait(&full[slot], phase, p.err, abort_flag)) break;
         const KqSlotMeta &m = meta[slot];
@@ -558,47 +587,55 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             if (lane == 0) mbar_arrive(act_bar);   // this warp's share is staged
             if (!mbar_wait(act_bar, 1u, p.err, abort_flag)) break;
         }
-        if ((uint32_t)warp < m.nrows) {
-            const uint32_t r = m.r0 + (uint32_t)warp;
-            const uint8_t *wrow = slots + (size_t)slot * SLOT_BYTES + (size_t)warp * row_bytes;
-            float acc[TOKG];
+        const uint32_t ra = 2u * (uint32_t)wr;
+        if (ra < m.nrows) {
+            const bool two = ra + 1u < m.nrows;
+            const uint8_t *wa = slots + (size_t)slot * SLOT_BYTES + (size_t)ra * row_bytes;
+            const uint8_t *wb = wa + (two ? row_bytes : 0);
+            float acc[2][TOKG];
 #pragma unroll
-            for (int t = 0; t < TOKG; ++t) acc[t] = 0.0f;
+            for (int t = 0; t < TOKG; ++t) acc[0][t] = acc[1][t] = 0.0f;
             for (uint32_t b0 = 0; b0 < nsb; b0 += BPP) {
                 const uint32_t b = b0 + (uint32_t)bsel;
                 if (b >= nsb) continue;
-                RawUnit<FMT> raw;
-                load_raw<FMT, true>(raw, wrow + (size_t)b * BB, unit);
-                Unit<FMT> un;
-                decode_unit<FMT>(un, raw, unit);
+                RawUnit<FMT> raw0, raw1;
+                load_raw<FMT, true>(raw0, wa + (size_t)b * BB, unit);
+                load_raw<FMT, true>(raw1, wb + (size_t)b * BB, unit);
+                Unit<FMT> u0, u1;
+                decode_unit<FMT>(u0, raw0, unit);
+                decode_unit<FMT>(u1, raw1, unit);
 #pragma unroll
                 for (int t = 0; t < TOKG; ++t) {
                     if (t >= ntok) break;
-                    const float term = unit_term<FMT, true>(un, qx_s + (size_t)t * in_dim, (b * kq::QKK + xoff) / 16u,
-                                                            xs_s + (size_t)t * nxs + b * 16 + grp);
-                    acc[t] = fmaf(dx_s[t * nsb + b], term, acc[t]);
+                    XUnit<FMT> xa;
+                    load_x<FMT, true>(xa, qx_s + (size_t)t * in_dim, (b * kq::QKK + xoff) / 16u,
+                                      xs_s + (size_t)t * nxs + b * 16 + grp);
+                    const float dxt = dx_s[t * nsb + b];
+                    acc[0][t] = fmaf(dxt, term_x<FMT>(u0, xa), acc[0][t]);
+                    acc[1][t] = fmaf(dxt, term_x<FMT>(u1, xa), acc[1][t]);
                 }
             }
-            float mine = 0.0f;
+            float mine[2] = {0.0f, 0.0f};
 #pragma unroll
-            for (int t = 0; t < TOKG; ++t) {
-                if (t >= ntok) break;
-                float v = acc[t];
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == t) mine = v;
-            }
+                for (int t = 0; t < TOKG; ++t) {
+                    if (t >= ntok) break;
+                    float v = acc[h][t];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    if (lane == t) mine[h] = v;
+                }
             if (lane < ntok) {
                 const int o = m.orow[lane];
-                if (o >= 0) p.out[(uint64_t)o * p.out_dim + r] = mine;
+                if (o >= 0) {
+                    p.out[(uint64_t)o * p.out_dim + m.r0 + ra] = mine[0];
+                    if (two) p.out[(uint64_t)o * p.out_dim + m.r0 + ra + 1u] = mine[1];
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == NSLOT) {
-            slot = 0;
-            phase ^= 1u;
-        }
     }
 }
 
