@@ -993,7 +993,12 @@ int q8_kq_matmul(float *out, const void *W, int fmt, uint64_t in_dim, uint64_t o
     p.err = s->err;
     p.n_tok = (uint32_t)n_tok;
     if (stream_rows) {   // weights staged through shared memory by bulk copies
-        p.rows_per_item = stream_rows;
+        // a dense call has few items: fewer rows an item (in steps of the 14 the
+        // consumers share) while that keeps fewer than two items per SM
+        uint32_t rows = stream_rows;
+        const uint64_t groups = (n_tok + tokg - 1) / tokg;
+        while (rows > 14 && ((out_dim + rows - 1) / rows) * groups < 2 * (uint64_t)s->num_sms) rows -= 14;
+        p.rows_per_item = rows;
         return status_of(timed_launch(st, [&] { return q8::launch_kq_stream(p, tokg, s->num_sms, st); }));
     }
     p.rows_per_item = kq_rows_per_item(out_dim, (n_tok + tokg - 1) / tokg, s->num_sms);

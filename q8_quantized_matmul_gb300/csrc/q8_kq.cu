@@ -526,10 +526,11 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             // one lane each so that the rows stream in parallel
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], kind == 2 ? it.nrows * (uint32_t)row_bytes : 0u);
             __syncwarp();
-            if (kind == 2 && (uint32_t)lane < it.nrows)
-                bulk_g2s(slots + (size_t)slot * SLOT_BYTES + (size_t)lane * row_bytes,
-                         p.W + (uint64_t)it.expert * p.expert_stride + (uint64_t)(it.r0 + (uint32_t)lane) * row_bytes,
-                         (uint32_t)row_bytes, &full[slot]);
+            if (kind == 2)
+                for (uint32_t rr = (uint32_t)lane; rr < it.nrows; rr += 32)
+                    bulk_g2s(slots + (size_t)slot * SLOT_BYTES + (size_t)rr * row_bytes,
+                             p.W + (uint64_t)it.expert * p.expert_stride + (uint64_t)(it.r0 + rr) * row_bytes,
+                             (uint32_t)row_bytes, &full[slot]);
             ++fills[slot];
             if (kind == 2) have = false;
             if (kind == 0) ++ends;
@@ -540,8 +541,9 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
         return;
     }
     // ---------------- consumers: two groups of WPG warps take alternate fills; warp
-    // w of a group takes rows 2w and 2w + 1 of its items, so each staged activation
-    // load serves two weight rows.
+    // w of a group takes rows 2w + 14j and 2w + 14j + 1 of its items (items hold a
+    // multiple of 14 rows when short rows allow), so each staged activation load
+    // serves two weight rows.
     // The token group's activations are staged in shared memory once per group:
     // a bounded barrier (act_bar, two phases) first lets every warp finish the
     // previous group, then every warp copies its share and arrives again.
@@ -587,8 +589,7 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
             if (lane == 0) mbar_arrive(act_bar);   // this warp's share is staged
             if (!mbar_wait(act_bar, 1u, p.err, abort_flag)) break;
         }
-        const uint32_t ra = 2u * (uint32_t)wr;
-        if (ra < m.nrows) {
+        for (uint32_t ra = 2u * (uint32_t)wr; ra < m.nrows; ra += 2u * WPG) {
             const bool two = ra + 1u < m.nrows;
             const uint8_t *wa = slots + (size_t)slot * SLOT_BYTES + (size_t)ra * row_bytes;
             const uint8_t *wb = wa + (two ? row_bytes : 0);
@@ -642,8 +643,10 @@ __global__ void __launch_bounds__(kqs::THREADS, 1) k_kq_stream(const KqParams p)
 uint32_t kq_stream_rows(uint64_t row_bytes, uint64_t in_dim, int tokg) {
     if (row_bytes == 0 || row_bytes % 16 || row_bytes > kqs::SLOT_BYTES) return 0;
     if (in_dim % 256 || kqs::act_row_bytes(in_dim) > 4864) return 0;
+    // whole multiples of the consumers' 14 rows (every warp takes the same number
+    // of row pairs) when a slot holds that many
     const uint64_t r = kqs::SLOT_BYTES / row_bytes;
-    return (uint32_t)(r < (uint64_t)kqs::NCONS ? r : (uint64_t)kqs::NCONS);
+    return (uint32_t)(r < (uint64_t)kqs::NCONS ? r : r / kqs::NCONS * kqs::NCONS);
 }
 
 template <int FMT, int TOKG> static cudaError_t launch_stream(const KqParams &p, int num_sms, cudaStream_t st) {
