@@ -216,3 +216,26 @@ def test_kq_moe_decode_config_sampled(q8, o, fmt):
         We = Wd[e * stride:(e + 1) * stride].cpu().numpy()
         ref, bound = o.kq_matmul(We, fmt, x[p // k][None], out_dim)
         assert_close(got[p][None], ref, bound, f"kq{fmt} pair {p} expert {e}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_kq_moe_down_shape_sampled(q8, o, fmt):
+    """The routed down projection's shape: 256 experts of [4096 x 2048] on per-pair rows, 64
+    tokens, uniform top-6.  Short rows fill items of 28 (Q4_K) or 56 (Q2_K) rows, the last of
+    each expert ragged (4096 = 146 x 28 + 8); 8 pairs checked in full against the oracle."""
+    n_exp, in_dim, out_dim, n_tok, k = 256, 2048, 4096, 64, 6
+    stride = out_dim * q8.q8_kq_row_bytes(in_dim, fmt)
+    Wd = torch.empty(n_exp * stride, dtype=torch.uint8, device=DEV)
+    chunk = 32
+    for e0 in range(0, n_exp, chunk):
+        Wd[e0 * stride:(e0 + chunk) * stride] = dev(
+            inputs.kq_weights(chunk * out_dim, in_dim, fmt, seed=51 + e0).reshape(-1))
+    ids = inputs.route_uniform(n_tok, k, n_exp, seed=52)
+    x = inputs.normal((n_tok * k, in_dim), seed=53, p_out=0.01)
+    got = _gpu_kq_moe(q8, Wd, fmt, n_exp, stride, ids, x, 1, out_dim)
+    assert q8.q8_last_error() == 0
+    for p in np.random.default_rng(54).choice(n_tok * k, size=8, replace=False):
+        e = int(ids.reshape(-1)[p])
+        We = Wd[e * stride:(e + 1) * stride].cpu().numpy()
+        ref, bound = o.kq_matmul(We, fmt, x[p][None], out_dim)
+        assert_close(got[p][None], ref, bound, f"kq{fmt} down pair {p} expert {e}")
