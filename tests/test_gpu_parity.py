@@ -143,6 +143,18 @@ def test_matmul_parity(q8, o, in_dim, out_dim, n_tok):
     assert_close(got, ref, bound, f"matmul {in_dim}x{out_dim}x{n_tok}")
 
 
+@pytest.mark.parametrize("out_dim,n_tok", [(40000, 1), (40000, 16), (70000, 4), (70000, 16)])
+def test_gemv_wide_outputs(q8, o, out_dim, n_tok):
+    """Outputs wider than 152 x 14 sixteen-row sub-items: each CTA item holds 17 (out
+    40000) or 29 (out 70000) sub-items, so the GEMV variants whose consumer warps hold two
+    or three sub-items run.  Every output against the oracle."""
+    in_dim = 256
+    Wh = inputs.weights(out_dim, in_dim, seed=out_dim + n_tok)
+    xh = inputs.normal((n_tok, in_dim), seed=n_tok, p_out=0.01)
+    ref, bound = o.matmul(Wh, xh, out_dim)
+    assert_close(gpu_matmul(q8, dev(Wh), dev(xh), out_dim), ref, bound, f"wide {out_dim} x {n_tok}")
+
+
 @pytest.mark.parametrize("in_dim,out_dim,n_tok", [(1024, 300, 40), (1024, 200, 700), (2048, 70, 12)])
 def test_matmul_q_matches_matmul_bitwise(q8, o, in_dim, out_dim, n_tok):
     """Pre-quantised activations give the same bits as fp32 ones: prefill with raw weights
