@@ -196,12 +196,47 @@ constexpr int KIND_DENSE = 0, KIND_GROUPED = 1, KIND_PAIR = 2;
 
 // GROUPED: p.plan is set (the variants are separate so that the dense kernel
 // carries none of the plan decoding).
+// Work enumeration (the producer and the consumers walk the same sequence).
+// Dense: n_items contiguous ranges of whole sub-items, sizes differing by at most
+// one (the split is computed on the host: a 64-bit division here would delay the
+// first weight copy), dealt in turn.  Grouped: the class's work is the sequence
+// of its token groups (plan order) times the output's units of U sixteen-row
+// sub-items (U = 2 when a gate/up pair writes Q8_0 planes: whole 32-row blocks);
+// CTA c takes units [c S / G, (c + 1) S / G) of the S units, so every SM streams
+// the same amount, cut into items at token-group ends and after rows_per_item
+// rows.  (Items of whole row blocks dealt in turn left the CTAs 6 or 7 items of
+// up to 28 sub-items: 7 % of the stream idle at the decode size.)
+struct ItemCursor {
+    int i;                 // dense: the next item index
+    uint64_t pos, end;     // grouped: the next unit and the end of this CTA's range
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ uint32_t group_units(const GemvParams &p) {
+    const uint32_t u = (GROUPED && p.W2 && p.q_out) ? 2u : 1u;
+    return ((p.out_dim + 15) / 16 + u - 1) / u;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ void cursor_init(const GemvParams &p, ItemCursor &c) {
+    c.i = (int)blockIdx.x;
+    c.pos = c.end = 0;
+    if constexpr (GROUPED) {
+        const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
+        const int prb = p.plan_rb ? (int)p.plan_rb : n_rb;
+        // a GEMV class's item count is a multiple of the plan's row blocks per group
+        const uint64_t total = (uint64_t)(p.plan->n_items / prb) * group_units<GROUPED>(p);
+        c.pos = total * blockIdx.x / gridDim.x;
+        c.end = total * (blockIdx.x + 1) / gridDim.x;
+    }
+}
+
+// Returns false past the CTA's last item.
 template <int TOKG, bool GROUPED>
-__device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it) {
+__device__ __forceinline__ bool next_item(const GemvParams &p, ItemCursor &c, GItem &it) {
     if constexpr (!GROUPED) {
-        // dense: n_items contiguous ranges of whole sub-items, sizes differing by at
-        // most one (the split is computed on the host: a 64-bit division here
-        // would delay the first weight copy)
+        const int i = c.i;
+        c.i += (int)gridDim.x;
         if ((uint32_t)i >= p.n_items) return false;
         const uint32_t ui = (uint32_t)i;
         const uint32_t s0 = ui * p.sub_base + min(ui, p.sub_rem);
@@ -214,29 +249,36 @@ __device__ __forceinline__ bool gemv_item(const GemvParams &p, int i, GItem &it)
         it.nrows = min((s1 - s0) * gv::ROWS, p.out_dim - it.r0);
         return true;
     } else {
-    // A GEMV class's segments start at multiples of the plan's row blocks per
-    // token group, so item_start / prb counts the token groups before a segment.
-    const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
-    const int prb = p.plan_rb ? (int)p.plan_rb : n_rb;
-    if (i >= p.plan->n_items / prb * n_rb) return false;
-    const int gstart = i / n_rb * prb;   // the item's token group, in the plan's item units
-    const Segment *segs = reinterpret_cast<const Segment *>(p.plan + 1);
-    int lo = 0, hi = p.plan->n_segments - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (segs[mid].item_start <= gstart) lo = mid;
-        else hi = mid - 1;
-    }
-    const Segment s = segs[lo];
-    const int local = i - s.item_start / prb * n_rb;
-    const int tg = local / n_rb, rb = local - tg * n_rb;
-    it.expert = s.expert;
-    it.tok0 = tg * TOKG;
-    it.ntok = min(TOKG, s.count - it.tok0);
-    it.xrow0 = s.row0 + it.tok0;
-    it.r0 = (uint32_t)rb * p.rows_per_item;
-    it.nrows = min(p.rows_per_item, p.out_dim - it.r0);
-    return true;
+        if (c.pos >= c.end) return false;
+        const uint32_t usub = (p.W2 && p.q_out) ? 2u : 1u;   // sub-items a unit
+        const uint64_t nu = group_units<GROUPED>(p);
+        const uint64_t g = c.pos / nu;                        // token group within the class
+        const uint32_t u0 = (uint32_t)(c.pos - g * nu);
+        const int n_rb = (int)((p.out_dim + p.rows_per_item - 1) / p.rows_per_item);
+        const int prb = p.plan_rb ? (int)p.plan_rb : n_rb;
+        // the segment holding group g: its item_start / prb groups come before it
+        const int gstart = (int)g * prb;
+        const Segment *segs = reinterpret_cast<const Segment *>(p.plan + 1);
+        int lo = 0, hi = p.plan->n_segments - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (segs[mid].item_start <= gstart) lo = mid;
+            else hi = mid - 1;
+        }
+        const Segment s = segs[lo];
+        const int tg = (int)g - s.item_start / prb;
+        const uint64_t maxu = p.rows_per_item / (gv::ROWS * usub);
+        uint64_t cnt = c.end - c.pos;
+        if (cnt > nu - u0) cnt = nu - u0;
+        if (cnt > maxu) cnt = maxu;
+        it.expert = s.expert;
+        it.tok0 = tg * TOKG;
+        it.ntok = min(TOKG, s.count - it.tok0);
+        it.xrow0 = s.row0 + it.tok0;
+        it.r0 = u0 * usub * gv::ROWS;
+        it.nrows = min((uint32_t)cnt * usub * gv::ROWS, p.out_dim - it.r0);
+        c.pos += cnt;
+        return true;
     }
 }
 
@@ -290,7 +332,9 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
     uint32_t seqbase = 0;
     GItem it;
     constexpr bool PAIR = KIND == KIND_PAIR;
-    for (int item_i = blockIdx.x; gemv_item<TOKG, KIND != KIND_DENSE>(p, item_i, it); item_i += gridDim.x) {
+    ItemCursor cur;
+    cursor_init<KIND != KIND_DENSE>(p, cur);
+    while (next_item<TOKG, KIND != KIND_DENSE>(p, cur, it)) {
         const uint32_t nh = (it.nrows + ROWS - 1) / ROWS;   // sub-items of one matrix
         const uint32_t nsub = PAIR ? 2 * nh : nh;           // a pair: the gate's, then the up's
         const uint32_t total = nk * nsub;
@@ -709,9 +753,11 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
     uint32_t seqbase = 0;
     bool waited_dep = false;
 
-    for (int item_i = blockIdx.x;; item_i += gridDim.x) {
+    ItemCursor cur;
+    cursor_init<KIND != KIND_DENSE>(p, cur);
+    for (;;) {
         GItem it;
-        if (!gemv_item<M::TOKG, KIND != KIND_DENSE>(p, item_i, it)) break;
+        if (!next_item<M::TOKG, KIND != KIND_DENSE>(p, cur, it)) break;
         // sub-items: with a gate/up pair, nh of the gate and then nh of the up;
         // sub-item v's results are staged at local row 16v + r, so the up rows
         // follow the gate rows at 16 nh
