@@ -128,21 +128,17 @@ __device__ __forceinline__ void block_scan2(int &a, int &b, int *sh, int *ta, in
 // One CTA.  Touched experts ordered by count (descending, ties by id); in that
 // order the classes are contiguous: [0, n2) tensor-core class, [n2, n_gt8)
 // class 1, the rest class 0.  Rows and items are exclusive scans over the order.
-__global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
-                                                               uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap,
-                                                               uint8_t *plans, size_t plan_stride,
-                                                               int32_t *__restrict__ row0_of) {
-    extern __shared__ int32_t sh_plan[];   // cnt[n_expert], order[n_expert]
-    int32_t *cnt = sh_plan;
-    int32_t *order = sh_plan + n_expert;
+// The plan from the experts' pair counts cnt[] (shared memory, read by the whole
+// CTA after a barrier); order[] (shared) receives the touched experts by rank and
+// row0_of[] each expert's first plane row (-1 untouched).
+__device__ void route_plan_core(const int32_t *cnt, int32_t *order, uint32_t n_expert, uint32_t out_dim,
+                                uint32_t rows_gemv, uint32_t tc_cap, uint8_t *plans, size_t plan_stride,
+                                int32_t *__restrict__ row0_of) {
     __shared__ int tot_sh[3];              // touched, > MOE_TC_MIN_ROWS, > 8
     __shared__ int scan_sh[2 * (ROUTE_THREADS / 32)];
     __shared__ int mark_sh[4];             // item / row scans at the class starts n2 and n_gt8
     if (threadIdx.x < 3) tot_sh[threadIdx.x] = 0;
-    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
-        cnt[e] = counts[e];
-        row0_of[e] = -1;
-    }
+    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) row0_of[e] = -1;
     __syncthreads();
     int my_active = 0, my_gt_t = 0, my_gt8 = 0;
     for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
@@ -246,6 +242,89 @@ __global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__r
     }
 }
 
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_plan(const int32_t *__restrict__ counts, uint32_t n_expert,
+                                                               uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap,
+                                                               uint8_t *plans, size_t plan_stride,
+                                                               int32_t *__restrict__ row0_of) {
+    extern __shared__ int32_t sh_plan[];   // cnt[n_expert], order[n_expert]
+    int32_t *cnt = sh_plan;
+    int32_t *order = sh_plan + n_expert;
+    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) cnt[e] = counts[e];
+    route_plan_core(cnt, order, n_expert, out_dim, rows_gemv, tc_cap, plans, plan_stride, row0_of);
+}
+
+// Small batches (the decode sizes): counting, the plan and the pair lists in one
+// CTA, with the ids in shared memory, instead of the three kernels above.  The
+// same plan and maps: counts are order-independent, the plan is route_plan_core,
+// and warp 0 lists each expert's pairs in increasing p (32 pairs at a time,
+// ranks within a batch from the lanes holding the same expert).
+constexpr uint32_t ROUTE_SMALL_PAIRS = 2048, ROUTE_SMALL_EXPERTS = 2048;
+
+__global__ void __launch_bounds__(ROUTE_THREADS) k_route_small(const int32_t *__restrict__ ids, uint64_t n_pairs,
+                                                                uint32_t k, uint32_t n_expert, int x_per_pair,
+                                                                uint32_t out_dim, uint32_t rows_gemv, uint32_t tc_cap,
+                                                                uint8_t *plans, size_t plan_stride,
+                                                                int32_t *__restrict__ row0_of,
+                                                                int32_t *__restrict__ row_to_out,
+                                                                int32_t *__restrict__ src_row,
+                                                                int32_t *__restrict__ dst_row, uint64_t max_rows,
+                                                                float *__restrict__ out, int *err) {
+    extern __shared__ int32_t sh_small[];   // ids[n_pairs], cnt[n_expert], order[n_expert], run[n_expert]
+    int32_t *ids_s = sh_small;
+    int32_t *cnt = ids_s + n_pairs;
+    int32_t *order = cnt + n_expert;
+    int32_t *run = order + n_expert;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (uint64_t i = threadIdx.x; i < max_rows; i += blockDim.x) {
+        row_to_out[i] = -1;
+        src_row[i] = -1;
+    }
+    if (dst_row)
+        for (uint64_t i = threadIdx.x; i < n_pairs; i += blockDim.x) dst_row[i] = -1;
+    for (uint32_t e = threadIdx.x; e < n_expert; e += blockDim.x) {
+        cnt[e] = 0;
+        run[e] = 0;
+    }
+    for (uint64_t i = threadIdx.x; i < n_pairs; i += blockDim.x) ids_s[i] = __ldg(ids + i);
+    __syncthreads();
+    // counts; each warp reads 32 consecutive ids and zeroes the (rare) bad pairs' rows
+    const uint64_t nwarp = blockDim.x >> 5;
+    for (uint64_t p0 = (uint64_t)warp * 32; p0 < n_pairs; p0 += nwarp * 32) {
+        const uint64_t p = p0 + lane;
+        const int32_t id = p < n_pairs ? ids_s[p] : 0;
+        const bool ok = id >= 0 && (uint32_t)id < n_expert;
+        if (p < n_pairs && ok) atomicAdd(&cnt[id], 1);
+        unsigned bad = __ballot_sync(0xffffffffu, p < n_pairs && !ok);
+        while (bad) {
+            const uint64_t pb = p0 + (uint64_t)(__ffs(bad) - 1);
+            bad &= bad - 1u;
+            for (uint32_t o = lane; o < out_dim; o += 32) out[pb * out_dim + o] = 0.0f;
+            if (lane == 0) raise_error(err, DEV_ERANGE);
+        }
+    }
+    route_plan_core(cnt, order, n_expert, out_dim, rows_gemv, tc_cap, plans, plan_stride, row0_of);
+    __syncthreads();   // row0_of is read back by warp 0
+    if (warp == 0) {
+        for (uint64_t p0 = 0; p0 < n_pairs; p0 += 32) {
+            const uint64_t p = p0 + lane;
+            const int32_t id = p < n_pairs ? ids_s[p] : -1;
+            const bool ok = id >= 0 && (uint32_t)id < n_expert;
+            // lanes holding the same expert; lanes without one get keys of their own
+            const unsigned same = __match_any_sync(0xffffffffu, ok ? id : -2 - lane);
+            if (ok) {
+                const int pos = run[id] + __popc(same & ((1u << lane) - 1u));
+                const int row = row0_of[id] + pos;
+                row_to_out[row] = (int32_t)p;
+                src_row[row] = (int32_t)(x_per_pair ? p : p / k);
+                if (dst_row) dst_row[p] = row;
+            }
+            __syncwarp();
+            if (ok && lane == __ffs(same) - 1) run[id] += __popc(same);
+            __syncwarp();
+        }
+    }
+}
+
 __global__ void __launch_bounds__(ROUTE_THREADS) k_route_fill(const int32_t *__restrict__ ids, uint64_t n_pairs,
                                                                uint32_t k, int x_per_pair,
                                                                const int32_t *__restrict__ row0_of,
@@ -286,6 +365,13 @@ cudaError_t launch_route(const int32_t *ids, uint64_t n_tok, uint32_t k, uint32_
                          float *out, int *err, int num_sms, cudaStream_t st) {
     const uint64_t n_pairs = n_tok * k;
     cudaError_t e;
+    if (n_pairs <= ROUTE_SMALL_PAIRS && n_expert <= ROUTE_SMALL_EXPERTS) {
+        const size_t smem = (n_pairs + 3 * (size_t)n_expert) * sizeof(int32_t);   // <= 32 KB
+        k_route_small<<<1, ROUTE_THREADS, smem, st>>>(ids, n_pairs, k, n_expert, x_per_pair, out_dim, rows_gemv, tc_cap,
+                                                      plans, route_plan_bytes(n_expert), row0_of, row_to_out, src_row,
+                                                      dst_row, max_rows, out, err);
+        return cudaGetLastError();
+    }
     k_route_count<<<n_expert + 1, ROUTE_THREADS, 0, st>>>(ids, n_pairs, n_expert, counts, out_dim, out, err,
                                                           row_to_out, src_row, max_rows, dst_row);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
