@@ -267,6 +267,21 @@ int run_tc(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64_t 
         const uint64_t max_split = nb / 16 > 0 ? nb / 16 : 1;   // keep >= 16 blocks per split
         if (ksplit > max_split) ksplit = max_split;
         if (ksplit < 1) ksplit = 1;
+        // With long K, more splits than fit one wave can fill the SMs better: 32 tiles
+        // in 4 splits leave 24 of 152 SMs idle, 9 splits run 288 units in two full
+        // waves of 114 blocks each (in 32768 -> out 1024 at 512 tokens: 114.3 ->
+        // 111.5 us).  Only while a split keeps >= 96 blocks (short splits pay the
+        // pipeline's fill: 7 splits of 18 blocks took 4096 -> 2048 from 35.6 to 42.9
+        // us); 0.004 per split for the partial sums.
+        double best = 1.0 / (double)ksplit + 0.004 * (double)ksplit;
+        for (uint64_t k = ksplit + 1; k <= 64 && nb / k >= 96; ++k) {
+            const uint64_t waves = (tiles * k + sms - 1) / sms;
+            const double t = (double)waves / (double)k + 0.004 * (double)k;
+            if (t < best - 1e-12) {
+                best = t;
+                ksplit = k;
+            }
+        }
     } else {
         // Tiles fill the SMs but may end in a thin last wave (256 tiles: 1.68 waves,
         // 0.84 of the SMs busy on average): split K when that fills the waves better,
