@@ -87,7 +87,7 @@ constexpr int SUBMAX = (512 + NCW * 16 - 1) / (NCW * 16);   // sub-items per war
 constexpr int ACT_BYTES = 40 * 1024;             // staged activations per chunk
 constexpr int DX_FLOATS = 1280;                  // staged activation scales per chunk
 constexpr int RING_BYTES = NSLOT * SLOT;
-constexpr int QT_BYTES = 20736;                  // fused quantiser: natural-order quants of a chunk
+constexpr int QT_BYTES = 20736;                  // qtmp: natural-order quants of a chunk (fused quantiser, planes staging)
 constexpr size_t SMEM = RING_BYTES + ACT_BYTES + DX_FLOATS * 4 + QT_BYTES + 2 * NSLOT * 8 + NSLOT * 4 + 16;
 constexpr int BAR_CONSUMERS = 1;                 // named barrier of the consumer warps
 constexpr int OUT_STRIDE = GEMV_MAX_ROWS_PER_ITEM;   // output staging: floats per token
@@ -105,7 +105,7 @@ template <int MODE> struct Mode {
     static constexpr int NACC = MODE == 0 ? 8 : NT * 4;             // fp32 results per lane and sub-item
     static_assert(KA * DXW <= DX_FLOATS, "scale buffer");
     static_assert(NCW * NACC * 32 * 4 <= ACT_BYTES, "split-K buffer");
-    static constexpr int QT_STRIDE = KA * QK + 16;                  // fused: bytes per token row of a chunk
+    static constexpr int QT_STRIDE = KA * QK + 16;                  // qtmp: bytes per token row of a chunk
     static_assert(MODE == 0 || TOKG * QT_STRIDE <= QT_BYTES, "fused quantiser buffer");
 };
 }  // namespace gv
@@ -373,12 +373,13 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
     return seqbase;
 }
 
-// Stage one K chunk [kb0, kb0 + ka) of the token group's activations (consumer
-// threads only).  All global loads of a thread are issued before any is used:
+// Stage one K chunk [kb0, kb0 + ka) of the token group's activations from the
+// Q8_0 planes (consumer threads only; qtmp is the MMA modes' shared-memory
+// copy of the rows).  All global loads of a thread are issued before any is used:
 // under a saturated HBM stream each round trip costs a microsecond or more.
-template <int MODE>
+template <int MODE, bool TWO_PHASE>
 __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it, uint32_t kb0, uint32_t ka,
-                                            uint8_t *act, float *dxs) {
+                                            uint8_t *act, float *dxs, uint8_t *qtmp) {
     using namespace gv;
     using M = Mode<MODE>;
     constexpr int NT = M::NT;
@@ -421,61 +422,72 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
         // MMA B fragments, fp16: [block][N tile][lane][16 bytes].  Rows past the
         // group's ntok are not read (routed planes leave their padding rows
         // unwritten): their fragments and scales are zero.
+        // TWO_PHASE (dense calls): the group's token rows of the chunk go to qtmp
+        // whole, in 16-byte loads (three per thread, all issued before the first
+        // store), with the scales; after a consumer barrier the fragments are
+        // built from qtmp.  Otherwise (routed items) each lane gathers its four
+        // fragment words per N tile straight from global memory.  A dense call
+        // stages once, at its start, where the load latency is exposed: there the
+        // two phases are 9% faster at 16 tokens.  Routed items stage while the
+        // weight stream runs, and the extra barrier cost them 0.3%.
         // Words of the activation block a lane's fragment is built from:
         //   odd block: words c, 4+c;  even block: x[4c+2..4c+5] from words c, c+1 and
         //   x[4c+18..4c+21] from words c+4, c+5 (c < 3); lane 3: x[14..17] from words 3, 4
         //   and [x0, x1, x30, x31] from words 0, 7.
-        constexpr int R = (M::KA * 32 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
-        uint32_t wv[R][NT][4];
+        if (TWO_PHASE) {
+            const uint32_t c16 = ka * (QK / 16);   // 16-byte pieces of a token row in the chunk
+            constexpr int RC = (M::TOKG * M::KA * (QK / 16) + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+            constexpr int RD = (M::KA * 16 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+            uint4 cv[RC];
+            float dv[RD];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
-            if (e < ka * 32) {
+            for (int r = 0; r < RC; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                const uint32_t t = e / c16, c = e - t * c16;
+                if (t < (uint32_t)it.ntok)
+                    cv[r] = __ldg(reinterpret_cast<const uint4 *>(p.qx + (uint64_t)(it.xrow0 + t) * p.in_dim +
+                                                                  (uint64_t)kb0 * QK) + c);
+            }
+#pragma unroll
+            for (int r = 0; r < RD; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                const uint32_t b = e >> 4, t = e & 15;
+                dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8) && t < (uint32_t)it.ntok)
+                            ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b)
+                            : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < RC; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                const uint32_t t = e / c16, c = e - t * c16;
+                if (t < (uint32_t)it.ntok) *reinterpret_cast<uint4 *>(qtmp + (size_t)t * M::QT_STRIDE + (size_t)c * 16) = cv[r];
+            }
+#pragma unroll
+            for (int r = 0; r < RD; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                if (e < ka * 16) dxs[e] = dv[r];
+            }
+            named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
+            for (uint32_t e = threadIdx.x; e < ka * 32; e += CONSUMER_THREADS) {
                 const uint32_t b = e >> 5, l = e & 31, lg = l >> 2, lc = l & 3;
                 const bool even = ((kb0 + b) & 1u) == 0;
                 const uint32_t i1 = even ? lc + 1 : 4 + lc;
                 const uint32_t i2 = lc < 3 ? lc + 4 : 0u;
                 const uint32_t i3 = lc < 3 ? lc + 5 : 7u;
-                const int8_t *xr = p.qx + (uint64_t)(it.xrow0 + lg) * p.in_dim + (uint64_t)(kb0 + b) * QK;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    if (lg + 8u * (uint32_t)t < (uint32_t)it.ntok) {
-                        const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
-                        wv[r][t][0] = __ldg(xt + lc);
-                        wv[r][t][1] = __ldg(xt + i1);
-                        wv[r][t][2] = __ldg(xt + i2);
-                        wv[r][t][3] = __ldg(xt + i3);
-                    } else {
-                        wv[r][t][0] = wv[r][t][1] = wv[r][t][2] = wv[r][t][3] = 0u;
-                    }
-                }
-            }
-        }
-        constexpr int RD = (M::KA * 16 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
-        float dv[RD];
-#pragma unroll
-        for (int r = 0; r < RD; ++r) {
-            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
-            const uint32_t b = e >> 4, t = e & 15;
-            dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8) && t < (uint32_t)it.ntok)
-                        ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b)
-                        : 0.0f;
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
-            if (e < ka * 32) {
-                const uint32_t b = e >> 5, l = e & 31, lc = l & 3;
-                const bool even = ((kb0 + b) & 1u) == 0;
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
+                    const uint32_t *xt = reinterpret_cast<const uint32_t *>(qtmp + (size_t)(lg + 8 * t) * M::QT_STRIDE +
+                                                                            (size_t)b * QK);
                     uint32_t f0, f1;
-                    if (!even) {
-                        f0 = wv[r][t][0];
-                        f1 = wv[r][t][1];
+                    if (lg + 8 * t >= (uint32_t)it.ntok) {
+                        f0 = 0;
+                        f1 = 0;
+                    } else if (!even) {
+                        f0 = xt[lc];
+                        f1 = xt[i1];
                     } else {
-                        f0 = funnel16(wv[r][t][0], wv[r][t][1]);
-                        f1 = lc < 3 ? funnel16(wv[r][t][2], wv[r][t][3]) : __byte_perm(wv[r][t][2], wv[r][t][3], 0x7610);
+                        f0 = funnel16(xt[lc], xt[i1]);
+                        f1 = lc < 3 ? funnel16(xt[i2], xt[i3]) : __byte_perm(xt[i2], xt[i3], 0x7610);
                     }
                     uint4 h;
                     s8x4_to_h2x2(f0, h.x, h.y);   // MMA over the first 16 quants: b0, b1
@@ -483,11 +495,71 @@ __device__ __forceinline__ void stage_chunk(const GemvParams &p, const GItem &it
                     *reinterpret_cast<uint4 *>(act + (size_t)b * M::ACT_BLOCK + (size_t)t * 512 + (size_t)l * 16) = h;
                 }
             }
-        }
+        } else {
+            constexpr int R = (M::KA * 32 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+            uint32_t wv[R][NT][4];
 #pragma unroll
-        for (int r = 0; r < RD; ++r) {
-            const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
-            if (e < ka * 16) dxs[e] = dv[r];
+            for (int r = 0; r < R; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                if (e < ka * 32) {
+                    const uint32_t b = e >> 5, l = e & 31, lg = l >> 2, lc = l & 3;
+                    const bool even = ((kb0 + b) & 1u) == 0;
+                    const uint32_t i1 = even ? lc + 1 : 4 + lc;
+                    const uint32_t i2 = lc < 3 ? lc + 4 : 0u;
+                    const uint32_t i3 = lc < 3 ? lc + 5 : 7u;
+                    const int8_t *xr = p.qx + (uint64_t)(it.xrow0 + lg) * p.in_dim + (uint64_t)(kb0 + b) * QK;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (lg + 8u * (uint32_t)t < (uint32_t)it.ntok) {
+                            const uint32_t *xt = reinterpret_cast<const uint32_t *>(xr + (uint64_t)t * 8 * p.in_dim);
+                            wv[r][t][0] = __ldg(xt + lc);
+                            wv[r][t][1] = __ldg(xt + i1);
+                            wv[r][t][2] = __ldg(xt + i2);
+                            wv[r][t][3] = __ldg(xt + i3);
+                        } else {
+                            wv[r][t][0] = wv[r][t][1] = wv[r][t][2] = wv[r][t][3] = 0u;
+                        }
+                    }
+                }
+            }
+            constexpr int RD = (M::KA * 16 + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+            float dv[RD];
+#pragma unroll
+            for (int r = 0; r < RD; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                const uint32_t b = e >> 4, t = e & 15;
+                dv[r] = (e < ka * 16 && t < (uint32_t)(NT * 8) && t < (uint32_t)it.ntok)
+                            ? __ldg(p.dx + (uint64_t)(it.xrow0 + t) * nb + kb0 + b)
+                            : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                if (e < ka * 32) {
+                    const uint32_t b = e >> 5, l = e & 31, lc = l & 3;
+                    const bool even = ((kb0 + b) & 1u) == 0;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        uint32_t f0, f1;
+                        if (!even) {
+                            f0 = wv[r][t][0];
+                            f1 = wv[r][t][1];
+                        } else {
+                            f0 = funnel16(wv[r][t][0], wv[r][t][1]);
+                            f1 = lc < 3 ? funnel16(wv[r][t][2], wv[r][t][3]) : __byte_perm(wv[r][t][2], wv[r][t][3], 0x7610);
+                        }
+                        uint4 h;
+                        s8x4_to_h2x2(f0, h.x, h.y);   // MMA over the first 16 quants: b0, b1
+                        s8x4_to_h2x2(f1, h.z, h.w);   // MMA over the second 16 quants
+                        *reinterpret_cast<uint4 *>(act + (size_t)b * M::ACT_BLOCK + (size_t)t * 512 + (size_t)l * 16) = h;
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RD; ++r) {
+                const uint32_t e = threadIdx.x + (uint32_t)r * CONSUMER_THREADS;
+                if (e < ka * 16) dxs[e] = dv[r];
+            }
         }
     }
 }
@@ -502,10 +574,9 @@ __device__ __forceinline__ void stage_chunk_fused(const GemvParams &p, const GIt
                                                   uint8_t *act, float *dxs, uint8_t *qtmp) {
     using namespace gv;
     using M = Mode<MODE>;
-    constexpr uint32_t TOKQ = M::TOKG;
     constexpr uint32_t GROUPS = CONSUMER_THREADS / 4;
     const uint32_t lane_q = threadIdx.x & 3u;
-    const uint32_t ntok = (uint32_t)it.ntok;              // <= TOKQ
+    const uint32_t ntok = (uint32_t)it.ntok;              // <= M::TOKG
     const uint32_t npair = ka * ntok;                     // (token, block) pairs, token-major
     const uint32_t rounds = (npair + GROUPS - 1) / GROUPS;
     constexpr int RB = 3;                                 // rounds whose loads are in flight together
@@ -787,7 +858,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 1) k_gemv(const GemvParams p, co
             const uint32_t ka = min((uint32_t)KA, nb - kb0);
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);   // previous chunk or item done with act
             if (p.x) stage_chunk_fused<MODE>(p, it, kb0, ka, act, dxs, qtmp);
-            else stage_chunk<MODE>(p, it, kb0, ka, act, dxs);
+            else stage_chunk<MODE, KIND == KIND_DENSE>(p, it, kb0, ka, act, dxs, qtmp);
             named_bar_sync(BAR_CONSUMERS, CONSUMER_THREADS);
             for (; kk < nk; kk += wpi) {
                 const uint32_t kb = kk * KC;
