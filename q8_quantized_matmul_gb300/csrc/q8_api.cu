@@ -621,8 +621,8 @@ int q8_rmsnorm_quantize(void *xq, float *y, const float *x, const float *gamma, 
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
-    return status_of(q8::launch_rmsnorm_quantize(static_cast<uint8_t *>(xq), y, x, gamma, dim, n_tok, eps, s->num_sms,
-                                                 static_cast<cudaStream_t>(stream)));
+    return status_of(q8::launch_rmsnorm_quantize(static_cast<uint8_t *>(xq), y, x, gamma, dim, n_tok, eps, s->err,
+                                                 s->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,

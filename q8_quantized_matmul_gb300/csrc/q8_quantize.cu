@@ -6,6 +6,8 @@
 // two 16-byte loads), the block maximum is two xor-shuffles away.  Work is
 // memory bound (4 bytes read per value); grids are sized as a multiple of
 // the SM count and loop over blocks.
+#include <cuda.h>
+
 #include "q8_common.cuh"
 #include "q8_kernels.h"
 
@@ -424,6 +426,228 @@ __global__ void __launch_bounds__(RMS_THREADS, MINB) k_rmsnorm_quantize_reg(uint
     }
 }
 
+// ------------------------------------------------------------------ RMSNorm, TMA-fed
+// The same operation for rows of at most 4096 values, one lane per Q8_0 block.
+// A CTA of T = 32 * ceil(nb / 32) threads takes one token row at a time (rows
+// blockIdx.x, + gridDim.x, ...); thread t owns block t (the kernel is written for
+// BPT blocks per thread, t, t + T, ...; two per thread for rows of 8192 held 2 CTAs
+// of 205 registers per SM and ran 1.5x slower than the register kernel).  One TMA box brings a whole row into a ring of RMS_STAGES
+// stages, so the CTA's next rows are in flight without holding registers.  The
+// tensor map's 128-byte swizzle puts chunk j of block b at chunk j ^ (b & 7), so
+// eight consecutive lanes reading chunk j of their own blocks hit eight different
+// bank groups.  With a whole block in one lane, the block maximum needs no
+// shuffles and the scale one division per block; one CTA barrier per row joins
+// the warps' sums of squares.
+// Sum of squares, in a fixed order: per thread, four accumulators over values
+// 8c..8c+7 of each of its blocks in turn (fused multiply-adds), combined as
+// (a0 + a1) + (a2 + a3); a 5-level warp tree; the warps' sums in sequence.  An x^2
+// term meets at most 8 BPT + 2 + 5 + 3 = 18 roundings, inside the 8 ceil(dim/2048) + 14
+// (at least 22) of the other kernels.
+// y and the quantiser's decisions are computed exactly as there (the same
+// products, quantize_block32 = quantize8's arithmetic), so the blocks are the
+// activation quantiser of the kernel's own y.
+constexpr int RMS_STAGES = 2;
+constexpr int RMS_TMA_THREADS = 128;
+constexpr uint32_t RMS_TMA_MAX_DIM = RMS_TMA_THREADS * QK;   // 4096: one block per lane
+
+__device__ __forceinline__ void tma_load_blocks(void *dst, const CUtensorMap *map, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The activation quantiser for one block held whole by one lane (v: its 32
+// values in order): amax = max |v_i|, d = amax / 127 (IEEE), q_i = roundf(v_i / d)
+// by quantize8's division-free test with the IEEE division where the test fails
+// (so the same bytes as quantize8 and q8_quantize_act).  Returns the binary16
+// scale; w: the quants packed, byte i of w[k] = q[4k + i].
+// The test's threshold: qa = fl(v fl(1/d)) and fl(v / d) differ by at most
+// (3u + u^2) 128 < 2.29e-5 (u = 2^-24, |v / d| <= 128), so |qa - k| < 0.5 - 3e-5
+// keeps both in k's rounding interval.  A whole warp takes the slow branch when
+// one of its lanes needs it, 32 blocks at a time: the tighter margin than
+// quantize8's 1e-4 cuts that from about one warp-block in five to one in sixteen.
+constexpr float RMS_TIE_TEST = 0.49997f;
+__device__ __forceinline__ uint16_t quantize_block32(const float (&v)[32], uint32_t (&w)[8]) {
+    float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i & 3] = fmaxf(m[i & 3], fabsf(v[i]));
+    const float amax = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    const float d = __fdiv_rn(amax, 127.0f);
+    if (d == 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = 0u;
+        return 0;
+    }
+    const float rd = __frcp_rn(d);   // inf for a subnormal d: every value then fails the test
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float qa = __fmul_rn(v[4 * k + j], rd);
+            const float sm = __fadd_rn(qa, ROUND_MAGIC);
+            t[j] = __float_as_uint(sm);
+            bad |= !(fabsf(__fsub_rn(qa, __fsub_rn(sm, ROUND_MAGIC))) < RMS_TIE_TEST);
+        }
+        w[k] = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    }
+    if (bad) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float qa = __fmul_rn(v[i], rd);
+            const float sm = __fadd_rn(qa, ROUND_MAGIC);
+            if (!(fabsf(__fsub_rn(qa, __fsub_rn(sm, ROUND_MAGIC))) < RMS_TIE_TEST)) {
+                const uint32_t q = (uint32_t)(uint8_t)(int8_t)(int)roundf(__fdiv_rn(v[i], d));
+                const int sh = 8 * (i & 3);
+                w[i >> 2] = (w[i >> 2] & ~(0xffu << sh)) | (q << sh);
+            }
+        }
+    }
+    return __half_as_ushort(__float2half_rn(d));
+}
+
+// A quantised row staged in shared memory goes out in 16-byte stores when its
+// global start is 16-byte aligned, else in 2-byte stores (coalesced either way:
+// one lane per block wrote 34-byte strides, two bytes at a time).
+__device__ __forceinline__ void store_row_out(uint8_t *dst, const uint8_t *src, uint32_t bytes, uint32_t t,
+                                              uint32_t T) {
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && (bytes & 15u) == 0) {
+        for (uint32_t c = t; c < bytes / 16; c += T)
+            reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+    } else {
+        for (uint32_t c = t; c < bytes / 2; c += T)
+            reinterpret_cast<uint16_t *>(dst)[c] = reinterpret_cast<const uint16_t *>(src)[c];
+    }
+}
+
+template <int BPT, int MINB>
+__global__ void __launch_bounds__(RMS_TMA_THREADS, MINB)
+    k_rmsnorm_quantize_tma(const __grid_constant__ CUtensorMap xmap, uint8_t *__restrict__ xq, float *__restrict__ y,
+                           const float *__restrict__ gamma, uint32_t dim, uint64_t n_tok, float eps, int *err) {
+    extern __shared__ uint8_t rms_dyn[];
+    __shared__ uint64_t full[RMS_STAGES];
+    __shared__ float part[2][RMS_TMA_THREADS / 32];
+    __shared__ int abort_flag;
+    const uint32_t T = blockDim.x, t = threadIdx.x, lane = t & 31u, warp = t >> 5, W = T >> 5;
+    const uint32_t nb = dim / QK;
+    const uint32_t stage_bytes = (nb * 128u + 1023u) & ~1023u;
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rms_dyn) + 1023) & ~(uintptr_t)1023);
+    const uint32_t row_out = nb * QB;                       // bytes of a quantised row
+    const uint32_t out_stride = (row_out + 15u) & ~15u;
+    uint8_t *outs = ring + RMS_STAGES * stage_bytes;       // two staged output rows
+    const uint64_t G = gridDim.x;
+    uint32_t issued = 0, par = 0;   // thread 0: stages with a copy not yet consumed, and its phase parity
+    if (t == 0) {
+        for (int s = 0; s < RMS_STAGES; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        for (uint32_t s = 0; s < (uint32_t)RMS_STAGES; ++s) {
+            const uint64_t row = blockIdx.x + s * G;
+            if (row < n_tok) {
+                mbar_arrive_expect_tx(&full[s], nb * 128u);
+                tma_load_blocks(ring + s * stage_bytes, &xmap, (int)(row * nb), &full[s]);
+                issued |= 1u << s;
+            }
+        }
+    }
+    __syncthreads();
+    float g[BPT][32];
+#pragma unroll
+    for (int bl = 0; bl < BPT; ++bl) {
+        const uint32_t bi = t + (uint32_t)bl * T;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float4 q4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            if (gamma && bi < nb) q4 = __ldg(reinterpret_cast<const float4 *>(gamma + (size_t)bi * QK) + c);
+            g[bl][4 * c] = q4.x; g[bl][4 * c + 1] = q4.y; g[bl][4 * c + 2] = q4.z; g[bl][4 * c + 3] = q4.w;
+        }
+    }
+    uint32_t i = 0;
+    for (uint64_t row = blockIdx.x; row < n_tok; row += G, ++i) {
+        const uint32_t s = i % RMS_STAGES, ph = (i / RMS_STAGES) & 1u;
+        const bool ok = mbar_wait(&full[s], ph, err, &abort_flag);
+        const uint8_t *st = ring + s * stage_bytes;
+        float v[BPT][32];
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int bl = 0; bl < BPT; ++bl) {
+            const uint32_t bi = t + (uint32_t)bl * T;
+            const bool live = ok && bi < nb;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 c4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (live) c4 = *reinterpret_cast<const float4 *>(st + bi * 128u + (((uint32_t)j ^ (bi & 7u)) << 4));
+                v[bl][4 * j] = c4.x; v[bl][4 * j + 1] = c4.y; v[bl][4 * j + 2] = c4.z; v[bl][4 * j + 3] = c4.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[c] = __fmaf_rn(v[bl][8 * c + e], v[bl][8 * c + e], acc[c]);
+        }
+        float sq = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, o));
+        if (lane == 0) part[i & 1u][warp] = sq;
+        // every thread has read stage s and written its warp's sum (part is double-buffered
+        // by row parity: the next row's writes cannot meet this row's reads)
+        if (__syncthreads_or(!ok)) break;
+        if (t == 0) {
+            issued &= ~(1u << s);
+            const uint64_t nrow = row + (uint64_t)RMS_STAGES * G;
+            if (nrow < n_tok) {
+                mbar_arrive_expect_tx(&full[s], nb * 128u);
+                tma_load_blocks(ring + s * stage_bytes, &xmap, (int)(nrow * nb), &full[s]);
+                issued |= 1u << s;
+                par = (par & ~(1u << s)) | ((((i + RMS_STAGES) / RMS_STAGES) & 1u) << s);
+            }
+        }
+        if (i > 0) store_row_out(xq + (row - G) * row_out, outs + ((i - 1) & 1u) * out_stride, row_out, t, T);
+        float tot = 0.0f;
+        for (uint32_t w = 0; w < W; ++w) tot = __fadd_rn(tot, part[i & 1u][w]);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)dim), eps)));
+#pragma unroll
+        for (int bl = 0; bl < BPT; ++bl) {
+            const uint32_t bi = t + (uint32_t)bl * T;
+            if (bi < nb) {
+                float yv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) yv[e] = __fmul_rn(__fmul_rn(v[bl][e], r), g[bl][e]);
+                if (y) {
+                    float4 *yo = reinterpret_cast<float4 *>(y + row * dim + (size_t)bi * QK);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) yo[c] = make_float4(yv[4 * c], yv[4 * c + 1], yv[4 * c + 2], yv[4 * c + 3]);
+                }
+                uint32_t w8[8];
+                const uint16_t dh = quantize_block32(yv, w8);
+                uint16_t *o = reinterpret_cast<uint16_t *>(outs + (i & 1u) * out_stride + bi * QB);
+                o[0] = dh;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    o[1 + 2 * k] = (uint16_t)w8[k];
+                    o[2 + 2 * k] = (uint16_t)(w8[k] >> 16);
+                }
+            }
+        }
+    }
+    // The CTA's last row (the loop ran to its end: i rows, none aborted).
+    __syncthreads();
+    if (i > 0 && !abort_flag) {
+        const uint64_t last = blockIdx.x + (uint64_t)(i - 1) * G;
+        if (last < n_tok) store_row_out(xq + last * row_out, outs + ((i - 1) & 1u) * out_stride, row_out, t, T);
+    }
+    // After an expired wait: let the copies still in flight land before the CTA's
+    // shared memory goes away (each stage has at most one, the last issued on it).
+    if (t == 0 && issued) {
+        const uint64_t t_end = global_timer_ns() + WAIT_LIMIT_NS;
+        for (uint32_t s = 0; s < (uint32_t)RMS_STAGES; ++s)
+            if (issued & (1u << s)) mbar_drain(&full[s], (par >> s) & 1u, t_end);
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 // Launch behind the previous kernel with programmatic serialisation: the
 // launch overlaps that kernel's drain; the kernel waits for it in
@@ -527,9 +751,40 @@ static cudaError_t launch_rms_reg(uint8_t *xq, float *y, const float *x, const f
     return cudaGetLastError();
 }
 
+bool encode_blocks_tmap(CUtensorMap *map, const float *x, uint64_t n_blocks, uint32_t box_blocks);
+
+template <int BPT, int MINB>
+static cudaError_t launch_rms_tma(const CUtensorMap &map, uint8_t *xq, float *y, const float *gamma, uint32_t dim,
+                                  uint64_t n_tok, float eps, int *err, int num_sms, cudaStream_t st) {
+    const uint32_t nb = dim / QK;
+    const uint32_t warps = (nb + 31) / 32 < 4 ? (nb + 31) / 32 : 4;
+    const int threads = (int)(32 * warps);
+    const size_t smem = 1024 + (size_t)RMS_STAGES * ((nb * 128u + 1023u) & ~1023u) + 2 * ((nb * QB + 15u) & ~15u);
+    auto k = k_rmsnorm_quantize_tma<BPT, MINB>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
+    if (e != cudaSuccess) return e;
+    const uint64_t cap = (uint64_t)num_sms * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(n_tok < cap ? n_tok : cap);
+    k<<<grid, threads, smem, st>>>(map, xq, y, gamma, dim, n_tok, eps, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
-                                    uint64_t n_tok, float eps, int num_sms, cudaStream_t st) {
+                                    uint64_t n_tok, float eps, int *err, int num_sms, cudaStream_t st) {
     if (n_tok == 0) return cudaSuccess;
+    // Rows of up to 4096 values, at least three per CTA (four CTAs per SM): the
+    // TMA-fed kernel, one lane per block.  It streams faster (4096 rows of 4096:
+    // 20.3 against 21.5 us; of 1024: 8.6 against 9.9 us), but its chain per row is
+    // longer, and with fewer rows the register kernel finishes first (1216 rows of
+    // 4096: 8.7 against 9.8 us; 64 rows: 3.4 against 4.1 us).
+    const uint64_t nb = dim / QK;
+    CUtensorMap map;
+    if (dim <= RMS_TMA_MAX_DIM && n_tok >= 12 * (uint64_t)num_sms && n_tok * nb < (1ull << 31) &&
+        encode_blocks_tmap(&map, x, n_tok * nb, (uint32_t)nb))
+        return launch_rms_tma<1, 4>(map, xq, y, gamma, (uint32_t)dim, n_tok, eps, err, num_sms, st);
     // rows of up to 8192 values stay in registers; longer rows are read twice
     if (dim <= RMS_THREADS * 8) return launch_rms_reg<1, 4>(xq, y, x, gamma, dim, n_tok, eps, num_sms, st);
     if (dim <= 2 * RMS_THREADS * 8) return launch_rms_reg<2, 4>(xq, y, x, gamma, dim, n_tok, eps, num_sms, st);

@@ -62,4 +62,21 @@ bool encode_f16_tmap(CUtensorMap *map, const void *base, uint64_t cols, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+// fp32 rows cut into Q8_0 blocks: a [n_blocks][32] view of x (one 128-byte row
+// per block) with a box of box_blocks blocks and the 128-byte swizzle, so that in
+// shared memory the 16-byte chunk j of block b lies at chunk j ^ (b & 7) of the
+// block's 128 bytes (the box must land 1024-byte aligned).
+bool encode_blocks_tmap(CUtensorMap *map, const float *x, uint64_t n_blocks, uint32_t box_blocks) {
+    if (!load_encoder()) return false;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || n_blocks == 0 || n_blocks > (1ull << 32)) return false;
+    cuuint64_t dims[2] = {32, n_blocks};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {32, box_blocks};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace q8

@@ -54,7 +54,12 @@ def check(q8, o, x, gamma, eps):
 
 @pytest.mark.parametrize("dim,n_tok", [(4096, 37), (1024, 5), (96, 3), (32, 7), (2080, 4), (6144, 9), (16384, 2),
                                        # more rows than resident CTAs: each CTA loops, the next row in flight
-                                       (4096, 1000), (8192, 700), (2048, 2000)])
+                                       (4096, 1000), (8192, 700), (2048, 2000),
+                                       # 12 * 152 rows and more (rows <= 4096 values): the TMA-fed kernel,
+                                       # one lane per block; 1, 3 and 65 blocks leave lanes of a warp idle
+                                       (4096, 1900), (1024, 1824), (32, 2000), (96, 1900), (2080, 1830),
+                                       # the long-prefill shape itself
+                                       (4096, 4096)])
 @pytest.mark.parametrize("with_gamma", [True, False])
 def test_rmsnorm_quantize_parity(q8, o, dim, n_tok, with_gamma):
     x = inputs.normal((n_tok, dim), seed=dim + n_tok, p_out=0.01)
@@ -67,6 +72,15 @@ def test_rmsnorm_quantize_many_rows_and_special_rows(q8, o):
     """More rows than resident CTAs (each CTA loops over rows), a zero row, a row where eps
     dominates, and a row of +/-1."""
     n_tok, dim = 152 * 8 + 5, 64
+    check_special_rows(q8, o, n_tok, dim)
+
+
+def test_rmsnorm_quantize_special_rows_tma(q8, o):
+    """The same special rows through the TMA-fed kernel (enough rows for three per CTA)."""
+    check_special_rows(q8, o, 152 * 12 + 7, 256)
+
+
+def check_special_rows(q8, o, n_tok, dim):
     x = inputs.normal((n_tok, dim), seed=7)
     x[3] = 0.0
     x[10] = (1e-6 * x[10]).astype(np.float32)
