@@ -214,7 +214,11 @@ int run_dense(DeviceState *s, float *out, const void *W, uint64_t in_dim, uint64
         g.row_to_out = nullptr;
         g.n_expert = 1;
         const int grid = (int)(g.n_items < (uint32_t)s->num_sms ? g.n_items : (uint32_t)s->num_sms);
-        g.weights_early = x_fused ? 0 : 1;   // planes: the preceding kernel is the quantiser
+        // Weights before the grid wait: behind the quantiser (planes), and for fused
+        // calls of 1-2 tokens, whose 4-8 KB of fp32 rows barely queue behind the
+        // early copies (1-token calls 8.17 -> 7.5 us, the mixed decode step 29.7 ->
+        // 29.0 us; fused 3-8-token calls measured slower that way, 8.6 -> 9.2-9.9 us).
+        g.weights_early = (!x_fused || n_tok <= 2) ? 1 : 0;
         take_expiry(g.wait_ns, g.withhold);
         return status_of(timed_launch(st, [&] { return q8::launch_gemv(g, q8::gemv_mode(n_tok), grid, st); }));
     }

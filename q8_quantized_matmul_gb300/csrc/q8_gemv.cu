@@ -57,10 +57,10 @@
 //   * Launched with programmatic stream serialisation, so the launch and the
 //     barrier set-up overlap the end of the preceding kernel.  Nothing written
 //     by an earlier kernel is read before griddepcontrol.wait, except the
-//     weights when the kernel runs behind this library's quantiser (which
-//     triggers early and writes nothing they depend on): then the first eight
-//     weight copies per SM go out while it runs (dense calls; grouped calls
-//     stream on), the rest once it is done.  This kernel does not trigger early: measured
+//     weights (which no kernel that triggers its dependents early writes),
+//     behind this library's quantiser and in fused calls of 1-2 tokens: then
+//     the first eight weight copies per SM go out before the wait (dense calls;
+//     grouped calls stream on), the rest once it returns.  This kernel does not trigger early: measured
 //     on GB300, an early trigger sped up runs of equal calls but slowed a
 //     mixed decode step (a fused call followed by quantiser + GEMV) by 10 %.
 #include <cuda.h>
@@ -341,10 +341,12 @@ __device__ __forceinline__ uint32_t produce(const GemvParams &p, const CUtensorM
         for (uint32_t base = 0; base < total; base += 32) {
             const uint32_t idx = base + (uint32_t)lane;
             // A dense call streaming ahead of griddepcontrol.wait (behind this
-            // library's quantiser) issues only its first EARLY_SLOTS copies before the
-            // wait, so that the consumers' activation loads, issued once the wait
-            // returns, queue behind 39 KB of weights per SM instead of 152 KB (decode
-            // step 31.3 -> 31.0 us; the grouped calls measured 1 % slower with it).
+            // library's quantiser, or a fused 1-2-token call) issues only its first
+            // EARLY_SLOTS copies before the wait, so that the consumers' activation
+            // loads, issued once the wait returns, queue behind 39 KB of weights per SM
+            // instead of 152 KB (decode step 31.3 -> 31.0 us; fused 1-token calls 7.5
+            // us against 8.6 with every copy early; the grouped calls measured 1 %
+            // slower with it).
             const bool hold = KIND == KIND_DENSE && p.weights_early && seqbase == 0 && base == 0;
             for (int pass = 0; pass < (hold ? 2 : 1); ++pass) {
                 if (pass == 1) {

@@ -100,8 +100,8 @@ struct GemvParams {
     const int8_t *qx;          // activation quant plane [rows][in_dim] (groups padded to 16 rows)
     const float *dx;           // activation scale plane [rows][nb]
     const float *x;            // dense only: fp32 rows [n_tok][in_dim] quantised in the kernel (qx, dx unused)
-    int weights_early;         // 1: launched behind this library's quantiser, which writes nothing the
-                               //    weights depend on: the weight stream starts before griddepcontrol.wait
+    int weights_early;         // 1: the weight stream starts before griddepcontrol.wait (W is never
+                               //    written by a kernel that triggers its dependents early)
     float *out;
     int *err;
     uint32_t n_tok;            // dense: the tokens (<= 8 or 16)
