@@ -402,7 +402,9 @@ void q8_debug_fail_next_alloc(int count);
  * tensor-parallel poll gates a time budget and fail instead of hanging: GPU
  * concepts page, §4, distributed inference).  The next `count` dense matmul
  * kernels (the weight-streaming GEMV and the tcgen05 GEMM that q8_matmul,
- * q8_matmul_q and q8_matmul_host launch) run with every wait limited to
+ * q8_matmul_q and q8_matmul_host launch, and the TMA-fed kernel that
+ * q8_rmsnorm_quantize runs for rows of at most 4096 values and at least 12
+ * rows per SM) run with every wait limited to
  * limit_ns nanoseconds (0: the normal 2 s) and with their producer issuing no
  * copy at all, so the consumers wait on buffers that never fill.  Each such
  * kernel then raises Q8_ETIMEOUT for q8_last_error(), stops waiting, lets any

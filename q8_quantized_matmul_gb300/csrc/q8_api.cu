@@ -32,7 +32,8 @@ int g_fail_next_alloc = 0;
 int g_expire_next = 0;            // q8_debug_expire_waits: dense kernels still to withhold their copies
 uint64_t g_expire_limit_ns = 0;   // ... and their wait limit
 
-// The failure-detection test hook, consumed by one dense GEMV or GEMM launch.
+// The failure-detection test hook, consumed by one dense GEMV or GEMM launch, or one
+// launch of the TMA-fed RMSNorm kernel.
 void take_expiry(uint64_t &wait_ns, int &withhold) {
     wait_ns = 0;
     withhold = 0;
@@ -625,8 +626,11 @@ int q8_rmsnorm_quantize(void *xq, float *y, const float *x, const float *gamma, 
     std::lock_guard<std::mutex> lk(g_mutex);
     DeviceState *s;
     if ((rc = get_device(&s))) return rc;
+    uint64_t wait_ns = 0;
+    int withhold = 0;
+    if (q8::rmsnorm_uses_tma(dim, n_tok, s->num_sms)) take_expiry(wait_ns, withhold);
     return status_of(q8::launch_rmsnorm_quantize(static_cast<uint8_t *>(xq), y, x, gamma, dim, n_tok, eps, s->err,
-                                                 s->num_sms, static_cast<cudaStream_t>(stream)));
+                                                 wait_ns, withhold, s->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 static int matmul_common(float *out, const void *W, uint64_t in_dim, uint64_t out_dim, const float *x,

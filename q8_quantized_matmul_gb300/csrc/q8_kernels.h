@@ -163,9 +163,13 @@ inline uint32_t gemv_dense_items(uint64_t out_dim, int num_sms) {
 // RMSNorm feeding the quantiser (q8_quantize.cu): per token row, y = x / sqrt(mean x^2 + eps)
 // * gamma (gamma null: ones), xq = the activation quantiser of y ([n_tok][dim/32] blocks).
 // x, gamma, y 16-byte aligned; y may be null; dim % 32 == 0.
-// err: the device error word (an expired bounded wait of the TMA-fed kernel).
+// err: the device error word (an expired bounded wait of the TMA-fed kernel); wait_ns (0: the
+// default limit) and withhold (issue no copy) are the failure-detection test hook, used only by
+// the TMA-fed kernel, which rmsnorm_uses_tma() says the call will run.
+bool rmsnorm_uses_tma(uint64_t dim, uint64_t n_tok, int num_sms);
 cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
-                                    uint64_t n_tok, float eps, int *err, int num_sms, cudaStream_t st);
+                                    uint64_t n_tok, float eps, int *err, uint64_t wait_ns, int withhold, int num_sms,
+                                    cudaStream_t st);
 
 // Elementwise steps of the routed expert FFN (q8_ffn.cu).
 //   launch_swiglu:  mid[i] = silu(min(gate[i], L)) * clamp(up[i], -L, L) (L = limit; 0: no

@@ -526,7 +526,8 @@ __device__ __forceinline__ void store_row_out(uint8_t *dst, const uint8_t *src, 
 template <int BPT, int MINB>
 __global__ void __launch_bounds__(RMS_TMA_THREADS, MINB)
     k_rmsnorm_quantize_tma(const __grid_constant__ CUtensorMap xmap, uint8_t *__restrict__ xq, float *__restrict__ y,
-                           const float *__restrict__ gamma, uint32_t dim, uint64_t n_tok, float eps, int *err) {
+                           const float *__restrict__ gamma, uint32_t dim, uint64_t n_tok, float eps, int *err,
+                           uint64_t wait_ns, int withhold) {
     extern __shared__ uint8_t rms_dyn[];
     __shared__ uint64_t full[RMS_STAGES];
     __shared__ float part[2][RMS_TMA_THREADS / 32];
@@ -540,11 +541,13 @@ __global__ void __launch_bounds__(RMS_TMA_THREADS, MINB)
     uint8_t *outs = ring + RMS_STAGES * stage_bytes;       // two staged output rows
     const uint64_t G = gridDim.x;
     uint32_t issued = 0, par = 0;   // thread 0: stages with a copy not yet consumed, and its phase parity
+    const uint64_t lim = wait_limit(wait_ns);
     if (t == 0) {
         for (int s = 0; s < RMS_STAGES; ++s) mbar_init(&full[s], 1);
         abort_flag = 0;
         fence_mbar_init();
-        for (uint32_t s = 0; s < (uint32_t)RMS_STAGES; ++s) {
+        // withhold (the failure-detection test hook): no copy is issued, every wait expires
+        for (uint32_t s = 0; s < (uint32_t)RMS_STAGES && !withhold; ++s) {
             const uint64_t row = blockIdx.x + s * G;
             if (row < n_tok) {
                 mbar_arrive_expect_tx(&full[s], nb * 128u);
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(RMS_TMA_THREADS, MINB)
     uint32_t i = 0;
     for (uint64_t row = blockIdx.x; row < n_tok; row += G, ++i) {
         const uint32_t s = i % RMS_STAGES, ph = (i / RMS_STAGES) & 1u;
-        const bool ok = mbar_wait(&full[s], ph, err, &abort_flag);
+        const bool ok = mbar_wait(&full[s], ph, err, &abort_flag, lim);
         const uint8_t *st = ring + s * stage_bytes;
         float v[BPT][32];
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -755,7 +758,8 @@ bool encode_blocks_tmap(CUtensorMap *map, const float *x, uint64_t n_blocks, uin
 
 template <int BPT, int MINB>
 static cudaError_t launch_rms_tma(const CUtensorMap &map, uint8_t *xq, float *y, const float *gamma, uint32_t dim,
-                                  uint64_t n_tok, float eps, int *err, int num_sms, cudaStream_t st) {
+                                  uint64_t n_tok, float eps, int *err, uint64_t wait_ns, int withhold, int num_sms,
+                                  cudaStream_t st) {
     const uint32_t nb = dim / QK;
     const uint32_t warps = (nb + 31) / 32 < 4 ? (nb + 31) / 32 : 4;
     const int threads = (int)(32 * warps);
@@ -768,12 +772,17 @@ static cudaError_t launch_rms_tma(const CUtensorMap &map, uint8_t *xq, float *y,
     if (e != cudaSuccess) return e;
     const uint64_t cap = (uint64_t)num_sms * (uint64_t)(per_sm > 0 ? per_sm : 1);
     const int grid = (int)(n_tok < cap ? n_tok : cap);
-    k<<<grid, threads, smem, st>>>(map, xq, y, gamma, dim, n_tok, eps, err);
+    k<<<grid, threads, smem, st>>>(map, xq, y, gamma, dim, n_tok, eps, err, wait_ns, withhold);
     return cudaGetLastError();
 }
 
+bool rmsnorm_uses_tma(uint64_t dim, uint64_t n_tok, int num_sms) {
+    return dim <= RMS_TMA_MAX_DIM && n_tok >= 12 * (uint64_t)num_sms && n_tok * (dim / QK) < (1ull << 31);
+}
+
 cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const float *gamma, uint64_t dim,
-                                    uint64_t n_tok, float eps, int *err, int num_sms, cudaStream_t st) {
+                                    uint64_t n_tok, float eps, int *err, uint64_t wait_ns, int withhold, int num_sms,
+                                    cudaStream_t st) {
     if (n_tok == 0) return cudaSuccess;
     // Rows of up to 4096 values, at least three per CTA (four CTAs per SM): the
     // TMA-fed kernel, one lane per block.  It streams faster (4096 rows of 4096:
@@ -782,9 +791,9 @@ cudaError_t launch_rmsnorm_quantize(uint8_t *xq, float *y, const float *x, const
     // 4096: 8.7 against 9.8 us; 64 rows: 3.4 against 4.1 us).
     const uint64_t nb = dim / QK;
     CUtensorMap map;
-    if (dim <= RMS_TMA_MAX_DIM && n_tok >= 12 * (uint64_t)num_sms && n_tok * nb < (1ull << 31) &&
-        encode_blocks_tmap(&map, x, n_tok * nb, (uint32_t)nb))
-        return launch_rms_tma<1, 4>(map, xq, y, gamma, (uint32_t)dim, n_tok, eps, err, num_sms, st);
+    if (rmsnorm_uses_tma(dim, n_tok, num_sms) && encode_blocks_tmap(&map, x, n_tok * nb, (uint32_t)nb))
+        return launch_rms_tma<1, 4>(map, xq, y, gamma, (uint32_t)dim, n_tok, eps, err, wait_ns, withhold, num_sms,
+                                    st);
     // rows of up to 8192 values stay in registers; longer rows are read twice
     if (dim <= RMS_THREADS * 8) return launch_rms_reg<1, 4>(xq, y, x, gamma, dim, n_tok, eps, num_sms, st);
     if (dim <= 2 * RMS_THREADS * 8) return launch_rms_reg<2, 4>(xq, y, x, gamma, dim, n_tok, eps, num_sms, st);

@@ -6,7 +6,8 @@ no copy at all (its consumers wait on buffers that never fill) and shortens the
 wait limit.  The call must still return, the error word must read Q8_ETIMEOUT,
 and the next call on the same context must pass oracle parity.  Covered: the
 weight-streaming GEMV (fused quantiser, and behind the quantiser kernel) on the
-decode projection shape, and the tcgen05 GEMM on raw and on expanded weights.
+decode projection shape, the tcgen05 GEMM on raw and on expanded weights, and
+the TMA-fed RMSNorm kernel (its rows' copies withheld).
 """
 import time
 
@@ -64,3 +65,30 @@ def test_expired_wait_reports_timeout_and_context_recovers(q8, in_dim, out_dim, 
     got = out.cpu().numpy().astype(np.float64)
     assert not np.any(np.isnan(got))
     assert np.all(np.abs(got - ref) <= oracle.tolerance(bound))
+
+
+def test_expired_wait_rmsnorm_tma(q8):
+    """The TMA-fed RMSNorm kernel (rows of 4096 values, 12 rows per SM and more) issues no row copy
+    under the hook: every CTA's waits expire, it skips its output and returns; the call ends promptly
+    with Q8_ETIMEOUT and the next call on the context agrees with the oracle."""
+    from tests import allowances
+    o = oracle.get()
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    n_tok, dim = 12 * n_sm + 3, 4096
+    xh = inputs.normal((n_tok, dim), seed=9, p_out=0.01)
+    gh = (1.0 + 0.3 * np.random.default_rng(9).standard_normal(dim)).astype(np.float32)
+    x, g = torch.from_numpy(xh).cuda(), torch.from_numpy(gh).cuda()
+    assert q8.q8_last_error() == 0
+    q8.q8_debug_expire_waits(1, LIMIT_NS)
+    try:
+        t0 = time.perf_counter()
+        q8.rmsnorm_quantize(x, g, 1e-6, want_y=True)
+        assert q8.q8_last_error() == q8.Q8_ETIMEOUT
+        assert time.perf_counter() - t0 < 1.5, "an expired wait did not end its kernel promptly"
+    finally:
+        q8.q8_debug_expire_waits(0, 0)
+    assert q8.q8_last_error() == 0
+    xq, y = q8.rmsnorm_quantize(x, g, 1e-6, want_y=True)
+    assert q8.q8_last_error() == 0
+    xq_o, y_o = o.rmsnorm_quantize(xh, gh, 1e-6)
+    allowances.check_rmsnorm(xq.cpu().numpy(), y.cpu().numpy(), xq_o, y_o)
