@@ -41,11 +41,12 @@
  *   - Kernels are launched with programmatic stream serialisation: a kernel
  *     may start while the one before it on the stream finishes, once that one
  *     has signalled its dependents.  Everything a kernel reads is read after
- *     it waits for its predecessor, except weight rows: the decode kernels may
- *     start streaming W before that wait.  So W must not be written by a
- *     kernel that signals programmatic dependents before its writes (none of
- *     this library's kernels writes weights; a kernel that does not use
- *     programmatic launches is always waited for in full).
+ *     it waits for its predecessor, except weights: the decode kernels may
+ *     start streaming W, and q8_rmsnorm_quantize may load gamma, before that
+ *     wait.  So W and gamma must not be written by a kernel that signals
+ *     programmatic dependents before its writes (none of this library's
+ *     kernels writes weights; a kernel that does not use programmatic
+ *     launches is always waited for in full).
  */
 #ifndef Q8_H
 #define Q8_H
