@@ -798,8 +798,17 @@ static cudaError_t launch_rms_tma(const CUtensorMap &map, uint8_t *xq, float *y,
     const int threads = (int)(32 * warps);
     const size_t smem = 1024 + (size_t)RMS_STAGES * ((nb * 128u + 1023u) & ~1023u) + 2 * ((nb * QB + 15u) & ~15u);
     auto k = k_rmsnorm_quantize_tma<BPT, MINB>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    // the attribute once, at the largest size a call can ask for (rows of RMS_TMA_MAX_DIM);
+    // the library's entry points run under one lock
+    static bool attr_done = false;
+    cudaError_t e;
+    if (!attr_done) {
+        const size_t smax = 1024 + (size_t)RMS_STAGES * (RMS_TMA_MAX_DIM / QK) * 128u +
+                            2 * (((RMS_TMA_MAX_DIM / QK) * QB + 15u) & ~15u);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
     if (e != cudaSuccess) return e;
