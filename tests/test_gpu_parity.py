@@ -143,6 +143,22 @@ def test_matmul_parity(q8, o, in_dim, out_dim, n_tok):
     assert_close(got, ref, bound, f"matmul {in_dim}x{out_dim}x{n_tok}")
 
 
+@pytest.mark.parametrize("n_tok,in_dim,out_dim", [(3, 4352, 300), (7, 4352, 130), (9, 4352, 150),
+                                                   (13, 2816, 77), (16, 6400, 50)])
+def test_planes_staging_ragged_chunks(q8, o, n_tok, in_dim, out_dim):
+    """The GEMV's MMA modes staging pre-quantised activations from the planes (dense calls
+    copy the token rows to shared memory in 16-byte pieces and build the fragments there):
+    token counts that leave rows of an 8-token tile empty, and K chunks of 80 (one tile) or
+    40 (two tiles) blocks with a ragged last chunk (136, 88 and 200 blocks)."""
+    Wh = inputs.weights(out_dim, in_dim, seed=in_dim + n_tok)
+    xh = inputs.normal((n_tok, in_dim), seed=n_tok + 5, p_out=0.01)
+    ref, bound = o.matmul(Wh, xh, out_dim)
+    xq = q8.quantize_act(dev(xh))
+    got = q8.matmul_q(dev(Wh), xq, in_dim, out_dim).cpu().numpy()
+    assert q8.q8_last_error() == 0
+    assert_close(got, ref, bound, f"matmul_q {in_dim}x{out_dim}x{n_tok}")
+
+
 @pytest.mark.parametrize("out_dim,n_tok", [(40000, 1), (40000, 16), (70000, 4), (70000, 16)])
 def test_gemv_wide_outputs(q8, o, out_dim, n_tok):
     """Outputs wider than 152 x 14 sixteen-row sub-items: each CTA item holds 17 (out
