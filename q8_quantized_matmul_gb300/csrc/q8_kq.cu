@@ -655,9 +655,12 @@ uint32_t kq_stream_rows(uint64_t row_bytes, uint64_t in_dim, int tokg) {
     if (row_bytes == 0 || row_bytes % 16 || row_bytes > kqs::SLOT_BYTES) return 0;
     if (in_dim % 256 || kqs::act_row_bytes(in_dim) > 4864) return 0;
     // whole multiples of the consumers' 14 rows (every warp takes the same number
-    // of row pairs) when a slot holds that many
+    // of row pairs) when a slot holds that many, at most 42: items of 56 short rows
+    // (Q2_K, in_dim 2048) made the routed down call slower (368.5 us at 42 against
+    // 387.9 us at 56; 381.8 us at 28)
     const uint64_t r = kqs::SLOT_BYTES / row_bytes;
-    return (uint32_t)(r < (uint64_t)kqs::NCONS ? r : r / kqs::NCONS * kqs::NCONS);
+    const uint64_t rows = r < (uint64_t)kqs::NCONS ? r : r / kqs::NCONS * kqs::NCONS;
+    return (uint32_t)(rows > 3 * kqs::NCONS ? 3 * kqs::NCONS : rows);
 }
 
 template <int FMT, int TOKG> static cudaError_t launch_stream(const KqParams &p, int num_sms, cudaStream_t st) {
